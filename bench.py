@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of one sparse decode step (select + attend + combine) on GB300.
+
+Default workload: the Qwen2.5-1.5B-like layer, bf16, batch 32, 12 query /
+2 KV heads, head_dim 128, 64k context, 16-token pages, 2048-token budget
+(128 pages incl. the sink page and the last 64 tokens).  Synthetic seeded
+inputs (no real KV cache exists here).
+
+value = algorithmic bytes of the step (page min/max metadata of every page
++ K and V of the selected tokens) / device time per step, in GB/s.
+
+The timed region replays one CUDA graph per buffer set; NSETS copies of the
+KV cache and metadata rotate so that consecutive steps never find their
+bytes in L2 (NSETS * step bytes >= 4 * L2).  `python bench.py --impl
+reference` times the fp64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_long_context_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak) for select+attend"
+
+
+# ------------------------------------------------------------------ helpers
+
+def algorithmic_bytes(s: W.Spec, kept_blocks_total: int = 0) -> dict:
+    """Bytes the step must read: selector metadata + selected K and V."""
+    esz = 2 if s.dtype == "bf16" else 4
+    rows = s.rows
+    if s.selector == "quest":
+        meta = 0
+        sel_tokens = 0
+        for b in range(s.batch):
+            n = s.ctx_len[b]
+            npg = -(-n // s.page_size)
+            per_page = (1 if s.page_size == 1 else 2) * s.head_dim * esz
+            meta += s.num_kv_heads * npg * per_page
+            sel_tokens += s.num_kv_heads * min(npg, s.k_pages) * s.page_size
+        kv = sel_tokens * 2 * s.head_dim * esz
+    else:
+        meta = 0
+        for b in range(s.batch):
+            n = s.ctx_len[b]
+            nfull = n // s.block
+            meta += s.num_kv_heads * (nfull * s.block * s.head_dim // 4 + nfull * s.head_dim * esz)
+            meta += s.num_kv_heads * min(n, 2 * s.block) * s.head_dim * esz  # pseudo-max keys
+        kv = kept_blocks_total * s.block * 2 * s.head_dim * esz
+    return {"select": int(meta), "attend": int(kv), "total": int(meta + kv), "rows": rows}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inwin = [r for r in rows if self.t0 is not None and self.t0 - 1 <= r[0] <= self.t1 + 1]
+        use = inwin or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use),
+                "window": "timed" if inwin else "run"}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def aggregate(elapsed_s: float, units: float, world: int):
+    """Max time and summed units over ranks (identity on one process)."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def _oracle_row_task(args):
+    """Time the oracle's select + sparse attention on one row (inputs and
+    page summaries are prepared outside the timed part)."""
+    spec_kw, b, h, pages_limit = args
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    from oracle import sls_oracle as O
+    s = W.spec(**spec_kw)
+    row = W.gen_row(s, b, h)
+    G = s.group
+    q = O.to_f64(row.q, s.dtype)
+    K = O.to_f64(row.K, s.dtype)
+    V = O.to_f64(row.V, s.dtype)
+    n = s.ctx_len[b]
+    if pages_limit:  # a bounded sample: the first pages of the row
+        n = min(n, pages_limit * s.page_size)
+    kmin, kmax = O.page_minmax(K, n, s.page_size)
+    t0 = time.perf_counter()
+    score = O.group_score(O.quest_bound(q, kmin, kmax))
+    pages = O.select_topk(score, s.k_pages, O.forced_pages(n, s.page_size, s.n_sink_pages, s.n_local_tokens))
+    O.sparse_attention_row(q, K, V, pages, n, s.page_size, s.scale)
+    dt = time.perf_counter() - t0
+    esz = 2
+    nbytes = kmin.shape[0] * 2 * s.head_dim * esz + len(O.pages_to_tokens(pages, n, s.page_size)) * 2 * s.head_dim * esz
+    return dt, nbytes
+
+
+def parity_check(s: W.Spec, host, sel, out):
+    """Sampled rows of the benchmarked step against the oracle (part of the
+    CPU-baseline leg).  Raises if a row disagrees."""
+    from tests import parity as PT
+    res = {"rows": [0, s.rows - 1], "ties": 0, "max_abs": 0.0, "rel_l2": 0.0}
+    for r in res["rows"]:
+        b, h = divmod(r, s.num_kv_heads)
+        orc = PT.oracle_row(s, host, b, h)
+        t = PT.check_quest_list(sel[r], orc, int(host.ctx_len[b]), s.page_size, s.k_pages)
+        res["ties"] += t
+        if t == 0:
+            mx, rel = PT.assert_close(s, out[b, h * s.group:(h + 1) * s.group], orc.o, f"row {r}")
+            res["max_abs"] = max(res["max_abs"], mx)
+            res["rel_l2"] = max(res["rel_l2"], rel)
+    return res
+
+
+def cpu_oracle(s: W.Spec, rows, pages_limit=0, cores=None):
+    cores = cores or min(os.cpu_count() or 1, max(len(rows), 1))
+    spec_kw = dict(name=s.name, batch=s.batch, ctx_len=list(s.ctx_len), capacity=s.capacity)
+    tasks = [(spec_kw, b, h, pages_limit) for b, h in rows]
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores, initializer=_pin_threads) as pool:
+        res = pool.map(_oracle_row_task, tasks)
+    busy = sum(r[0] for r in res)
+    nbytes = sum(r[1] for r in res)
+    wall = busy / cores  # rows run `cores` at a time
+    return nbytes / wall / 1e9, cores, wall, nbytes
+
+
+def _pin_threads():
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+
+
+# ----------------------------------------------------------------- reference
+
+def run_reference(args, s: W.Spec):
+    """The fp64 oracle as the reference arm, on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    # each step: one row of the workload restricted to its first `pl` pages,
+    # sized so that warmup + steps finish within about two minutes
+    total = args.steps + args.warmup
+    budget = 120.0
+    per_step = budget / max(total, 1)
+    full_pages = -(-s.ctx_len[0] // s.page_size)
+    est_per_page = 25e-6  # seconds of oracle work per page (bound + top-k + attend share)
+    pl = int(max(s.k_pages + 8, min(full_pages, per_step / est_per_page)))
+    rows = [(i % s.batch, (i // s.batch) % s.num_kv_heads) for i in range(total)]
+    cores = 1
+    spec_kw = dict(name=s.name, batch=s.batch, ctx_len=list(s.ctx_len), capacity=s.capacity)
+    _pin_threads()
+    times, nbytes = [], []
+    for i, (b, h) in enumerate(rows):
+        dt, nb = _oracle_row_task((spec_kw, b, h, pl))
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes.append(nb)
+    t = sum(times)
+    value = sum(nbytes) / t / 1e9
+    sample = f"one (b, kv head) row per step, first {pl} of {full_pages} pages, fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * t / max(len(times), 1), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": _workload_name(s), "batch": s.batch, "ctx_len": s.ctx_len[0],
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _workload_name(s: W.Spec) -> str:
+    return (f"{s.name}: B={s.batch} Hq={s.num_q_heads} Hkv={s.num_kv_heads} D={s.head_dim} "
+            f"ctx={s.ctx_len[0]} P={s.page_size} budget={s.k_pages * s.page_size} tokens {s.dtype}")
+
+
+# ---------------------------------------------------------------------- ours
+
+def run_ours(args, s: W.Spec):
+    import torch
+    import torch.distributed as dist
+    from sparse_long_context_gb300 import _lib
+    from sparse_long_context_gb300 import harness as H
+    from sparse_long_context_gb300 import ops
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _lib.load()
+
+    host = W.generate(s, batch_offset=rank * s.batch)
+    dw = H.upload(s, host)
+    nbytes = algorithmic_bytes(s)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(2, math.ceil(4 * l2 / nbytes["total"]))
+
+    # one untimed step whose sampled rows the CPU-baseline leg checks
+    first_sel, _, first_out, _ = H.run_step(dw)
+
+    # buffer sets: distinct copies of cache + metadata
+    sets = [(dw.K, dw.V, dw.kmin, dw.kmax)]
+    for _ in range(nsets - 1):
+        sets.append(tuple(t.clone() for t in sets[0]))
+    steps_obj = [ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens) for _ in sets]
+    S = steps_obj[0].S
+    stream = torch.cuda.Stream()
+    graphs = []
+    with torch.cuda.stream(stream):
+        for st, (K, V, kmin, kmax) in zip(steps_obj, sets):
+            st(dw.q, K, V, kmin, kmax, dw.ctx)  # warm the kernels before capture
+        torch.cuda.synchronize()
+        for st, (K, V, kmin, kmax) in zip(steps_obj, sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                st(dw.q, K, V, kmin, kmax, dw.ctx)
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % nsets].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % nsets].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    clocks.window(w0, w1)
+    elapsed = e0.elapsed_time(e1) / 1e3
+    t_max, total_bytes = aggregate(elapsed, float(nbytes["total"] * args.steps), world)
+
+    # per-kernel device time: eager launches bracketed by events on the
+    # launching stream, queued behind a sleep so the host stays ahead
+    ksteps = max(50, min(args.steps, 400))
+    ev = {k: ([], []) for k in ("select", "attend", "combine")}
+    with torch.cuda.stream(stream):
+        for i in range(ksteps):
+            if i % 25 == 0:
+                torch.cuda._sleep(int(4e7))  # keeps the queue ahead of the device
+            st = steps_obj[i % nsets]
+            K, V, kmin, kmax = sets[i % nsets]
+            for name, fn in (("select", lambda: st.select(dw.q, kmin, kmax, dw.ctx)),
+                             ("attend", lambda: ops.sparse_decode_attend(st.desc, dw.q, K, V, st.page_idx,
+                                                                          dw.ctx, st.S, parts=st.parts)),
+                             ("combine", lambda: ops.combine_splits(st.desc, st.parts, None, out=st.out,
+                                                                    lse=st.lse))):
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b_.record(stream)
+                ev[name][0].append(a)
+                ev[name][1].append(b_)
+    torch.cuda.synchronize()
+    kern_us = {k: 1e3 * statistics.mean(a.elapsed_time(b_) for a, b_ in zip(*v)) for k, v in ev.items()}
+    clk = clocks.stop()
+
+    # end to end through the public API with host buffers
+    q_host = dw.q.cpu().pin_memory()
+    out_host = torch.empty(steps_obj[0].out.shape, dtype=steps_obj[0].out.dtype).pin_memory()
+    q_dev = torch.empty_like(dw.q)
+    esteps = max(10, min(args.steps, 300))
+    for i in range(3):
+        K, V, kmin, kmax = sets[i % nsets]
+        steps_obj[i % nsets](q_dev, K, V, kmin, kmax, dw.ctx)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(esteps):
+        K, V, kmin, kmax = sets[i % nsets]
+        q_dev.copy_(q_host, non_blocking=True)
+        o, _ = steps_obj[i % nsets](q_dev, K, V, kmin, kmax, dw.ctx)
+        out_host.copy_(o, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_t = time.perf_counter() - t0
+    e2e_max, e2e_bytes = aggregate(e2e_t, float(nbytes["total"] * esteps), world)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = load_peaks()
+    value = total_bytes / t_max / 1e9
+    ms_step = 1e3 * t_max / args.steps
+    # dominant kernel by algorithmic bytes: the selector's metadata stream
+    dom = "select" if nbytes["select"] >= nbytes["attend"] else "attend"
+    dom_bytes = nbytes[dom]
+    achieved = dom_bytes / (kern_us[dom] * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(1e3 * ms_step, 2), "tokens_per_s": round(s.batch * world / (ms_step / 1e3), 1),
+        "frac_of_peak": round(value / peak, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy, see workloads.py)",
+        "config": {"workload": _workload_name(s), "batch": s.batch, "ctx_len": s.ctx_len[0],
+                   "seq_len": s.ctx_len[0], "page_size": s.page_size, "budget_tokens": s.k_pages * s.page_size,
+                   "num_splits": S, "buffer_sets": nsets,
+                   "l2": f"inputs rotate over {nsets} buffer sets ({nsets * nbytes['total'] / 1e6:.0f} MB >= 4x L2 {l2 / 1e6:.0f} MB)",
+                   "parallelism": f"weak: {world} GPU(s), {s.batch} sequences each"},
+        "bytes_per_step": nbytes["total"], "bytes_select": nbytes["select"], "bytes_attend": nbytes["attend"],
+        "kernel_us": {k: round(v, 2) for k, v in kern_us.items()},
+        "roofline": {"bound": "hbm", "kernel": f"select_pages_kernel ({dom})" if dom == "select" else "attend",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": f"{peak_kind} (burst copy)"},
+        "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "e2e": {"value": round(e2e_bytes / e2e_max / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(1e6 * e2e_max / esteps, 2),
+                "h2d_bytes_per_step": int(q_host.numel() * q_host.element_size()),
+                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["parity"] = parity_check(s, host, first_sel, first_out)
+        rows = [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
+        ncore = min(os.cpu_count() or 1, 16)
+        take = rows[:max(ncore, 1) * 2]
+        gbs, cores, wall, nb = cpu_oracle(s, take, cores=ncore)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{len(take)} of {s.rows} rows of one step (full rows), "
+                                          f"{nb / 1e6:.0f} MB in {wall:.1f} s of {cores}-core time"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="qwen1p5b", choices=("qwen1p5b", "qwen7b"))
+    ap.add_argument("--ctx", type=int, default=None, help="context length (default: the workload's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    s = W.spec(args.workload, ctx_len=args.ctx) if args.ctx else W.spec(args.workload)
+    if args.impl == "reference":
+        run_reference(args, s)
+    else:
+        run_ours(args, s)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,273 @@
+/*
+ * sls.h - C ABI of the GB300 sparse decode-attention library (libsls.so).
+ *
+ * One decode step of sparse long-context attention:
+ *
+ *   select   sls_select_pages   Quest-style page bound + per-KV-head top-k
+ *            sls_select_delta   2-bit thumbnail scan + top-delta
+ *   attend   sls_sparse_decode_attend   split-K online softmax over the
+ *                                       selected pages (flash-decoding)
+ *   combine  sls_combine_splits         log-sum-exp merge of the splits,
+ *                                       with the optional sink
+ *
+ * plus the selector metadata kept next to the KV cache (page min/max keys,
+ * 2-bit thumbnails), built in bulk or updated on append.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *   stated otherwise.  The library allocates no memory; scratch comes from a
+ *   caller buffer whose size a *_workspace_size() call reports.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Calls only enqueue work: they never synchronise the device
+ *   and never read device memory from the host, so they can be captured in
+ *   a CUDA graph.
+ * - Every call returns an sls_status.  Arguments are validated on the host
+ *   before anything is launched; on error nothing is enqueued and
+ *   sls_last_error() describes the problem (thread-local string).
+ * - KV cache layout: K and V are [B, Hkv, Cap, D] row-major, element type
+ *   desc->dtype.  Row r = b*Hkv + h of the cache is the contiguous slice of
+ *   request (b, kv head h); seen as a page pool it holds Cap/P pages of P
+ *   tokens, page p covering positions [p*P, p*P+P) ("perf(core): fused
+ *   sparse-attention decode via page indirection", section "The reduction":
+ *   a dense [B, H, Cap, D] allocation viewed as a pool by a pure reshape,
+ *   with the KV-head axis folded into the request axis).
+ * - Query heads: q is [B, Hq, D]; query head hq belongs to KV head
+ *   hq / (Hq/Hkv) (grouped-query attention), and every page list is shared
+ *   by the G = Hq/Hkv query heads of its KV head.
+ * - ctx_len[b] is the number of valid positions of sequence b; positions
+ *   >= ctx_len[b] are never read by selection and never attended.  Values
+ *   outside [0, Cap] are clamped to that range on the device.
+ * - Page indices in page lists are LOGICAL page numbers within the row
+ *   (0 .. Cap/P - 1); -1 marks an empty slot that is skipped.
+ */
+#ifndef SLS_H
+#define SLS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+typedef int sls_status;
+#define SLS_OK            0
+#define SLS_EINVAL       -1  /* null pointer, bad size or out-of-range parameter */
+#define SLS_EUNSUPPORTED -2  /* valid but unsupported combination (dtype, D, G, P) */
+#define SLS_EOVERFLOW    -3  /* a size product overflows the index range */
+#define SLS_EWORKSPACE   -4  /* workspace missing or too small */
+#define SLS_ECUDA        -5  /* a CUDA launch or attribute call failed */
+
+/* ---- element types ----------------------------------------------------- */
+#define SLS_DTYPE_F32  0
+#define SLS_DTYPE_BF16 1
+
+/* ---- descriptor flags -------------------------------------------------- */
+/* Use the CUDA-core kernels even where a tensor-core kernel exists (for
+ * comparison; results agree within the same tolerances). */
+#define SLS_FLAG_CUDA_CORES 1
+
+/*
+ * Shapes and element type of one attention layer's decode step.
+ *   batch        B >= 1
+ *   num_q_heads  Hq >= 1
+ *   num_kv_heads Hkv >= 1, Hq % Hkv == 0, G = Hq/Hkv <= 8
+ *   head_dim     D in {64, 128}
+ *   page_size    P, a power of two in [1, 256]; Cap % P == 0
+ *   capacity     Cap >= 1 cache slots per (b, kv head)
+ *   dtype        SLS_DTYPE_F32 or SLS_DTYPE_BF16: K, V, q, page min/max,
+ *                thumbnail scales and the combined output use this type
+ *   flags        bitwise OR of SLS_FLAG_* (0 by default)
+ *   scale        softmax scale applied to q.k; 0 selects 1/sqrt(D)
+ *                ("Attention: Undivided & Uncompressed", Notation:
+ *                S = QK^T / sqrt(d))
+ */
+typedef struct sls_attn_desc {
+  int32_t batch;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t capacity;
+  int32_t dtype;
+  int32_t flags;
+  float scale;
+} sls_attn_desc;
+
+/* ---- metadata: Quest page min/max -------------------------------------- */
+
+/*
+ * Per-page, per-channel min and max of the keys ("Don't read the haystack",
+ * Part two: for each page keep the elementwise min and max of its keys).
+ *   k_cache  [B, Hkv, Cap, D]  dtype            (read)
+ *   ctx_len  [B] int32                          (read)
+ *   kmin     [B, Hkv, Cap/P, D] dtype           (written)
+ *   kmax     [B, Hkv, Cap/P, D] dtype           (written)
+ * Pages p < ceil(ctx_len[b]/P) are written; a partial last page summarises
+ * only its positions < ctx_len[b]; later pages are left untouched.  The
+ * stored values are exact copies of key elements.
+ */
+sls_status sls_pagemeta_build(const sls_attn_desc* desc, const void* k_cache,
+                              const int32_t* ctx_len, void* kmin, void* kmax,
+                              void* stream);
+
+/*
+ * Fold one appended key per sequence into its page's min/max ("Don't read
+ * the haystack", Part two: summaries maintained incrementally as tokens
+ * append).  The caller has already written the key at position pos[b] of
+ * every kv head of sequence b.  When pos[b] % P == 0 the page is reset to
+ * that key; otherwise min/max are taken with the stored values.  pos[b] < 0
+ * skips sequence b; pos[b] >= Cap is clamped away (skipped) on the device.
+ *   k_cache [B, Hkv, Cap, D] (read), pos [B] int32 (read),
+ *   kmin, kmax [B, Hkv, Cap/P, D] (read-modify-write)
+ */
+sls_status sls_pagemeta_update(const sls_attn_desc* desc, const void* k_cache,
+                               const int32_t* pos, void* kmin, void* kmax,
+                               void* stream);
+
+/* ---- metadata: 2-bit key thumbnails ------------------------------------ */
+
+/*
+ * 2-bit symmetric zero-free (mid-rise) thumbnails of every complete block
+ * of `block` tokens ("Faster Than Flash", Methodology 1): per block and
+ * channel s = max|k|; each key element gets a 2-bit code for the levels
+ * -0.75s, -0.25s, +0.25s, +0.75s (codes 0..3) with thresholds -s/2, 0,
+ * +s/2, a value on a threshold taking the upper level.
+ *   k_cache [B, Hkv, Cap, D] dtype (read), ctx_len [B] (read)
+ *   block   power of two in [16, 256], Cap % block == 0
+ *   codes   [B, Hkv, Cap, D/4] uint8 (written): channel c of a token is
+ *           bits 2*(c%4) of byte c/4
+ *   scales  [B, Hkv, Cap/block, D] dtype (written; exact, since max|k| is
+ *           a key magnitude)
+ * Only blocks that are complete (all positions < ctx_len[b]) are written.
+ */
+sls_status sls_thumb_build(const sls_attn_desc* desc, const void* k_cache,
+                           const int32_t* ctx_len, int32_t block,
+                           uint8_t* codes, void* scales, void* stream);
+
+/*
+ * Quantise the block that the key at position pos[b] completes, if any
+ * (pos[b] % block == block - 1).  pos[b] < 0 skips sequence b.  Same
+ * layouts as sls_thumb_build.
+ */
+sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache,
+                            const int32_t* pos, int32_t block,
+                            uint8_t* codes, void* scales, void* stream);
+
+/* ---- selection --------------------------------------------------------- */
+
+/*
+ * Quest page selection with a fixed budget ("Don't read the haystack",
+ * Part two): for every (b, kv head) row and query head g of its group,
+ * U[g,p] = sum_c max(q[g,c]*kmin[p,c], q[g,c]*kmax[p,c]); the row's page
+ * score is max_g U[g,p] (one list per KV head, shared by its query heads).
+ * Forced pages: the first n_sink_pages pages and every page holding one of
+ * the last n_local_tokens positions.  The list holds the forced pages plus
+ * the top (k - #forced) other pages by score, ties to the lower page
+ * index, sorted ascending.  When the row has <= k pages all of them are
+ * listed and the rest of the list is -1.
+ *   q        [B, Hq, D] dtype (read)
+ *   kmin     [B, Hkv, Cap/P, D] dtype (read); kmax likewise.  With P == 1
+ *            a page is one token, its min and max are the key itself:
+ *            pass the K cache as kmin and kmax == kmin (read once).
+ *   ctx_len  [B] int32 (read)
+ *   k        budget in pages, 1 <= k <= Cap/P, and k must cover the forced
+ *            pages: k >= n_sink_pages + ceil(n_local_tokens/P) + 1
+ *   page_idx [B*Hkv, k] int32 (written)
+ * The score is computed in fp32; two pages whose scores differ by less
+ * than the fp32 rounding of the sum may rank either way.
+ */
+sls_status sls_select_pages(const sls_attn_desc* desc, const void* q,
+                            const void* kmin, const void* kmax,
+                            const int32_t* ctx_len, int32_t k,
+                            int32_t n_sink_pages, int32_t n_local_tokens,
+                            int32_t* page_idx, void* stream);
+
+/* Bytes of workspace sls_select_delta needs for this descriptor/block. */
+size_t sls_select_delta_workspace_size(const sls_attn_desc* desc, int32_t block);
+
+/*
+ * Top-delta block selection over 2-bit thumbnails ("Faster Than Flash",
+ * Methodology 2, eqs. 1-3, with eq. 4's 1/sqrt(d) scaling):
+ *   m~[g]  = max over the tokens of block 0 and of the newest block
+ *            (partial or not) of the exact score scale * q[g] . k
+ *   a complete block b other than those two is kept when
+ *            max_g max_{t in b} (scale * q[g] . k^[t] - m~[g]) >= -delta
+ *            with k^ the thumbnail levels;
+ *   block 0 and the newest block are always kept.
+ * Output: count[r] kept blocks, block_idx[r, 0..count[r]) the kept block
+ * numbers ascending (entries past count[r] are unspecified).
+ *   q [B, Hq, D], k_cache [B, Hkv, Cap, D], codes/scales as written by
+ *   sls_thumb_build with the same block; ctx_len [B]
+ *   idx_stride >= Cap/block
+ *   workspace  >= sls_select_delta_workspace_size() bytes
+ * Scores are computed in fp32.
+ */
+sls_status sls_select_delta(const sls_attn_desc* desc, const void* q,
+                            const void* k_cache, const uint8_t* codes,
+                            const void* scales, const int32_t* ctx_len,
+                            int32_t block, float delta, int32_t* count,
+                            int32_t* block_idx, int32_t idx_stride,
+                            void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* ---- attention --------------------------------------------------------- */
+
+/*
+ * Split-K sparse decode attention, stage one of two-stage flash-decoding
+ * ("Don't read the haystack", Part one; the sparse twin of Part two walks
+ * a page list instead of a range).  For every row r = (b, h), the page list
+ * page_idx[r*idx_stride + i], i < n_r (n_r = count[r] if count != NULL,
+ * else k_fixed) is cut into num_splits contiguous slices; slice s of every
+ * query head g of the group produces
+ *   m = max x, l = sum exp(x - m), acc = sum exp(x - m) v
+ * over the valid tokens of its pages (position < ctx_len[b]), with
+ * x = scale * q.k.  The sink is NOT applied here (see combine).
+ * page_idx == NULL attends every page 0..ceil(ctx_len/P)-1 (dense decode).
+ *   q [B, Hq, D], k_cache/v_cache [B, Hkv, Cap, D] dtype (read)
+ *   o_part [B, Hq, num_splits, D] f32, m_part/l_part [B, Hq, num_splits]
+ *   f32 (written; m in natural-log units; an empty slice gives m = -inf,
+ *   l = 0, acc = 0)
+ *   1 <= num_splits <= 1024
+ */
+sls_status sls_sparse_decode_attend(const sls_attn_desc* desc, const void* q,
+                                    const void* k_cache, const void* v_cache,
+                                    const int32_t* page_idx, int32_t idx_stride,
+                                    const int32_t* count, int32_t k_fixed,
+                                    const int32_t* ctx_len, int32_t num_splits,
+                                    float* o_part, float* m_part, float* l_part,
+                                    void* stream);
+
+/*
+ * Stage two: merge the splits with the log-sum-exp rescale ("Don't read the
+ * haystack", Part one) and fold in the optional per-query-head sink as a
+ * virtual key with value 0 ("Training-free sparse attention for
+ * long-context LLM decode", section 1): with M = max(max_s m_s, sink_h),
+ *   L = sum_s l_s e^(m_s - M) + e^(sink_h - M),
+ *   out = sum_s acc_s e^(m_s - M) / L,   lse = M + log L.
+ * The sink is a raw logit (not scaled).  Rows with no token and no sink
+ * give out = 0, lse = -inf.
+ *   o_part/m_part/l_part as written by sls_sparse_decode_attend
+ *   sink [Hq] f32 or NULL
+ *   out [B, Hq, D] dtype (written); lse [B, Hq] f32 or NULL (written)
+ */
+sls_status sls_combine_splits(const sls_attn_desc* desc, const float* o_part,
+                              const float* m_part, const float* l_part,
+                              int32_t num_splits, const float* sink, void* out,
+                              float* lse, void* stream);
+
+/* ---- diagnostics ------------------------------------------------------- */
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* sls_last_error(void);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int32_t sls_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLS_H */

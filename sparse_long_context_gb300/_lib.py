@@ -1,0 +1,82 @@
+"""ctypes binding of libsls.so (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+SLS_OK, SLS_EINVAL, SLS_EUNSUPPORTED, SLS_EOVERFLOW, SLS_EWORKSPACE, SLS_ECUDA = 0, -1, -2, -3, -4, -5
+SLS_DTYPE_F32, SLS_DTYPE_BF16 = 0, 1
+SLS_FLAG_CUDA_CORES = 1
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("capacity", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("scale", ctypes.c_float)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_D = ctypes.POINTER(AttnDesc)
+SIGNATURES = {
+    "sls_pagemeta_build": (_I, [_D, _P, _P, _P, _P, _P]),
+    "sls_pagemeta_update": (_I, [_D, _P, _P, _P, _P, _P]),
+    "sls_thumb_build": (_I, [_D, _P, _P, _I, _P, _P, _P]),
+    "sls_thumb_update": (_I, [_D, _P, _P, _I, _P, _P, _P]),
+    "sls_select_pages": (_I, [_D, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "sls_select_delta_workspace_size": (ctypes.c_size_t, [_D, _I]),
+    "sls_select_delta": (_I, [_D, _P, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _I, _P,
+                              ctypes.c_size_t, _P]),
+    "sls_sparse_decode_attend": (_I, [_D, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P]),
+    "sls_combine_splits": (_I, [_D, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "sls_last_error": (ctypes.c_char_p, []),
+    "sls_version": (_I, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SlsError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} failed with status {code}: {msg}")
+        self.code = code
+
+
+def load(build_if_missing: bool = False):
+    """Load libsls.so.  Raises if it is missing (unless asked to build it)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -m sparse_long_context_gb300.build)")
+            _build.build()
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def check(fn_name: str, status: int) -> None:
+    if status != SLS_OK:
+        msg = _lib.sls_last_error().decode() if _lib is not None else ""
+        raise SlsError(fn_name, status, msg)
+
+
+def call(name: str, *args) -> None:
+    lib = load()
+    check(name, getattr(lib, name)(*args))

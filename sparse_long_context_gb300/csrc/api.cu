@@ -1,0 +1,237 @@
+// C ABI of libsls: host-side validation, then launch.  Nothing here touches
+// device memory or synchronises; a failed check returns before any launch.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "launch.h"
+#include "sls.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+sls_status fail(sls_status code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+sls_status ok() {
+  g_err[0] = '\0';
+  return SLS_OK;
+}
+
+sls_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(SLS_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// a*b*... with overflow detection against int64 and against the int32
+// indexing the kernels use for per-row positions.
+bool checked_mul(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+sls_status check_desc(const sls_attn_desc* d, sls::Shape* s) {
+  if (!d) return fail(SLS_EINVAL, "desc is NULL");
+  if (d->batch < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1)
+    return fail(SLS_EINVAL, "batch/heads must be >= 1 (B=%d Hq=%d Hkv=%d)", d->batch,
+                d->num_q_heads, d->num_kv_heads);
+  if (d->num_q_heads % d->num_kv_heads)
+    return fail(SLS_EINVAL, "num_q_heads %d not a multiple of num_kv_heads %d", d->num_q_heads,
+                d->num_kv_heads);
+  const int G = d->num_q_heads / d->num_kv_heads;
+  if (G > 8) return fail(SLS_EUNSUPPORTED, "query heads per kv head G=%d > 8", G);
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return fail(SLS_EUNSUPPORTED, "head_dim %d not in {64, 128}", d->head_dim);
+  if (d->dtype != SLS_DTYPE_F32 && d->dtype != SLS_DTYPE_BF16)
+    return fail(SLS_EUNSUPPORTED, "dtype %d", d->dtype);
+  if (!pow2(d->page_size) || d->page_size > 256)
+    return fail(SLS_EINVAL, "page_size %d must be a power of two in [1, 256]", d->page_size);
+  if (d->capacity < 1 || d->capacity % d->page_size)
+    return fail(SLS_EINVAL, "capacity %d must be >= 1 and a multiple of page_size %d", d->capacity,
+                d->page_size);
+  if (!(d->scale >= 0.f) || std::isinf(d->scale)) return fail(SLS_EINVAL, "scale must be finite and >= 0");
+  if (d->flags & ~SLS_FLAG_CUDA_CORES) return fail(SLS_EINVAL, "unknown flags 0x%x", d->flags);
+  // element counts of the caches and of the per-row index space
+  int64_t rows, elems;
+  if (!checked_mul(d->batch, d->num_kv_heads, &rows) || !checked_mul(rows, d->capacity, &elems) ||
+      !checked_mul(elems, d->head_dim, &elems) || rows > INT32_MAX || elems > (int64_t(1) << 48) ||
+      (int64_t)d->batch * d->num_q_heads > INT32_MAX)
+    return fail(SLS_EOVERFLOW, "cache size overflows");
+  s->B = d->batch;
+  s->Hq = d->num_q_heads;
+  s->Hkv = d->num_kv_heads;
+  s->G = G;
+  s->D = d->head_dim;
+  s->P = d->page_size;
+  s->pshift = __builtin_ctz((unsigned)d->page_size);
+  s->Cap = d->capacity;
+  s->dtype = d->dtype;
+  s->flags = d->flags;
+  s->scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt((float)d->head_dim);
+  return SLS_OK;
+}
+
+#define REQUIRE(ptr) \
+  if (!(ptr)) return fail(SLS_EINVAL, "%s is NULL", #ptr)
+
+}  // namespace
+
+extern "C" {
+
+const char* sls_last_error(void) { return g_err; }
+
+int32_t sls_version(void) { return 10000; }
+
+sls_status sls_pagemeta_build(const sls_attn_desc* desc, const void* k_cache, const int32_t* ctx_len,
+                              void* kmin, void* kmax, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(kmin); REQUIRE(kmax);
+  return cuda_status(sls::launch_pagemeta_build(s, k_cache, ctx_len, kmin, kmax, (cudaStream_t)stream),
+                     "sls_pagemeta_build");
+}
+
+sls_status sls_pagemeta_update(const sls_attn_desc* desc, const void* k_cache, const int32_t* pos,
+                               void* kmin, void* kmax, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(k_cache); REQUIRE(pos); REQUIRE(kmin); REQUIRE(kmax);
+  return cuda_status(sls::launch_pagemeta_update(s, k_cache, pos, kmin, kmax, (cudaStream_t)stream),
+                     "sls_pagemeta_update");
+}
+
+static sls_status check_block(const sls::Shape& s, int32_t block) {
+  if (!pow2(block) || block < 16 || block > 256)
+    return fail(SLS_EINVAL, "block %d must be a power of two in [16, 256]", block);
+  if (s.Cap % block) return fail(SLS_EINVAL, "capacity %d not a multiple of block %d", s.Cap, block);
+  return SLS_OK;
+}
+
+sls_status sls_thumb_build(const sls_attn_desc* desc, const void* k_cache, const int32_t* ctx_len,
+                           int32_t block, uint8_t* codes, void* scales, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  if ((r = check_block(s, block))) return r;
+  REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(codes); REQUIRE(scales);
+  return cuda_status(sls::launch_thumb_build(s, k_cache, ctx_len, block, codes, scales, (cudaStream_t)stream),
+                     "sls_thumb_build");
+}
+
+sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache, const int32_t* pos,
+                            int32_t block, uint8_t* codes, void* scales, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  if ((r = check_block(s, block))) return r;
+  REQUIRE(k_cache); REQUIRE(pos); REQUIRE(codes); REQUIRE(scales);
+  return cuda_status(sls::launch_thumb_update(s, k_cache, pos, block, codes, scales, (cudaStream_t)stream),
+                     "sls_thumb_update");
+}
+
+sls_status sls_select_pages(const sls_attn_desc* desc, const void* q, const void* kmin,
+                            const void* kmax, const int32_t* ctx_len, int32_t k,
+                            int32_t n_sink_pages, int32_t n_local_tokens, int32_t* page_idx,
+                            void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(q); REQUIRE(kmin); REQUIRE(kmax); REQUIRE(ctx_len); REQUIRE(page_idx);
+  const int npcap = s.Cap >> s.pshift;
+  if (k < 1 || k > npcap) return fail(SLS_EINVAL, "k=%d must be in [1, Cap/P=%d]", k, npcap);
+  if (n_sink_pages < 0 || n_local_tokens < 0)
+    return fail(SLS_EINVAL, "n_sink_pages and n_local_tokens must be >= 0");
+  const int64_t forced_max =
+      (int64_t)n_sink_pages + (n_local_tokens > 0 ? ((int64_t)n_local_tokens + s.P - 1) / s.P + 1 : 0);
+  if (forced_max > k)
+    return fail(SLS_EINVAL, "budget k=%d cannot hold the forced pages (up to %lld)", k,
+                (long long)forced_max);
+  if (s.P == 1 && kmin != kmax)
+    return fail(SLS_EINVAL, "page_size 1: pass the key cache as both kmin and kmax");
+  const size_t chunk = (size_t)(npcap + sls::select_pages_cluster() - 1) / sls::select_pages_cluster();
+  if (chunk * 4 > sls::select_pages_smem_limit())
+    return fail(SLS_EUNSUPPORTED, "Cap/P=%d pages per row exceeds the supported %zu", npcap,
+                sls::select_pages_smem_limit() / 4 * sls::select_pages_cluster());
+  return cuda_status(sls::launch_select_pages(s, q, kmin, kmax, ctx_len, k, n_sink_pages, n_local_tokens,
+                                              page_idx, (cudaStream_t)stream),
+                     "sls_select_pages");
+}
+
+size_t sls_select_delta_workspace_size(const sls_attn_desc* desc, int32_t block) {
+  sls::Shape s;
+  if (check_desc(desc, &s) || check_block(s, block)) return 0;
+  return sls::select_delta_workspace(s, block);
+}
+
+sls_status sls_select_delta(const sls_attn_desc* desc, const void* q, const void* k_cache,
+                            const uint8_t* codes, const void* scales, const int32_t* ctx_len,
+                            int32_t block, float delta, int32_t* count, int32_t* block_idx,
+                            int32_t idx_stride, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  if ((r = check_block(s, block))) return r;
+  REQUIRE(q); REQUIRE(k_cache); REQUIRE(codes); REQUIRE(scales); REQUIRE(ctx_len);
+  REQUIRE(count); REQUIRE(block_idx);
+  if (!(delta >= 0.f) || std::isinf(delta)) return fail(SLS_EINVAL, "delta must be finite and >= 0");
+  if (idx_stride < s.Cap / block)
+    return fail(SLS_EINVAL, "idx_stride %d < Cap/block %d", idx_stride, s.Cap / block);
+  const size_t need = sls::select_delta_workspace(s, block);
+  if (!workspace || workspace_bytes < need)
+    return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  return cuda_status(sls::launch_select_delta(s, q, k_cache, codes, scales, ctx_len, block, delta, count,
+                                              block_idx, idx_stride, workspace, (cudaStream_t)stream),
+                     "sls_select_delta");
+}
+
+sls_status sls_sparse_decode_attend(const sls_attn_desc* desc, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* page_idx, int32_t idx_stride,
+                                    const int32_t* count, int32_t k_fixed, const int32_t* ctx_len,
+                                    int32_t num_splits, float* o_part, float* m_part, float* l_part,
+                                    void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(ctx_len);
+  REQUIRE(o_part); REQUIRE(m_part); REQUIRE(l_part);
+  if (num_splits < 1 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [1, 1024]", num_splits);
+  if (page_idx) {
+    if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
+    if (!count && (k_fixed < 0 || k_fixed > idx_stride))
+      return fail(SLS_EINVAL, "k_fixed %d not in [0, idx_stride=%d]", k_fixed, idx_stride);
+  }
+  int64_t ctas;
+  if (!checked_mul((int64_t)s.B * s.Hkv, num_splits, &ctas) || ctas > INT32_MAX)
+    return fail(SLS_EOVERFLOW, "grid too large");
+  return cuda_status(sls::launch_attend(s, q, k_cache, v_cache, page_idx, idx_stride, count, k_fixed, ctx_len,
+                                        num_splits, o_part, m_part, l_part, (cudaStream_t)stream),
+                     "sls_sparse_decode_attend");
+}
+
+sls_status sls_combine_splits(const sls_attn_desc* desc, const float* o_part, const float* m_part,
+                              const float* l_part, int32_t num_splits, const float* sink, void* out,
+                              float* lse, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(o_part); REQUIRE(m_part); REQUIRE(l_part); REQUIRE(out);
+  if (num_splits < 1 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [1, 1024]", num_splits);
+  return cuda_status(sls::launch_combine(s, o_part, m_part, l_part, num_splits, sink, out, lse, (cudaStream_t)stream),
+                     "sls_combine_splits");
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Internal (C++) launch interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Arguments have been validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sls {
+
+struct Shape {
+  int B, Hq, Hkv, G, D, P, pshift, Cap, dtype, flags;
+  float scale;
+};
+
+cudaError_t launch_pagemeta_build(const Shape& s, const void* k, const int32_t* ctx_len,
+                                  void* kmin, void* kmax, cudaStream_t st);
+cudaError_t launch_pagemeta_update(const Shape& s, const void* k, const int32_t* pos,
+                                   void* kmin, void* kmax, cudaStream_t st);
+cudaError_t launch_thumb_build(const Shape& s, const void* k, const int32_t* ctx_len,
+                               int block, uint8_t* codes, void* scales, cudaStream_t st);
+cudaError_t launch_thumb_update(const Shape& s, const void* k, const int32_t* pos,
+                                int block, uint8_t* codes, void* scales, cudaStream_t st);
+
+cudaError_t launch_select_pages(const Shape& s, const void* q, const void* kmin,
+                                const void* kmax, const int32_t* ctx_len, int k,
+                                int n_sink_pages, int n_local_tokens, int32_t* page_idx,
+                                cudaStream_t st);
+
+size_t select_delta_workspace(const Shape& s, int block);
+cudaError_t launch_select_delta(const Shape& s, const void* q, const void* k,
+                                const uint8_t* codes, const void* scales,
+                                const int32_t* ctx_len, int block, float delta,
+                                int32_t* count, int32_t* block_idx, int idx_stride,
+                                void* ws, cudaStream_t st);
+
+cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const void* v,
+                          const int32_t* page_idx, int idx_stride, const int32_t* count,
+                          int k_fixed, const int32_t* ctx_len, int num_splits,
+                          float* o_part, float* m_part, float* l_part, cudaStream_t st);
+
+cudaError_t launch_combine(const Shape& s, const float* o_part, const float* m_part,
+                           const float* l_part, int num_splits, const float* sink,
+                           void* out, float* lse, cudaStream_t st);
+
+// Largest dynamic shared memory one select_pages CTA may use.
+size_t select_pages_smem_limit();
+int select_pages_cluster();
+
+}  // namespace sls

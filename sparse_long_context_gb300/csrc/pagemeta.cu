@@ -1,0 +1,212 @@
+// Selector metadata kept beside the KV cache:
+//  * per-page, per-channel min/max keys ("Don't read the haystack", Part
+//    two), built for a whole prefix or folded in one appended key at a time;
+//  * 2-bit symmetric mid-rise thumbnails of complete 64-token blocks
+//    ("Faster Than Flash", Methodology 1; the append path mirrors its
+//    graph-friendly, tensor-indexed cache writes of Methodology 3).
+#include "common.cuh"
+#include "launch.h"
+
+namespace sls {
+
+// ---------------------------------------------------------------- min / max
+
+// One thread per (page, 16-byte channel vector).
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+pagemeta_build_kernel(const T* __restrict__ k, const int32_t* __restrict__ ctx_len, T* kmin,
+                      T* kmax, int Hkv, int Cap, int P, int pshift, int pages_per_cta) {
+  constexpr int EPL = Vec16<T>::N;
+  constexpr int L = D / EPL;
+  const int row = blockIdx.y;
+  const int b = row / Hkv;
+  const int N = clamp_len(ctx_len[b], Cap);
+  const int NP = (N + P - 1) >> pshift;
+  const int p = blockIdx.x * pages_per_cta + threadIdx.x / L;
+  const int sub = threadIdx.x % L;
+  if (threadIdx.x / L >= pages_per_cta || p >= NP) return;
+  const T* src = k + ((size_t)row * Cap + ((size_t)p << pshift)) * D + sub * EPL;
+  const int t1 = min(P, N - (p << pshift));
+  float lo[EPL], hi[EPL];
+  load_vec(src, lo);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) hi[e] = lo[e];
+  for (int t = 1; t < t1; ++t) {
+    float x[EPL];
+    load_vec(src + (size_t)t * D, x);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      lo[e] = fminf(lo[e], x[e]);
+      hi[e] = fmaxf(hi[e], x[e]);
+    }
+  }
+  const size_t o = ((size_t)row * (Cap >> pshift) + p) * D + sub * EPL;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    kmin[o + e] = from_f32<T>(lo[e]);  // exact: the value is one of the keys
+    kmax[o + e] = from_f32<T>(hi[e]);
+  }
+}
+
+// One warp per (b, kv head) row.
+template <typename T, int D>
+__global__ void __launch_bounds__(128)
+pagemeta_update_kernel(const T* __restrict__ k, const int32_t* __restrict__ pos, T* kmin,
+                       T* kmax, int rows, int Hkv, int Cap, int P, int pshift) {
+  constexpr int EPL = Vec16<T>::N;
+  constexpr int L = D / EPL;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows || lane >= L) return;
+  const int t = pos[row / Hkv];
+  if (t < 0 || t >= Cap) return;
+  const int p = t >> pshift;
+  float x[EPL];
+  load_vec(k + ((size_t)row * Cap + t) * D + lane * EPL, x);
+  const size_t o = ((size_t)row * (Cap >> pshift) + p) * D + lane * EPL;
+  if ((t & (P - 1)) == 0) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      kmin[o + e] = from_f32<T>(x[e]);
+      kmax[o + e] = from_f32<T>(x[e]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      kmin[o + e] = from_f32<T>(fminf(to_f32<T>(kmin[o + e]), x[e]));
+      kmax[o + e] = from_f32<T>(fmaxf(to_f32<T>(kmax[o + e]), x[e]));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- thumbnails
+
+// Code of one element: 3 if k >= s/2, 2 if 0 <= k < s/2, 1 if -s/2 <= k < 0,
+// 0 below; s/2 of a bf16 or fp32 magnitude is exact, so the comparisons are.
+__device__ __forceinline__ uint32_t thumb_code(float x, float half) {
+  return x >= half ? 3u : (x >= 0.f ? 2u : (x >= -half ? 1u : 0u));
+}
+
+// Quantise block j of `row` (block tokens, all valid).  blockDim.x == D.
+template <typename T, int D>
+__device__ __forceinline__ void quantise_block(const T* __restrict__ k, uint8_t* codes, T* scales,
+                                               int row, int j, int Cap, int block, int nblk_cap) {
+  __shared__ float s_half[D];
+  const int c = threadIdx.x;
+  const T* src = k + ((size_t)row * Cap + (size_t)j * block) * D;
+  float s = 0.f;
+  for (int t = 0; t < block; ++t) s = fmaxf(s, fabsf(to_f32<T>(src[(size_t)t * D + c])));
+  scales[((size_t)row * nblk_cap + j) * D + c] = from_f32<T>(s);
+  s_half[c] = 0.5f * s;
+  __syncthreads();
+  constexpr int BPT = D / 4;  // code bytes per token
+  uint8_t* dst = codes + ((size_t)row * Cap + (size_t)j * block) * BPT;
+  for (int i = threadIdx.x; i < block * BPT; i += D) {
+    const int t = i / BPT, by = i % BPT;
+    const T* x = src + (size_t)t * D + by * 4;
+    uint32_t v = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v |= thumb_code(to_f32<T>(x[u]), s_half[by * 4 + u]) << (2 * u);
+    dst[i] = (uint8_t)v;
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(D)
+thumb_build_kernel(const T* __restrict__ k, const int32_t* __restrict__ ctx_len, uint8_t* codes,
+                   T* scales, int Hkv, int Cap, int block, int nblk_cap) {
+  const int row = blockIdx.y, j = blockIdx.x;
+  const int N = clamp_len(ctx_len[row / Hkv], Cap);
+  if ((j + 1) * block > N) return;
+  quantise_block<T, D>(k, codes, scales, row, j, Cap, block, nblk_cap);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(D)
+thumb_update_kernel(const T* __restrict__ k, const int32_t* __restrict__ pos, uint8_t* codes,
+                    T* scales, int Hkv, int Cap, int block, int nblk_cap) {
+  const int row = blockIdx.x;
+  const int t = pos[row / Hkv];
+  if (t < 0 || t >= Cap || (t + 1) % block != 0) return;
+  quantise_block<T, D>(k, codes, scales, row, t / block, Cap, block, nblk_cap);
+}
+
+// ---------------------------------------------------------------- launches
+
+template <typename T, int D>
+static cudaError_t pm_build(const Shape& s, const void* k, const int32_t* ctx, void* kmin,
+                            void* kmax, cudaStream_t st) {
+  constexpr int L = D / Vec16<T>::N;
+  const int ppc = 256 / L;
+  dim3 grid(((s.Cap >> s.pshift) + ppc - 1) / ppc, s.B * s.Hkv);
+  pagemeta_build_kernel<T, D><<<grid, 256, 0, st>>>(static_cast<const T*>(k), ctx, static_cast<T*>(kmin),
+                                                    static_cast<T*>(kmax), s.Hkv, s.Cap, s.P, s.pshift, ppc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pagemeta_build(const Shape& s, const void* k, const int32_t* ctx_len,
+                                  void* kmin, void* kmax, cudaStream_t st) {
+  if (s.dtype == 0)
+    return s.D == 64 ? pm_build<float, 64>(s, k, ctx_len, kmin, kmax, st)
+                     : pm_build<float, 128>(s, k, ctx_len, kmin, kmax, st);
+  return s.D == 64 ? pm_build<bf16, 64>(s, k, ctx_len, kmin, kmax, st)
+                   : pm_build<bf16, 128>(s, k, ctx_len, kmin, kmax, st);
+}
+
+template <typename T, int D>
+static cudaError_t pm_update(const Shape& s, const void* k, const int32_t* pos, void* kmin,
+                             void* kmax, cudaStream_t st) {
+  const int rows = s.B * s.Hkv;
+  pagemeta_update_kernel<T, D><<<(rows + 3) / 4, 128, 0, st>>>(
+      static_cast<const T*>(k), pos, static_cast<T*>(kmin), static_cast<T*>(kmax), rows, s.Hkv, s.Cap,
+      s.P, s.pshift);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pagemeta_update(const Shape& s, const void* k, const int32_t* pos, void* kmin,
+                                   void* kmax, cudaStream_t st) {
+  if (s.dtype == 0)
+    return s.D == 64 ? pm_update<float, 64>(s, k, pos, kmin, kmax, st)
+                     : pm_update<float, 128>(s, k, pos, kmin, kmax, st);
+  return s.D == 64 ? pm_update<bf16, 64>(s, k, pos, kmin, kmax, st)
+                   : pm_update<bf16, 128>(s, k, pos, kmin, kmax, st);
+}
+
+template <typename T, int D>
+static cudaError_t th_build(const Shape& s, const void* k, const int32_t* ctx, int block,
+                            uint8_t* codes, void* scales, cudaStream_t st) {
+  const int nblk = s.Cap / block;
+  dim3 grid(nblk, s.B * s.Hkv);
+  thumb_build_kernel<T, D><<<grid, D, 0, st>>>(static_cast<const T*>(k), ctx, codes, static_cast<T*>(scales),
+                                               s.Hkv, s.Cap, block, nblk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_thumb_build(const Shape& s, const void* k, const int32_t* ctx_len, int block,
+                               uint8_t* codes, void* scales, cudaStream_t st) {
+  if (s.dtype == 0)
+    return s.D == 64 ? th_build<float, 64>(s, k, ctx_len, block, codes, scales, st)
+                     : th_build<float, 128>(s, k, ctx_len, block, codes, scales, st);
+  return s.D == 64 ? th_build<bf16, 64>(s, k, ctx_len, block, codes, scales, st)
+                   : th_build<bf16, 128>(s, k, ctx_len, block, codes, scales, st);
+}
+
+template <typename T, int D>
+static cudaError_t th_update(const Shape& s, const void* k, const int32_t* pos, int block,
+                             uint8_t* codes, void* scales, cudaStream_t st) {
+  thumb_update_kernel<T, D><<<s.B * s.Hkv, D, 0, st>>>(static_cast<const T*>(k), pos, codes,
+                                                        static_cast<T*>(scales), s.Hkv, s.Cap, block,
+                                                        s.Cap / block);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_thumb_update(const Shape& s, const void* k, const int32_t* pos, int block,
+                                uint8_t* codes, void* scales, cudaStream_t st) {
+  if (s.dtype == 0)
+    return s.D == 64 ? th_update<float, 64>(s, k, pos, block, codes, scales, st)
+                     : th_update<float, 128>(s, k, pos, block, codes, scales, st);
+  return s.D == 64 ? th_update<bf16, 64>(s, k, pos, block, codes, scales, st)
+                   : th_update<bf16, 128>(s, k, pos, block, codes, scales, st);
+}
+
+}  // namespace sls

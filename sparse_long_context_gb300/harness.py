@@ -1,0 +1,77 @@
+"""Moves a generated workload onto the GPU and builds the selector metadata
+with the library's own kernels (used by the benchmark, the smoke check and
+the tests)."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+from . import ops
+from . import workloads as W
+
+
+def to_device(arr: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    """Host array (bf16 bit patterns as uint16, or fp32) -> CUDA tensor."""
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
+
+
+@dataclasses.dataclass
+class DeviceWorkload:
+    spec: W.Spec
+    host: W.Tensors
+    K: torch.Tensor
+    V: torch.Tensor
+    q: torch.Tensor
+    ctx: torch.Tensor
+    sink: object
+    desc: object
+    kmin: object = None
+    kmax: object = None
+    codes: object = None
+    scales: object = None
+
+
+def upload(spec: W.Spec, host: W.Tensors, cuda_cores: bool = False, device="cuda") -> DeviceWorkload:
+    K = to_device(host.K, spec.dtype, device)
+    V = to_device(host.V, spec.dtype, device)
+    q = to_device(host.q, spec.dtype, device)
+    ctx = torch.from_numpy(host.ctx_len).to(device)
+    sink = torch.from_numpy(host.sink).to(device) if host.sink is not None else None
+    desc = ops.make_desc(spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                         spec.page_size, spec.capacity, K.dtype, cuda_cores=cuda_cores)
+    dw = DeviceWorkload(spec, host, K, V, q, ctx, sink, desc)
+    if spec.selector == "quest":
+        if spec.page_size == 1:
+            dw.kmin = dw.kmax = K
+        else:
+            dw.kmin, dw.kmax = ops.pagemeta_build(desc, K, ctx)
+    else:
+        dw.codes, dw.scales = ops.thumb_build(desc, K, ctx, spec.block)
+    return dw
+
+
+def make_step(dw: DeviceWorkload, num_splits=None):
+    s = dw.spec
+    if s.selector == "quest":
+        return ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, num_splits)
+    return ops.DeltaDecode(dw.desc, s.block, s.delta, num_splits)
+
+
+def run_step(dw: DeviceWorkload, num_splits=None):
+    """Select + attend + combine on the device.  Returns host arrays:
+    (selection rows, counts or None, out [B,Hq,D] float64, lse [B,Hq])."""
+    s = dw.spec
+    step = make_step(dw, num_splits)
+    if s.selector == "quest":
+        out, lse = step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx, dw.sink)
+        sel, cnt = step.page_idx, None
+    else:
+        out, lse = step(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink)
+        sel, cnt = step.block_idx, step.count
+    torch.cuda.synchronize()
+    return (sel.cpu().numpy(), None if cnt is None else cnt.cpu().numpy(),
+            out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))

@@ -1,0 +1,238 @@
+"""Python binding over the C ABI: turns torch CUDA tensors into the raw
+pointers, sizes and stream the C calls take.  Every step of the path runs in
+libsls.so kernels; this module only marshals arguments and, where asked,
+allocates output tensors with torch (the C library itself allocates
+nothing).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+
+_DTYPES = {torch.float32: L.SLS_DTYPE_F32, torch.bfloat16: L.SLS_DTYPE_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def make_desc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, dtype,
+              scale: float = 0.0, cuda_cores: bool = False) -> L.AttnDesc:
+    code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return L.AttnDesc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, code,
+                      L.SLS_FLAG_CUDA_CORES if cuda_cores else 0, float(scale))
+
+
+def desc_for(k_cache: torch.Tensor, num_q_heads: int, page_size: int, scale: float = 0.0,
+             cuda_cores: bool = False) -> L.AttnDesc:
+    B, Hkv, Cap, D = k_cache.shape
+    return make_desc(B, num_q_heads, Hkv, D, page_size, Cap, k_cache.dtype, scale, cuda_cores)
+
+
+def default_splits(rows: int, max_entries: int, page_size: int, device=None) -> int:
+    """Splits per row: enough CTAs to cover the SMs about four times, each
+    slice holding at least 64 tokens."""
+    sms = torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count
+    want = max(1, math.ceil(4 * sms / max(rows, 1)))
+    cap = max(1, (max_entries * page_size) // 64)
+    return int(max(1, min(want, cap, 1024)))
+
+
+# ----------------------------------------------------------------- metadata
+
+def pagemeta_build(desc: L.AttnDesc, k_cache, ctx_len, kmin=None, kmax=None):
+    _need(k_cache, "k_cache")
+    _need(ctx_len, "ctx_len", torch.int32)
+    B, Hkv, Cap, D = k_cache.shape
+    shape = (B, Hkv, Cap // desc.page_size, D)
+    kmin = torch.empty(shape, dtype=k_cache.dtype, device=k_cache.device) if kmin is None else kmin
+    kmax = torch.empty(shape, dtype=k_cache.dtype, device=k_cache.device) if kmax is None else kmax
+    _need(kmin, "kmin", k_cache.dtype, shape)
+    _need(kmax, "kmax", k_cache.dtype, shape)
+    L.call("sls_pagemeta_build", ctypes.byref(desc), _ptr(k_cache), _ptr(ctx_len), _ptr(kmin),
+           _ptr(kmax), _stream())
+    return kmin, kmax
+
+
+def pagemeta_update(desc: L.AttnDesc, k_cache, pos, kmin, kmax):
+    _need(pos, "pos", torch.int32)
+    L.call("sls_pagemeta_update", ctypes.byref(desc), _ptr(k_cache), _ptr(pos), _ptr(kmin),
+           _ptr(kmax), _stream())
+
+
+def thumb_build(desc: L.AttnDesc, k_cache, ctx_len, block: int, codes=None, scales=None):
+    _need(k_cache, "k_cache")
+    _need(ctx_len, "ctx_len", torch.int32)
+    B, Hkv, Cap, D = k_cache.shape
+    if codes is None:
+        codes = torch.zeros((B, Hkv, Cap, D // 4), dtype=torch.uint8, device=k_cache.device)
+    if scales is None:
+        scales = torch.zeros((B, Hkv, Cap // block, D), dtype=k_cache.dtype, device=k_cache.device)
+    _need(codes, "codes", torch.uint8, (B, Hkv, Cap, D // 4))
+    _need(scales, "scales", k_cache.dtype, (B, Hkv, Cap // block, D))
+    L.call("sls_thumb_build", ctypes.byref(desc), _ptr(k_cache), _ptr(ctx_len), int(block),
+           _ptr(codes), _ptr(scales), _stream())
+    return codes, scales
+
+
+def thumb_update(desc: L.AttnDesc, k_cache, pos, block: int, codes, scales):
+    _need(pos, "pos", torch.int32)
+    L.call("sls_thumb_update", ctypes.byref(desc), _ptr(k_cache), _ptr(pos), int(block),
+           _ptr(codes), _ptr(scales), _stream())
+
+
+# ---------------------------------------------------------------- selection
+
+def select_pages(desc: L.AttnDesc, q, kmin, kmax, ctx_len, k: int, n_sink_pages: int = 0,
+                 n_local_tokens: int = 0, out=None):
+    _need(q, "q")
+    rows = desc.batch * desc.num_kv_heads
+    out = torch.empty((rows, k), dtype=torch.int32, device=q.device) if out is None else out
+    _need(out, "page_idx", torch.int32, (rows, k))
+    L.call("sls_select_pages", ctypes.byref(desc), _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(ctx_len),
+           int(k), int(n_sink_pages), int(n_local_tokens), _ptr(out), _stream())
+    return out
+
+
+def select_delta_workspace(desc: L.AttnDesc, block: int, device="cuda"):
+    n = L.load().sls_select_delta_workspace_size(ctypes.byref(desc), int(block))
+    return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
+def select_delta(desc: L.AttnDesc, q, k_cache, codes, scales, ctx_len, block: int, delta: float,
+                 count=None, block_idx=None, workspace=None):
+    rows = desc.batch * desc.num_kv_heads
+    nblk = desc.capacity // block
+    count = torch.empty(rows, dtype=torch.int32, device=q.device) if count is None else count
+    block_idx = torch.empty((rows, nblk), dtype=torch.int32, device=q.device) if block_idx is None else block_idx
+    workspace = select_delta_workspace(desc, block, q.device) if workspace is None else workspace
+    _need(block_idx, "block_idx", torch.int32)
+    L.call("sls_select_delta", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(codes), _ptr(scales),
+           _ptr(ctx_len), int(block), float(delta), _ptr(count), _ptr(block_idx),
+           int(block_idx.shape[1]), _ptr(workspace), workspace.numel(), _stream())
+    return count, block_idx
+
+
+# ---------------------------------------------------------------- attention
+
+def partials(desc: L.AttnDesc, num_splits: int, device="cuda"):
+    B, Hq, D = desc.batch, desc.num_q_heads, desc.head_dim
+    return (torch.empty((B, Hq, num_splits, D), dtype=torch.float32, device=device),
+            torch.empty((B, Hq, num_splits), dtype=torch.float32, device=device),
+            torch.empty((B, Hq, num_splits), dtype=torch.float32, device=device))
+
+
+def sparse_decode_attend(desc: L.AttnDesc, q, k_cache, v_cache, page_idx, ctx_len, num_splits: int,
+                         count=None, k_fixed: Optional[int] = None, parts=None):
+    """page_idx [rows, stride] int32 (or None for every page); count [rows]
+    int32 or None (then k_fixed, default stride, entries per row)."""
+    _need(q, "q")
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache")
+    o, m, l = partials(desc, num_splits, q.device) if parts is None else parts
+    stride = int(page_idx.shape[1]) if page_idx is not None else 0
+    kf = stride if k_fixed is None else int(k_fixed)
+    L.call("sls_sparse_decode_attend", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+           _ptr(page_idx), stride, _ptr(count), kf, _ptr(ctx_len), int(num_splits), _ptr(o),
+           _ptr(m), _ptr(l), _stream())
+    return o, m, l
+
+
+def combine_splits(desc: L.AttnDesc, parts, sink=None, out=None, lse=None, want_lse: bool = True):
+    o, m, l = parts
+    B, Hq, S, D = o.shape
+    dtype = torch.bfloat16 if desc.dtype == L.SLS_DTYPE_BF16 else torch.float32
+    out = torch.empty((B, Hq, D), dtype=dtype, device=o.device) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=o.device)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, (Hq,))
+    L.call("sls_combine_splits", ctypes.byref(desc), _ptr(o), _ptr(m), _ptr(l), int(S), _ptr(sink),
+           _ptr(out), _ptr(lse), _stream())
+    return out, lse
+
+
+# ------------------------------------------------------------ decode step
+
+class QuestDecode:
+    """One Quest decode step (select + attend + combine) over preallocated
+    buffers, so the three launches can be captured in a CUDA graph."""
+
+    def __init__(self, desc: L.AttnDesc, k_budget: int, n_sink_pages: int, n_local_tokens: int,
+                 num_splits: Optional[int] = None, device="cuda"):
+        self.desc = desc
+        self.k = int(k_budget)
+        self.n_sink, self.n_local = int(n_sink_pages), int(n_local_tokens)
+        rows = desc.batch * desc.num_kv_heads
+        self.S = num_splits or default_splits(rows, self.k, desc.page_size, device)
+        self.page_idx = torch.empty((rows, self.k), dtype=torch.int32, device=device)
+        self.parts = partials(desc, self.S, device)
+        dtype = torch.bfloat16 if desc.dtype == L.SLS_DTYPE_BF16 else torch.float32
+        self.out = torch.empty((desc.batch, desc.num_q_heads, desc.head_dim), dtype=dtype, device=device)
+        self.lse = torch.empty((desc.batch, desc.num_q_heads), dtype=torch.float32, device=device)
+
+    def select(self, q, kmin, kmax, ctx_len):
+        return select_pages(self.desc, q, kmin, kmax, ctx_len, self.k, self.n_sink, self.n_local,
+                            out=self.page_idx)
+
+    def attend(self, q, k_cache, v_cache, ctx_len, sink=None):
+        sparse_decode_attend(self.desc, q, k_cache, v_cache, self.page_idx, ctx_len, self.S,
+                             parts=self.parts)
+        return combine_splits(self.desc, self.parts, sink, out=self.out, lse=self.lse)
+
+    def __call__(self, q, k_cache, v_cache, kmin, kmax, ctx_len, sink=None):
+        self.select(q, kmin, kmax, ctx_len)
+        return self.attend(q, k_cache, v_cache, ctx_len, sink)
+
+
+class DeltaDecode:
+    """One top-delta decode step (select_delta + attend + combine)."""
+
+    def __init__(self, desc: L.AttnDesc, block: int, delta: float, num_splits: Optional[int] = None,
+                 device="cuda"):
+        if desc.page_size != block:
+            raise ValueError("attend page_size must equal the thumbnail block")
+        self.desc, self.block, self.delta = desc, int(block), float(delta)
+        rows = desc.batch * desc.num_kv_heads
+        nblk = desc.capacity // block
+        self.S = num_splits or default_splits(rows, nblk, block, device)
+        self.count = torch.empty(rows, dtype=torch.int32, device=device)
+        self.block_idx = torch.empty((rows, nblk), dtype=torch.int32, device=device)
+        self.workspace = select_delta_workspace(desc, block, device)
+        self.parts = partials(desc, self.S, device)
+        dtype = torch.bfloat16 if desc.dtype == L.SLS_DTYPE_BF16 else torch.float32
+        self.out = torch.empty((desc.batch, desc.num_q_heads, desc.head_dim), dtype=dtype, device=device)
+        self.lse = torch.empty((desc.batch, desc.num_q_heads), dtype=torch.float32, device=device)
+
+    def select(self, q, k_cache, codes, scales, ctx_len):
+        return select_delta(self.desc, q, k_cache, codes, scales, ctx_len, self.block, self.delta,
+                            count=self.count, block_idx=self.block_idx, workspace=self.workspace)
+
+    def attend(self, q, k_cache, v_cache, ctx_len, sink=None):
+        sparse_decode_attend(self.desc, q, k_cache, v_cache, self.block_idx, ctx_len, self.S,
+                             count=self.count, parts=self.parts)
+        return combine_splits(self.desc, self.parts, sink, out=self.out, lse=self.lse)
+
+    def __call__(self, q, k_cache, v_cache, codes, scales, ctx_len, sink=None):
+        self.select(q, k_cache, codes, scales, ctx_len)
+        return self.attend(q, k_cache, v_cache, ctx_len, sink)

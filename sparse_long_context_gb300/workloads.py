@@ -181,9 +181,11 @@ def _pick_needles(rng, s: Spec, n: int) -> np.ndarray:
     return np.sort(units) * L
 
 
-def gen_row(s: Spec, b: int, h: int, sigma: Optional[np.ndarray] = None) -> Row:
-    """Generate row (b, h) of the workload."""
-    rng = np.random.default_rng([s.seed, b, h])
+def gen_row(s: Spec, b: int, h: int, sigma: Optional[np.ndarray] = None,
+            seq: Optional[int] = None) -> Row:
+    """Generate row (b, h) of the workload (seeded by sequence number ``seq``,
+    default b)."""
+    rng = np.random.default_rng([s.seed, b if seq is None else seq, h])
     n = s.ctx_len[b]
     cap, d, g = s.capacity, s.head_dim, s.group
     if s.generator == "planted":
@@ -236,9 +238,11 @@ class Tensors:
     needles: list        # [B][Hkv] arrays of needle token positions
 
 
-def generate(s: Spec, rows=None) -> Tensors:
+def generate(s: Spec, rows=None, batch_offset: int = 0) -> Tensors:
     """Generate the whole workload (``rows=None``) or only the listed
-    (b, h) rows (others stay zero)."""
+    (b, h) rows (others stay zero).  ``batch_offset`` shifts the sequence
+    numbers the rows are seeded with (shard r of a multi-GPU run draws
+    sequences r*B .. r*B+B-1)."""
     B, Hkv, Cap, D, G = s.batch, s.num_kv_heads, s.capacity, s.head_dim, s.group
     dt = np.uint16 if s.dtype == "bf16" else np.float32
     K = np.zeros((B, Hkv, Cap, D), dtype=dt)
@@ -248,7 +252,7 @@ def generate(s: Spec, rows=None) -> Tensors:
     sigma = _sigma(s) if s.generator == "outlier" else None
     todo = [(b, h) for b in range(B) for h in range(Hkv)] if rows is None else rows
     for b, h in todo:
-        r = gen_row(s, b, h, sigma)
+        r = gen_row(s, b, h, sigma, seq=b + batch_offset)
         K[b, h], V[b, h] = r.K, r.V
         q[b, h * G:(h + 1) * G] = r.q
         needles[b][h] = r.needles

@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports
+every symbol include/sls.h declares, and rejects bad arguments before it
+launches anything.  Every call here fails validation, so no kernel runs."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_long_context_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sls.h")
+BAD = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:sls_status|size_t|const char\*|int32_t)\s+(sls_\w+)\(",
+                                 text, re.M)))
+
+
+def desc(**kw):
+    d = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+             capacity=1024, dtype=L.SLS_DTYPE_BF16, flags=0, scale=0.0)
+    d.update(kw)
+    return L.AttnDesc(**d)
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 10
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(syms) == set(L.SIGNATURES)
+    assert lib.sls_version() == 10000
+
+
+def err(lib):
+    return lib.sls_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), L.SLS_EUNSUPPORTED),
+    (dict(num_q_heads=18, num_kv_heads=2), L.SLS_EUNSUPPORTED),   # G = 9
+    (dict(num_q_heads=7, num_kv_heads=2), L.SLS_EINVAL),
+    (dict(page_size=3), L.SLS_EINVAL),
+    (dict(page_size=512, capacity=1024), L.SLS_EINVAL),
+    (dict(capacity=1000), L.SLS_EINVAL),                          # not a multiple of P
+    (dict(dtype=7), L.SLS_EUNSUPPORTED),
+    (dict(batch=0), L.SLS_EINVAL),
+    (dict(scale=-1.0), L.SLS_EINVAL),
+    (dict(flags=8), L.SLS_EINVAL),
+    (dict(batch=1 << 30, num_q_heads=4, num_kv_heads=4), L.SLS_EOVERFLOW),    # rows > 2^31
+    (dict(batch=1 << 20, num_kv_heads=2, capacity=1 << 30), L.SLS_EOVERFLOW),  # > 2^48 elements
+])
+def test_descriptor_validation(lib, kw, code):
+    d = desc(**kw)
+    st = lib.sls_pagemeta_build(ctypes.byref(d), BAD, BAD, BAD, BAD, None)
+    assert st == code, err(lib)
+    assert err(lib)
+
+
+def test_null_arguments(lib):
+    d = desc()
+    assert lib.sls_pagemeta_build(None, BAD, BAD, BAD, BAD, None) == L.SLS_EINVAL
+    assert lib.sls_pagemeta_build(ctypes.byref(d), None, BAD, BAD, BAD, None) == L.SLS_EINVAL
+    assert "k_cache" in err(lib)
+    assert lib.sls_sparse_decode_attend(ctypes.byref(d), BAD, BAD, BAD, BAD, 8, None, 8, BAD, 4,
+                                        None, BAD, BAD, None) == L.SLS_EINVAL
+    assert lib.sls_combine_splits(ctypes.byref(d), BAD, BAD, BAD, 4, None, None, None, None) == L.SLS_EINVAL
+
+
+def test_select_pages_validation(lib):
+    d = desc()
+    sel = lambda k, ns, nl, kmin=BAD, kmax=BAD, dd=d: lib.sls_select_pages(
+        ctypes.byref(dd), BAD, kmin, kmax, BAD, k, ns, nl, BAD, None)
+    assert sel(0, 0, 0) == L.SLS_EINVAL                  # k < 1
+    assert sel(65, 0, 0) == L.SLS_EINVAL                 # k > Cap/P = 64
+    assert sel(4, 1, 64) == L.SLS_EINVAL                 # forced pages do not fit
+    assert "forced" in err(lib)
+    assert sel(8, -1, 0) == L.SLS_EINVAL
+    d1 = desc(page_size=1)
+    assert sel(8, 4, 0, kmin=BAD, kmax=ctypes.c_void_p(0x2000), dd=d1) == L.SLS_EINVAL
+    big = desc(page_size=1, capacity=1 << 22)            # 4M pages per row > supported
+    assert sel(8, 0, 0, dd=big) == L.SLS_EUNSUPPORTED
+
+
+def test_select_delta_validation_and_workspace(lib):
+    d = desc(page_size=64, capacity=4096)
+    ws = lib.sls_select_delta_workspace_size(ctypes.byref(d), 64)
+    assert ws == ((2 * 2 * 64 + 255) // 256) * 256
+    assert lib.sls_select_delta_workspace_size(ctypes.byref(d), 48) == 0
+    call = lambda block=64, delta=5.0, stride=64, wsb=ws, wsp=BAD: lib.sls_select_delta(
+        ctypes.byref(d), BAD, BAD, BAD, BAD, BAD, block, delta, BAD, BAD, stride, wsp, wsb, None)
+    assert call(block=48) == L.SLS_EINVAL
+    assert call(delta=-1.0) == L.SLS_EINVAL
+    assert call(delta=float("inf")) == L.SLS_EINVAL
+    assert call(stride=63) == L.SLS_EINVAL
+    assert call(wsb=ws - 1) == L.SLS_EWORKSPACE
+    assert call(wsp=None) == L.SLS_EWORKSPACE
+
+
+def test_attend_validation(lib):
+    d = desc()
+    att = lambda stride=8, count=None, kf=8, S=4: lib.sls_sparse_decode_attend(
+        ctypes.byref(d), BAD, BAD, BAD, BAD, stride, count, kf, BAD, S, BAD, BAD, BAD, None)
+    assert att(S=0) == L.SLS_EINVAL
+    assert att(S=1025) == L.SLS_EINVAL
+    assert att(stride=0) == L.SLS_EINVAL
+    assert att(kf=9) == L.SLS_EINVAL
+    assert att(kf=-1) == L.SLS_EINVAL
+
+
+def test_python_layer_raises_on_status(lib):
+    d = desc(head_dim=96)
+    with pytest.raises(L.SlsError) as e:
+        L.call("sls_pagemeta_build", ctypes.byref(d), BAD, BAD, BAD, BAD, None)
+    assert e.value.code == L.SLS_EUNSUPPORTED

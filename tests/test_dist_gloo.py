@@ -1,0 +1,60 @@
+"""The multi-GPU bench path shards sequences across ranks with no data-path
+collective; the only exchange is the timing/units reduction.  Checked here
+with two gloo ranks on the CPU."""
+import os
+import socket
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t, u = bench.aggregate(1.0 + rank, 10.0 * (rank + 1), world)
+    r, w, lr = bench.dist_env()
+    q.put((rank, t, u, r, w))
+    dist.destroy_process_group()
+
+
+def test_aggregate_max_time_sum_units_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, t, u, r, w in res:
+        assert t == 2.0 and u == 30.0 and r == rank and w == 2
+
+
+def test_shards_draw_distinct_sequences():
+    from sparse_long_context_gb300 import workloads as W
+    s = W.spec("qwen7b", batch=2, ctx_len=256)
+    a = W.generate(s, batch_offset=0)
+    b = W.generate(s, batch_offset=2)
+    assert not (a.K == b.K).all()
+    one = W.generate(W.spec("qwen7b", batch=4, ctx_len=256))
+    assert (one.K[2:] == b.K).all()
+
+
+def test_algorithmic_bytes_of_the_benchmark_workload():
+    from sparse_long_context_gb300 import workloads as W
+    nb = bench.algorithmic_bytes(W.spec("qwen1p5b"))
+    assert nb["select"] == 32 * 2 * 4096 * 2 * 128 * 2          # 134.2 MB of page min/max
+    assert nb["attend"] == 32 * 2 * 2048 * 2 * 128 * 2          # 67.1 MB of selected K+V
+    assert abs(nb["total"] / 1e6 - 201.3) < 0.1

@@ -1,0 +1,290 @@
+"""CUDA path vs the fp64 oracle, through the C ABI, on seeded workloads.
+
+Small cases cover every row; full-size workloads (the benchmark's launch
+configuration) check sampled rows the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import sls_oracle as O
+from sparse_long_context_gb300 import ops
+from sparse_long_context_gb300 import workloads as W
+
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def small(name, **kw):
+    return W.spec(name, **kw)
+
+
+# The small parity cases: several tiles, ragged tails, partial last pages.
+SMALL_QUEST = {
+    "tiny": dict(),
+    "tiny_ragged": dict(name="tiny", ctx_len=[1000]),
+    "qwen7b_ragged": dict(name="qwen7b", ctx_len=[8197, 3000, 700], capacity=8208),
+    "qwen1p5b_4k": dict(name="qwen1p5b", batch=3, ctx_len=4096),
+    "gptoss_ragged": dict(name="gptoss", ctx_len=[20000, 5003], capacity=20000),
+}
+SMALL_DELTA = {
+    "ffd_ragged": dict(name="ffd", ctx_len=[65536 + 100, 20000], capacity=65536 + 128),
+    "ffd_aligned": dict(name="ffd", batch=1, ctx_len=8192),
+}
+
+
+def make(case):
+    kw = dict(case)
+    name = kw.pop("name", None)
+    return W.spec(name, **kw)
+
+
+def quest_case(key):
+    return make(dict(SMALL_QUEST[key], name=SMALL_QUEST[key].get("name", key)))
+
+
+# ----------------------------------------------------------------- metadata
+
+@pytest.mark.parametrize("key", ["tiny_ragged", "qwen7b_ragged"])
+def test_pagemeta_build_is_exact(key):
+    s = quest_case(key)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    kmin, kmax = dw.kmin.float().cpu().numpy(), dw.kmax.float().cpu().numpy()
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            n = host.ctx_len[b]
+            omin, omax = O.page_minmax(O.to_f64(host.K[b, h], s.dtype), n, s.page_size)
+            np.testing.assert_array_equal(kmin[b, h, :len(omin)], omin)
+            np.testing.assert_array_equal(kmax[b, h, :len(omax)], omax)
+
+
+def test_pagemeta_update_matches_oracle():
+    s = W.spec("qwen7b", batch=2, ctx_len=[300, 517], capacity=640)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    # start from summaries of shorter prefixes, then append one token at a time
+    n0 = np.array([260, 490], dtype=np.int32)
+    kmin, kmax = ops.pagemeta_build(dw.desc, dw.K, torch.from_numpy(n0).cuda())
+    cur = n0.copy()
+    while np.any(cur < host.ctx_len):
+        pos = np.where(cur < host.ctx_len, cur, -1).astype(np.int32)
+        ops.pagemeta_update(dw.desc, dw.K, torch.from_numpy(pos).cuda(), kmin, kmax)
+        cur = np.minimum(cur + 1, host.ctx_len)
+    got_min, got_max = kmin.float().cpu().numpy(), kmax.float().cpu().numpy()
+    for b in range(2):
+        for h in range(s.num_kv_heads):
+            omin, omax = O.page_minmax(O.to_f64(host.K[b, h], s.dtype), host.ctx_len[b], 16)
+            np.testing.assert_array_equal(got_min[b, h, :len(omin)], omin)
+            np.testing.assert_array_equal(got_max[b, h, :len(omax)], omax)
+
+
+@pytest.mark.parametrize("ctx", [[64 * 9 + 5, 64 * 3], [64 * 40]])
+def test_thumbnails_are_bit_exact(ctx):
+    s = W.spec("ffd", ctx_len=ctx, capacity=64 * 40)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    codes, scales = dw.codes.cpu().numpy(), dw.scales.float().cpu().numpy()
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            n = host.ctx_len[b]
+            oc, osc = O.thumbnails_row(O.to_f64(host.K[b, h], s.dtype), n, 64)
+            nfull = n // 64
+            np.testing.assert_array_equal(codes[b, h, :nfull * 64], O.pack_codes(oc))
+            np.testing.assert_array_equal(scales[b, h, :nfull], osc)
+
+
+def test_thumb_update_completes_blocks():
+    s = W.spec("ffd", batch=2, ctx_len=[64 * 5, 64 * 7], capacity=64 * 8)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    start = torch.tensor([64 * 3 + 10, 64 * 6 + 60], dtype=torch.int32, device="cuda")
+    codes, scales = ops.thumb_build(dw.desc, dw.K, start, 64)
+    cur = start.cpu().numpy().copy()
+    end = host.ctx_len
+    while np.any(cur < end):
+        pos = np.where(cur < end, cur, -1).astype(np.int32)
+        ops.thumb_update(dw.desc, dw.K, torch.from_numpy(pos).cuda(), 64, codes, scales)
+        cur = np.minimum(cur + 1, end)
+    codes, scales = codes.cpu().numpy(), scales.float().cpu().numpy()
+    for b in range(2):
+        for h in range(s.num_kv_heads):
+            oc, osc = O.thumbnails_row(O.to_f64(host.K[b, h], s.dtype), end[b], 64)
+            nfull = end[b] // 64
+            np.testing.assert_array_equal(codes[b, h, :nfull * 64], O.pack_codes(oc))
+            np.testing.assert_array_equal(scales[b, h, :nfull], osc)
+
+
+# ---------------------------------------------------------- select + attend
+
+def check_all_rows(s, host, sel, cnt, out, lse, dw=None):
+    """Every row: selection parity (ties counted), output parity where the
+    sets are identical, and attend parity on the oracle's own page list."""
+    G = s.group
+    ties = 0
+    orcs = []
+    exact_rows = []
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            r = b * s.num_kv_heads + h
+            orc = PT.oracle_row(s, host, b, h)
+            orcs.append(orc)
+            if s.selector == "quest":
+                t = PT.check_quest_list(sel[r], orc, int(host.ctx_len[b]), s.page_size, s.k_pages)
+            else:
+                t = PT.check_delta_list(int(cnt[r]), sel[r], orc, s.delta)
+            ties += t
+            if t == 0:
+                exact_rows.append((b, h, orc))
+    for b, h, orc in exact_rows:
+        PT.assert_close(s, out[b, h * G:(h + 1) * G], orc.o, f"output row {(b, h)}")
+        fin = np.isfinite(orc.lse)
+        np.testing.assert_allclose(lse[b, h * G:(h + 1) * G][fin], orc.lse[fin], rtol=1e-4, atol=1e-4)
+    if dw is not None:
+        o2, _ = PT.attend_on(dw, [o.pages for o in orcs])
+        for b in range(s.batch):
+            for h in range(s.num_kv_heads):
+                ref = orcs[b * s.num_kv_heads + h].o
+                PT.assert_close(s, o2[b, h * G:(h + 1) * G], ref, f"attend on oracle set {(b, h)}")
+    return ties
+
+
+@pytest.mark.parametrize("key", list(SMALL_QUEST))
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_quest_step_small(key, cuda_cores):
+    s = quest_case(key)
+    host = W.generate(s)
+    dw = PT.upload(s, host, cuda_cores=cuda_cores)
+    sel, cnt, out, lse = PT.run_step(dw)
+    ties = check_all_rows(s, host, sel, cnt, out, lse, dw)
+    print(f"{key}: boundary ties {ties}")
+
+
+@pytest.mark.parametrize("key", list(SMALL_DELTA))
+def test_delta_step_small(key):
+    s = make(SMALL_DELTA[key])
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, cnt, out, lse = PT.run_step(dw)
+    ties = check_all_rows(s, host, sel, cnt, out, lse, dw)
+    kept = cnt.sum() / sum((n + 63) // 64 for n in host.ctx_len for _ in range(s.num_kv_heads))
+    print(f"{key}: kept fraction {kept:.3f}, boundary ties {ties}")
+
+
+@pytest.mark.parametrize("splits", [1, 3, 64, 1024])
+def test_split_counts_do_not_change_the_result(splits):
+    s = W.spec("qwen7b", batch=2, ctx_len=[2000, 33], capacity=2048)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, cnt, out, lse = PT.run_step(dw, num_splits=splits)
+    check_all_rows(s, host, sel, cnt, out, lse)
+
+
+def test_dense_attend_matches_oracle():
+    s = W.spec("qwen7b", batch=2, ctx_len=[3001, 64], capacity=3008)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    parts = ops.sparse_decode_attend(dw.desc, dw.q, dw.K, dw.V, None, dw.ctx, 8)
+    out, _ = ops.combine_splits(dw.desc, parts)
+    out = out.float().cpu().numpy()
+    G = s.group
+    for b in range(2):
+        for h in range(s.num_kv_heads):
+            n = host.ctx_len[b]
+            q = O.to_f64(host.q[b, h * G:(h + 1) * G], "bf16")
+            K, V = O.to_f64(host.K[b, h, :n], "bf16"), O.to_f64(host.V[b, h, :n], "bf16")
+            ref, _ = O.softmax_attention(q, K, V, s.scale)
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], ref, "dense")
+
+
+def test_budget_covering_every_page_equals_dense():
+    s = W.spec("qwen7b", batch=1, ctx_len=[1000], capacity=2048)
+    s.k_pages = 128  # >= 63 pages
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, _, out, _ = PT.run_step(dw)
+    assert np.array_equal(sel[0, :63], np.arange(63)) and np.all(sel[:, 63:] == -1)
+    G = s.group
+    for h in range(s.num_kv_heads):
+        q = O.to_f64(host.q[0, h * G:(h + 1) * G], "bf16")
+        ref, _ = O.softmax_attention(q, O.to_f64(host.K[0, h, :1000], "bf16"),
+                                     O.to_f64(host.V[0, h, :1000], "bf16"), s.scale)
+        PT.assert_close(s, out[0, h * G:(h + 1) * G], ref, "dense-equivalent")
+
+
+def test_sparse_output_differs_from_dense():
+    """A kernel that ignored the page list would return dense attention."""
+    s = W.spec("qwen7b", batch=1, ctx_len=[16384])
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    _, _, out, _ = PT.run_step(dw)
+    parts = ops.sparse_decode_attend(dw.desc, dw.q, dw.K, dw.V, None, dw.ctx, 16)
+    dense, _ = ops.combine_splits(dw.desc, parts)
+    _, rel = PT.out_errors(out, dense.float().cpu().numpy())
+    assert rel > 1e-3
+
+
+def test_empty_and_single_token_rows():
+    s = W.spec("gptoss", batch=3, ctx_len=[0, 1, 4100], capacity=4352)
+    s.k_pages = 4096
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, _, out, lse = PT.run_step(dw)
+    rows = s.num_kv_heads
+    assert np.all(sel[:rows] == -1)
+    assert np.all(out[0] == 0)
+    np.testing.assert_allclose(lse[0], host.sink.astype(np.float64), rtol=1e-6)  # only the sink
+    check_all_rows(s, host, sel, None, out, lse)
+    # without a sink an empty row gives 0 and -inf
+    parts = ops.sparse_decode_attend(dw.desc, dw.q, dw.K, dw.V, torch.from_numpy(sel).cuda(), dw.ctx, 4)
+    out2, lse2 = ops.combine_splits(dw.desc, parts, None)
+    assert torch.all(out2[0] == 0) and torch.all(torch.isinf(lse2[0]))
+
+
+def test_padded_page_lists_are_skipped():
+    s = W.spec("qwen7b", batch=1, ctx_len=[640], capacity=640)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    lists = [np.array([3, 7, 39]), np.array([0]), np.array([], dtype=np.int64), np.array([12, 13])]
+    o, lse = PT.attend_on(dw, lists, num_splits=2)
+    G = s.group
+    for h, pages in enumerate(lists):
+        q = O.to_f64(host.q[0, h * G:(h + 1) * G], "bf16")
+        ref, rl = O.sparse_attention_row(q, O.to_f64(host.K[0, h], "bf16"), O.to_f64(host.V[0, h], "bf16"),
+                                         pages, 640, 16, s.scale)
+        PT.assert_close(s, o[0, h * G:(h + 1) * G], ref, f"list {h}")
+
+
+# ------------------------------------------------- full sizes, sampled rows
+
+FULL = ["qwen1p5b", "qwen7b", "gptoss", "ffd"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(name):
+    s = W.spec(name)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, cnt, out, lse = PT.run_step(dw)   # default launch configuration, as benchmarked
+    rng = np.random.default_rng(7)
+    rows = sorted(set([0, s.rows - 1] + rng.choice(s.rows, size=2, replace=False).tolist()))
+    G = s.group
+    ties = 0
+    for r in rows:
+        b, h = divmod(r, s.num_kv_heads)
+        orc = PT.oracle_row(s, host, b, h)
+        if s.selector == "quest":
+            t = PT.check_quest_list(sel[r], orc, int(host.ctx_len[b]), s.page_size, s.k_pages)
+        else:
+            t = PT.check_delta_list(int(cnt[r]), sel[r], orc, s.delta)
+        ties += t
+        if t == 0:
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], orc.o, f"{name} row {r}")
+    print(f"{name}: rows {rows} boundary ties {ties}"
+          + (f" kept {cnt.sum() / (s.rows * (s.ctx_len[0] // 64)):.3f}" if cnt is not None else ""))
