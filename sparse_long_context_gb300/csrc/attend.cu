@@ -199,7 +199,8 @@ attend_cc_kernel(const AttendArgs a) {
   }
 }
 
-// Stage two: one warp per (b, query head).
+// Stage two: one warp per (b, query head).  Lane s holds split s's max and
+// normaliser; the accumulators of up to 8 splits are loaded together.
 template <typename T, int D>
 __global__ void __launch_bounds__(128)
 combine_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
@@ -216,21 +217,39 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ m_par
   float M = kNegInf;
   for (int s = lane; s < S; s += 32) M = fmaxf(M, mp[s]);
   M = warp_max(M);
-  if (sink) M = fmaxf(M, sink[hq]);
+  const float sk = sink ? sink[hq] : kNegInf;
+  M = fmaxf(M, sk);
   float acc[CPL];
 #pragma unroll
   for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
   float Ls = 0.f;
   if (M != kNegInf) {
-    for (int s = 0; s < S; ++s) {
-      const float ms = mp[s];
-      if (ms == kNegInf) continue;
-      const float w = expf(ms - M);
-      Ls += lp[s] * w;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int s = s0 + lane;
+      float w = 0.f;
+      if (s < S) {
+        const float ms = mp[s];
+        w = ms == kNegInf ? 0.f : expf(ms - M);
+        Ls += lp[s] * w;
+      }
+      const int n = min(32, S - s0);
+      for (int j0 = 0; j0 < n; j0 += 8) {
+        float v[8][CPL];
 #pragma unroll
-      for (int i = 0; i < CPL; ++i) acc[i] += op[(size_t)s * D + i] * w;
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) v[j][i] = j0 + j < n ? op[(size_t)(s0 + j0 + j) * D + i] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) acc[i] = fmaf(v[j][i], wj, acc[i]);
+        }
+      }
     }
-    if (sink) Ls += expf(sink[hq] - M);
+    Ls = warp_sum(Ls);
+    if (sink) Ls += expf(sk - M);
   }
   const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
 #pragma unroll
