@@ -331,7 +331,7 @@ def run_ours(args, s: W.Spec):
     # per-kernel device time: eager launches bracketed by events on the
     # launching stream, queued behind a sleep so the host stays ahead
     ksteps = max(50, min(args.steps, 400))
-    ev = {k: ([], []) for k in ("select", "attend", "combine")}
+    ev = {k: ([], []) for k in ("select", "attend")}
     with torch.cuda.stream(stream):
         for i in range(ksteps):
             if i % 25 == 0:
@@ -339,10 +339,7 @@ def run_ours(args, s: W.Spec):
             st = steps_obj[i % nsets]
             K, V, kmin, kmax = sets[i % nsets]
             for name, fn in (("select", lambda: st.select(dw.q, kmin, kmax, dw.ctx)),
-                             ("attend", lambda: ops.sparse_decode_attend(st.desc, dw.q, K, V, st.page_idx,
-                                                                          dw.ctx, st.S, parts=st.parts)),
-                             ("combine", lambda: ops.combine_splits(st.desc, st.parts, None, out=st.out,
-                                                                    lse=st.lse))):
+                             ("attend", lambda: st.attend(dw.q, K, V, dw.ctx))):
                 a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 fn()
@@ -399,12 +396,14 @@ def run_ours(args, s: W.Spec):
                    "parallelism": f"weak: {world} GPU(s), {s.batch} sequences each"},
         "bytes_per_step": nbytes["total"], "bytes_select": nbytes["select"], "bytes_attend": nbytes["attend"],
         "kernel_us": {k: round(v, 2) for k, v in kern_us.items()},
-        "roofline": {"bound": "hbm", "kernel": f"select_pages_kernel ({dom})" if dom == "select" else "attend",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("select: quest_score_kernel + topk_kernel" if dom == "select"
+                                else "attend: attend_mma_kernel with fused combine"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_kind": f"{peak_kind} (burst copy)"},
         "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 3 * args.steps,  # quest_score, topk, attend (+combine) per step
         "clocks": clk,
         "e2e": {"value": round(e2e_bytes / e2e_max / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(1e6 * e2e_max / esteps, 2),

@@ -176,14 +176,23 @@ sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache,
  *   k        budget in pages, 1 <= k <= Cap/P, and k must cover the forced
  *            pages: k >= n_sink_pages + ceil(n_local_tokens/P) + 1
  *   page_idx [B*Hkv, k] int32 (written)
+ *   workspace >= sls_select_pages_workspace_size() bytes of device memory
+ *            (one 32-bit key per page of every row; contents on entry are
+ *            ignored and on exit unspecified)
  * The score is computed in fp32; two pages whose scores differ by less
- * than the fp32 rounding of the sum may rank either way.
+ * than the fp32 rounding of the sum may rank either way.  Rows may hold at
+ * most 8 * 32768 pages (Cap/P); larger capacities return SLS_EUNSUPPORTED.
  */
 sls_status sls_select_pages(const sls_attn_desc* desc, const void* q,
                             const void* kmin, const void* kmax,
                             const int32_t* ctx_len, int32_t k,
                             int32_t n_sink_pages, int32_t n_local_tokens,
-                            int32_t* page_idx, void* stream);
+                            int32_t* page_idx, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace sls_select_pages needs for this descriptor (0 if the
+ * descriptor is invalid). */
+size_t sls_select_pages_workspace_size(const sls_attn_desc* desc);
 
 /* Bytes of workspace sls_select_delta needs for this descriptor/block. */
 size_t sls_select_delta_workspace_size(const sls_attn_desc* desc, int32_t block);
@@ -257,6 +266,38 @@ sls_status sls_combine_splits(const sls_attn_desc* desc, const float* o_part,
                               const float* m_part, const float* l_part,
                               int32_t num_splits, const float* sink, void* out,
                               float* lse, void* stream);
+
+/*
+ * A split count for sls_sparse_decode_attend(_combine) that gives about two
+ * waves of CTAs on this GPU, each slice holding at least 64 tokens of a
+ * list of up to max_entries pages.  Returns 1 for an invalid descriptor.
+ */
+int32_t sls_attend_default_splits(const sls_attn_desc* desc, int32_t max_entries);
+
+/* Bytes of workspace sls_sparse_decode_attend_combine needs. */
+size_t sls_attend_combine_workspace_size(const sls_attn_desc* desc,
+                                         int32_t num_splits);
+
+/*
+ * Both stages in one launch: sls_sparse_decode_attend followed, inside the
+ * same kernel, by the combine of each row.  Every CTA of a row takes an
+ * arrival ticket after writing its partials; the CTA that arrives last
+ * merges the row's splits exactly as sls_combine_splits does (no CTA ever
+ * waits for another).  Arguments as in the two separate calls; the partials
+ * live in the workspace, whose first 4*B*Hkv bytes hold the tickets.
+ *   workspace  >= sls_attend_combine_workspace_size() bytes; it must be
+ *              zero-filled before its first use, and every call leaves the
+ *              tickets at zero again.  Calls sharing a workspace must not
+ *              run concurrently.
+ */
+sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const void* q,
+                                            const void* k_cache, const void* v_cache,
+                                            const int32_t* page_idx, int32_t idx_stride,
+                                            const int32_t* count, int32_t k_fixed,
+                                            const int32_t* ctx_len, int32_t num_splits,
+                                            const float* sink, void* out, float* lse,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* stream);
 
 /* ---- diagnostics ------------------------------------------------------- */
 

@@ -30,12 +30,17 @@ SIGNATURES = {
     "sls_pagemeta_update": (_I, [_D, _P, _P, _P, _P, _P]),
     "sls_thumb_build": (_I, [_D, _P, _P, _I, _P, _P, _P]),
     "sls_thumb_update": (_I, [_D, _P, _P, _I, _P, _P, _P]),
-    "sls_select_pages": (_I, [_D, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
+    "sls_select_pages": (_I, [_D, _P, _P, _P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P]),
+    "sls_select_pages_workspace_size": (ctypes.c_size_t, [_D]),
     "sls_select_delta_workspace_size": (ctypes.c_size_t, [_D, _I]),
     "sls_select_delta": (_I, [_D, _P, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _I, _P,
                               ctypes.c_size_t, _P]),
     "sls_sparse_decode_attend": (_I, [_D, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P]),
     "sls_combine_splits": (_I, [_D, _P, _P, _P, _I, _P, _P, _P, _P]),
+    "sls_attend_default_splits": (_I, [_D, _I]),
+    "sls_attend_combine_workspace_size": (ctypes.c_size_t, [_D, _I]),
+    "sls_sparse_decode_attend_combine": (_I, [_D, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P,
+                                              ctypes.c_size_t, _P]),
     "sls_last_error": (ctypes.c_char_p, []),
     "sls_version": (_I, []),
 }

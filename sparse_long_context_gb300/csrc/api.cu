@@ -142,10 +142,16 @@ sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache, cons
                      "sls_thumb_update");
 }
 
+size_t sls_select_pages_workspace_size(const sls_attn_desc* desc) {
+  sls::Shape s;
+  if (check_desc(desc, &s)) return 0;
+  return sls::select_pages_workspace(s);
+}
+
 sls_status sls_select_pages(const sls_attn_desc* desc, const void* q, const void* kmin,
                             const void* kmax, const int32_t* ctx_len, int32_t k,
                             int32_t n_sink_pages, int32_t n_local_tokens, int32_t* page_idx,
-                            void* stream) {
+                            void* workspace, size_t workspace_bytes, void* stream) {
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
@@ -165,8 +171,11 @@ sls_status sls_select_pages(const sls_attn_desc* desc, const void* q, const void
   if (chunk * 4 > sls::select_pages_smem_limit())
     return fail(SLS_EUNSUPPORTED, "Cap/P=%d pages per row exceeds the supported %zu", npcap,
                 sls::select_pages_smem_limit() / 4 * sls::select_pages_cluster());
+  const size_t need = sls::select_pages_workspace(s);
+  if (!workspace || workspace_bytes < need)
+    return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
   return cuda_status(sls::launch_select_pages(s, q, kmin, kmax, ctx_len, k, n_sink_pages, n_local_tokens,
-                                              page_idx, (cudaStream_t)stream),
+                                              page_idx, workspace, (cudaStream_t)stream),
                      "sls_select_pages");
 }
 
@@ -220,6 +229,60 @@ sls_status sls_sparse_decode_attend(const sls_attn_desc* desc, const void* q, co
   return cuda_status(sls::launch_attend(s, q, k_cache, v_cache, page_idx, idx_stride, count, k_fixed, ctx_len,
                                         num_splits, o_part, m_part, l_part, (cudaStream_t)stream),
                      "sls_sparse_decode_attend");
+}
+
+int32_t sls_attend_default_splits(const sls_attn_desc* desc, int32_t max_entries) {
+  sls::Shape s;
+  if (check_desc(desc, &s) || max_entries < 1) return 1;
+  return sls::attend_default_splits(s, max_entries);
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+size_t sls_attend_combine_workspace_size(const sls_attn_desc* desc, int32_t num_splits) {
+  sls::Shape s;
+  if (check_desc(desc, &s) || num_splits < 1 || num_splits > 1024) return 0;
+  const size_t heads = (size_t)s.B * s.Hq * num_splits;
+  return align256((size_t)s.B * s.Hkv * 4) + align256(heads * s.D * 4) + 2 * align256(heads * 4);
+}
+
+sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const void* q, const void* k_cache,
+                                            const void* v_cache, const int32_t* page_idx, int32_t idx_stride,
+                                            const int32_t* count, int32_t k_fixed, const int32_t* ctx_len,
+                                            int32_t num_splits, const float* sink, void* out, float* lse,
+                                            void* workspace, size_t workspace_bytes, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(ctx_len); REQUIRE(out);
+  if (num_splits < 1 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [1, 1024]", num_splits);
+  if (page_idx) {
+    if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
+    if (!count && (k_fixed < 0 || k_fixed > idx_stride))
+      return fail(SLS_EINVAL, "k_fixed %d not in [0, idx_stride=%d]", k_fixed, idx_stride);
+  }
+  int64_t ctas;
+  if (!checked_mul((int64_t)s.B * s.Hkv, num_splits, &ctas) || ctas > INT32_MAX)
+    return fail(SLS_EOVERFLOW, "grid too large");
+  const size_t need = sls_attend_combine_workspace_size(desc, num_splits);
+  if (!workspace || workspace_bytes < need)
+    return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  char* w = static_cast<char*>(workspace);
+  const size_t heads = (size_t)s.B * s.Hq * num_splits;
+  sls::FusedCombine f;
+  f.tickets = reinterpret_cast<int32_t*>(w);
+  w += align256((size_t)s.B * s.Hkv * 4);
+  float* o_part = reinterpret_cast<float*>(w);
+  w += align256(heads * s.D * 4);
+  float* m_part = reinterpret_cast<float*>(w);
+  w += align256(heads * 4);
+  float* l_part = reinterpret_cast<float*>(w);
+  f.sink = sink;
+  f.out = out;
+  f.lse = lse;
+  return cuda_status(sls::launch_attend(s, q, k_cache, v_cache, page_idx, idx_stride, count, k_fixed, ctx_len,
+                                        num_splits, o_part, m_part, l_part, (cudaStream_t)stream, &f),
+                     "sls_sparse_decode_attend_combine");
 }
 
 sls_status sls_combine_splits(const sls_attn_desc* desc, const float* o_part, const float* m_part,

@@ -197,6 +197,7 @@ attend_cc_kernel(const AttendArgs a) {
       a.l_part[hq * a.S + split] = lv;
     }
   }
+  if (a.tickets) combine_row_if_last<T, D, NW * 32>(a, row);
 }
 
 // Stage two: one warp per (b, query head).  Lane s holds split s's max and
@@ -273,12 +274,42 @@ static cudaError_t attend_cc_g(const AttendArgs& a, int rows, cudaStream_t st) {
 }
 
 cudaError_t launch_attend_mma(const Shape& s, const AttendArgs& a, cudaStream_t st, bool* handled);
+const void* attend_mma_kernel_ptr();
+size_t attend_mma_kernel_smem();
+int attend_mma_kernel_threads();
+
+int attend_default_splits(const Shape& s, int max_entries) {
+  // one wave of attend CTAs over all rows (at most one CTA per slot), each
+  // slice at least 64 tokens
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    cudaFuncSetAttribute(attend_mma_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)attend_mma_kernel_smem());
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_mma_kernel_ptr(),
+                                                      attend_mma_kernel_threads(),
+                                                      attend_mma_kernel_smem()) != cudaSuccess)
+      per_sm = 1;
+  }
+  const int rows = s.B * s.Hkv;
+  const int slots = sm_count() * (per_sm > 0 ? per_sm : 1);
+  int S = slots / rows;
+  const int cap = (int)(((long long)max_entries << s.pshift) / 64);
+  if (S > cap) S = cap;
+  if (S < 1) S = 1;
+  if (S > 1024) S = 1024;
+  return S;
+}
 
 cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const void* v,
                           const int32_t* page_idx, int idx_stride, const int32_t* count,
                           int k_fixed, const int32_t* ctx_len, int num_splits,
-                          float* o_part, float* m_part, float* l_part, cudaStream_t st) {
+                          float* o_part, float* m_part, float* l_part, cudaStream_t st,
+                          const FusedCombine* fused) {
   AttendArgs a;
+  a.tickets = fused ? fused->tickets : nullptr;
+  a.sink = fused ? fused->sink : nullptr;
+  a.out = fused ? fused->out : nullptr;
+  a.lse = fused ? fused->lse : nullptr;
   a.q = q; a.k = k; a.v = v;
   a.page_idx = page_idx; a.count = count; a.ctx_len = ctx_len;
   a.o_part = o_part; a.m_part = m_part; a.l_part = l_part;

@@ -22,10 +22,11 @@ cudaError_t launch_thumb_build(const Shape& s, const void* k, const int32_t* ctx
 cudaError_t launch_thumb_update(const Shape& s, const void* k, const int32_t* pos,
                                 int block, uint8_t* codes, void* scales, cudaStream_t st);
 
+size_t select_pages_workspace(const Shape& s);
 cudaError_t launch_select_pages(const Shape& s, const void* q, const void* kmin,
                                 const void* kmax, const int32_t* ctx_len, int k,
                                 int n_sink_pages, int n_local_tokens, int32_t* page_idx,
-                                cudaStream_t st);
+                                void* ws, cudaStream_t st);
 
 size_t select_delta_workspace(const Shape& s, int block);
 cudaError_t launch_select_delta(const Shape& s, const void* q, const void* k,
@@ -34,16 +35,35 @@ cudaError_t launch_select_delta(const Shape& s, const void* q, const void* k,
                                 int32_t* count, int32_t* block_idx, int idx_stride,
                                 void* ws, cudaStream_t st);
 
+struct FusedCombine {
+  int32_t* tickets;
+  const float* sink;
+  void* out;
+  float* lse;
+};
+int attend_default_splits(const Shape& s, int max_entries);
 cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const void* v,
                           const int32_t* page_idx, int idx_stride, const int32_t* count,
                           int k_fixed, const int32_t* ctx_len, int num_splits,
-                          float* o_part, float* m_part, float* l_part, cudaStream_t st);
+                          float* o_part, float* m_part, float* l_part, cudaStream_t st,
+                          const FusedCombine* fused = nullptr);
 
 cudaError_t launch_combine(const Shape& s, const float* o_part, const float* m_part,
                            const float* l_part, int num_splits, const float* sink,
                            void* out, float* lse, cudaStream_t st);
 
-// Largest dynamic shared memory one select_pages CTA may use.
+// Streaming multiprocessors of the current device (cached per device).
+inline int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+  return cache[dev] > 0 ? cache[dev] : 1;
+}
+
+// Largest dynamic shared memory one top-k CTA may use, and the largest
+// cluster it may spread a row over.
 size_t select_pages_smem_limit();
 int select_pages_cluster();
 

@@ -1,22 +1,22 @@
-// Quest-style page selection, fused: page scores and the per-row top-k in
-// one launch ("Don't read the haystack", Part two: bound every page's
-// score by sum_c max(q_c*kmin_c, q_c*kmax_c), keep the top k plus the sink
-// page and the last local pages).
+// Quest-style page selection ("Don't read the haystack", Part two: bound
+// every page's score by sum_c max(q_c*kmin_c, q_c*kmax_c), keep the top k
+// plus the sink page and the last local pages).  Two kernels:
 //
-// One thread-block cluster of kCluster CTAs owns one (b, kv head) row.
-// Each CTA scores a contiguous chunk of the row's pages into shared memory
-// as order-preserving 32-bit keys, then the cluster runs an MSB-first radix
-// select (4 passes of 8-bit digits) whose histograms are summed across the
-// cluster through distributed shared memory.  The k-th key T and the number
-// of T-valued keys still to take come out of the passes; the chosen pages
-// are then written in ascending order, each CTA at an offset it derives from
-// the other CTAs' counts.  Ties on T go to the lowest page indices.
-//
-// Scoring of bf16 metadata runs on the tensor cores: for 16 pages at a time
-// the bound is U = [kmax | kmin] . [max(q,0) ; min(q,0)], a 16 x 2D by
-// 2D x 8 product (rows = pages, columns = the group's query heads) whose
-// A operand comes straight from 16-byte loads of the min/max rows.  fp32
-// metadata (and SLS_FLAG_CUDA_CORES) uses the CUDA-core scorer.
+// score   streams the page min/max metadata once and writes one
+//         order-preserving 32-bit key per page to a workspace.  bf16
+//         metadata is scored on the tensor cores: for 16 pages at a time
+//         U = [kmax | kmin] . [max(q,0) ; min(q,0)], a 16 x 2D by 2D x 8
+//         product (rows = pages, columns = the GQA group's query heads) whose
+//         A operand comes straight from 16-byte loads of the min/max rows;
+//         fp32 metadata (and SLS_FLAG_CUDA_CORES) uses a CUDA-core scorer.
+//         The grid is one wave of CTAs, each a contiguous run of one row.
+// topk    one CTA per row (or a cluster of CTAs for rows longer than one
+//         CTA's shared memory) loads the row's keys and runs an MSB-first
+//         radix select (4 passes of 8-bit digits; cluster histograms are
+//         summed through distributed shared memory).  The k-th key T and the
+//         count of T-valued keys still to take come out of the passes; the
+//         chosen pages are written in ascending order.  Ties on T go to the
+//         lowest page indices.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -27,13 +27,15 @@ namespace cg = cooperative_groups;
 
 namespace sls {
 
-constexpr int kCluster = 8;
 constexpr int kSelThreads = 256;     // CUDA-core scorer
 constexpr int kSelThreadsMma = 128;  // tensor-core scorer
+constexpr int kTopkThreads = 512;
+constexpr int kTopkMaxKeys = 32768;  // keys per top-k CTA (128 KB of shared memory)
+constexpr int kTopkMaxCluster = 8;
 constexpr uint32_t kForcedKey = 0xffffffffu;
 
-int select_pages_cluster() { return kCluster; }
-size_t select_pages_smem_limit() { return 200 * 1024; }
+int select_pages_cluster() { return kTopkMaxCluster; }
+size_t select_pages_smem_limit() { return (size_t)kTopkMaxKeys * 4; }
 
 struct SelectArgs {
   const void* q;
@@ -41,8 +43,10 @@ struct SelectArgs {
   const void* kmax;
   const int32_t* ctx_len;
   int32_t* page_idx;
+  uint32_t* keys;  // workspace [rows, Cap/P]
   int k, n_sink, n_local;
-  int Hq, Hkv, G, Cap, P, pshift;
+  int Hq, Hkv, G, Cap, P, pshift, npcap;
+  int chunk;       // pages per scoring CTA (multiple of 16)
 };
 
 // Exclusive scan of one int per thread over the CTA; `total` gets the sum.
@@ -251,21 +255,28 @@ struct TopkShared {
   int cnt[2];
 };
 
-// The cluster's k largest keys (ties to the lower index), written ascending
-// by page index to out[0 .. k).  keys[0 .. nloc) hold pages p0 + i.
-template <int NT>
-__device__ __forceinline__ void cluster_topk(cg::cluster_group& cl, const uint32_t* keys, int nloc,
-                                             int rank, int k, int p0, int32_t* out, TopkShared& sh) {
-  constexpr int BPT = 256 / NT;  // histogram bins per thread
+// The k largest keys of a row (ties to the lower index), written ascending
+// by page index to out[0 .. k).  keys[0 .. nloc) hold pages p0 + i; with
+// CL > 1 the row is spread over the CTAs of a cluster.
+template <int NT, int CL>
+__device__ __forceinline__ void row_topk(const uint32_t* keys, int nloc, int rank, int k, int p0,
+                                         int32_t* out, TopkShared& sh) {
+  constexpr int BPT = NT >= 256 ? 1 : 256 / NT;  // histogram bins per owner thread
   const int tid = threadIdx.x, lane = tid & 31;
+  const bool owner = tid * BPT < 256;
+  auto sync_all = [] {
+    if constexpr (CL > 1) cg::this_cluster().sync(); else __syncthreads();
+  };
   uint32_t prefix = 0, mask = 0;
   int rem = k;
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
     uint32_t* hb = sh.hist[pass & 1];
+    if (owner) {
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) hb[tid * BPT + i] = 0;
+      for (int i = 0; i < BPT; ++i) hb[tid * BPT + i] = 0;
+    }
     __syncthreads();
     for (int i0 = 0; i0 < nloc; i0 += NT) {
       const int i = i0 + tid;
@@ -278,28 +289,37 @@ __device__ __forceinline__ void cluster_topk(cg::cluster_group& cl, const uint32
         if (lane == __ffs(peers) - 1) atomicAdd(&hb[dig], (uint32_t)__popc(peers));
       }
     }
-    cl.sync();
-    // thread tid owns bins 255 - tid*BPT - i, i < BPT (descending)
+    sync_all();
+    // owner thread tid holds bins 255 - tid*BPT - i, i < BPT (descending)
     uint32_t tot[BPT];
     int sum = 0;
 #pragma unroll
     for (int i = 0; i < BPT; ++i) {
-      const int bin = 255 - tid * BPT - i;
       tot[i] = 0;
+      if (owner) {
+        const int bin = 255 - tid * BPT - i;
+        if constexpr (CL > 1) {
+          cg::cluster_group cl = cg::this_cluster();
 #pragma unroll
-      for (int q = 0; q < kCluster; ++q) tot[i] += cl.map_shared_rank(hb, q)[bin];
+          for (int q = 0; q < CL; ++q) tot[i] += cl.map_shared_rank(hb, q)[bin];
+        } else {
+          tot[i] = hb[bin];
+        }
+      }
       sum += (int)tot[i];
     }
     int total;
     int above = block_excl_scan<NT>(sum, sh.scan_tmp, total);  // keys with a larger digit
+    if (owner) {
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) {
-      const int incl = above + (int)tot[i];
-      if (incl >= rem && above < rem) {
-        sh.digit = (uint32_t)(255 - tid * BPT - i);
-        sh.rem = rem - above;
+      for (int i = 0; i < BPT; ++i) {
+        const int incl = above + (int)tot[i];
+        if (incl >= rem && above < rem) {
+          sh.digit = (uint32_t)(255 - tid * BPT - i);
+          sh.rem = rem - above;
+        }
+        above = incl;
       }
-      above = incl;
     }
     __syncthreads();
     prefix |= sh.digit << shift;
@@ -319,19 +339,23 @@ __device__ __forceinline__ void cluster_topk(cg::cluster_group& cl, const uint32
   int gt_tot, eq_tot;
   block_excl_scan<NT>(gt, sh.scan_tmp, gt_tot);
   const int eq_excl = block_excl_scan<NT>(eq, sh.scan_tmp, eq_tot);
-  if (tid == 0) {
-    sh.cnt[0] = gt_tot;
-    sh.cnt[1] = eq_tot;
-  }
-  cl.sync();
-  int out_off = 0, take = 0, eq_seen = 0;
-  for (int q = 0; q < kCluster; ++q) {
-    const int* rc = cl.map_shared_rank(sh.cnt, q);
-    const int g_r = rc[0], e_r = rc[1];
-    const int t_r = min(max(rem - eq_seen, 0), e_r);
-    if (q < rank) out_off += g_r + t_r;
-    if (q == rank) take = t_r;
-    eq_seen += e_r;
+  int out_off = 0, take = min(rem, eq_tot);
+  if constexpr (CL > 1) {
+    if (tid == 0) {
+      sh.cnt[0] = gt_tot;
+      sh.cnt[1] = eq_tot;
+    }
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    int eq_seen = 0;
+    for (int q = 0; q < CL; ++q) {
+      const int* rc = cl.map_shared_rank(sh.cnt, q);
+      const int g_r = rc[0], e_r = rc[1];
+      const int t_r = min(max(rem - eq_seen, 0), e_r);
+      if (q < rank) out_off += g_r + t_r;
+      if (q == rank) take = t_r;
+      eq_seen += e_r;
+    }
   }
   int nsel = 0, run = eq_excl;
   for (int i = i0; i < i1; ++i) {
@@ -348,85 +372,320 @@ __device__ __forceinline__ void cluster_topk(cg::cluster_group& cl, const uint32
     if (kk == Tk) f = run++ < take;
     if (f && pos < k) out[pos++] = p0 + i;
   }
-  cl.sync();  // peers may still read sh.cnt
+  if constexpr (CL > 1) cg::this_cluster().sync();  // peers may still read sh.cnt
 }
+
+// Fast path for a row held by one CTA (keys[0 .. n) with n > k): one
+// histogram of the keys' top 16 bits over a window of kWin values below the
+// largest non-forced key locates T's 16-bit bin; the few keys in that bin
+// are ranked exactly against each other; one pair scan then writes the
+// chosen pages in ascending order.  Returns false (having written nothing)
+// when T lies below the window or its bin holds more than kCand keys; the
+// caller then runs the general radix select.
+constexpr int kWin = 2048;
+constexpr int kCand = 1024;
+
+struct TopkFastShared {
+  uint32_t hist[kWin];
+  uint32_t cand[kCand];
+  int scan_tmp[32];
+  uint32_t red[32];
+  int ncand;
+  int bin;
+  int rem;
+  int take;
+  uint32_t T;
+  int ok;
+};
+
+template <int NT>
+__device__ __forceinline__ void block_pair_excl_scan(int a, int b, int* tmp, int& ea, int& eb) {
+  // scans two counts packed in one int: b in the low 16 bits, a above; the
+  // callers' totals stay below 2^15 (a) and 2^16 (b), so nothing carries
+  int tot;
+  const int e = block_excl_scan<NT>((a << 16) | b, tmp, tot);
+  ea = e >> 16;
+  eb = e & 0xffff;
+}
+
+template <int NT>
+__device__ __forceinline__ bool row_topk_fast(const uint32_t* keys, int n, int k, int32_t* out,
+                                              TopkFastShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NWp = NT / 32;
+  // 1. largest non-forced top-16 value and the number of forced keys
+  uint32_t mx = 0;
+  int nf = 0;
+  for (int i = tid; i < n; i += NT) {
+    const uint32_t kk = keys[i];
+    if (kk == kForcedKey) ++nf;
+    else mx = max(mx, kk >> 16);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    nf += __shfl_xor_sync(0xffffffffu, nf, o);
+  }
+  if (lane == 0) sh.red[warp] = mx | ((uint32_t)0);
+  if (lane == 0) sh.scan_tmp[warp] = nf;
+  for (int i = tid; i < kWin; i += NT) sh.hist[i] = 0;
+  if (tid == 0) sh.ncand = 0;
+  __syncthreads();
+  uint32_t top = 0;
+  int nforced = 0;
+#pragma unroll
+  for (int w = 0; w < NWp; ++w) {
+    top = max(top, sh.red[w]);
+    nforced += sh.scan_tmp[w];
+  }
+  __syncthreads();
+  const int need = k - nforced;  // non-forced keys to take (>= 0 by validation)
+  if (need <= 0) {
+    if (tid == 0) {
+      sh.T = kForcedKey;
+      sh.take = k;
+    }
+  } else {
+    // 2. window histogram: bin j counts keys whose top 16 bits equal top - j
+    for (int i = tid; i < n; i += NT) {
+      const uint32_t kk = keys[i];
+      if (kk == kForcedKey) continue;
+      const uint32_t j = top - (kk >> 16);
+      if (j < (uint32_t)kWin) atomicAdd(&sh.hist[j], 1u);
+    }
+    __syncthreads();
+    // 3. the bin holding the need-th largest (bins in increasing j)
+    constexpr int BPT = kWin / NT;
+    int c[BPT], sum = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      c[i] = (int)sh.hist[tid * BPT + i];
+      sum += c[i];
+    }
+    int total;
+    int above = block_excl_scan<NT>(sum, sh.scan_tmp, total);
+    if (tid == 0) sh.ok = total >= need;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      if (above < need && above + c[i] >= need) {
+        sh.bin = tid * BPT + i;
+        sh.rem = need - above;
+      }
+      above += c[i];
+    }
+    __syncthreads();
+    if (!sh.ok) return false;
+    // 4. collect the keys of that bin
+    const uint32_t t16 = top - (uint32_t)sh.bin;
+    for (int i = tid; i < n; i += NT) {
+      const uint32_t kk = keys[i];
+      if (kk != kForcedKey && (kk >> 16) == t16) {
+        const int slot = atomicAdd(&sh.ncand, 1);
+        if (slot < kCand) sh.cand[slot] = kk;
+      }
+    }
+    __syncthreads();
+    const int m = sh.ncand;
+    if (m > kCand) return false;  // uniform: every thread read the same count
+    // 5. exact rank inside the bin: T has fewer than rem larger keys and at
+    //    least rem keys >= it
+    const int rem = sh.rem;
+    for (int i = tid; i < m; i += NT) {
+      const uint32_t v = sh.cand[i];
+      int gt = 0, ge = 0;
+      for (int j = 0; j < m; ++j) {
+        gt += sh.cand[j] > v;
+        ge += sh.cand[j] >= v;
+      }
+      if (gt < rem && ge >= rem) {
+        sh.T = v;            // every writer writes the same value
+        sh.take = rem - gt;  // T-valued keys to take (same for all writers)
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t T = sh.T;
+  const int take = sh.take;
+  // 6. ascending output: position = (#keys > T before) + min(#T-keys before, take)
+  const int per_t = (n + NT - 1) / NT;
+  const int i0 = min(tid * per_t, n), i1 = min(i0 + per_t, n);
+  int gt = 0, eq = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t kk = keys[i];
+    gt += kk > T;
+    eq += kk == T;
+  }
+  int G, E;
+  block_pair_excl_scan<NT>(gt, eq, sh.scan_tmp, G, E);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t kk = keys[i];
+    if (kk > T) {
+      const int pos = G + min(E, take);
+      if (pos < k) out[pos] = i;
+      ++G;
+    } else if (kk == T) {
+      if (E < take && G + E < k) out[G + E] = i;
+      ++E;
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- kernels
 
 // MODE 0: CUDA-core scorer (any dtype); 1: tensor-core scorer (bf16, P > 1);
 // 2: tensor-core scorer of one-token pages (bf16, P == 1).
+// Grid (CTAs per row, rows); CTA c scores pages [c*chunk, (c+1)*chunk).
 template <typename T, int D, int GM, int MODE>
-__global__ void __cluster_dims__(kCluster, 1, 1)
-__launch_bounds__(MODE == 0 ? kSelThreads : kSelThreadsMma)
-select_pages_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(MODE == 0 ? kSelThreads : kSelThreadsMma)
+quest_score_kernel(const SelectArgs a) {
   constexpr int NT = MODE == 0 ? kSelThreads : kSelThreadsMma;
-  extern __shared__ uint32_t keys[];
-  __shared__ TopkShared sh;
-
-  cg::cluster_group cl = cg::this_cluster();
-  const int rank = (int)cl.block_rank();
-  const int tid = threadIdx.x;
-  const int row = blockIdx.x / kCluster;
+  const int row = blockIdx.y;
   const int b = row / a.Hkv, h = row % a.Hkv;
   const int N = clamp_len(a.ctx_len[b], a.Cap);
   const int NP = (N + a.P - 1) >> a.pshift;
-  int32_t* out = a.page_idx + (size_t)row * a.k;
-
-  if (NP <= a.k) {  // the budget covers every page: no ranking needed
-    for (int i = rank * NT + tid; i < a.k; i += NT * kCluster) out[i] = i < NP ? i : -1;
-    return;
-  }
-  const int chunk = (NP + kCluster - 1) / kCluster;
-  const int p0 = rank * chunk;
-  const int nloc = max(min(chunk, NP - p0), 0);
+  if (NP <= a.k) return;  // the top-k kernel lists every page
+  const int p0 = blockIdx.x * a.chunk;
+  const int nloc = min(a.chunk, NP - p0);
+  if (nloc <= 0) return;
   const int first_local = a.n_local > 0 ? (max(N - a.n_local, 0) >> a.pshift) : NP;
+  uint32_t* keys = a.keys + (size_t)row * a.npcap + p0;
   if constexpr (MODE == 0) {
     score_chunk<T, D, GM>(a, row, b, h, p0, nloc, first_local, keys);
   } else {
     score_chunk_mma<D, MODE == 2, NT>(a, row, b, h, p0, nloc, first_local, keys);
   }
-  __syncthreads();
-  cluster_topk<NT>(cl, keys, nloc, rank, a.k, p0, out, sh);
 }
 
+template <int CL>
+__global__ void __launch_bounds__(kTopkThreads)
+topk_kernel(const SelectArgs a) {
+  extern __shared__ uint32_t skeys[];
+  __shared__ union {
+    TopkShared radix;
+    TopkFastShared fast;
+  } sh;
+  const int rank = CL > 1 ? (int)cg::this_cluster().block_rank() : 0;
+  const int row = blockIdx.x / CL;
+  const int b = row / a.Hkv;
+  const int N = clamp_len(a.ctx_len[b], a.Cap);
+  const int NP = (N + a.P - 1) >> a.pshift;
+  int32_t* out = a.page_idx + (size_t)row * a.k;
+  if (NP <= a.k) {  // the budget covers every page: no ranking needed
+    for (int i = rank * kTopkThreads + threadIdx.x; i < a.k; i += kTopkThreads * CL) out[i] = i < NP ? i : -1;
+    return;
+  }
+  const int chunk = (NP + CL - 1) / CL;
+  const int p0 = rank * chunk;
+  const int nloc = max(min(chunk, NP - p0), 0);
+  const uint32_t* src = a.keys + (size_t)row * a.npcap + p0;
+  for (int i = threadIdx.x; i < nloc; i += kTopkThreads) skeys[i] = src[i];
+  __syncthreads();
+  if constexpr (CL == 1) {
+    if (row_topk_fast<kTopkThreads>(skeys, nloc, a.k, out, sh.fast)) return;
+    __syncthreads();
+  }
+  row_topk<kTopkThreads, CL>(skeys, nloc, rank, a.k, p0, out, sh.radix);
+}
+
+// ---------------------------------------------------------------- launches
+
 template <typename T, int D, int GM, int MODE>
-static cudaError_t select_launch(const SelectArgs& a, int rows, size_t smem, cudaStream_t st) {
-  auto kern = select_pages_kernel<T, D, GM, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+static cudaError_t score_launch(const SelectArgs& a, int rows, cudaStream_t st) {
+  auto kern = quest_score_kernel<T, D, GM, MODE>;
+  constexpr int NT = MODE == 0 ? kSelThreads : kSelThreadsMma;
+  static int per_sm = 0;  // resident CTAs per SM of this kernel (same on every GB300)
+  if (per_sm == 0) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NT, 0);
+  SelectArgs b = a;
+  const int slots = max(1, sm_count() * max(per_sm, 1));
+  const int cpr = max(1, slots / rows);  // at most one wave over all rows
+  b.chunk = max(16, ((a.npcap + cpr - 1) / cpr + 15) / 16 * 16);
+  dim3 grid((a.npcap + b.chunk - 1) / b.chunk, rows);
+  kern<<<grid, NT, 0, st>>>(b);
+  return cudaGetLastError();
+}
+
+static cudaError_t topk_launch(const SelectArgs& a, int rows, cudaStream_t st) {
+  int cl = 1;
+  while (cl < kTopkMaxCluster && (a.npcap + cl - 1) / cl > kTopkMaxKeys) cl *= 2;
+  const size_t smem = (size_t)((a.npcap + cl - 1) / cl) * sizeof(uint32_t);
+  cudaError_t e;
+  if (cl == 1) {
+    e = cudaFuncSetAttribute(topk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<1><<<rows, kTopkThreads, smem, st>>>(a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(rows * cl);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  switch (cl) {
+    case 2:
+      e = cudaFuncSetAttribute(topk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, topk_kernel<2>, a);
+      break;
+    case 4:
+      e = cudaFuncSetAttribute(topk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, topk_kernel<4>, a);
+      break;
+    default:
+      e = cudaFuncSetAttribute(topk_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, topk_kernel<8>, a);
+      break;
+  }
   if (e != cudaSuccess) return e;
-  kern<<<rows * kCluster, MODE == 0 ? kSelThreads : kSelThreadsMma, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-static cudaError_t select_g(const SelectArgs& a, int rows, size_t smem, cudaStream_t st) {
-  if (a.G <= 1) return select_launch<T, D, 1, 0>(a, rows, smem, st);
-  if (a.G <= 2) return select_launch<T, D, 2, 0>(a, rows, smem, st);
-  if (a.G <= 4) return select_launch<T, D, 4, 0>(a, rows, smem, st);
-  return select_launch<T, D, 8, 0>(a, rows, smem, st);
+static cudaError_t score_g(const SelectArgs& a, int rows, cudaStream_t st) {
+  if (a.G <= 1) return score_launch<T, D, 1, 0>(a, rows, st);
+  if (a.G <= 2) return score_launch<T, D, 2, 0>(a, rows, st);
+  if (a.G <= 4) return score_launch<T, D, 4, 0>(a, rows, st);
+  return score_launch<T, D, 8, 0>(a, rows, st);
 }
 
 template <int D>
-static cudaError_t select_mma(const SelectArgs& a, int rows, size_t smem, cudaStream_t st) {
-  if (a.P == 1) return select_launch<bf16, D, 8, 2>(a, rows, smem, st);
-  return select_launch<bf16, D, 8, 1>(a, rows, smem, st);
+static cudaError_t score_mma(const SelectArgs& a, int rows, cudaStream_t st) {
+  if (a.P == 1) return score_launch<bf16, D, 8, 2>(a, rows, st);
+  return score_launch<bf16, D, 8, 1>(a, rows, st);
+}
+
+size_t select_pages_workspace(const Shape& s) {
+  const size_t bytes = (size_t)s.B * s.Hkv * (size_t)(s.Cap >> s.pshift) * sizeof(uint32_t);
+  return (bytes + 255) & ~(size_t)255;
 }
 
 cudaError_t launch_select_pages(const Shape& s, const void* q, const void* kmin,
                                 const void* kmax, const int32_t* ctx_len, int k,
                                 int n_sink_pages, int n_local_tokens, int32_t* page_idx,
-                                cudaStream_t st) {
+                                void* ws, cudaStream_t st) {
   SelectArgs a;
   a.q = q; a.kmin = kmin; a.kmax = kmax; a.ctx_len = ctx_len; a.page_idx = page_idx;
+  a.keys = static_cast<uint32_t*>(ws);
   a.k = k; a.n_sink = n_sink_pages; a.n_local = n_local_tokens;
   a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.G; a.Cap = s.Cap; a.P = s.P; a.pshift = s.pshift;
-  const int npcap = s.Cap >> s.pshift;
-  const size_t chunk = (size_t)(npcap + kCluster - 1) / kCluster;
-  const size_t smem = chunk * sizeof(uint32_t) < 16 ? 16 : chunk * sizeof(uint32_t);
+  a.npcap = s.Cap >> s.pshift;
+  a.chunk = 0;
   const int rows = s.B * s.Hkv;
+  cudaError_t e;
   if (s.dtype == 1 && !(s.flags & 1))
-    return s.D == 64 ? select_mma<64>(a, rows, smem, st) : select_mma<128>(a, rows, smem, st);
-  if (s.dtype == 0)
-    return s.D == 64 ? select_g<float, 64>(a, rows, smem, st) : select_g<float, 128>(a, rows, smem, st);
-  return s.D == 64 ? select_g<bf16, 64>(a, rows, smem, st) : select_g<bf16, 128>(a, rows, smem, st);
+    e = s.D == 64 ? score_mma<64>(a, rows, st) : score_mma<128>(a, rows, st);
+  else if (s.dtype == 0)
+    e = s.D == 64 ? score_g<float, 64>(a, rows, st) : score_g<float, 128>(a, rows, st);
+  else
+    e = s.D == 64 ? score_g<bf16, 64>(a, rows, st) : score_g<bf16, 128>(a, rows, st);
+  if (e != cudaSuccess) return e;
+  return topk_launch(a, rows, st);
 }
 
 }  // namespace sls

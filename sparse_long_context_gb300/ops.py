@@ -7,7 +7,6 @@ nothing).
 from __future__ import annotations
 
 import ctypes
-import math
 from typing import Optional
 
 import torch
@@ -49,13 +48,9 @@ def desc_for(k_cache: torch.Tensor, num_q_heads: int, page_size: int, scale: flo
     return make_desc(B, num_q_heads, Hkv, D, page_size, Cap, k_cache.dtype, scale, cuda_cores)
 
 
-def default_splits(rows: int, max_entries: int, page_size: int, device=None) -> int:
-    """Splits per row: enough CTAs to cover the SMs about four times, each
-    slice holding at least 64 tokens."""
-    sms = torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count
-    want = max(1, math.ceil(4 * sms / max(rows, 1)))
-    cap = max(1, (max_entries * page_size) // 64)
-    return int(max(1, min(want, cap, 1024)))
+def default_splits(desc: L.AttnDesc, max_entries: int) -> int:
+    """The library's split count: one wave of attend CTAs, >= 64 tokens each."""
+    return int(L.load().sls_attend_default_splits(ctypes.byref(desc), int(max_entries)))
 
 
 # ----------------------------------------------------------------- metadata
@@ -103,14 +98,21 @@ def thumb_update(desc: L.AttnDesc, k_cache, pos, block: int, codes, scales):
 
 # ---------------------------------------------------------------- selection
 
+def select_pages_workspace(desc: L.AttnDesc, device="cuda"):
+    n = L.load().sls_select_pages_workspace_size(ctypes.byref(desc))
+    return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
 def select_pages(desc: L.AttnDesc, q, kmin, kmax, ctx_len, k: int, n_sink_pages: int = 0,
-                 n_local_tokens: int = 0, out=None):
+                 n_local_tokens: int = 0, out=None, workspace=None):
     _need(q, "q")
     rows = desc.batch * desc.num_kv_heads
     out = torch.empty((rows, k), dtype=torch.int32, device=q.device) if out is None else out
     _need(out, "page_idx", torch.int32, (rows, k))
+    workspace = select_pages_workspace(desc, q.device) if workspace is None else workspace
     L.call("sls_select_pages", ctypes.byref(desc), _ptr(q), _ptr(kmin), _ptr(kmax), _ptr(ctx_len),
-           int(k), int(n_sink_pages), int(n_local_tokens), _ptr(out), _stream())
+           int(k), int(n_sink_pages), int(n_local_tokens), _ptr(out), _ptr(workspace),
+           workspace.numel(), _stream())
     return out
 
 
@@ -158,6 +160,35 @@ def sparse_decode_attend(desc: L.AttnDesc, q, k_cache, v_cache, page_idx, ctx_le
     return o, m, l
 
 
+def attend_combine_workspace(desc: L.AttnDesc, num_splits: int, device="cuda"):
+    """Zero-filled workspace of sparse_decode_attend_combine (reusable)."""
+    n = L.load().sls_attend_combine_workspace_size(ctypes.byref(desc), int(num_splits))
+    return torch.zeros(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
+def sparse_decode_attend_combine(desc: L.AttnDesc, q, k_cache, v_cache, page_idx, ctx_len,
+                                 num_splits: int, count=None, k_fixed: Optional[int] = None,
+                                 sink=None, out=None, lse=None, workspace=None, want_lse: bool = True):
+    """Attend and combine in one launch; returns (out, lse)."""
+    _need(q, "q")
+    _need(k_cache, "k_cache")
+    _need(v_cache, "v_cache")
+    B, Hq, D = desc.batch, desc.num_q_heads, desc.head_dim
+    dtype = torch.bfloat16 if desc.dtype == L.SLS_DTYPE_BF16 else torch.float32
+    out = torch.empty((B, Hq, D), dtype=dtype, device=q.device) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, (Hq,))
+    workspace = attend_combine_workspace(desc, num_splits, q.device) if workspace is None else workspace
+    stride = int(page_idx.shape[1]) if page_idx is not None else 0
+    kf = stride if k_fixed is None else int(k_fixed)
+    L.call("sls_sparse_decode_attend_combine", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+           _ptr(page_idx), stride, _ptr(count), kf, _ptr(ctx_len), int(num_splits), _ptr(sink),
+           _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream())
+    return out, lse
+
+
 def combine_splits(desc: L.AttnDesc, parts, sink=None, out=None, lse=None, want_lse: bool = True):
     o, m, l = parts
     B, Hq, S, D = o.shape
@@ -179,23 +210,30 @@ class QuestDecode:
     buffers, so the three launches can be captured in a CUDA graph."""
 
     def __init__(self, desc: L.AttnDesc, k_budget: int, n_sink_pages: int, n_local_tokens: int,
-                 num_splits: Optional[int] = None, device="cuda"):
+                 num_splits: Optional[int] = None, device="cuda", fused: bool = True):
         self.desc = desc
         self.k = int(k_budget)
         self.n_sink, self.n_local = int(n_sink_pages), int(n_local_tokens)
+        self.fused = fused
         rows = desc.batch * desc.num_kv_heads
-        self.S = num_splits or default_splits(rows, self.k, desc.page_size, device)
+        self.S = num_splits or default_splits(desc, self.k)
         self.page_idx = torch.empty((rows, self.k), dtype=torch.int32, device=device)
+        self.workspace = select_pages_workspace(desc, device)
         self.parts = partials(desc, self.S, device)
+        self.ac_workspace = attend_combine_workspace(desc, self.S, device)
         dtype = torch.bfloat16 if desc.dtype == L.SLS_DTYPE_BF16 else torch.float32
         self.out = torch.empty((desc.batch, desc.num_q_heads, desc.head_dim), dtype=dtype, device=device)
         self.lse = torch.empty((desc.batch, desc.num_q_heads), dtype=torch.float32, device=device)
 
     def select(self, q, kmin, kmax, ctx_len):
         return select_pages(self.desc, q, kmin, kmax, ctx_len, self.k, self.n_sink, self.n_local,
-                            out=self.page_idx)
+                            out=self.page_idx, workspace=self.workspace)
 
     def attend(self, q, k_cache, v_cache, ctx_len, sink=None):
+        if self.fused:
+            return sparse_decode_attend_combine(self.desc, q, k_cache, v_cache, self.page_idx, ctx_len,
+                                                self.S, sink=sink, out=self.out, lse=self.lse,
+                                                workspace=self.ac_workspace)
         sparse_decode_attend(self.desc, q, k_cache, v_cache, self.page_idx, ctx_len, self.S,
                              parts=self.parts)
         return combine_splits(self.desc, self.parts, sink, out=self.out, lse=self.lse)
@@ -209,17 +247,19 @@ class DeltaDecode:
     """One top-delta decode step (select_delta + attend + combine)."""
 
     def __init__(self, desc: L.AttnDesc, block: int, delta: float, num_splits: Optional[int] = None,
-                 device="cuda"):
+                 device="cuda", fused: bool = True):
         if desc.page_size != block:
             raise ValueError("attend page_size must equal the thumbnail block")
         self.desc, self.block, self.delta = desc, int(block), float(delta)
+        self.fused = fused
         rows = desc.batch * desc.num_kv_heads
         nblk = desc.capacity // block
-        self.S = num_splits or default_splits(rows, nblk, block, device)
+        self.S = num_splits or default_splits(desc, nblk)
         self.count = torch.empty(rows, dtype=torch.int32, device=device)
         self.block_idx = torch.empty((rows, nblk), dtype=torch.int32, device=device)
         self.workspace = select_delta_workspace(desc, block, device)
         self.parts = partials(desc, self.S, device)
+        self.ac_workspace = attend_combine_workspace(desc, self.S, device)
         dtype = torch.bfloat16 if desc.dtype == L.SLS_DTYPE_BF16 else torch.float32
         self.out = torch.empty((desc.batch, desc.num_q_heads, desc.head_dim), dtype=dtype, device=device)
         self.lse = torch.empty((desc.batch, desc.num_q_heads), dtype=torch.float32, device=device)
@@ -229,6 +269,10 @@ class DeltaDecode:
                             count=self.count, block_idx=self.block_idx, workspace=self.workspace)
 
     def attend(self, q, k_cache, v_cache, ctx_len, sink=None):
+        if self.fused:
+            return sparse_decode_attend_combine(self.desc, q, k_cache, v_cache, self.block_idx, ctx_len,
+                                                self.S, count=self.count, sink=sink, out=self.out,
+                                                lse=self.lse, workspace=self.ac_workspace)
         sparse_decode_attend(self.desc, q, k_cache, v_cache, self.block_idx, ctx_len, self.S,
                              count=self.count, parts=self.parts)
         return combine_splits(self.desc, self.parts, sink, out=self.out, lse=self.lse)

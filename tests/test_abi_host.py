@@ -73,8 +73,10 @@ def test_null_arguments(lib):
 
 def test_select_pages_validation(lib):
     d = desc()
-    sel = lambda k, ns, nl, kmin=BAD, kmax=BAD, dd=d: lib.sls_select_pages(
-        ctypes.byref(dd), BAD, kmin, kmax, BAD, k, ns, nl, BAD, None)
+    ws = lib.sls_select_pages_workspace_size(ctypes.byref(d))
+    assert ws == 2 * 2 * 64 * 4
+    sel = lambda k, ns, nl, kmin=BAD, kmax=BAD, dd=d, wsb=1 << 40: lib.sls_select_pages(
+        ctypes.byref(dd), BAD, kmin, kmax, BAD, k, ns, nl, BAD, BAD, wsb, None)
     assert sel(0, 0, 0) == L.SLS_EINVAL                  # k < 1
     assert sel(65, 0, 0) == L.SLS_EINVAL                 # k > Cap/P = 64
     assert sel(4, 1, 64) == L.SLS_EINVAL                 # forced pages do not fit
@@ -84,6 +86,7 @@ def test_select_pages_validation(lib):
     assert sel(8, 4, 0, kmin=BAD, kmax=ctypes.c_void_p(0x2000), dd=d1) == L.SLS_EINVAL
     big = desc(page_size=1, capacity=1 << 22)            # 4M pages per row > supported
     assert sel(8, 0, 0, dd=big) == L.SLS_EUNSUPPORTED
+    assert sel(8, 0, 0, wsb=ws - 1) == L.SLS_EWORKSPACE
 
 
 def test_select_delta_validation_and_workspace(lib):
@@ -110,6 +113,20 @@ def test_attend_validation(lib):
     assert att(stride=0) == L.SLS_EINVAL
     assert att(kf=9) == L.SLS_EINVAL
     assert att(kf=-1) == L.SLS_EINVAL
+
+
+def test_attend_combine_validation(lib):
+    d = desc()
+    ws = lib.sls_attend_combine_workspace_size(ctypes.byref(d), 4)
+    # tickets (2*2 rows) + o_part (2*8*4*128 floats) + m and l (2*8*4 floats each), 256-aligned
+    assert ws == 256 + 2 * 8 * 4 * 128 * 4 + 2 * 256
+    assert lib.sls_attend_combine_workspace_size(ctypes.byref(d), 0) == 0
+    call = lambda S=4, wsb=ws, out=BAD: lib.sls_sparse_decode_attend_combine(
+        ctypes.byref(d), BAD, BAD, BAD, BAD, 8, None, 8, BAD, S, None, out, None, BAD, wsb, None)
+    assert call(S=0) == L.SLS_EINVAL
+    assert call(out=None) == L.SLS_EINVAL
+    assert call(wsb=ws - 1) == L.SLS_EWORKSPACE
+    assert lib.sls_attend_default_splits(None, 8) == 1
 
 
 def test_python_layer_raises_on_status(lib):

@@ -177,6 +177,67 @@ def test_delta_step_small(key):
     print(f"{key}: kept fraction {kept:.3f}, boundary ties {ties}")
 
 
+@pytest.mark.parametrize("key", ["qwen7b_ragged", "gptoss_ragged"])
+def test_fused_and_separate_combine_agree_and_reuse_workspace(key):
+    s = quest_case(key)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    step = PT.H.make_step(dw, fused=True)
+    outs = []
+    for _ in range(3):  # the arrival tickets must be back at zero after every call
+        o, l = step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx, dw.sink)
+        outs.append((o.float().clone(), l.clone()))
+    sel, _, out_sep, lse_sep = PT.run_step(dw, fused=False)
+    for o, l in outs:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    check_all_rows(s, host, sel, None, outs[0][0].cpu().numpy().astype(np.float64),
+                   outs[0][1].cpu().numpy().astype(np.float64))
+    check_all_rows(s, host, sel, None, out_sep, lse_sep)
+    assert np.abs(outs[0][0].cpu().numpy() - out_sep).max() < 2e-2
+
+
+def _bits(x):
+    from sparse_long_context_gb300.workloads import round_to_bf16_bits
+    return round_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def test_topk_exact_ties_go_to_lower_pages():
+    """Pages repeat a few key patterns, so many bounds are exactly equal."""
+    s = W.spec("qwen7b", batch=1, ctx_len=[8192])
+    host = W.generate(s)
+    pat = host.K[0, :, :4 * 16].copy()                      # 4 distinct pages per row
+    for p in range(1, 512):
+        host.K[0, :, p * 16:(p + 1) * 16] = pat[:, (p % 4) * 16:(p % 4 + 1) * 16]
+    dw = PT.upload(s, host)
+    sel, cnt, out, lse = PT.run_step(dw)
+    for h in range(s.num_kv_heads):
+        orc = PT.oracle_row(s, host, 0, h)
+        assert np.array_equal(sel[h], orc.pages), h   # equal scores: no tolerance needed
+
+
+def test_topk_scores_spanning_many_octaves():
+    """Bounds spread over far more than 16 octaves: the k-th score lies below
+    the fast path's window and the general radix select decides."""
+    s = W.spec("qwen7b", batch=1, ctx_len=[8192])
+    s.k_pages = 256
+    host = W.generate(s)
+    K = W.bf16_bits_to_f32(host.K[0]).copy()
+    q = W.bf16_bits_to_f32(host.q[0])
+    for h in range(s.num_kv_heads):
+        g = np.abs(q[h * s.group:(h + 1) * s.group]).mean(axis=0)
+        sgn = np.sign(q[h * s.group])                        # keys aligned with head 0's query
+        base = np.abs(K[h]) * sgn[None, :]
+        scale = np.exp2(-(np.arange(8192) // 16) / 8.0).astype(np.float32)[:, None]
+        K[h] = base * scale
+    host.K[0] = _bits(K)
+    dw = PT.upload(s, host)
+    sel, _, out, lse = PT.run_step(dw)
+    for h in range(s.num_kv_heads):
+        orc = PT.oracle_row(s, host, 0, h)
+        t = PT.check_quest_list(sel[h], orc, 8192, 16, s.k_pages)
+        assert t <= 2
+
+
 @pytest.mark.parametrize("splits", [1, 3, 64, 1024])
 def test_split_counts_do_not_change_the_result(splits):
     s = W.spec("qwen7b", batch=2, ctx_len=[2000, 33], capacity=2048)
