@@ -194,6 +194,31 @@ sls_status sls_select_pages(const sls_attn_desc* desc, const void* q,
  * descriptor is invalid). */
 size_t sls_select_pages_workspace_size(const sls_attn_desc* desc);
 
+/*
+ * sls_select_pages without a workspace argument, for callers that cannot
+ * allocate device memory for one (for example a plugin whose host framework
+ * only passes it input and output tensors, or a process whose memory is all
+ * reserved up front so that a cudaMalloc during decoding would fail or stall
+ * the device).  It is not an operation of the source pages: only the origin
+ * of the scratch differs.  The per-page keys go to a 4 MiB array compiled
+ * into the library (held on every device that loads it, until exit) instead
+ * of a caller buffer; the call allocates nothing.
+ *   Arguments, results and validation: as sls_select_pages.
+ *   Shapes whose keys need more than 4 MiB (sls_select_pages_workspace_size)
+ *   return SLS_EWORKSPACE and enqueue nothing.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before capturing a stream.
+ *   All calls share the array: calls whose kernels may overlap on the GPU
+ *   (other streams, other host threads) race on it and must be serialised
+ *   by the caller.  No part of it needs to be zero.
+ */
+sls_status sls_select_pages_static(const sls_attn_desc* desc, const void* q,
+                                   const void* kmin, const void* kmax,
+                                   const int32_t* ctx_len, int32_t k,
+                                   int32_t n_sink_pages, int32_t n_local_tokens,
+                                   int32_t* page_idx, void* stream);
+
 /* Bytes of workspace sls_select_delta needs for this descriptor/block. */
 size_t sls_select_delta_workspace_size(const sls_attn_desc* desc, int32_t block);
 

@@ -32,6 +32,7 @@ SIGNATURES = {
     "sls_thumb_update": (_I, [_D, _P, _P, _I, _P, _P, _P]),
     "sls_select_pages": (_I, [_D, _P, _P, _P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P]),
     "sls_select_pages_workspace_size": (ctypes.c_size_t, [_D]),
+    "sls_select_pages_static": (_I, [_D, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "sls_select_delta_workspace_size": (ctypes.c_size_t, [_D, _I]),
     "sls_select_delta": (_I, [_D, _P, _P, _P, _P, _P, _I, ctypes.c_float, _P, _P, _I, _P,
                               ctypes.c_size_t, _P]),

@@ -82,6 +82,15 @@ sls_status check_desc(const sls_attn_desc* d, sls::Shape* s) {
   return SLS_OK;
 }
 
+}  // namespace
+
+namespace sls {
+// Records a failure message for sls_last_error() from another translation unit.
+sls_status record_error(sls_status code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace sls
+
+namespace {
+
 #define REQUIRE(ptr) \
   if (!(ptr)) return fail(SLS_EINVAL, "%s is NULL", #ptr)
 
