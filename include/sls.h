@@ -299,13 +299,15 @@ sls_status sls_combine_splits(const sls_attn_desc* desc, const float* o_part,
  */
 int32_t sls_attend_default_splits(const sls_attn_desc* desc, int32_t max_entries);
 
-/* Bytes of workspace sls_sparse_decode_attend_combine needs. */
+/* Bytes of workspace sls_sparse_decode_attend_combine needs (num_splits 0:
+ * the library's own schedule on the current device). */
 size_t sls_attend_combine_workspace_size(const sls_attn_desc* desc,
                                          int32_t num_splits);
 
 /*
  * Both stages in one launch: sls_sparse_decode_attend followed, inside the
- * same kernel, by the combine of each row.  Every CTA of a row takes an
+ * same kernel, by the combine of each row.  num_splits == 0 lets the library
+ * pick the split count (sls_attend_default_splits).  Every CTA of a row takes an
  * arrival ticket after writing its partials; the CTA that arrives last
  * merges the row's splits exactly as sls_combine_splits does (no CTA ever
  * waits for another).  Arguments as in the two separate calls; the partials

@@ -250,7 +250,8 @@ static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 size_t sls_attend_combine_workspace_size(const sls_attn_desc* desc, int32_t num_splits) {
   sls::Shape s;
-  if (check_desc(desc, &s) || num_splits < 1 || num_splits > 1024) return 0;
+  if (check_desc(desc, &s) || num_splits < 0 || num_splits > 1024) return 0;
+  if (num_splits == 0) num_splits = sls::max_auto_splits(s);
   const size_t heads = (size_t)s.B * s.Hq * num_splits;
   return align256((size_t)s.B * s.Hkv * 4) + align256(heads * s.D * 4) + 2 * align256(heads * 4);
 }
@@ -264,7 +265,7 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
   sls_status r = check_desc(desc, &s);
   if (r) return r;
   REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(ctx_len); REQUIRE(out);
-  if (num_splits < 1 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [1, 1024]", num_splits);
+  if (num_splits < 0 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [0, 1024]", num_splits);
   if (page_idx) {
     if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
     if (!count && (k_fixed < 0 || k_fixed > idx_stride))
@@ -277,7 +278,7 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
   char* w = static_cast<char*>(workspace);
-  const size_t heads = (size_t)s.B * s.Hq * num_splits;
+  const size_t heads = (size_t)s.B * s.Hq * (num_splits ? num_splits : sls::max_auto_splits(s));
   sls::FusedCombine f;
   f.tickets = reinterpret_cast<int32_t*>(w);
   w += align256((size_t)s.B * s.Hkv * 4);

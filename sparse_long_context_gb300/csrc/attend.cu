@@ -19,6 +19,7 @@ namespace sls {
 template <typename T, int D, int GM, int NW>
 __global__ void __launch_bounds__(NW * 32)
 attend_cc_kernel(const AttendArgs a) {
+  pdl_wait_then_release();
   constexpr int EPL = Vec16<T>::N;
   constexpr int L = D / EPL;
   constexpr int TPW = 32 / L;
@@ -197,7 +198,7 @@ attend_cc_kernel(const AttendArgs a) {
       a.l_part[hq * a.S + split] = lv;
     }
   }
-  if (a.tickets) combine_row_if_last<T, D, NW * 32>(a, row);
+  if (a.tickets) combine_row_if_last<T, D, NW * 32>(a, row, a.S);
 }
 
 // Stage two: one warp per (b, query head).  Lane s holds split s's max and
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(128)
 combine_kernel(const float* __restrict__ o_part, const float* __restrict__ m_part,
                const float* __restrict__ l_part, int S, const float* __restrict__ sink,
                T* __restrict__ out, float* __restrict__ lse, int Hq, int total) {
+  pdl_wait_then_release();
   constexpr int CPL = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int idx = blockIdx.x * 4 + warp;
@@ -261,7 +263,8 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ m_par
 template <typename T, int D, int GM>
 static cudaError_t attend_cc(const AttendArgs& a, int rows, cudaStream_t st) {
   constexpr int NW = 4;
-  attend_cc_kernel<T, D, GM, NW><<<rows * a.S, NW * 32, 0, st>>>(a);
+  cudaError_t e = launch_pdl(attend_cc_kernel<T, D, GM, NW>, dim3(rows * a.S), dim3(NW * 32), 0, st, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -277,6 +280,12 @@ cudaError_t launch_attend_mma(const Shape& s, const AttendArgs& a, cudaStream_t 
 const void* attend_mma_kernel_ptr();
 size_t attend_mma_kernel_smem();
 int attend_mma_kernel_threads();
+
+int max_auto_splits(const Shape& s) {
+  // splits per row the library may choose by itself (sizes the workspace)
+  const int rows = s.B * s.Hkv;
+  return (2 * sm_count() + rows - 1) / rows;
+}
 
 int attend_default_splits(const Shape& s, int max_entries) {
   // one wave of attend CTAs over all rows (at most one CTA per slot), each
@@ -314,6 +323,11 @@ cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const vo
   a.page_idx = page_idx; a.count = count; a.ctx_len = ctx_len;
   a.o_part = o_part; a.m_part = m_part; a.l_part = l_part;
   a.idx_stride = idx_stride; a.k_fixed = k_fixed; a.S = num_splits;
+  if (num_splits == 0) {  // the library schedules (fused call only)
+    const int entries = page_idx ? (count ? idx_stride : k_fixed) : (s.Cap >> s.pshift);
+    a.S = attend_default_splits(s, entries > 0 ? entries : 1);
+    if (a.S > max_auto_splits(s)) a.S = max_auto_splits(s);
+  }
   a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.G; a.Cap = s.Cap; a.P = s.P; a.pshift = s.pshift;
   a.qscale = s.scale * kLog2e;
   const int rows = s.B * s.Hkv;
@@ -333,21 +347,23 @@ cudaError_t launch_combine(const Shape& s, const float* o_part, const float* m_p
                            void* out, float* lse, cudaStream_t st) {
   const int total = s.B * s.Hq;
   const int grid = (total + 3) / 4;
+  cudaError_t e;
   if (s.dtype == 0) {
     if (s.D == 64)
-      combine_kernel<float, 64><<<grid, 128, 0, st>>>(o_part, m_part, l_part, num_splits, sink,
-                                                      static_cast<float*>(out), lse, s.Hq, total);
+      e = launch_pdl(combine_kernel<float, 64>, dim3(grid), dim3(128), 0, st, o_part, m_part, l_part, num_splits, sink,
+                     static_cast<float*>(out), lse, (int)s.Hq, total);
     else
-      combine_kernel<float, 128><<<grid, 128, 0, st>>>(o_part, m_part, l_part, num_splits, sink,
-                                                       static_cast<float*>(out), lse, s.Hq, total);
+      e = launch_pdl(combine_kernel<float, 128>, dim3(grid), dim3(128), 0, st, o_part, m_part, l_part, num_splits, sink,
+                     static_cast<float*>(out), lse, (int)s.Hq, total);
   } else {
     if (s.D == 64)
-      combine_kernel<bf16, 64><<<grid, 128, 0, st>>>(o_part, m_part, l_part, num_splits, sink,
-                                                     static_cast<bf16*>(out), lse, s.Hq, total);
+      e = launch_pdl(combine_kernel<bf16, 64>, dim3(grid), dim3(128), 0, st, o_part, m_part, l_part, num_splits, sink,
+                     static_cast<bf16*>(out), lse, (int)s.Hq, total);
     else
-      combine_kernel<bf16, 128><<<grid, 128, 0, st>>>(o_part, m_part, l_part, num_splits, sink,
-                                                      static_cast<bf16*>(out), lse, s.Hq, total);
+      e = launch_pdl(combine_kernel<bf16, 128>, dim3(grid), dim3(128), 0, st, o_part, m_part, l_part, num_splits, sink,
+                     static_cast<bf16*>(out), lse, (int)s.Hq, total);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

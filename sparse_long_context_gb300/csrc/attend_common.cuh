@@ -64,24 +64,24 @@ __device__ __forceinline__ int token_position(const AttendArgs& a, int pg, int j
 constexpr int kCombineMaxS = 64;  // splits whose weights are kept in shared memory
 
 template <typename T, int D, int NT>
-__device__ __forceinline__ void combine_row_if_last(const AttendArgs& a, int row) {
+__device__ __forceinline__ void combine_row_if_last(const AttendArgs& a, int row, int nseg) {
   __shared__ int s_last;
   __shared__ float s_w[8][kCombineMaxS];
   __shared__ float s_m[8], s_inv[8];
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(a.tickets + row, 1) == a.S - 1;
+  if (threadIdx.x == 0) s_last = atomicAdd(a.tickets + row, 1) == nseg - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   const int b = row / a.Hkv, h = row % a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int NW = NT / 32;
-  const int S = a.S;
+  const int S = nseg;  // partials written for this row (slot stride a.S)
   const size_t hq0 = (size_t)b * a.Hq + (size_t)h * a.G;
   for (int g = warp; g < a.G; g += NW) {
-    const float* mp = a.m_part + (hq0 + g) * S;
-    const float* lp = a.l_part + (hq0 + g) * S;
+    const float* mp = a.m_part + (hq0 + g) * a.S;
+    const float* lp = a.l_part + (hq0 + g) * a.S;
     float M = kNegInf;
     for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(mp + s));
     M = warp_max(M);
@@ -106,8 +106,8 @@ __device__ __forceinline__ void combine_row_if_last(const AttendArgs& a, int row
   constexpr int C4 = D / 4;
   for (int it = threadIdx.x; it < a.G * C4; it += NT) {
     const int g = it / C4, c = it % C4;
-    const float4* op = reinterpret_cast<const float4*>(a.o_part + (hq0 + g) * S * D) + c;
-    const float* mp = a.m_part + (hq0 + g) * S;
+    const float4* op = reinterpret_cast<const float4*>(a.o_part + (hq0 + g) * a.S * D) + c;
+    const float* mp = a.m_part + (hq0 + g) * a.S;
     const float M = s_m[g];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < S; s0 += 8) {

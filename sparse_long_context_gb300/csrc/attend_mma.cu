@@ -35,6 +35,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// A contiguous run of one row's token list handled by one CTA: tokens
+// j = 0 .. ntok-1 of the run sit at list position joff + j after entry e0
+// (entry = e0 + ((joff + j) >> log2 P), offset in the page = (joff + j) & (P-1)).
+struct Seg {
+  int N, e0, joff, ntok, nent;
+};
+
 template <int D>
 struct Group {
   static constexpr int NS = D / 32, VL = D / 64;
@@ -47,19 +54,21 @@ struct Group {
 // pages of at least 16 tokens a group lies inside one page, so the lane
 // derives them from the group's page without shuffles.
 template <bool PAGED>
-__device__ __forceinline__ void group_positions(const AttendArgs& a, const Slice& sl, const int* s_pg,
-                                                const int32_t* plist, int gi, int ntok, int lane, int& pk0,
-                                                int& pk1, int (&pv)[4]) {
+__device__ __forceinline__ void group_positions(const AttendArgs& a, const Seg& sl, const int* s_pg,
+                                                const int32_t* plist, int gi, int lane, int& pk0, int& pk1,
+                                                int (&pv)[4]) {
   const int r = lane >> 2, m = lane & 3;
+  const int ntok = sl.ntok;
   if constexpr (PAGED) {
-    const int j0 = gi << 4;
+    const int j0 = gi << 4;  // a 16-token group starts at a multiple of 16 and stays inside one page
     int base = -1, lim = 0;
     if (j0 < ntok) {
-      const int e = j0 >> a.pshift;
+      const int J = sl.joff + j0;
+      const int e = J >> a.pshift;
       const int pg = e < kStagedEntries ? s_pg[e] : (plist ? __ldg(plist + e) : sl.e0 + e);
       if ((unsigned)pg < (unsigned)(a.Cap >> a.pshift)) {
-        base = (pg << a.pshift) + (j0 & (a.P - 1));
-        lim = sl.N - base;  // tokens t < lim are inside the context
+        base = (pg << a.pshift) + (J & (a.P - 1));
+        lim = min(sl.N - base, ntok - j0);  // inside the context and inside the run
       }
     }
     auto at = [&](int t) { return (base >= 0 && t < lim) ? base + t : -1; };
@@ -73,9 +82,10 @@ __device__ __forceinline__ void group_positions(const AttendArgs& a, const Slice
     int mypos = -1;
     const int j = (gi << 4) + (lane & 15);
     if (j < ntok) {
-      const int e = j >> a.pshift;
+      const int J = sl.joff + j;
+      const int e = J >> a.pshift;
       const int pg = e < kStagedEntries ? s_pg[e] : (plist ? __ldg(plist + e) : sl.e0 + e);
-      mypos = token_position(a, pg, j, sl.N);
+      mypos = token_position(a, pg, J, sl.N);
     }
     pk0 = __shfl_sync(0xffffffffu, mypos, r);
     pk1 = __shfl_sync(0xffffffffu, mypos, r + 8);
@@ -87,12 +97,11 @@ __device__ __forceinline__ void group_positions(const AttendArgs& a, const Slice
 }
 
 template <int D, bool PAGED>
-__device__ __forceinline__ void load_group(Group<D>& g, const AttendArgs& a, const Slice& sl, const int* s_pg,
-                                           const int32_t* plist, int gi, int ntok, const bf16* kl,
-                                           const bf16* vl) {
+__device__ __forceinline__ void load_group(Group<D>& g, const AttendArgs& a, const Seg& sl, const int* s_pg,
+                                           const int32_t* plist, int gi, const bf16* kl, const bf16* vl) {
   constexpr int NS = Group<D>::NS, VL = Group<D>::VL;
   int pk0, pk1;
-  group_positions<PAGED>(a, sl, s_pg, plist, gi, ntok, threadIdx.x & 31, pk0, pk1, g.pv);
+  group_positions<PAGED>(a, sl, s_pg, plist, gi, threadIdx.x & 31, pk0, pk1, g.pv);
   const bf16* k0 = kl + (size_t)max(pk0, 0) * D;
   const bf16* k1 = kl + (size_t)max(pk1, 0) * D;
 #pragma unroll
@@ -173,31 +182,31 @@ constexpr size_t attend_mma_smem() {
   return (size_t)kAttnWarps * 8 * D * sizeof(float);  // the warps' partial outputs
 }
 
+struct AttendSmem {
+  float sM[kAttnWarps][8];
+  float sL[kAttnWarps][8];
+  int s_pg[kStagedEntries];
+};
+
+// One CTA's work on one row: the run `sl` of the row's list, written to
+// partial slot `slot`; `nseg` CTAs write partials of this row.
 template <int D, bool PAGED>
-__global__ void __launch_bounds__(kAttnWarps * 32, 1)
-attend_mma_kernel(const AttendArgs a) {
+__device__ __forceinline__ void attend_run(const AttendArgs& a, int row, const Seg& sl, int slot, int nseg,
+                                           float* sO, AttendSmem& sh) {
   constexpr int NW = kAttnWarps;
   constexpr int NS = D / 32;   // 16-byte chunks of a row per lane (chunk 4s + m)
   constexpr int MT = D / 16;   // m-tiles of the P.V product (channels)
   constexpr int CPR = D / 8;   // channels of V owned by one lane row r
-  extern __shared__ float sO[];  // [NW][8][D]
-  __shared__ float sM[NW][8];
-  __shared__ float sL[NW][8];
-  __shared__ int s_pg[kStagedEntries];
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, m = lane & 3;
-  const int row = blockIdx.x / a.S, split = blockIdx.x % a.S;
   const int b = row / a.Hkv, h = row % a.Hkv;
   const int G = a.G;
-  const Slice sl = attend_slice(a, row, split);
-  const int ntok = sl.nent << a.pshift;
   const int32_t* plist = a.page_idx ? a.page_idx + (size_t)row * a.idx_stride + sl.e0 : nullptr;
   const bf16* kl = static_cast<const bf16*>(a.k) + (size_t)row * a.Cap * D + m * 8;    // chunk 4s+m: +32s
   const bf16* vl = static_cast<const bf16*>(a.v) + (size_t)row * a.Cap * D + r * CPR;  // lane's V channels
 
   for (int i = threadIdx.x; i < min(sl.nent, kStagedEntries); i += NW * 32)
-    s_pg[i] = plist ? __ldg(plist + i) : sl.e0 + i;
+    sh.s_pg[i] = plist ? __ldg(plist + i) : sl.e0 + i;
 
   // Q as the A operand: row r = head r (rows 8..15 are zero)
   uint32_t qa[NS][4];
@@ -216,16 +225,16 @@ attend_mma_kernel(const AttendArgs a) {
   const float sl2 = a.qscale;
   __syncthreads();
 
-  const int ngroups = (ntok + 15) >> 4;
+  const int ngroups = (sl.ntok + 15) >> 4;
   Group<D> ga, gb;
   int gi = warp;
-  if (gi < ngroups) load_group<D, PAGED>(ga, a, sl, s_pg, plist, gi, ntok, kl, vl);
+  if (gi < ngroups) load_group<D, PAGED>(ga, a, sl, sh.s_pg, plist, gi, kl, vl);
   while (gi < ngroups) {
-    if (gi + NW < ngroups) load_group<D, PAGED>(gb, a, sl, s_pg, plist, gi + NW, ntok, kl, vl);
+    if (gi + NW < ngroups) load_group<D, PAGED>(gb, a, sl, sh.s_pg, plist, gi + NW, kl, vl);
     compute_group<D>(ga, qa, o, m_run, l_run, sl2, lane);
     gi += NW;
     if (gi >= ngroups) break;
-    if (gi + NW < ngroups) load_group<D, PAGED>(ga, a, sl, s_pg, plist, gi + NW, ntok, kl, vl);
+    if (gi + NW < ngroups) load_group<D, PAGED>(ga, a, sl, sh.s_pg, plist, gi + NW, kl, vl);
     compute_group<D>(gb, qa, o, m_run, l_run, sl2, lane);
     gi += NW;
   }
@@ -234,8 +243,8 @@ attend_mma_kernel(const AttendArgs a) {
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
   if (m == 0) {
-    sM[warp][r] = m_run;
-    sL[warp][r] = l_run;
+    sh.sM[warp][r] = m_run;
+    sh.sL[warp][r] = l_run;
   }
 #pragma unroll
   for (int t = 0; t < MT; ++t) {
@@ -251,25 +260,43 @@ attend_mma_kernel(const AttendArgs a) {
     const int g = i / D, d = i % D;
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, sM[w][g]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sh.sM[w][g]);
     float av = 0.f, lv = 0.f;
     if (M != kNegInf) {
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
-        if (sM[w][g] == kNegInf) continue;
-        const float f = exp2f(sM[w][g] - M);
+        if (sh.sM[w][g] == kNegInf) continue;
+        const float f = exp2f(sh.sM[w][g] - M);
         av += sO[(w * 8 + g) * D + d] * f;
-        lv += sL[w][g] * f;
+        lv += sh.sL[w][g] * f;
       }
     }
     const size_t hq = (size_t)b * a.Hq + (size_t)h * G + g;
-    a.o_part[(hq * a.S + split) * D + d] = av;
+    a.o_part[(hq * a.S + slot) * D + d] = av;
     if (d == 0) {
-      a.m_part[hq * a.S + split] = M == kNegInf ? kNegInf : M * kLn2;
-      a.l_part[hq * a.S + split] = lv;
+      a.m_part[hq * a.S + slot] = M == kNegInf ? kNegInf : M * kLn2;
+      a.l_part[hq * a.S + slot] = lv;
     }
   }
-  if (a.tickets) combine_row_if_last<bf16, D, NW * 32>(a, row);
+  if (a.tickets) combine_row_if_last<bf16, D, NW * 32>(a, row, nseg);
+  __syncthreads();  // shared memory is reused by the next run of this CTA
+}
+
+template <int D, bool PAGED>
+__global__ void __launch_bounds__(kAttnWarps * 32, 1)
+attend_mma_kernel(const AttendArgs a) {
+  pdl_wait_then_release();
+  extern __shared__ float sO[];  // [NW][8][D]
+  __shared__ AttendSmem sh;
+  const int row = blockIdx.x / a.S, split = blockIdx.x % a.S;
+  const Slice sl = attend_slice(a, row, split);
+  Seg sg;
+  sg.N = sl.N;
+  sg.e0 = sl.e0;
+  sg.joff = 0;
+  sg.ntok = sl.nent << a.pshift;
+  sg.nent = sl.nent;
+  attend_run<D, PAGED>(a, row, sg, split, a.S, sO, sh);
 }
 
 template <int D, bool PAGED>
@@ -278,7 +305,8 @@ static cudaError_t attend_mma_launch(const AttendArgs& a, int grid, cudaStream_t
   cudaError_t e = cudaFuncSetAttribute(attend_mma_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  attend_mma_kernel<D, PAGED><<<grid, kAttnWarps * 32, smem, st>>>(a);
+  e = launch_pdl(attend_mma_kernel<D, PAGED>, dim3(grid), dim3(kAttnWarps * 32), smem, st, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -76,4 +76,13 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ int clamp_len(int n, int cap) { return n < 0 ? 0 : (n > cap ? cap : n); }
 
+// Programmatic dependent launch: every kernel of the decode step waits for
+// the grid it depends on (no-op when launched without the attribute) before
+// touching global memory, and only then lets its own dependents start their
+// launch, so a dependent can never read data its predecessors still write.
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace sls

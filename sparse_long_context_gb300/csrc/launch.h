@@ -6,7 +6,28 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace sls {
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel in the stream drains; it waits for it in
+// pdl_wait_then_release() before touching memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 struct Shape {
   int B, Hq, Hkv, G, D, P, pshift, Cap, dtype, flags;
@@ -42,6 +63,7 @@ struct FusedCombine {
   float* lse;
 };
 int attend_default_splits(const Shape& s, int max_entries);
+int max_auto_splits(const Shape& s);
 cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const void* v,
                           const int32_t* page_idx, int idx_stride, const int32_t* count,
                           int k_fixed, const int32_t* ctx_len, int num_splits,

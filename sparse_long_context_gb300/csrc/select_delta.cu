@@ -41,6 +41,7 @@ __device__ __forceinline__ void delta_layout(int N, int bshift, int block, int& 
 template <typename T, int D, int GM>
 __global__ void __launch_bounds__(kDeltaThreads)
 delta_scan_kernel(const DeltaArgs a) {
+  pdl_wait_then_release();
   constexpr int EPL = Vec16<T>::N;
   constexpr int L = D / EPL;       // lanes per exact key
   constexpr int TPW = 32 / L;
@@ -204,6 +205,7 @@ delta_scan_kernel(const DeltaArgs a) {
 // One CTA per row: ordered list of the kept blocks and its length.
 __global__ void __launch_bounds__(1024)
 delta_compact_kernel(const DeltaArgs a) {
+  pdl_wait_then_release();
   __shared__ int tmp[32];
   const int row = blockIdx.x;
   const int b = row / a.Hkv;
@@ -251,10 +253,10 @@ size_t select_delta_workspace(const Shape& s, int block) {
 
 template <typename T, int D, int GM>
 static cudaError_t delta_launch(const DeltaArgs& a, int rows, cudaStream_t st) {
-  delta_scan_kernel<T, D, GM><<<rows * a.SPL, kDeltaThreads, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(delta_scan_kernel<T, D, GM>, dim3(rows * a.SPL), dim3(kDeltaThreads), 0, st, a);
   if (e != cudaSuccess) return e;
-  delta_compact_kernel<<<rows, 1024, 0, st>>>(a);
+  e = launch_pdl(delta_compact_kernel, dim3(rows), dim3(1024), 0, st, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -539,6 +539,7 @@ __device__ __forceinline__ bool row_topk_fast(const uint32_t* keys, int n, int k
 template <typename T, int D, int GM, int MODE>
 __global__ void __launch_bounds__(MODE == 0 ? kSelThreads : kSelThreadsMma)
 quest_score_kernel(const SelectArgs a) {
+  pdl_wait_then_release();
   constexpr int NT = MODE == 0 ? kSelThreads : kSelThreadsMma;
   const int row = blockIdx.y;
   const int b = row / a.Hkv, h = row % a.Hkv;
@@ -560,6 +561,7 @@ quest_score_kernel(const SelectArgs a) {
 template <int CL>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const SelectArgs a) {
+  pdl_wait_then_release();
   extern __shared__ uint32_t skeys[];
   __shared__ union {
     TopkShared radix;
@@ -588,6 +590,207 @@ topk_kernel(const SelectArgs a) {
   row_topk<kTopkThreads, CL>(skeys, nloc, rank, a.k, p0, out, sh.radix);
 }
 
+// Rows of at most NT*KPT pages: one CTA of NT threads per row, each thread
+// holding KPT consecutive keys in registers (thread t: pages t*KPT ..).
+// Same algorithm as row_topk_fast (window histogram over the top 16 bits,
+// exact rank inside T's bin, ascending output), but every pass is a sweep
+// over registers and every scan costs two barriers.  Rows whose threshold
+// leaves the window, or whose bin is too full, fall back to the radix
+// select over the keys written to shared memory.
+constexpr int kRegTopkThreads = 1024;
+constexpr int kRegTopkKeys = 8;  // keys per thread
+
+template <int NT>
+__device__ __forceinline__ int scan2(int v, int* tmp, int& total) {
+  // exclusive scan of one int per thread, two barriers (NT/32 <= 32 warps)
+  constexpr int NWp = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  int t = lane < NWp ? tmp[lane] : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, t, o);
+    if (lane >= o) t += y;
+  }
+  const int before = warp > 0 ? __shfl_sync(0xffffffffu, t, warp - 1) : 0;
+  total = __shfl_sync(0xffffffffu, t, NWp - 1);
+  __syncthreads();  // tmp may be reused right after
+  return before + x - v;
+}
+
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT)
+topk_reg_kernel(const SelectArgs a) {
+  pdl_wait_then_release();
+  constexpr int NWp = NT / 32;
+  constexpr int BPT = kWin / NT;  // window bins per thread
+  __shared__ uint32_t hist[kWin];
+  __shared__ uint32_t cand[kCand];
+  __shared__ int tmp[32];
+  __shared__ uint32_t red_max[32];
+  __shared__ int red_nf[32];
+  __shared__ int s_bin, s_rem, s_take, s_ncand;
+  __shared__ uint32_t s_T;
+  extern __shared__ uint32_t skeys[];  // only for the fallback
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
+  const int b = row / a.Hkv;
+  const int N = clamp_len(a.ctx_len[b], a.Cap);
+  const int n = (N + a.P - 1) >> a.pshift;
+  const int k = a.k;
+  int32_t* out = a.page_idx + (size_t)row * k;
+  if (n <= k) {
+    for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
+    return;
+  }
+  const uint32_t* src = a.keys + (size_t)row * a.npcap;
+  // 0 sorts below every real key (the key of -inf is 0x007fffff), so it
+  // pads the slots past n without taking part in any count
+  uint32_t kk[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int i = tid * KPT + j;
+    kk[j] = i < n ? __ldcg(src + i) : 0u;
+  }
+  // 1. largest non-forced top-16 value, forced count; clear the window
+  uint32_t mx = 0;
+  int nf = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    if (kk[j] == kForcedKey) ++nf;
+    else mx = max(mx, kk[j] >> 16);
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  nf = __reduce_add_sync(0xffffffffu, nf);
+  if (lane == 0) {
+    red_max[warp] = mx;
+    red_nf[warp] = nf;
+  }
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) hist[tid * BPT + i] = 0;
+  if (tid == 0) s_ncand = 0;
+  __syncthreads();
+  const uint32_t top = __reduce_max_sync(0xffffffffu, lane < NWp ? red_max[lane] : 0u);
+  const int nforced = __reduce_add_sync(0xffffffffu, lane < NWp ? red_nf[lane] : 0);
+  const int need = k - nforced;
+  bool fast = true;
+  uint32_t T = kForcedKey;
+  int take = k;
+  if (need > 0) {
+    // 2. window histogram: bin j counts non-forced keys whose top 16 bits are top - j
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (kk[j] == kForcedKey || kk[j] == 0u) continue;
+      const uint32_t d = top - (kk[j] >> 16);
+      if (d < (uint32_t)kWin) atomicAdd(&hist[d], 1u);
+    }
+    __syncthreads();
+    // 3. the bin of the need-th largest (bins by increasing j)
+    int c[BPT], sum = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      c[i] = (int)hist[tid * BPT + i];
+      sum += c[i];
+    }
+    int total;
+    int above = scan2<NT>(sum, tmp, total);
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      if (above < need && above + c[i] >= need) {
+        s_bin = tid * BPT + i;
+        s_rem = need - above;
+      }
+      above += c[i];
+    }
+    __syncthreads();
+    fast = total >= need;
+    if (fast) {
+      // 4. the keys of that bin
+      const uint32_t t16 = top - (uint32_t)s_bin;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {  // one shared-memory atomic per warp and key slot
+        const bool in = kk[j] != kForcedKey && kk[j] != 0u && (kk[j] >> 16) == t16;
+        const unsigned bal = __ballot_sync(0xffffffffu, in);
+        if (bal == 0u) continue;
+        int base = 0;
+        if (lane == __ffs(bal) - 1) base = atomicAdd(&s_ncand, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, __ffs(bal) - 1);
+        const int slot = base + __popc(bal & ((1u << lane) - 1u));
+        if (in && slot < kCand) cand[slot] = kk[j];
+      }
+      __syncthreads();
+      const int m = s_ncand;
+      fast = m <= kCand;
+      if (fast) {
+        // 5. exact rank inside the bin: 8 threads per candidate
+        const int rem = s_rem;
+        const int sub = tid & 7;
+        for (int i0 = 0; i0 < m; i0 += NT / 8) {
+          const int i = i0 + (tid >> 3);
+          const uint32_t v = i < m ? cand[i] : 0u;
+          int gt = 0, ge = 0;
+          for (int q = sub; q < m; q += 8) {
+            const uint32_t w = cand[q];
+            gt += w > v;
+            ge += w >= v;
+          }
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) {
+            gt += __shfl_xor_sync(0xffffffffu, gt, o);
+            ge += __shfl_xor_sync(0xffffffffu, ge, o);
+          }
+          if (i < m && sub == 0 && gt < rem && ge >= rem) {
+            s_T = v;
+            s_take = rem - gt;
+          }
+        }
+        __syncthreads();
+        T = s_T;
+        take = s_take;
+      }
+    }
+  }
+  if (!fast) {  // uniform: every thread read the same shared values
+    for (int j = 0; j < KPT; ++j) {
+      const int i = tid * KPT + j;
+      if (i < n) skeys[i] = kk[j];
+    }
+    __syncthreads();
+    row_topk<NT, 1>(skeys, n, 0, k, 0, out, *reinterpret_cast<TopkShared*>(hist));
+    return;
+  }
+  // 6. ascending output: position = (#keys > T before) + min(#T-keys before, take)
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    gt += kk[j] > T;
+    eq += kk[j] == T;
+  }
+  int tot;
+  const int e = scan2<NT>((gt << 16) | eq, tmp, tot);  // both totals < 2^15
+  int G = e >> 16, E = e & 0xffff;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int i = tid * KPT + j;
+    if (kk[j] > T) {
+      const int pos = G + min(E, take);
+      if (pos < k) out[pos] = i;
+      ++G;
+    } else if (kk[j] == T) {
+      if (E < take && G + E < k) out[G + E] = i;
+      ++E;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- launches
 
 template <typename T, int D, int GM, int MODE>
@@ -601,11 +804,22 @@ static cudaError_t score_launch(const SelectArgs& a, int rows, cudaStream_t st) 
   const int cpr = max(1, slots / rows);  // at most one wave over all rows
   b.chunk = max(16, ((a.npcap + cpr - 1) / cpr + 15) / 16 * 16);
   dim3 grid((a.npcap + b.chunk - 1) / b.chunk, rows);
-  kern<<<grid, NT, 0, st>>>(b);
+  cudaError_t e = launch_pdl(kern, grid, dim3(NT), 0, st, b);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 static cudaError_t topk_launch(const SelectArgs& a, int rows, cudaStream_t st) {
+  if (a.npcap <= kRegTopkThreads * kRegTopkKeys) {
+    constexpr int NT = kRegTopkThreads, KPT = kRegTopkKeys;
+    const size_t smem = (size_t)a.npcap * sizeof(uint32_t);  // fallback keys
+    cudaError_t e = cudaFuncSetAttribute(topk_reg_kernel<NT, KPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(topk_reg_kernel<NT, KPT>, dim3(rows), dim3(NT), smem, st, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   int cl = 1;
   while (cl < kTopkMaxCluster && (a.npcap + cl - 1) / cl > kTopkMaxKeys) cl *= 2;
   const size_t smem = (size_t)((a.npcap + cl - 1) / cl) * sizeof(uint32_t);
@@ -613,21 +827,24 @@ static cudaError_t topk_launch(const SelectArgs& a, int rows, cudaStream_t st) {
   if (cl == 1) {
     e = cudaFuncSetAttribute(topk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_kernel<1><<<rows, kTopkThreads, smem, st>>>(a);
+    e = launch_pdl(topk_kernel<1>, dim3(rows), dim3(kTopkThreads), smem, st, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(rows * cl);
   cfg.blockDim = dim3(kTopkThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   switch (cl) {
     case 2:
       e = cudaFuncSetAttribute(topk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -120,10 +120,12 @@ def test_attend_combine_validation(lib):
     ws = lib.sls_attend_combine_workspace_size(ctypes.byref(d), 4)
     # tickets (2*2 rows) + o_part (2*8*4*128 floats) + m and l (2*8*4 floats each), 256-aligned
     assert ws == 256 + 2 * 8 * 4 * 128 * 4 + 2 * 256
-    assert lib.sls_attend_combine_workspace_size(ctypes.byref(d), 0) == 0
+    assert lib.sls_attend_combine_workspace_size(ctypes.byref(d), -1) == 0
+    assert lib.sls_attend_combine_workspace_size(ctypes.byref(d), 0) > 0   # library schedule
     call = lambda S=4, wsb=ws, out=BAD: lib.sls_sparse_decode_attend_combine(
         ctypes.byref(d), BAD, BAD, BAD, BAD, 8, None, 8, BAD, S, None, out, None, BAD, wsb, None)
-    assert call(S=0) == L.SLS_EINVAL
+    assert call(S=-1) == L.SLS_EINVAL
+    assert call(S=1025) == L.SLS_EINVAL
     assert call(out=None) == L.SLS_EINVAL
     assert call(wsb=ws - 1) == L.SLS_EWORKSPACE
     assert lib.sls_attend_default_splits(None, 8) == 1
