@@ -287,7 +287,8 @@ def run_ours(args, s: W.Spec):
     sets = [(dw.K, dw.V, dw.kmin, dw.kmax)]
     for _ in range(nsets - 1):
         sets.append(tuple(t.clone() for t in sets[0]))
-    steps_obj = [ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens) for _ in sets]
+    steps_obj = [ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, args.splits)
+                 for _ in sets]
     S = steps_obj[0].S
     stream = torch.cuda.Stream()
     graphs = []
@@ -433,6 +434,8 @@ def main():
     ap.add_argument("--workload", default="qwen1p5b", choices=("qwen1p5b", "qwen7b"))
     ap.add_argument("--ctx", type=int, default=None, help="context length (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="attend splits per (sequence, KV head) (default: the library's choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

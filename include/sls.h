@@ -59,6 +59,7 @@ typedef int sls_status;
 #define SLS_EOVERFLOW    -3  /* a size product overflows the index range */
 #define SLS_EWORKSPACE   -4  /* workspace missing or too small */
 #define SLS_ECUDA        -5  /* a CUDA launch or attribute call failed */
+#define SLS_ETIMEOUT     -6  /* a pipelined kernel gave up waiting for its own copies */
 
 /* ---- element types ----------------------------------------------------- */
 #define SLS_DTYPE_F32  0
@@ -68,6 +69,10 @@ typedef int sls_status;
 /* Use the CUDA-core kernels even where a tensor-core kernel exists (for
  * comparison; results agree within the same tolerances). */
 #define SLS_FLAG_CUDA_CORES 1
+/* Feed the bf16 tensor-core attend kernel from registers (16-byte loads)
+ * instead of the shared-memory ring filled by tensor-map copies (for
+ * comparison; results agree within the same tolerances). */
+#define SLS_FLAG_NO_TMA 2
 
 /*
  * Shapes and element type of one attention layer's decode step.
@@ -330,6 +335,16 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
 
 /* Message of the last failing call on this thread ("" if none). */
 const char* sls_last_error(void);
+
+/*
+ * Health of the pipelined kernels.  Kernels that stage data through shared
+ * memory wait for their copies with a bounded number of polls; a wait that
+ * gives up makes the affected outputs NaN and is counted on the device.
+ * This call synchronises the device, reads and clears that count, and returns
+ * SLS_ETIMEOUT if it was non-zero (SLS_ECUDA if the device cannot be read),
+ * else SLS_OK.
+ */
+sls_status sls_pipeline_check(void);
 
 /* Library ABI version (major*10000 + minor*100 + patch). */
 int32_t sls_version(void);

@@ -10,8 +10,10 @@ from . import build as _build
 LIB_PATH = _build.LIB
 
 SLS_OK, SLS_EINVAL, SLS_EUNSUPPORTED, SLS_EOVERFLOW, SLS_EWORKSPACE, SLS_ECUDA = 0, -1, -2, -3, -4, -5
+SLS_ETIMEOUT = -6
 SLS_DTYPE_F32, SLS_DTYPE_BF16 = 0, 1
 SLS_FLAG_CUDA_CORES = 1
+SLS_FLAG_NO_TMA = 2
 
 
 class AttnDesc(ctypes.Structure):
@@ -42,6 +44,7 @@ SIGNATURES = {
     "sls_attend_combine_workspace_size": (ctypes.c_size_t, [_D, _I]),
     "sls_sparse_decode_attend_combine": (_I, [_D, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P,
                                               ctypes.c_size_t, _P]),
+    "sls_pipeline_check": (_I, []),
     "sls_last_error": (ctypes.c_char_p, []),
     "sls_version": (_I, []),
 }

@@ -61,7 +61,7 @@ sls_status check_desc(const sls_attn_desc* d, sls::Shape* s) {
     return fail(SLS_EINVAL, "capacity %d must be >= 1 and a multiple of page_size %d", d->capacity,
                 d->page_size);
   if (!(d->scale >= 0.f) || std::isinf(d->scale)) return fail(SLS_EINVAL, "scale must be finite and >= 0");
-  if (d->flags & ~SLS_FLAG_CUDA_CORES) return fail(SLS_EINVAL, "unknown flags 0x%x", d->flags);
+  if (d->flags & ~(SLS_FLAG_CUDA_CORES | SLS_FLAG_NO_TMA)) return fail(SLS_EINVAL, "unknown flags 0x%x", d->flags);
   // element counts of the caches and of the per-row index space
   int64_t rows, elems;
   if (!checked_mul(d->batch, d->num_kv_heads, &rows) || !checked_mul(rows, d->capacity, &elems) ||
@@ -101,6 +101,13 @@ extern "C" {
 const char* sls_last_error(void) { return g_err; }
 
 int32_t sls_version(void) { return 10000; }
+
+sls_status sls_pipeline_check(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(SLS_ECUDA, "device synchronisation failed");
+  const unsigned int n = sls::take_attend_wait_timeouts();
+  if (n) return fail(SLS_ETIMEOUT, "%u pipelined CTA(s) gave up waiting for their copies", n);
+  return SLS_OK;
+}
 
 sls_status sls_pagemeta_build(const sls_attn_desc* desc, const void* k_cache, const int32_t* ctx_len,
                               void* kmin, void* kmax, void* stream) {

@@ -277,6 +277,7 @@ static cudaError_t attend_cc_g(const AttendArgs& a, int rows, cudaStream_t st) {
 }
 
 cudaError_t launch_attend_mma(const Shape& s, const AttendArgs& a, cudaStream_t st, bool* handled);
+cudaError_t launch_attend_tma(const Shape& s, const AttendArgs& a, cudaStream_t st, bool* handled);
 const void* attend_mma_kernel_ptr();
 size_t attend_mma_kernel_smem();
 int attend_mma_kernel_threads();
@@ -284,21 +285,23 @@ int attend_mma_kernel_threads();
 int max_auto_splits(const Shape& s) {
   // splits per row the library may choose by itself (sizes the workspace)
   const int rows = s.B * s.Hkv;
-  return (2 * sm_count() + rows - 1) / rows;
+  return (4 * sm_count() + rows - 1) / rows;
 }
 
 int attend_default_splits(const Shape& s, int max_entries) {
   // one wave of attend CTAs over all rows (at most one CTA per slot), each
   // slice at least 64 tokens
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  static int mma_per_sm = 0;
+  if (mma_per_sm == 0) {
     cudaFuncSetAttribute(attend_mma_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)attend_mma_kernel_smem());
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attend_mma_kernel_ptr(),
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&mma_per_sm, attend_mma_kernel_ptr(),
                                                       attend_mma_kernel_threads(),
                                                       attend_mma_kernel_smem()) != cudaSuccess)
-      per_sm = 1;
+      mma_per_sm = 1;
   }
+  if (attend_tma_eligible(s)) return attend_tma_splits(s, (int)(((long long)max_entries << s.pshift) / 16));
+  const int per_sm = mma_per_sm;
   const int rows = s.B * s.Hkv;
   const int slots = sm_count() * (per_sm > 0 ? per_sm : 1);
   int S = slots / rows;
@@ -323,6 +326,7 @@ cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const vo
   a.page_idx = page_idx; a.count = count; a.ctx_len = ctx_len;
   a.o_part = o_part; a.m_part = m_part; a.l_part = l_part;
   a.idx_stride = idx_stride; a.k_fixed = k_fixed; a.S = num_splits;
+  a.cluster = 0;
   if (num_splits == 0) {  // the library schedules (fused call only)
     const int entries = page_idx ? (count ? idx_stride : k_fixed) : (s.Cap >> s.pshift);
     a.S = attend_default_splits(s, entries > 0 ? entries : 1);
@@ -333,7 +337,9 @@ cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const vo
   const int rows = s.B * s.Hkv;
   if (!(s.flags & 1)) {
     bool handled = false;
-    cudaError_t e = launch_attend_mma(s, a, st, &handled);
+    cudaError_t e = launch_attend_tma(s, a, st, &handled);
+    if (handled) return e;
+    e = launch_attend_mma(s, a, st, &handled);
     if (handled) return e;
   }
   if (s.dtype == 0) {

@@ -23,6 +23,8 @@ struct AttendArgs {
   const float* sink;  // [Hq] or null
   void* out;          // [B, Hq, D] dtype
   float* lse;         // [B, Hq] or null
+  int cluster;        // 1: the S splits of a row form one thread-block cluster and
+                      // combine through distributed shared memory (no partials in global memory)
 };
 
 // Slice [e0, e1) of row `row`'s page list handled by split `split`.

@@ -27,6 +27,7 @@ namespace sls {
 //   V of tokens 2m, 2m+1, 2m+8, 2m+9, VL chunks each (A operand of O^T),
 // and the positions that decide which tokens are valid.
 constexpr int kAttnWarps = 8;
+constexpr int kAttnMinBlocks = 1;  // resident CTAs per SM the register budget is sized for
 constexpr int kStagedEntries = 1024;  // page-list entries staged in shared memory
 
 __device__ __forceinline__ float ex2(float x) {
@@ -283,7 +284,7 @@ __device__ __forceinline__ void attend_run(const AttendArgs& a, int row, const S
 }
 
 template <int D, bool PAGED>
-__global__ void __launch_bounds__(kAttnWarps * 32, 1)
+__global__ void __launch_bounds__(kAttnWarps * 32, kAttnMinBlocks)
 attend_mma_kernel(const AttendArgs a) {
   pdl_wait_then_release();
   extern __shared__ float sO[];  // [NW][8][D]

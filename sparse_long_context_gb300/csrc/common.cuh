@@ -78,11 +78,16 @@ __device__ __forceinline__ int clamp_len(int n, int cap) { return n < 0 ? 0 : (n
 
 // Programmatic dependent launch: every kernel of the decode step waits for
 // the grid it depends on (no-op when launched without the attribute) before
-// touching global memory, and only then lets its own dependents start their
-// launch, so a dependent can never read data its predecessors still write.
+// touching global memory.  Its own dependents may start their launch once
+// every CTA has released them (or exited); a release always follows the
+// wait, so a dependent can never read data its predecessors still write.
+// Kernels whose dependents would crowd their SMs release late or not at all
+// (then the release happens at exit).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_then_release() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_wait();
+  pdl_release();
 }
 
 }  // namespace sls

@@ -13,20 +13,36 @@ namespace sls {
 // Launch with programmatic stream serialisation: the kernel may be scheduled
 // while the previous kernel in the stream drains; it waits for it in
 // pdl_wait_then_release() before touching memory.
+// With cluster > 1, consecutive groups of `cluster` CTAs along x form a
+// thread-block cluster (grid.x must be a multiple of it).
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                              Args&&... args) {
+inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster,
+                                      cudaStream_t st, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  return launch_pdl_cluster(kern, grid, block, smem, 1, st, std::forward<Args>(args)...);
 }
 
 struct Shape {
@@ -63,6 +79,12 @@ struct FusedCombine {
   float* lse;
 };
 int attend_default_splits(const Shape& s, int max_entries);
+// Tensor-map fed attend kernel (bf16, pages of >= 16 tokens).
+bool attend_tma_eligible(const Shape& s);
+int attend_tma_per_sm(const Shape& s);
+int attend_tma_splits(const Shape& s, int groups_per_row);
+// Reads and clears the count of attend CTAs whose bounded waits gave up.
+unsigned int take_attend_wait_timeouts();
 int max_auto_splits(const Shape& s);
 cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const void* v,
                           const int32_t* page_idx, int idx_stride, const int32_t* count,

@@ -561,7 +561,7 @@ quest_score_kernel(const SelectArgs a) {
 template <int CL>
 __global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const SelectArgs a) {
-  pdl_wait_then_release();
+  pdl_wait();  // released at exit: the attend CTAs queued behind it spread over every SM
   extern __shared__ uint32_t skeys[];
   __shared__ union {
     TopkShared radix;
@@ -628,7 +628,7 @@ __device__ __forceinline__ int scan2(int v, int* tmp, int& total) {
 template <int NT, int KPT>
 __global__ void __launch_bounds__(NT)
 topk_reg_kernel(const SelectArgs a) {
-  pdl_wait_then_release();
+  pdl_wait();  // released at exit: the attend CTAs queued behind it spread over every SM
   constexpr int NWp = NT / 32;
   constexpr int BPT = kWin / NT;  // window bins per thread
   __shared__ uint32_t hist[kWin];

@@ -35,14 +35,15 @@ class DeviceWorkload:
     scales: object = None
 
 
-def upload(spec: W.Spec, host: W.Tensors, cuda_cores: bool = False, device="cuda") -> DeviceWorkload:
+def upload(spec: W.Spec, host: W.Tensors, cuda_cores: bool = False, device="cuda",
+           no_tma: bool = False) -> DeviceWorkload:
     K = to_device(host.K, spec.dtype, device)
     V = to_device(host.V, spec.dtype, device)
     q = to_device(host.q, spec.dtype, device)
     ctx = torch.from_numpy(host.ctx_len).to(device)
     sink = torch.from_numpy(host.sink).to(device) if host.sink is not None else None
     desc = ops.make_desc(spec.batch, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
-                         spec.page_size, spec.capacity, K.dtype, cuda_cores=cuda_cores)
+                         spec.page_size, spec.capacity, K.dtype, cuda_cores=cuda_cores, no_tma=no_tma)
     dw = DeviceWorkload(spec, host, K, V, q, ctx, sink, desc)
     if spec.selector == "quest":
         if spec.page_size == 1:
@@ -73,6 +74,6 @@ def run_step(dw: DeviceWorkload, num_splits=None, fused: bool = True):
     else:
         out, lse = step(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink)
         sel, cnt = step.block_idx, step.count
-    torch.cuda.synchronize()
+    ops.pipeline_check()  # synchronises; raises if a pipelined kernel gave up waiting
     return (sel.cpu().numpy(), None if cnt is None else cnt.cpu().numpy(),
             out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))

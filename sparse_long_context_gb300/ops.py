@@ -36,10 +36,17 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
 
 
 def make_desc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, dtype,
-              scale: float = 0.0, cuda_cores: bool = False) -> L.AttnDesc:
+              scale: float = 0.0, cuda_cores: bool = False, no_tma: bool = False) -> L.AttnDesc:
     code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    flags = (L.SLS_FLAG_CUDA_CORES if cuda_cores else 0) | (L.SLS_FLAG_NO_TMA if no_tma else 0)
     return L.AttnDesc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, code,
-                      L.SLS_FLAG_CUDA_CORES if cuda_cores else 0, float(scale))
+                      flags, float(scale))
+
+
+def pipeline_check() -> None:
+    """Synchronises the device; raises SlsError if a pipelined kernel gave up
+    waiting for its copies since the last check."""
+    L.call("sls_pipeline_check")
 
 
 def desc_for(k_cache: torch.Tensor, num_q_heads: int, page_size: int, scale: float = 0.0,

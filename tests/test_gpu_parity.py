@@ -32,6 +32,9 @@ SMALL_QUEST = {
     "qwen7b_ragged": dict(name="qwen7b", ctx_len=[8197, 3000, 700], capacity=8208),
     "qwen1p5b_4k": dict(name="qwen1p5b", batch=3, ctx_len=4096),
     "gptoss_ragged": dict(name="gptoss", ctx_len=[20000, 5003], capacity=20000),
+    # D = 64 and G = 8 with 16-token pages (the tensor-map path at its other head size)
+    "gptoss_p16": dict(name="gptoss", ctx_len=[5003, 1000], capacity=5008, page_size=16, k_pages=64,
+                       n_sink_pages=1),
 }
 SMALL_DELTA = {
     "ffd_ragged": dict(name="ffd", ctx_len=[65536 + 100, 20000], capacity=65536 + 128),
@@ -42,7 +45,11 @@ SMALL_DELTA = {
 def make(case):
     kw = dict(case)
     name = kw.pop("name", None)
-    return W.spec(name, **kw)
+    fields = {f: kw.pop(f) for f in ("page_size", "k_pages", "n_sink_pages") if f in kw}
+    s = W.spec(name, **kw)
+    for f, v in fields.items():
+        setattr(s, f, v)
+    return s
 
 
 def quest_case(key):
@@ -155,22 +162,28 @@ def check_all_rows(s, host, sel, cnt, out, lse, dw=None):
     return ties
 
 
+# attend kernels: tensor cores fed by tensor-map copies (the default for bf16
+# pages of >= 16 tokens), tensor cores fed by register loads, CUDA cores
+PATHS = {"tma": dict(), "registers": dict(no_tma=True), "cuda_cores": dict(cuda_cores=True)}
+
+
 @pytest.mark.parametrize("key", list(SMALL_QUEST))
-@pytest.mark.parametrize("cuda_cores", [False, True])
-def test_quest_step_small(key, cuda_cores):
+@pytest.mark.parametrize("path", list(PATHS))
+def test_quest_step_small(key, path):
     s = quest_case(key)
     host = W.generate(s)
-    dw = PT.upload(s, host, cuda_cores=cuda_cores)
+    dw = PT.upload(s, host, **PATHS[path])
     sel, cnt, out, lse = PT.run_step(dw)
     ties = check_all_rows(s, host, sel, cnt, out, lse, dw)
     print(f"{key}: boundary ties {ties}")
 
 
 @pytest.mark.parametrize("key", list(SMALL_DELTA))
-def test_delta_step_small(key):
+@pytest.mark.parametrize("path", ["tma", "registers"])
+def test_delta_step_small(key, path):
     s = make(SMALL_DELTA[key])
     host = W.generate(s)
-    dw = PT.upload(s, host)
+    dw = PT.upload(s, host, **PATHS[path])
     sel, cnt, out, lse = PT.run_step(dw)
     ties = check_all_rows(s, host, sel, cnt, out, lse, dw)
     kept = cnt.sum() / sum((n + 63) // 64 for n in host.ctx_len for _ in range(s.num_kv_heads))
@@ -238,7 +251,8 @@ def test_topk_scores_spanning_many_octaves():
         assert t <= 2
 
 
-@pytest.mark.parametrize("splits", [1, 3, 64, 1024])
+# 2..16 splits combine inside a thread-block cluster, more through global memory
+@pytest.mark.parametrize("splits", [1, 2, 3, 8, 13, 16, 17, 64, 1024])
 def test_split_counts_do_not_change_the_result(splits):
     s = W.spec("qwen7b", batch=2, ctx_len=[2000, 33], capacity=2048)
     host = W.generate(s)
@@ -306,6 +320,32 @@ def test_empty_and_single_token_rows():
     parts = ops.sparse_decode_attend(dw.desc, dw.q, dw.K, dw.V, torch.from_numpy(sel).cuda(), dw.ctx, 4)
     out2, lse2 = ops.combine_splits(dw.desc, parts, None)
     assert torch.all(out2[0] == 0) and torch.all(torch.isinf(lse2[0]))
+
+
+@pytest.mark.parametrize("path", ["tma", "registers"])
+def test_cache_past_the_context_is_never_used(path):
+    """Slots past each sequence's context hold NaN: the partial last page must
+    be masked (scores and values), not multiplied by a zero weight."""
+    s = W.spec("qwen7b", batch=2, ctx_len=[1000 + 5, 37], capacity=1024)
+    host = W.generate(s)
+    dw = PT.upload(s, host, **PATHS[path])
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16, device="cuda")
+    for b, n in enumerate(host.ctx_len):
+        dw.K[b, :, n:] = nan
+        dw.V[b, :, n:] = nan
+    npages = [-(-int(n) // 16) for n in host.ctx_len]
+    lists = [np.arange(npages[b]) for b in range(2) for _ in range(s.num_kv_heads)]
+    o, _ = PT.attend_on(dw, lists, num_splits=3)
+    ops.pipeline_check()
+    assert np.isfinite(o).all()
+    G = s.group
+    for b in range(2):
+        n = int(host.ctx_len[b])
+        for h in range(s.num_kv_heads):
+            q = O.to_f64(host.q[b, h * G:(h + 1) * G], "bf16")
+            ref, _ = O.softmax_attention(q, O.to_f64(host.K[b, h, :n], "bf16"),
+                                         O.to_f64(host.V[b, h, :n], "bf16"), s.scale)
+            PT.assert_close(s, o[b, h * G:(h + 1) * G], ref, f"row {(b, h)}")
 
 
 def test_padded_page_lists_are_skipped():
