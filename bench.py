@@ -332,15 +332,19 @@ def run_ours(args, s: W.Spec):
     # per-kernel device time: eager launches bracketed by events on the
     # launching stream, queued behind a sleep so the host stays ahead
     ksteps = max(50, min(args.steps, 400))
-    ev = {k: ([], []) for k in ("select", "attend")}
+    one = steps_obj[0].one_launch and ops.quest_step_splits(dw.desc, s.k_pages) > 0
+    ev = {k: ([], []) for k in (("step",) if one else ()) + ("select", "attend")}
     with torch.cuda.stream(stream):
         for i in range(ksteps):
             if i % 25 == 0:
                 torch.cuda._sleep(int(4e7))  # keeps the queue ahead of the device
             st = steps_obj[i % nsets]
             K, V, kmin, kmax = sets[i % nsets]
-            for name, fn in (("select", lambda: st.select(dw.q, kmin, kmax, dw.ctx)),
-                             ("attend", lambda: st.attend(dw.q, K, V, dw.ctx))):
+            stages = [("select", lambda: st.select(dw.q, kmin, kmax, dw.ctx)),
+                      ("attend", lambda: st.attend(dw.q, K, V, dw.ctx))]
+            if one:
+                stages.insert(0, ("step", lambda: st(dw.q, K, V, kmin, kmax, dw.ctx)))
+            for name, fn in stages:
                 a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 fn()
@@ -380,9 +384,15 @@ def run_ours(args, s: W.Spec):
     peak, peak_kind = load_peaks()
     value = total_bytes / t_max / 1e9
     ms_step = 1e3 * t_max / args.steps
-    # dominant kernel by algorithmic bytes: the selector's metadata stream
-    dom = "select" if nbytes["select"] >= nbytes["attend"] else "attend"
-    dom_bytes = nbytes[dom]
+    # dominant kernel: the one-launch step (all bytes of the step), else the
+    # larger of the two stages by algorithmic bytes
+    if one:
+        dom, dom_bytes, dom_name = "step", nbytes["total"], "quest_step_kernel (score + top-k + attend + combine)"
+    else:
+        dom = "select" if nbytes["select"] >= nbytes["attend"] else "attend"
+        dom_bytes = nbytes[dom]
+        dom_name = ("select: quest_score_kernel + topk_kernel" if dom == "select"
+                    else "attend: attend_tma_kernel with the cluster combine")
     achieved = dom_bytes / (kern_us[dom] * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -392,19 +402,18 @@ def run_ours(args, s: W.Spec):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy, see workloads.py)",
         "config": {"workload": _workload_name(s), "batch": s.batch, "ctx_len": s.ctx_len[0],
                    "seq_len": s.ctx_len[0], "page_size": s.page_size, "budget_tokens": s.k_pages * s.page_size,
-                   "num_splits": S, "buffer_sets": nsets,
+                   "num_splits": ops.quest_step_splits(dw.desc, s.k_pages) if one else S,
+                   "launches_per_step": 1 if one else 2, "buffer_sets": nsets,
                    "l2": f"inputs rotate over {nsets} buffer sets ({nsets * nbytes['total'] / 1e6:.0f} MB >= 4x L2 {l2 / 1e6:.0f} MB)",
                    "parallelism": f"weak: {world} GPU(s), {s.batch} sequences each"},
         "bytes_per_step": nbytes["total"], "bytes_select": nbytes["select"], "bytes_attend": nbytes["attend"],
         "kernel_us": {k: round(v, 2) for k, v in kern_us.items()},
-        "roofline": {"bound": "hbm",
-                     "kernel": ("select: quest_score_kernel + topk_kernel" if dom == "select"
-                                else "attend: attend_mma_kernel with fused combine"),
+        "roofline": {"bound": "hbm", "kernel": dom_name,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_kind": f"{peak_kind} (burst copy)"},
         "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4)},
-        "gpu_launches": 3 * args.steps,  # quest_score, topk, attend (+combine) per step
+        "gpu_launches": (1 if one else 3) * args.steps,  # one step kernel, or score, top-k, attend
         "clocks": clk,
         "e2e": {"value": round(e2e_bytes / e2e_max / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(1e6 * e2e_max / esteps, 2),

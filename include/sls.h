@@ -312,11 +312,14 @@ size_t sls_attend_combine_workspace_size(const sls_attn_desc* desc,
 /*
  * Both stages in one launch: sls_sparse_decode_attend followed, inside the
  * same kernel, by the combine of each row.  num_splits == 0 lets the library
- * pick the split count (sls_attend_default_splits).  Every CTA of a row takes an
- * arrival ticket after writing its partials; the CTA that arrives last
- * merges the row's splits exactly as sls_combine_splits does (no CTA ever
- * waits for another).  Arguments as in the two separate calls; the partials
- * live in the workspace, whose first 4*B*Hkv bytes hold the tickets.
+ * pick the split count (sls_attend_default_splits).  Where the tensor-map
+ * fed kernel runs (bf16, pages of >= 16 tokens) with at most 16 splits, the
+ * splits of a row form one thread-block cluster and combine through
+ * distributed shared memory; otherwise every CTA of a row takes an arrival
+ * ticket after writing its partials and the CTA that arrives last merges the
+ * row's splits exactly as sls_combine_splits does (no CTA ever waits for
+ * another).  Arguments as in the two separate calls; the partials live in
+ * the workspace, whose first 4*B*Hkv bytes hold the tickets.
  *   workspace  >= sls_attend_combine_workspace_size() bytes; it must be
  *              zero-filled before its first use, and every call leaves the
  *              tickets at zero again.  Calls sharing a workspace must not
@@ -330,6 +333,45 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
                                             const float* sink, void* out, float* lse,
                                             void* workspace, size_t workspace_bytes,
                                             void* stream);
+
+/* ---- the whole Quest decode step ---------------------------------------- */
+
+/* Bytes of workspace sls_quest_decode_step needs for this budget and split
+ * count (0 on an invalid descriptor). */
+size_t sls_quest_decode_step_workspace_size(const sls_attn_desc* desc, int32_t k, int32_t num_splits);
+
+/* CTAs per row (the cluster size) the one-launch Quest step uses for this
+ * shape and budget by default; 0 when the shape takes the two-launch path. */
+int32_t sls_quest_decode_step_splits(const sls_attn_desc* desc, int32_t k);
+
+/*
+ * One Quest decode step: the selection of sls_select_pages (budget k,
+ * n_sink_pages, n_local_tokens, same tie rule and list order) and the
+ * sparse attention with the combine of sls_sparse_decode_attend_combine
+ * over the chosen pages ("Don't read the haystack", Part two).
+ *
+ * For bf16 caches with pages of >= 16 tokens (k <= 4096, Cap/P <= 131072,
+ * 16-byte aligned cache and metadata pointers) this is ONE kernel launch: a
+ * thread-block cluster per (sequence, KV head) scores its row's pages from
+ * the min/max metadata, selects the top k inside the cluster and attends to
+ * them; the scores and the page list never leave shared memory.  Otherwise
+ * the call runs sls_select_pages then sls_sparse_decode_attend_combine.
+ *   kmin, kmax  [B, Hkv, Cap/P, D] page metadata (sls_pagemeta_build)
+ *   page_idx    [B*Hkv, k] int32 receiving the chosen pages (ascending, -1
+ *               padded), or NULL
+ *   out, lse    as in sls_combine_splits
+ *   num_splits  CTAs per row (0: the library's choice; the one-launch kernel
+ *               uses at most 16)
+ *   workspace   >= sls_quest_decode_step_workspace_size() bytes, zero-filled
+ *               before its first use (the one-launch kernel leaves it alone;
+ *               the two-launch path keeps its tickets at zero).
+ */
+sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const void* k_cache,
+                                 const void* v_cache, const void* kmin, const void* kmax,
+                                 const int32_t* ctx_len, int32_t k, int32_t n_sink_pages,
+                                 int32_t n_local_tokens, const float* sink, int32_t* page_idx,
+                                 void* out, float* lse, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* ---- diagnostics ------------------------------------------------------- */
 

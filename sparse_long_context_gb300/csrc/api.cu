@@ -104,7 +104,7 @@ int32_t sls_version(void) { return 10000; }
 
 sls_status sls_pipeline_check(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(SLS_ECUDA, "device synchronisation failed");
-  const unsigned int n = sls::take_attend_wait_timeouts();
+  const unsigned int n = sls::take_attend_wait_timeouts() + sls::take_step_wait_timeouts();
   if (n) return fail(SLS_ETIMEOUT, "%u pipelined CTA(s) gave up waiting for their copies", n);
   return SLS_OK;
 }
@@ -300,6 +300,76 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
   return cuda_status(sls::launch_attend(s, q, k_cache, v_cache, page_idx, idx_stride, count, k_fixed, ctx_len,
                                         num_splits, o_part, m_part, l_part, (cudaStream_t)stream, &f),
                      "sls_sparse_decode_attend_combine");
+}
+
+size_t sls_quest_decode_step_workspace_size(const sls_attn_desc* desc, int32_t k, int32_t num_splits) {
+  sls::Shape s;
+  if (check_desc(desc, &s) || k < 1 || num_splits < 0 || num_splits > 1024) return 0;
+  // what the two-launch path needs (the one-launch kernel uses none of it)
+  return align256(sls::select_pages_workspace(s)) + align256((size_t)s.B * s.Hkv * k * 4) +
+         sls_attend_combine_workspace_size(desc, num_splits);
+}
+
+int32_t sls_quest_decode_step_splits(const sls_attn_desc* desc, int32_t k) {
+  sls::Shape s;
+  if (check_desc(desc, &s) || k < 1 || k > (s.Cap >> s.pshift) || !sls::quest_step_eligible(s, k)) return 0;
+  return sls::quest_step_splits(s, k);
+}
+
+sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const void* k_cache, const void* v_cache,
+                                 const void* kmin, const void* kmax, const int32_t* ctx_len, int32_t k,
+                                 int32_t n_sink_pages, int32_t n_local_tokens, const float* sink, int32_t* page_idx,
+                                 void* out, float* lse, int32_t num_splits, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(kmin); REQUIRE(kmax); REQUIRE(ctx_len); REQUIRE(out);
+  const int npcap = s.Cap >> s.pshift;
+  if (k < 1 || k > npcap) return fail(SLS_EINVAL, "k=%d must be in [1, Cap/P=%d]", k, npcap);
+  if (n_sink_pages < 0 || n_local_tokens < 0) return fail(SLS_EINVAL, "n_sink_pages and n_local_tokens must be >= 0");
+  const int64_t forced_max =
+      (int64_t)n_sink_pages + (n_local_tokens > 0 ? ((int64_t)n_local_tokens + s.P - 1) / s.P + 1 : 0);
+  if (forced_max > k)
+    return fail(SLS_EINVAL, "budget k=%d cannot hold the forced pages (up to %lld)", k, (long long)forced_max);
+  if (s.P == 1 && kmin != kmax) return fail(SLS_EINVAL, "page_size 1: pass the key cache as both kmin and kmax");
+  if (num_splits < 0 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [0, 1024]", num_splits);
+  const size_t need = sls_quest_decode_step_workspace_size(desc, k, num_splits);
+  if (!workspace || workspace_bytes < need)
+    return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  bool handled = false;
+  cudaError_t e = sls::launch_quest_step(s, q, k_cache, v_cache, kmin, kmax, ctx_len, k, n_sink_pages,
+                                         n_local_tokens, sink, page_idx, out, lse, num_splits,
+                                         (cudaStream_t)stream, &handled);
+  if (handled) return cuda_status(e, "sls_quest_decode_step");
+  // two launches: select into page_idx (or the workspace), then attend with the fused combine
+  const size_t chunk = (size_t)(npcap + sls::select_pages_cluster() - 1) / sls::select_pages_cluster();
+  if (chunk * 4 > sls::select_pages_smem_limit())
+    return fail(SLS_EUNSUPPORTED, "Cap/P=%d pages per row exceeds the supported %zu", npcap,
+                sls::select_pages_smem_limit() / 4 * sls::select_pages_cluster());
+  char* w = static_cast<char*>(workspace);
+  void* sel_ws = w;
+  w += align256(sls::select_pages_workspace(s));
+  int32_t* list = page_idx ? page_idx : reinterpret_cast<int32_t*>(w);
+  w += align256((size_t)s.B * s.Hkv * k * 4);
+  e = sls::launch_select_pages(s, q, kmin, kmax, ctx_len, k, n_sink_pages, n_local_tokens, list, sel_ws,
+                               (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "sls_quest_decode_step (select)");
+  const size_t heads = (size_t)s.B * s.Hq * (num_splits ? num_splits : sls::max_auto_splits(s));
+  sls::FusedCombine f;
+  f.tickets = reinterpret_cast<int32_t*>(w);
+  w += align256((size_t)s.B * s.Hkv * 4);
+  float* o_part = reinterpret_cast<float*>(w);
+  w += align256(heads * s.D * 4);
+  float* m_part = reinterpret_cast<float*>(w);
+  w += align256(heads * 4);
+  float* l_part = reinterpret_cast<float*>(w);
+  f.sink = sink;
+  f.out = out;
+  f.lse = lse;
+  return cuda_status(sls::launch_attend(s, q, k_cache, v_cache, list, k, nullptr, k, ctx_len, num_splits, o_part,
+                                        m_part, l_part, (cudaStream_t)stream, &f),
+                     "sls_quest_decode_step (attend)");
 }
 
 sls_status sls_combine_splits(const sls_attn_desc* desc, const float* o_part, const float* m_part,

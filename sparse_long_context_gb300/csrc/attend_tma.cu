@@ -18,42 +18,18 @@
 // Each K and V byte is read from memory once for all heads of the group.
 // Tokens of a group that lie past the context are masked: their scores are
 // set to -inf and their V values to zero before the product.
-#include "attend_common.cuh"
+#include "attend_tma.cuh"
 #include "launch.h"
-#include "mma.cuh"
-#include "tma.cuh"
 
 #include <algorithm>
-#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 namespace sls {
 
-constexpr int kTmaConsumers = 4;      // consumer warps per CTA
-constexpr int kTmaStages = 8;         // ring stages (a multiple of the consumer warps)
 constexpr int kTmaMinBlocks = 3;      // resident CTAs per SM the budgets are sized for
 constexpr int kTmaStaged = 256;       // page-list entries staged in shared memory
-constexpr int kMaxClusterSplits = 16;  // splits of a row that may combine inside one cluster
-static_assert(kTmaStages % kTmaConsumers == 0, "a stage must always be consumed by the same warp");
 
 __device__ unsigned int g_attend_wait_timeouts = 0;
-
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-template <int D>
-struct TmaLayout {
-  static constexpr int GROUP = 16 * D * 2;          // bytes of K (or V) of a 16-token group
-  static constexpr int STAGE = 2 * GROUP;           // K then V
-  static constexpr int BOX = 16 * 128;              // one 64-channel box: 16 rows of 128 bytes
-  static constexpr int NBOX = D / 64;
-  static constexpr size_t RING = (size_t)kTmaStages * STAGE;
-  static constexpr size_t MERGE = (size_t)kTmaConsumers * 8 * D * sizeof(float);  // warps' accumulators
-  static constexpr size_t SMEM = (RING > MERGE ? RING : MERGE) + 1024;  // + alignment slack
-};
 
 // First cache position of group gi of the slice and the number of its tokens
 // inside the context (<= 0 when the group is empty: padded entry, page out
@@ -70,80 +46,6 @@ __device__ __forceinline__ int group_base(const AttendArgs& a, const Slice& sl, 
   return base;
 }
 
-// One group from the stage at shared address `stage`.  Lane (r, m) supplies
-// ldmatrix row addresses for matrix j = lane / 8, row i = lane % 8: token
-// 8 * (j / 2) + i and 8-channel chunk 2 * step + (j % 2), which makes the
-// four matrices the two n-tiles' (or the k-halves') fragments in the order
-// the mma wants.
-template <int D>
-__device__ __forceinline__ void tma_group(uint32_t stage, int lim, const uint32_t (&qa)[D / 16][2],
-                                          float (&o)[D / 16][4], float& m_run, float& l_run, float sl2,
-                                          int lane) {
-  using L = TmaLayout<D>;
-  constexpr int KS = D / 16;
-  const int m = lane & 3;
-  const int j = lane >> 3, i = lane & 7;
-  const int tok = 8 * (j >> 1) + i;
-  // 128-byte swizzle: 16-byte chunk c of the row of token t sits at chunk c ^ (t % 8)
-  auto row_addr = [&](uint32_t half_base, int c16) -> uint32_t {
-    const int bx = c16 >> 3, c = c16 & 7;
-    return half_base + bx * L::BOX + tok * 128 + ((c ^ i) << 4);
-  };
-  float sc[2][2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int c = 0; c < 2; ++c) sc[nt][c][0] = sc[nt][c][1] = sc[nt][c][2] = sc[nt][c][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    uint32_t b00, b01, b10, b11;
-    ldsm_x4(row_addr(stage, 2 * ks + (j & 1)), b00, b01, b10, b11);
-    mma_bf16(sc[0][ks & 1], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
-    mma_bf16(sc[1][ks & 1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
-  }
-  // lane (r, m): head r, tokens 2m, 2m+1 (n-tile 0) and 8+2m, 9+2m (n-tile 1)
-  const int t0 = 2 * m;
-  float s4[4];
-  s4[0] = t0 < lim ? (sc[0][0][0] + sc[0][1][0]) * sl2 : kNegInf;
-  s4[1] = t0 + 1 < lim ? (sc[0][0][1] + sc[0][1][1]) * sl2 : kNegInf;
-  s4[2] = t0 + 8 < lim ? (sc[1][0][0] + sc[1][1][0]) * sl2 : kNegInf;
-  s4[3] = t0 + 9 < lim ? (sc[1][0][1] + sc[1][1][1]) * sl2 : kNegInf;
-  float gm = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
-  gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
-  gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
-  const float mn = fmaxf(m_run, gm);
-  const bool live = mn != kNegInf;
-  const float alpha = live ? ex2_approx(m_run - mn) : 1.f;
-  m_run = mn;
-  float p[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) p[k] = live ? ex2_approx(s4[k] - mn) : 0.f;
-  l_run = fmaf(l_run, alpha, (p[0] + p[1]) + (p[2] + p[3]));
-  const uint32_t pb0 = pack_bf16(p[0], p[1]), pb1 = pack_bf16(p[2], p[3]);
-  // accumulator columns are heads 2m and 2m+1
-  const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * m);
-  const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * m + 4);
-  if (!__all_sync(0xffffffffu, a_lo == 1.f && a_hi == 1.f)) {
-#pragma unroll
-    for (int t = 0; t < KS; ++t) {
-      o[t][0] *= a_lo; o[t][1] *= a_hi; o[t][2] *= a_lo; o[t][3] *= a_hi;
-    }
-  }
-  // V values of tokens past the context may be anything (even NaN): zero them
-  const uint32_t mlo = (t0 < lim ? 0x0000ffffu : 0u) | (t0 + 1 < lim ? 0xffff0000u : 0u);
-  const uint32_t mhi = (t0 + 8 < lim ? 0x0000ffffu : 0u) | (t0 + 9 < lim ? 0xffff0000u : 0u);
-  const uint32_t vstage = stage + L::GROUP;
-#pragma unroll
-  for (int t = 0; t < KS; ++t) {
-    uint32_t a0, a1, a2, a3;
-    ldsm_x4_t(row_addr(vstage, 2 * t + (j & 1)), a0, a1, a2, a3);
-    if (lim < 16) {
-      a0 &= mlo; a1 &= mlo; a2 &= mhi; a3 &= mhi;
-    }
-    mma_bf16(o[t], a0, a1, a2, a3, pb0, pb1);
-  }
-}
-
 template <int D>
 __global__ void __launch_bounds__((kTmaConsumers + 1) * 32, kTmaMinBlocks)
 attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -158,10 +60,7 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   __shared__ int s_pg[kTmaStaged];
   __shared__ float sM[W][8], sL[W][8], sF[W][8];  // warps' max, sum and merge weight per head
   __shared__ float sHm[8], sHl[8];                 // the CTA's merged max (natural log) and sum
-  // cluster mode: the partials pushed here by the row's splits (this CTA owns
-  // a contiguous share of the row's G x D outputs)
-  __shared__ float s_in_o[8 * D + kMaxClusterSplits];
-  __shared__ float s_in_m[kMaxClusterSplits * 8], s_in_l[kMaxClusterSplits * 8];
+  __shared__ ClusterInbox<D> inbox;                // cluster mode: partials pushed by the row's splits
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // every CTA of the cluster announces that it runs; the matching wait comes
@@ -210,11 +109,8 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
           mbar_arrive_expect_tx(&full[st], L::STAGE);
           const int y = row * a.Cap + base;
           unsigned char* dst = ring + st * L::STAGE;
-#pragma unroll
-          for (int bx = 0; bx < L::NBOX; ++bx) tma_load_2d(dst + bx * L::BOX, &tk, 64 * bx, y, &full[st]);
-#pragma unroll
-          for (int bx = 0; bx < L::NBOX; ++bx)
-            tma_load_2d(dst + L::GROUP + bx * L::BOX, &tv, 64 * bx, y, &full[st]);
+          tma_load_3d(dst, &tk, 0, y, 0, &full[st]);
+          tma_load_3d(dst + L::GROUP, &tv, 0, y, 0, &full[st]);
         } else {
           mbar_arrive(&full[st]);  // nothing to copy: the phase completes at once
         }
@@ -264,79 +160,11 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   __syncthreads();  // every stage has been consumed (or drained): the ring becomes the merge area
 
   float* sO = reinterpret_cast<float*>(ring);  // [W][8 heads][D]
-  if (warp < W) {
-    const int r = lane >> 2, m = lane & 3;
-#pragma unroll
-    for (int t = 0; t < KS; ++t) {
-      const int ch = 16 * t + r;
-      sO[(warp * 8 + 2 * m) * D + ch] = o[t][0];
-      sO[(warp * 8 + 2 * m + 1) * D + ch] = o[t][1];
-      sO[(warp * 8 + 2 * m) * D + ch + 8] = o[t][2];
-      sO[(warp * 8 + 2 * m + 1) * D + ch + 8] = o[t][3];
-    }
-  }
-  // per head: the warps' weights exp2(m_w - M) and the CTA's max and sum
-  if (threadIdx.x < G) {
-    const int g = threadIdx.x;
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < W; ++w) M = fmaxf(M, sM[w][g]);
-    float Lh = 0.f;
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float f = (M == kNegInf || sM[w][g] == kNegInf) ? 0.f : exp2f(sM[w][g] - M);
-      sF[w][g] = f;
-      Lh = fmaf(sL[w][g], f, Lh);
-    }
-    sHm[g] = M == kNegInf ? kNegInf : M * kLn2;
-    sHl[g] = Lh;
-  }
-  __syncthreads();
+  merge_warps<D, W>(o, G, sO, sM, sL, sF, sHm, sHl);
   const int GD = G * D;
   if (a.cluster) {
-    // stage two inside the row's cluster: each split pushes its merged
-    // partial into the shared memory of the CTAs owning the outputs, one
-    // cluster barrier publishes the pushes, each owner combines locally
-    namespace cg = cooperative_groups;
-    cg::cluster_group cl = cg::this_cluster();
-    const int S = a.S;
-    const int chunk = (GD + S - 1) / S;
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    for (int it = threadIdx.x; it < GD; it += NT) {
-      const int g = it / D, d = it % D;
-      float av = 0.f;
-#pragma unroll
-      for (int w = 0; w < W; ++w) av = fmaf(sO[(w * 8 + g) * D + d], sF[w][g], av);
-      const int owner = it / chunk;
-      cl.map_shared_rank(s_in_o, owner)[split * chunk + (it - owner * chunk)] = av;
-    }
-    if (threadIdx.x < S * G) {
-      const int owner = threadIdx.x / G, g = threadIdx.x % G;
-      cl.map_shared_rank(s_in_m, owner)[split * 8 + g] = sHm[g];
-      cl.map_shared_rank(s_in_l, owner)[split * 8 + g] = sHl[g];
-    }
-    cl.sync();
-    const size_t hq0 = (size_t)b * a.Hq + (size_t)h * G;
-    const int i0 = split * chunk, i1 = min(GD, i0 + chunk);
-    for (int it = i0 + threadIdx.x; it < i1; it += NT) {
-      const int g = it / D, d = it % D;
-      float M = kNegInf;
-      for (int s = 0; s < S; ++s) M = fmaxf(M, s_in_m[s * 8 + g]);
-      const float sk = a.sink ? a.sink[h * G + g] : kNegInf;
-      M = fmaxf(M, sk);
-      float Ls = 0.f, acc = 0.f;
-      for (int s = 0; s < S; ++s) {
-        const float ms = s_in_m[s * 8 + g];
-        if (ms == kNegInf || M == kNegInf) continue;
-        const float w = expf(ms - M);
-        Ls = fmaf(s_in_l[s * 8 + g], w, Ls);
-        acc = fmaf(s_in_o[s * chunk + (it - i0)], w, acc);
-      }
-      if (a.sink && M != kNegInf) Ls += expf(sk - M);
-      static_cast<bf16*>(a.out)[(hq0 + g) * D + d] = __float2bfloat16_rn(Ls > 0.f ? acc / Ls : 0.f);
-      if (d == 0 && a.lse) a.lse[hq0 + g] = Ls > 0.f ? M + logf(Ls) : kNegInf;
-    }
-    return;  // nothing reads this CTA's shared memory after the barrier
+    cluster_push_combine<D, W, NT>(a, row, split, sO, sF, sHm, sHl, &inbox, true);
+    return;
   }
   for (int it = threadIdx.x; it < GD; it += NT) {
     const int g = it / D, d = it % D;
@@ -370,15 +198,16 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [tokens, D] bf16 rows of D * 2 bytes; 64-channel x 16-token boxes, 128-byte swizzle.
-static bool encode_cache_map(CUtensorMap* map, const void* base, uint64_t tokens, int D) {
+bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, int D) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)tokens};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, 16};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  // dims: 64 channels, rows, D/64 halves (the halves' stride, 128 bytes, is
+  // smaller than the rows' one: the box lands as [half][16 rows][64])
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+  cuuint32_t box[3] = {64, 16, (cuuint32_t)(D / 64)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -457,7 +286,7 @@ template <int D>
 static cudaError_t tma_launch(const Shape& s, const AttendArgs& a, cudaStream_t st, bool* handled) {
   CUtensorMap tk, tv;
   const uint64_t tokens = (uint64_t)s.B * s.Hkv * s.Cap;
-  if (!encode_cache_map(&tk, a.k, tokens, D) || !encode_cache_map(&tv, a.v, tokens, D)) return cudaSuccess;
+  if (!encode_rows_map(&tk, a.k, tokens, D) || !encode_rows_map(&tv, a.v, tokens, D)) return cudaSuccess;
   *handled = true;
   cudaError_t e = cudaFuncSetAttribute(attend_tma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)TmaLayout<D>::SMEM);

@@ -85,6 +85,17 @@ int attend_tma_per_sm(const Shape& s);
 int attend_tma_splits(const Shape& s, int groups_per_row);
 // Reads and clears the count of attend CTAs whose bounded waits gave up.
 unsigned int take_attend_wait_timeouts();
+
+// Fused Quest step (bf16, pages of >= 16 tokens): select + attend + combine
+// in one launch.  *handled is false (and nothing is enqueued) when the shape
+// is not covered.
+bool quest_step_eligible(const Shape& s, int k);
+int quest_step_splits(const Shape& s, int k);
+cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache, const void* v_cache,
+                              const void* kmin, const void* kmax, const int32_t* ctx_len, int k, int n_sink,
+                              int n_local, const float* sink, int32_t* page_idx, void* out, float* lse,
+                              int num_splits, cudaStream_t st, bool* handled);
+unsigned int take_step_wait_timeouts();
 int max_auto_splits(const Shape& s);
 cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const void* v,
                           const int32_t* page_idx, int idx_stride, const int32_t* count,

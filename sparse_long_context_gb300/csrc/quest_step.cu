@@ -1,0 +1,996 @@
+// Fused Quest decode step for bf16 caches with pages of >= 16 tokens: page
+// selection (bound, top-k) and sparse attention with the split combine in
+// one launch ("Don't read the haystack", Part two: the page bound
+// sum_c max(q_c * kmin_c, q_c * kmax_c), max over the GQA group, budget k
+// including the sink page and the local pages; then attention over the
+// chosen pages only).
+//
+// One thread-block cluster of C CTAs per (sequence, KV head) row; CTA c:
+//   1. score   streams the page min/max of pages [c*chunk, (c+1)*chunk)
+//              through a ring of shared-memory stages (tensor-map copies of
+//              16 pages of kmax and of kmin) and scores them on the tensor
+//              cores: U = kmax . max(q, 0) + kmin . min(q, 0), a 16-page x
+//              8-head product per stage; the page score is the max over the
+//              group's heads.  One order-preserving 32-bit key per page stays
+//              in shared memory (forced pages get the largest key).
+//   2. top-k   the cluster finds the k-th largest key T by four MSB-first
+//              passes over 8-bit digits (each CTA histograms its keys, every
+//              CTA sums the C histograms through distributed shared memory),
+//              and how many T-valued keys to take (ties go to lower pages).
+//              Each CTA writes its chosen pages, ascending, into the row's
+//              list in CTA 0 (and to page_idx) at offsets from the cluster's
+//              per-CTA counts.
+//   3. attend  CTA c takes a contiguous 1/C of the list and runs the
+//              tensor-core online-softmax attention of the split-K kernel on
+//              its 16-token groups, fed by the same ring.
+//   4. combine the splits' partials meet in distributed shared memory.
+// Nothing of the step goes through global memory but its inputs and outputs.
+#include "attend_tma.cuh"
+#include "launch.h"
+
+#include <algorithm>
+
+namespace sls {
+
+constexpr int kStepMinBlocks = 3;
+constexpr int kStepMaxChunk = 8192;  // pages scored by one CTA (keys kept in shared memory)
+constexpr int kStepMaxK = 4096;      // page budget (the row's list sits in shared memory)
+constexpr uint32_t kForcedKey32 = 0xffffffffu;
+
+__device__ unsigned int g_step_wait_timeouts = 0;
+
+struct StepArgs {
+  AttendArgs a;  // q, k, v, ctx_len, sink, out, lse, shapes, qscale; S = C; cluster = 1
+  const void* kmin;   // [rows, Cap / P, D] page minima
+  const void* kmax;   // [rows, Cap / P, D] page maxima
+  int32_t* page_idx;  // [rows, k] or null
+  int k, n_sink, n_local;
+  int chunk;  // pages scored per CTA (multiple of 16)
+  int npcap;  // Cap / P
+  size_t keys_bytes;   // shared-memory region of the keys (also the combine inbox)
+  int scratch_off;     // top-k scratch in the ring, after the row's keys (all-keys selection)
+  int topk_mode;       // 0: candidates of every CTA, 1: all keys to every CTA
+  int cand_cap;        // candidates one CTA may send
+};
+
+template <int D>
+struct StepLayout {
+  static constexpr size_t RING = (size_t)kTmaStages * TmaLayout<D>::STAGE;
+  static constexpr size_t MERGE = (size_t)kTmaConsumers * 8 * D * sizeof(float);
+  static constexpr size_t RING_REGION = RING > MERGE ? RING : MERGE;
+};
+
+// Scores of the 16 pages of the stage at `stage` (kmax tile then kmin
+// tile).  A = the page tile (rows = pages) from ldmatrix; lane (r, m) gives
+// the row address of matrix j = lane / 8, row i = lane % 8: page
+// 8 * (j % 2) + i, 8-channel chunk 2 * step + j / 2.  B = max(q, 0) for
+// kmax and min(q, 0) for kmin (heads as columns).
+template <int D>
+__device__ __forceinline__ void score_stage(uint32_t stage, const uint32_t (&bp)[D / 16][2],
+                                            const uint32_t (&bn)[D / 16][2], int G, int lane, float& v0,
+                                            float& v1) {
+  using L = TmaLayout<D>;
+  constexpr int KS = D / 16;
+  const int m = lane & 3;
+  const int j = lane >> 3, i = lane & 7;
+  const int page = 8 * (j & 1) + i;
+  auto row_addr = [&](uint32_t base, int c16) -> uint32_t {
+    const int bx = c16 >> 3, c = c16 & 7;
+    return base + bx * L::BOX + page * 128 + ((c ^ i) << 4);
+  };
+  float ch[4] = {0.f, 0.f, 0.f, 0.f}, cl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(row_addr(stage, 2 * ks + (j >> 1)), a0, a1, a2, a3);
+    mma_bf16(ch, a0, a1, a2, a3, bp[ks][0], bp[ks][1]);
+    ldsm_x4(row_addr(stage + L::GROUP, 2 * ks + (j >> 1)), a0, a1, a2, a3);
+    mma_bf16(cl, a0, a1, a2, a3, bn[ks][0], bn[ks][1]);
+  }
+  // C[page][head]: c0, c1 = page r, heads 2m, 2m+1; c2, c3 = page r + 8
+  const bool h0 = 2 * m < G, h1 = 2 * m + 1 < G;
+  v0 = kNegInf;
+  v1 = kNegInf;
+  if (h0) {
+    v0 = ch[0] + cl[0];
+    v1 = ch[2] + cl[2];
+  }
+  if (h1) {
+    v0 = fmaxf(v0, ch[1] + cl[1]);
+    v1 = fmaxf(v1, ch[3] + cl[3]);
+  }
+  v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, 1));
+  v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, 2));
+  v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 1));
+  v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 2));
+}
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive scan of one int per thread over the CTA; `total` gets the sum.
+template <int NT>
+__device__ __forceinline__ int block_scan_excl(int v, int* tmp, int& total) {
+  constexpr int NWp = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < NWp ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < NWp) tmp[lane] = t;
+  }
+  __syncthreads();
+  const int before = warp > 0 ? tmp[warp - 1] : 0;
+  total = tmp[NWp - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+constexpr int kWinBins = 2048;  // window of top-16-bit values below the largest
+constexpr int kRegKeys = 32;    // keys per thread when the row's keys fit in registers
+constexpr int kLocalKeys = 8;   // keys per thread of a CTA's own selection (chunk <= NT * 8)
+constexpr int kCandMax = 1024;  // keys of the threshold bin ranked exactly
+constexpr int kTopkScratchBytes = (kWinBins + 32 + kCandMax + 256) * 4;
+
+struct TopkScalars {
+  uint32_t red_max[32];
+  uint32_t red_min[32];
+  int red_n[32];
+  int bin, rem, ncand, digit;
+  uint32_t T;
+  int take;
+};
+
+// Largest digit d (descending order) where the running count of `cnt`
+// (256 digits, counts of keys above in cnt order) reaches rem: warp 0.
+__device__ __forceinline__ void find_digit(const uint32_t* cnt, int rem, TopkScalars& sc) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c8[8], s = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    c8[u] = cnt[255 - 8 * lane - u];
+    s += c8[u];
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t above = incl - s;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    if (above < (uint32_t)rem && above + c8[u] >= (uint32_t)rem) {
+      sc.digit = 255 - 8 * lane - u;
+      sc.rem = rem - (int)above;
+    }
+    above += c8[u];
+  }
+}
+
+// MSB-first radix select over keys[0 .. n) restricted to keys whose bits
+// above `shift0 + 8` equal `prefix`: the rem-th largest T and how many
+// T-valued keys to take.  scratch: 256 words.
+template <int NT>
+__device__ __forceinline__ void radix_select(const uint32_t* keys, int n, uint32_t prefix, uint32_t pmask, int shift0,
+                                             int rem, uint32_t* hist, TopkScalars& sc, uint32_t& T, int& take) {
+  for (int shift = shift0; shift >= 0; shift -= 8) {
+    for (int d = threadIdx.x; d < 256; d += NT) hist[d] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += NT) {
+      const uint32_t key = keys[i];
+      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) find_digit(hist, rem, sc);
+    __syncthreads();
+    prefix |= (uint32_t)sc.digit << shift;
+    pmask |= 255u << shift;
+    rem = sc.rem;
+    __syncthreads();
+  }
+  T = prefix;
+  take = rem;
+}
+
+// The k-th largest of keys[0 .. n) (n > k) and how many keys equal to it to
+// take (the lowest pages first), computed by every CTA of the cluster on its
+// own copy in shared memory (rows too long for select_share_reg): the same
+// range-scaled histogram, threshold bin and exact rank; a full radix select
+// when the bin is crowded.  scratch: kWinBins + kCandMax + 256 words.
+template <int NT>
+__device__ __forceinline__ void local_topk(const uint32_t* keys, int n, int k, uint32_t* scratch, int* scan_tmp,
+                                           uint32_t& T, int& take) {
+  __shared__ TopkScalars sc;
+  uint32_t* hist = scratch;             // [kWinBins]
+  uint32_t* cand = scratch + kWinBins;  // [kCandMax]
+  uint32_t* h256 = cand + kCandMax;     // [256]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int NWp = NT / 32;
+  uint32_t mx = 0, mn = 0xffffffffu;
+  int nf = 0;
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint32_t key = keys[i];
+    if (key == kForcedKey32) {
+      ++nf;
+    } else {
+      mx = max(mx, key);
+      mn = min(mn, key);
+    }
+  }
+  for (int d = threadIdx.x; d < kWinBins; d += NT) hist[d] = 0;
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  nf = __reduce_add_sync(0xffffffffu, nf);
+  if (lane == 0) {
+    sc.red_max[warp] = mx;
+    sc.red_min[warp] = mn;
+    sc.red_n[warp] = nf;
+  }
+  if (threadIdx.x == 0) {
+    sc.ncand = 0;
+    sc.bin = -1;
+  }
+  __syncthreads();
+  const uint32_t top = __reduce_max_sync(0xffffffffu, lane < NWp ? sc.red_max[lane] : 0u);
+  const uint32_t bot = __reduce_min_sync(0xffffffffu, lane < NWp ? sc.red_min[lane] : 0xffffffffu);
+  const int nforced = __reduce_add_sync(0xffffffffu, lane < NWp ? sc.red_n[lane] : 0);
+  const int need = k - nforced;
+  if (need <= 0) {  // the first k forced pages
+    T = kForcedKey32;
+    take = k;
+    return;
+  }
+  int shift = 0;
+  while (((top - bot) >> shift) >= (uint32_t)kWinBins) ++shift;
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint32_t key = keys[i];
+    if (key != kForcedKey32) atomicAdd(&hist[(top - key) >> shift], 1u);
+  }
+  __syncthreads();
+  constexpr int BPT = (kWinBins + NT - 1) / NT;
+  const int b0 = threadIdx.x * BPT;
+  int sum = 0;
+  for (int i = 0; i < BPT; ++i) sum += b0 + i < kWinBins ? (int)hist[b0 + i] : 0;
+  int total;
+  int above = block_scan_excl<NT>(sum, scan_tmp, total);
+  for (int i = 0; i < BPT; ++i) {
+    const int c = b0 + i < kWinBins ? (int)hist[b0 + i] : 0;
+    if (above < need && above + c >= need) {
+      sc.bin = b0 + i;
+      sc.rem = need - above;
+    }
+    above += c;
+  }
+  __syncthreads();
+  if (sc.bin >= 0) {
+    const uint32_t bin = (uint32_t)sc.bin;
+    const int rem = sc.rem;
+    for (int i = threadIdx.x; i < n; i += NT) {
+      const uint32_t key = keys[i];
+      if (key != kForcedKey32 && ((top - key) >> shift) == bin) {
+        const int slot = atomicAdd(&sc.ncand, 1);
+        if (slot < kCandMax) cand[slot] = key;
+      }
+    }
+    __syncthreads();
+    const int m = sc.ncand;
+    if (m <= kCandMax) {
+      radix_select<NT>(cand, m, 0u, 0u, 24, rem, h256, sc, T, take);
+      return;
+    }
+  }
+  __syncthreads();
+  radix_select<NT>(keys, n, 0u, 0u, 24, k, h256, sc, T, take);
+}
+
+// Keys[0 .. n) into registers, thread t owning positions [t*KPT, t*KPT+KPT)
+// (position order = thread order); slots past n hold 0, below every key.
+template <int NT, int KPT>
+__device__ __forceinline__ void load_keys_reg(const uint32_t* keys, int n, uint32_t (&kk)[KPT]) {
+  const uint4* src = reinterpret_cast<const uint4*>(keys + threadIdx.x * KPT);
+#pragma unroll
+  for (int v = 0; v < KPT / 4; ++v) {
+    const int i = threadIdx.x * KPT + 4 * v;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (i + 3 < n) {
+      x = src[v];
+    } else if (i < n) {  // ragged end
+      x.x = keys[i];
+      x.y = i + 1 < n ? keys[i + 1] : 0u;
+      x.z = i + 2 < n ? keys[i + 2] : 0u;
+    }
+    kk[4 * v] = x.x; kk[4 * v + 1] = x.y; kk[4 * v + 2] = x.z; kk[4 * v + 3] = x.w;
+  }
+}
+
+// The k-th largest T of the keys held in registers (zero slots excluded;
+// k <= the number of keys) and how many T-valued keys to take, the first in
+// position order.  Bound scores cluster tightly, so the histogram spans the
+// keys' own range: bin (top - key) >> shift, with the smallest shift that
+// fits the range into kWinBins bins.  The threshold bin's keys are ranked
+// exactly (by counting, or a radix select when the bin is crowded).  Forced
+// keys (the largest value) are counted first.  Returns false when the bin
+// holds more than kCandMax keys (T and take are then undefined).
+template <int NT, int KPT>
+__device__ __forceinline__ bool kth_largest_reg(const uint32_t (&kk)[KPT], int k, uint32_t* scratch, int* scan_tmp,
+                                                uint32_t& T, int& take) {
+  // Loops over the keys are branch-free (selects, a spill bin, one slot
+  // reservation per warp): divergent branches per key cost far more here
+  // than the work they guard.
+  __shared__ TopkScalars sc;
+  uint32_t* hist = scratch;                  // [kWinBins + 32]: the last 32 bins absorb excluded keys
+  uint32_t* cand = scratch + kWinBins + 32;  // [kCandMax]
+  uint32_t* h256 = cand + kCandMax;          // [256]
+  constexpr int NWp = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // 1. range of the non-forced keys and the forced count
+  uint32_t mx = 0, mn = 0xffffffffu;
+  int nf = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t x = kk[j];
+    const bool forced = x == kForcedKey32, real = !forced && x != 0u;
+    nf += forced;
+    mx = max(mx, real ? x : 0u);
+    mn = min(mn, real ? x : 0xffffffffu);
+  }
+  for (int d = threadIdx.x; d < kWinBins + 32; d += NT) hist[d] = 0;
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  nf = __reduce_add_sync(0xffffffffu, nf);
+  if (lane == 0) {
+    sc.red_max[warp] = mx;
+    sc.red_min[warp] = mn;
+    sc.red_n[warp] = nf;
+  }
+  if (threadIdx.x == 0) {
+    sc.ncand = 0;
+    sc.bin = -1;
+  }
+  __syncthreads();
+  const uint32_t top = __reduce_max_sync(0xffffffffu, lane < NWp ? sc.red_max[lane] : 0u);
+  const uint32_t bot = __reduce_min_sync(0xffffffffu, lane < NWp ? sc.red_min[lane] : 0xffffffffu);
+  const int nforced = __reduce_add_sync(0xffffffffu, lane < NWp ? sc.red_n[lane] : 0);
+  const int need = k - nforced;
+  T = kForcedKey32;
+  take = k;
+  if (need <= 0) return true;  // the first k forced keys
+  // 2. histogram of (top - key) >> shift, the smallest shift fitting the range
+  const uint32_t span = top - bot;
+  const int shift = span >= (uint32_t)kWinBins ? 32 - __clz(span >> 11) : 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t x = kk[j];
+    const bool real = x != kForcedKey32 && x != 0u;
+    atomicAdd(&hist[real ? (top - x) >> shift : kWinBins + lane], 1u);
+  }
+  __syncthreads();
+  // 3. the bin of the need-th largest
+  constexpr int BPT = (kWinBins + NT - 1) / NT;
+  const int b0 = threadIdx.x * BPT;
+  int cnt[BPT], sum = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    cnt[i] = b0 + i < kWinBins ? (int)hist[b0 + i] : 0;
+    sum += cnt[i];
+  }
+  int total;
+  int above = block_scan_excl<NT>(sum, scan_tmp, total);
+  int mybin = -1, myrem = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    const bool hit = above < need && above + cnt[i] >= need;
+    mybin = hit ? b0 + i : mybin;
+    myrem = hit ? need - above : myrem;
+    above += cnt[i];
+  }
+  if (mybin >= 0) {
+    sc.bin = mybin;
+    sc.rem = myrem;
+  }
+  __syncthreads();
+  if (sc.bin < 0) return false;  // fewer non-forced keys than needed
+  // 4. the bin's keys, one slot reservation per warp
+  const uint32_t bin = (uint32_t)sc.bin;
+  unsigned bal[KPT];
+  int wcount = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t x = kk[j];
+    const bool in = x != kForcedKey32 && x != 0u && ((top - x) >> shift) == bin;
+    bal[j] = __ballot_sync(0xffffffffu, in);
+    wcount += __popc(bal[j]);
+  }
+  int base = 0;
+  if (lane == 0 && wcount) base = atomicAdd(&sc.ncand, wcount);
+  base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int slot = base + __popc(bal[j] & ((1u << lane) - 1u));
+    if (((bal[j] >> lane) & 1u) && slot < kCandMax) cand[slot] = kk[j];
+    base += __popc(bal[j]);
+  }
+  __syncthreads();
+  const int m = sc.ncand;
+  const int rem = sc.rem;
+  if (m > kCandMax) return false;
+  if (m <= 2 * NT) {
+    // 5. exact rank by counting (each candidate against all of them)
+    for (int i = threadIdx.x; i < m; i += NT) {
+      const uint32_t v = cand[i];
+      int gt = 0, ge = 0;
+      for (int q = 0; q < m; ++q) {
+        const uint32_t w = cand[q];
+        gt += w > v;
+        ge += w >= v;
+      }
+      if (gt < rem && ge >= rem) {
+        sc.T = v;
+        sc.take = rem - gt;
+      }
+    }
+    __syncthreads();
+    T = sc.T;
+    take = sc.take;
+  } else {
+    radix_select<NT>(cand, m, 0u, 0u, 24, rem, h256, sc, T, take);
+  }
+  return true;
+}
+
+// Positions in the ascending list of the keys chosen by (T, take): for the
+// key at position i, (#keys > T before i) + min(#T-keys before i, take).
+// Entries that land in [e0, e0 + nent) get share[pos - e0] = value[i]
+// (value = position when `values` is null).
+template <int NT, int KPT>
+__device__ __forceinline__ void place_chosen(const uint32_t (&kk)[KPT], uint32_t T, int take, int e0, int nent,
+                                             const int32_t* values, int32_t* share, int* scan_tmp) {
+  int gt = 0, eq = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    gt += kk[j] > T;
+    eq += kk[j] == T;
+  }
+  int tot;
+  const int excl = block_scan_excl<NT>((gt << 16) | eq, scan_tmp, tot);  // both totals < 2^15
+  int Gp = excl >> 16, Ep = excl & 0xffff;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t x = kk[j];
+    const bool g = x > T, e = x == T;
+    const int pos = g ? Gp + min(Ep, take) : ((e && Ep < take) ? Gp + Ep : -1);
+    Gp += g;
+    Ep += e;
+    const int i = threadIdx.x * KPT + j;
+    if (pos >= e0 && pos < e0 + nent) share[pos - e0] = values ? values[i] : i;
+  }
+}
+
+// All-keys selection of the row (keys[0 .. n) by page, n <= NT * KPT) into
+// this CTA's share of the list.  False when the exact rank overflows.
+template <int NT, int KPT>
+__device__ __forceinline__ bool select_share_reg(const uint32_t* keys, int n, int k, uint32_t* scratch, int e0,
+                                                 int nent, int32_t* share, int* scan_tmp) {
+  uint32_t kk[KPT];
+  load_keys_reg<NT, KPT>(keys, n, kk);
+  uint32_t T;
+  int take;
+  if (!kth_largest_reg<NT, KPT>(kk, k, scratch, scan_tmp, T, take)) return false;
+  place_chosen<NT, KPT>(kk, T, take, e0, nent, nullptr, share, scan_tmp);
+  return true;
+}
+
+// Candidate selection: the row's chosen pages from the cluster's candidate
+// lists (cand_key / cand_page, n candidates in page order, n <= NT * KPT).
+template <int NT, int KPT>
+__device__ __forceinline__ bool select_share_cand(const uint32_t* cand_key, const int32_t* cand_page, int n, int k,
+                                                  uint32_t* scratch, int e0, int nent, int32_t* share,
+                                                  int* scan_tmp) {
+  uint32_t kk[KPT];
+  load_keys_reg<NT, KPT>(cand_key, n, kk);
+  uint32_t T;
+  int take;
+  if (!kth_largest_reg<NT, KPT>(kk, k, scratch, scan_tmp, T, take)) return false;
+  place_chosen<NT, KPT>(kk, T, take, e0, nent, cand_page, share, scan_tmp);
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__((kTmaConsumers + 1) * 32, kStepMinBlocks)
+quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                  const __grid_constant__ CUtensorMap tmin, const __grid_constant__ CUtensorMap tmax,
+                  const StepArgs sa) {
+  namespace cg = cooperative_groups;
+  using L = TmaLayout<D>;
+  constexpr int W = kTmaConsumers, NST = kTmaStages, KS = D / 16;
+  constexpr int NT = (W + 1) * 32;
+  const AttendArgs& a = sa.a;
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* ring = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint32_t* keys = reinterpret_cast<uint32_t*>(ring + StepLayout<D>::RING_REGION);
+  ClusterInbox<D>* inbox = reinterpret_cast<ClusterInbox<D>*>(keys);  // after the top-k
+  int32_t* list = reinterpret_cast<int32_t*>(ring + StepLayout<D>::RING_REGION + sa.keys_bytes);
+  __shared__ uint64_t full[NST], empty[NST];
+  __shared__ float sM[W][8], sL[W][8], sF[W][8];
+  __shared__ float sHm[8], sHl[8];
+  __shared__ int scan_tmp[32];
+  __shared__ int s_cand_n[kMaxClusterSplits], s_cand_pre[kMaxClusterSplits], s_cand_tot;
+
+  cg::cluster_group cl = cg::this_cluster();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_fence_init();
+    tma_prefetch_map(&tk);
+    tma_prefetch_map(&tv);
+    tma_prefetch_map(&tmin);
+    tma_prefetch_map(&tmax);
+  }
+  pdl_wait();
+
+  const int C = a.S;
+  const int row = blockIdx.x / C, split = blockIdx.x % C;  // split = rank in the cluster
+  const int b = row / a.Hkv, h = row % a.Hkv;
+  const int G = a.G, k = sa.k;
+  const int N = clamp_len(a.ctx_len[b], a.Cap);
+  const int NP = (N + a.P - 1) >> a.pshift;
+  const int per = (k + C - 1) / C;  // list entries attended per CTA
+  const int e0 = split * per;
+  const int nent = max(0, min(per, k - e0));
+  __syncthreads();
+
+  uint32_t seq = 0;  // ring position (identical in every thread)
+  bool ok = true;    // this thread's waits all succeeded
+
+  // producer's and consumers' walk of `n` stages starting at ring position seq0
+  auto producer_wait = [&](uint32_t q) -> bool {
+    const int st = q % NST;
+    const uint32_t use = q / NST;
+    return use == 0 || mbar_wait(&empty[st], (use - 1) & 1);
+  };
+
+  if (NP > k) {
+    // ------------------------------------------------------------ 1. score
+    const int p0 = split * sa.chunk;
+    const int nloc = max(0, min(sa.chunk, NP - p0));
+    const int n1 = (nloc + 15) >> 4;
+    const int first_local = a.P > 0 && sa.n_local > 0 ? (max(N - sa.n_local, 0) >> a.pshift) : NP;
+    if (warp == W) {
+      if (lane == 0) {
+        int issued = 0;
+        for (int i = 0; i < n1; ++i) {
+          const uint32_t q = seq + i;
+          const int st = q % NST;
+          if (!producer_wait(q)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], L::STAGE);
+          const int y = row * sa.npcap + p0 + 16 * i;
+          unsigned char* dst = ring + st * L::STAGE;
+          tma_load_3d(dst, &tmax, 0, y, 0, &full[st]);
+          tma_load_3d(dst + L::GROUP, &tmin, 0, y, 0, &full[st]);
+          issued = i + 1;
+        }
+        // the copies have landed before the ring turns into scratch space
+        for (int i = max(0, issued - NST); i < issued; ++i) {
+          const uint32_t q = seq + i;
+          if (!mbar_wait(&full[q % NST], (q / NST) & 1)) ok = false;
+        }
+      }
+    } else {
+      const int r = lane >> 2, m = lane & 3;
+      // q split by sign as the B operand: b0 = q[head r][16ks + 2m, +1], b1 = q[r][16ks + 8 + 2m, +1]
+      uint32_t bp[KS][2], bn[KS][2];
+      {
+        const bf16* qp = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G + r) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t w = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 * u + 2 * m)) : 0u;
+            bp[ks][u] = bf16x2_relu(w);
+            bn[ks][u] = bf16x2_negpart(w);
+          }
+        }
+      }
+      const uint32_t ring_u32 = smem_u32(ring);
+      for (int i = (W + warp - (int)(seq % W)) % W; i < n1; i += W) {
+        const uint32_t q = seq + i;
+        const int st = q % NST;
+        if (!mbar_wait(&full[st], (q / NST) & 1)) {
+          ok = false;
+          break;
+        }
+        float v0, v1;
+        score_stage<D>(ring_u32 + st * L::STAGE, bp, bn, G, lane, v0, v1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (m == 0) {
+          const int i0 = 16 * i + r, i1 = i0 + 8;
+          const int pg0 = p0 + i0, pg1 = p0 + i1;
+          if (i0 < nloc) keys[i0] = (pg0 < sa.n_sink || pg0 >= first_local) ? kForcedKey32 : order_key(v0);
+          if (i1 < nloc) keys[i1] = (pg1 < sa.n_sink || pg1 >= first_local) ? kForcedKey32 : order_key(v1);
+        }
+      }
+    }
+    seq += n1;
+    __syncthreads();  // keys complete; the ring is free
+
+    // ------------------------------------------------------------ 2. top-k
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // completes the arrive made at entry
+    bool use_all = sa.topk_mode != 0;
+    if (!use_all) {
+      // Candidates: every page of the row's top k is among its own CTA's
+      // top k (ties at the CTA's threshold included), so each CTA sends
+      // only its keys >= its local k-th largest; every CTA then selects
+      // among the cluster's candidates, which stay in page order.
+      const int cap = sa.cand_cap;
+      uint32_t* scratch = reinterpret_cast<uint32_t*>(ring);
+      uint32_t* gkp = reinterpret_cast<uint32_t*>(ring + kTopkScratchBytes);  // [C][cap] (key, page) pairs
+      uint32_t* dk = gkp + 2 * C * cap;                                         // dense keys, page order
+      int32_t* dp = reinterpret_cast<int32_t*>(dk + C * cap);                   // dense pages
+      uint32_t kk[kLocalKeys];
+      load_keys_reg<NT, kLocalKeys>(keys, nloc, kk);
+      uint32_t tau = 1u;  // every real key (all are > 0) when the CTA holds at most k pages
+      if (nloc > k) {
+        int tk;
+        if (!kth_largest_reg<NT, kLocalKeys>(kk, k, scratch, scan_tmp, tau, tk)) tau = 1u;
+      }
+      const int j0 = threadIdx.x * kLocalKeys;
+      int cnt = 0;
+#pragma unroll
+      for (int j = 0; j < kLocalKeys; ++j) cnt += kk[j] >= tau;  // slots past nloc hold 0
+      int total;
+      const int off = block_scan_excl<NT>(cnt, scan_tmp, total);
+      const bool ovf = total > cap;
+      cl.sync();  // every CTA has its candidates; every ring is free
+      for (int c = 0; c < C; ++c) {
+        uint2* rkp = reinterpret_cast<uint2*>(cl.map_shared_rank(gkp, c)) + split * cap;
+        if (!ovf) {
+          int o = off;
+#pragma unroll
+          for (int j = 0; j < kLocalKeys; ++j) {
+            const bool in = kk[j] >= tau;
+            if (in) rkp[o] = make_uint2(kk[j], (uint32_t)(sa.chunk * split + j0 + j));
+            o += in;
+          }
+        }
+        if (threadIdx.x == 0) cl.map_shared_rank(s_cand_n, c)[split] = ovf ? -1 : total;
+      }
+      cl.sync();  // the cluster's candidates are delivered
+      if (threadIdx.x == 0) {
+        int t = 0;
+        for (int c = 0; c < C; ++c) {
+          s_cand_pre[c] = t;
+          t = (t < 0 || s_cand_n[c] < 0) ? -1 : t + s_cand_n[c];
+        }
+        s_cand_tot = t;
+      }
+      __syncthreads();
+      const int n = s_cand_tot;
+      if (n < 0 || n > NT * kRegKeys) {
+        use_all = true;  // same decision in every CTA: the counts are the cluster's
+      } else {
+        for (int c = 0; c < C; ++c)
+          for (int i = threadIdx.x; i < s_cand_n[c]; i += NT) {
+            const uint2 e = reinterpret_cast<const uint2*>(gkp)[c * cap + i];
+            dk[s_cand_pre[c] + i] = e.x;
+            dp[s_cand_pre[c] + i] = (int32_t)e.y;
+          }
+        __syncthreads();
+        bool okc;
+        if (n <= NT * 4) okc = select_share_cand<NT, 4>(dk, dp, n, k, scratch, e0, nent, list, scan_tmp);
+        else if (n <= NT * 8) okc = select_share_cand<NT, 8>(dk, dp, n, k, scratch, e0, nent, list, scan_tmp);
+        else if (n <= NT * 16) okc = select_share_cand<NT, 16>(dk, dp, n, k, scratch, e0, nent, list, scan_tmp);
+        else okc = select_share_cand<NT, 32>(dk, dp, n, k, scratch, e0, nent, list, scan_tmp);
+        if (!okc) use_all = true;  // identical candidates everywhere: the same in every CTA
+      }
+    }
+    if (use_all) {
+      // every CTA receives the row's keys in its ring and selects locally
+      cl.sync();  // every ring is free (and every candidate list read)
+      uint32_t* allk = reinterpret_cast<uint32_t*>(ring);  // [NP] keys of the row, by page
+      {
+        const int n4 = nloc >> 2;
+        const uint4* src4 = reinterpret_cast<const uint4*>(keys);
+        for (int c = 0; c < C; ++c) {
+          uint32_t* dst = cl.map_shared_rank(allk, c) + sa.chunk * split;  // 16-byte aligned: chunk % 16 == 0
+          uint4* dst4 = reinterpret_cast<uint4*>(dst);
+          for (int i = threadIdx.x; i < n4; i += NT) dst4[i] = src4[i];
+          for (int i = 4 * n4 + threadIdx.x; i < nloc; i += NT) dst[i] = keys[i];
+        }
+      }
+      cl.sync();  // the row's keys are complete in every CTA
+      uint32_t* scratch = reinterpret_cast<uint32_t*>(ring + sa.scratch_off);
+      bool done = false;
+      if (NP <= NT * kRegKeys) done = select_share_reg<NT, kRegKeys>(allk, NP, k, scratch, e0, nent, list, scan_tmp);
+      __syncthreads();
+      if (!done) {
+        uint32_t T;
+        int take;
+        local_topk<NT>(allk, NP, k, scratch, scan_tmp, T, take);
+        // the list positions of the chosen pages; this CTA keeps [e0, e0 + nent)
+        const int RUN = (NP + NT - 1) / NT;
+        const int i_beg = min(NP, threadIdx.x * RUN), i_end = min(NP, i_beg + RUN);
+        int gt = 0, eq = 0;
+        for (int i = i_beg; i < i_end; ++i) {
+          gt += allk[i] > T;
+          eq += allk[i] == T;
+        }
+        int tot;
+        const int excl = block_scan_excl<NT>((gt << 16) | eq, scan_tmp, tot);  // both totals < 2^15
+        int Gp = excl >> 16, Ep = excl & 0xffff;
+        for (int i = i_beg; i < i_end; ++i) {
+          const uint32_t key = allk[i];
+          int pos = -1;
+          if (key > T) {
+            pos = Gp + min(Ep, take);
+            ++Gp;
+          } else if (key == T) {
+            if (Ep < take) pos = Gp + Ep;
+            ++Ep;
+          }
+          if (pos >= e0 && pos < e0 + nent) list[pos - e0] = i;
+        }
+      }
+    }
+    __syncthreads();
+    if (sa.page_idx)
+      for (int e = threadIdx.x; e < nent; e += NT) sa.page_idx[(size_t)row * k + e0 + e] = list[e];
+  } else {
+    // every page of the context is chosen: 0 .. NP-1, then -1
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // completes the arrive made at entry
+    int32_t* gout = sa.page_idx ? sa.page_idx + (size_t)row * k : nullptr;
+    for (int e = threadIdx.x; e < nent; e += NT) {
+      const int v = e0 + e < NP ? e0 + e : -1;
+      list[e] = v;
+      if (gout) gout[e0 + e] = v;
+    }
+  }
+  fence_proxy_async_smem();  // scratch writes in the ring before the copies reuse it
+  __syncthreads();
+
+  // -------------------------------------------------------------- 3. attend
+  const int ngroups = (nent << a.pshift) >> 4;
+  auto group_at = [&](int gi, int& lim) -> int {
+    const int j0 = gi << 4;
+    const int pg = list[j0 >> a.pshift];
+    lim = 0;
+    if ((unsigned)pg >= (unsigned)(a.Cap >> a.pshift)) return 0;
+    const int base = (pg << a.pshift) + (j0 & (a.P - 1));
+    lim = min(N - base, 16);
+    return base;
+  };
+  float o[KS][4];
+  float m_run = kNegInf, l_run = 0.f;
+#pragma unroll
+  for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  if (warp == W) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int gi = 0; gi < ngroups; ++gi) {
+        const uint32_t q = seq + gi;
+        const int st = q % NST;
+        if (!producer_wait(q)) {
+          ok = false;
+          break;
+        }
+        int lim;
+        const int base = group_at(gi, lim);
+        if (lim > 0) {
+          mbar_arrive_expect_tx(&full[st], L::STAGE);
+          const int y = row * a.Cap + base;
+          unsigned char* dst = ring + st * L::STAGE;
+          tma_load_3d(dst, &tk, 0, y, 0, &full[st]);
+          tma_load_3d(dst + L::GROUP, &tv, 0, y, 0, &full[st]);
+        } else {
+          mbar_arrive(&full[st]);
+        }
+        issued = gi + 1;
+      }
+      // every copy issued has landed before the ring is reused or left
+      for (int gi = max(0, issued - NST); gi < issued; ++gi) {
+        const uint32_t q = seq + gi;
+        if (!mbar_wait(&full[q % NST], (q / NST) & 1)) ok = false;
+      }
+      if (!ok) atomicAdd(&g_step_wait_timeouts, 1u);
+    }
+  } else {
+    const int r = lane >> 2, m = lane & 3;
+    uint32_t qa[KS][2];
+    const bf16* qp = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G + r) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * m)) : 0u;
+      qa[ks][1] = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * m)) : 0u;
+    }
+    const uint32_t ring_u32 = smem_u32(ring);
+    for (int gi = (W + warp - (int)(seq % W)) % W; gi < ngroups; gi += W) {
+      const uint32_t q = seq + gi;
+      const int st = q % NST;
+      if (!mbar_wait(&full[st], (q / NST) & 1)) {
+        ok = false;
+        break;
+      }
+      int lim;
+      group_at(gi, lim);
+      if (lim > 0) tma_group<D>(ring_u32 + st * L::STAGE, lim, qa, o, m_run, l_run, a.qscale, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) atomicAdd(&g_step_wait_timeouts, 1u);
+      m_run = __int_as_float(0x7fffffff);  // the row's output becomes NaN
+    }
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (m == 0) {
+      sM[warp][r] = m_run;
+      sL[warp][r] = l_run;
+    }
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------- 4. combine
+  float* sO = reinterpret_cast<float*>(ring);
+  merge_warps<D, W>(o, G, sO, sM, sL, sF, sHm, sHl);
+  cluster_push_combine<D, W, NT>(a, row, split, sO, sF, sHm, sHl, inbox, false);
+}
+
+// ---------------------------------------------------------------- host side
+
+// Ring bytes the top-k needs: the row's keys, then its scratch.
+static size_t topk_ring_bytes(int npcap) { return ((size_t)npcap * 4 + 15) / 16 * 16 + (size_t)kTopkScratchBytes; }
+
+bool quest_step_eligible(const Shape& s, int k) {
+  const long long npcap = s.Cap >> s.pshift;
+  const size_t ring = s.D == 64 ? StepLayout<64>::RING_REGION : StepLayout<128>::RING_REGION;
+  return s.dtype == 1 && !(s.flags & 3) && s.G <= 8 && s.P >= 16 && (s.D == 64 || s.D == 128) &&
+         k <= kStepMaxK && (long long)s.B * s.Hkv * s.Cap < (1ll << 31) &&
+         (long long)s.B * s.Hkv * npcap < (1ll << 31) && topk_ring_bytes((int)npcap) <= ring &&
+         attend_tma_eligible(s);
+}
+
+template <int D>
+static size_t step_smem(int chunk, int k) {
+  const size_t keys = std::max((size_t)chunk * 4, sizeof(ClusterInbox<D>));
+  const size_t keys_al = (keys + 15) / 16 * 16;
+  return StepLayout<D>::RING_REGION + keys_al + (size_t)k * 4 + 1024;
+}
+
+template <int D>
+static int step_max_clusters(int C, size_t smem) {
+  cudaFuncSetAttribute(quest_step_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (C > 8) cudaFuncSetAttribute(quest_step_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C);
+  cfg.blockDim = dim3((kTmaConsumers + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, quest_step_kernel<D>, &cfg) != cudaSuccess) return -1;
+  return n;
+}
+
+static int chunk_for(int npcap, int C) { return ((npcap + C - 1) / C + 15) / 16 * 16; }
+
+// Cluster size: about two CTAs per SM over all rows, at most 16, each CTA
+// scoring at most kStepMaxChunk pages, all clusters resident at once when
+// that is possible.
+int quest_step_splits(const Shape& s, int k) {
+  const int rows = s.B * s.Hkv;
+  const int npcap = s.Cap >> s.pshift;
+  int C = std::min((2 * sm_count()) / rows + 1, kMaxClusterSplits);
+  while (C < kMaxClusterSplits && chunk_for(npcap, C) > kStepMaxChunk) ++C;
+  C = std::max(C, 1);
+  while (C > 1) {
+    const size_t smem = s.D == 64 ? step_smem<64>(chunk_for(npcap, C), k) : step_smem<128>(chunk_for(npcap, C), k);
+    const int fit = s.D == 64 ? step_max_clusters<64>(C, smem) : step_max_clusters<128>(C, smem);
+    if (fit < 0 || fit >= rows || (fit > 0 && rows > fit * 4)) break;  // unknown, one wave, or many waves
+    if (chunk_for(npcap, C - 1) > kStepMaxChunk) break;
+    --C;
+  }
+  return C;
+}
+
+template <int D>
+static cudaError_t step_launch(const Shape& s, const StepArgs& sa0, cudaStream_t st, bool* handled) {
+  StepArgs sa = sa0;
+  const int C = sa.a.S;
+  sa.chunk = chunk_for(sa.npcap, C);
+  if (sa.chunk > kStepMaxChunk) return cudaSuccess;
+  const size_t keys = std::max((size_t)sa.chunk * 4, sizeof(ClusterInbox<D>));
+  sa.keys_bytes = (keys + 15) / 16 * 16;
+  sa.scratch_off = (int)(((size_t)sa.npcap * 4 + 15) / 16 * 16);
+  // candidate selection when a CTA's keys fit its registers and the lists fit the ring
+  sa.cand_cap = (sa.k + 64 + 15) / 16 * 16;
+  const size_t cand_bytes = (size_t)kTopkScratchBytes + (size_t)16 * C * sa.cand_cap;
+  sa.topk_mode = (sa.chunk <= (kTmaConsumers + 1) * 32 * kLocalKeys && cand_bytes <= StepLayout<D>::RING_REGION &&
+                  C * sa.cand_cap <= (kTmaConsumers + 1) * 32 * kRegKeys)
+                     ? 0
+                     : 1;
+  const size_t smem = step_smem<D>(sa.chunk, sa.k);
+  if (smem > 227 * 1024) return cudaSuccess;
+  if (step_max_clusters<D>(C, smem) <= 0) return cudaSuccess;
+  const uint64_t rows = (uint64_t)s.B * s.Hkv;
+  CUtensorMap tk, tv, tmin, tmax;
+  if (!encode_rows_map(&tk, sa.a.k, rows * s.Cap, D) || !encode_rows_map(&tv, sa.a.v, rows * s.Cap, D) ||
+      !encode_rows_map(&tmin, sa.kmin, rows * sa.npcap, D) || !encode_rows_map(&tmax, sa.kmax, rows * sa.npcap, D))
+    return cudaSuccess;
+  *handled = true;
+  cudaError_t e = launch_pdl_cluster(quest_step_kernel<D>, dim3((unsigned)(rows * C)), dim3((kTmaConsumers + 1) * 32),
+                                     smem, C, st, tk, tv, tmin, tmax, sa);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache, const void* v_cache,
+                              const void* kmin, const void* kmax, const int32_t* ctx_len, int k, int n_sink,
+                              int n_local, const float* sink, int32_t* page_idx, void* out, float* lse,
+                              int num_splits, cudaStream_t st, bool* handled) {
+  *handled = false;
+  if (!quest_step_eligible(s, k)) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(kmin) | reinterpret_cast<uintptr_t>(kmax)) & 15)
+    return cudaSuccess;
+  StepArgs sa = {};
+  AttendArgs& a = sa.a;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  sa.kmin = kmin;
+  sa.kmax = kmax;
+  a.ctx_len = ctx_len;
+  a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.G; a.Cap = s.Cap; a.P = s.P; a.pshift = s.pshift;
+  a.qscale = s.scale * kLog2e;
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
+  a.cluster = 1;
+  a.S = num_splits > 0 ? std::min(num_splits, kMaxClusterSplits) : quest_step_splits(s, k);
+  sa.page_idx = page_idx;
+  sa.k = k;
+  sa.n_sink = n_sink;
+  sa.n_local = n_local;
+  sa.npcap = s.Cap >> s.pshift;
+  return s.D == 64 ? step_launch<64>(s, sa, st, handled) : step_launch<128>(s, sa, st, handled);
+}
+
+unsigned int take_step_wait_timeouts() {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_step_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
+  if (v) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_step_wait_timeouts, &zero, sizeof(zero));
+  }
+  return v;
+}
+
+}  // namespace sls

@@ -55,19 +55,19 @@ def upload(spec: W.Spec, host: W.Tensors, cuda_cores: bool = False, device="cuda
     return dw
 
 
-def make_step(dw: DeviceWorkload, num_splits=None, fused: bool = True):
+def make_step(dw: DeviceWorkload, num_splits=None, fused: bool = True, one_launch: bool = True):
     s = dw.spec
     if s.selector == "quest":
         return ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, num_splits,
-                               fused=fused)
+                               fused=fused, one_launch=one_launch)
     return ops.DeltaDecode(dw.desc, s.block, s.delta, num_splits, fused=fused)
 
 
-def run_step(dw: DeviceWorkload, num_splits=None, fused: bool = True):
+def run_step(dw: DeviceWorkload, num_splits=None, fused: bool = True, one_launch: bool = True):
     """Select + attend + combine on the device.  Returns host arrays:
     (selection rows, counts or None, out [B,Hq,D] float64, lse [B,Hq])."""
     s = dw.spec
-    step = make_step(dw, num_splits, fused)
+    step = make_step(dw, num_splits, fused, one_launch)
     if s.selector == "quest":
         out, lse = step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx, dw.sink)
         sel, cnt = step.page_idx, None

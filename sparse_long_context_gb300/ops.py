@@ -210,20 +210,60 @@ def combine_splits(desc: L.AttnDesc, parts, sink=None, out=None, lse=None, want_
     return out, lse
 
 
+def quest_step_workspace(desc: L.AttnDesc, k: int, num_splits: int = 0, device="cuda"):
+    """Zero-filled workspace of quest_decode_step (reusable)."""
+    n = L.load().sls_quest_decode_step_workspace_size(ctypes.byref(desc), int(k), int(num_splits))
+    return torch.zeros(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
+def quest_step_splits(desc: L.AttnDesc, k: int) -> int:
+    """Cluster size of the one-launch step for this shape (0: two launches)."""
+    return int(L.load().sls_quest_decode_step_splits(ctypes.byref(desc), int(k)))
+
+
+def quest_decode_step(desc: L.AttnDesc, q, k_cache, v_cache, kmin, kmax, ctx_len, k: int,
+                      n_sink_pages: int = 0, n_local_tokens: int = 0, sink=None, page_idx=None,
+                      out=None, lse=None, num_splits: int = 0, workspace=None, want_lse: bool = True):
+    """The whole Quest step (select + attend + combine), one launch where the
+    shape allows; returns (out, lse).  page_idx, if given, receives the list."""
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (kmin, "kmin"), (kmax, "kmax")):
+        _need(t, nm)
+    B, Hq, D = desc.batch, desc.num_q_heads, desc.head_dim
+    dtype = torch.bfloat16 if desc.dtype == L.SLS_DTYPE_BF16 else torch.float32
+    out = torch.empty((B, Hq, D), dtype=dtype, device=q.device) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, (Hq,))
+    if page_idx is not None:
+        _need(page_idx, "page_idx", torch.int32, (desc.batch * desc.num_kv_heads, int(k)))
+    workspace = quest_step_workspace(desc, k, num_splits, q.device) if workspace is None else workspace
+    L.call("sls_quest_decode_step", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kmin),
+           _ptr(kmax), _ptr(ctx_len), int(k), int(n_sink_pages), int(n_local_tokens), _ptr(sink),
+           _ptr(page_idx), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), workspace.numel(), _stream())
+    return out, lse
+
+
 # ------------------------------------------------------------ decode step
 
 class QuestDecode:
     """One Quest decode step (select + attend + combine) over preallocated
-    buffers, so the three launches can be captured in a CUDA graph."""
+    buffers, capturable in a CUDA graph.  one_launch: the whole step in one
+    kernel where the shape allows (quest_decode_step); otherwise select, then
+    attend with the combine fused (fused=True) or as its own launch."""
 
     def __init__(self, desc: L.AttnDesc, k_budget: int, n_sink_pages: int, n_local_tokens: int,
-                 num_splits: Optional[int] = None, device="cuda", fused: bool = True):
+                 num_splits: Optional[int] = None, device="cuda", fused: bool = True,
+                 one_launch: bool = True):
         self.desc = desc
         self.k = int(k_budget)
         self.n_sink, self.n_local = int(n_sink_pages), int(n_local_tokens)
         self.fused = fused
+        self.one_launch = fused and one_launch
         rows = desc.batch * desc.num_kv_heads
         self.S = num_splits or default_splits(desc, self.k)
+        self.step_splits = int(num_splits or 0)
+        self.step_workspace = quest_step_workspace(desc, self.k, self.step_splits, device)
         self.page_idx = torch.empty((rows, self.k), dtype=torch.int32, device=device)
         self.workspace = select_pages_workspace(desc, device)
         self.parts = partials(desc, self.S, device)
@@ -246,6 +286,10 @@ class QuestDecode:
         return combine_splits(self.desc, self.parts, sink, out=self.out, lse=self.lse)
 
     def __call__(self, q, k_cache, v_cache, kmin, kmax, ctx_len, sink=None):
+        if self.one_launch:
+            return quest_decode_step(self.desc, q, k_cache, v_cache, kmin, kmax, ctx_len, self.k, self.n_sink,
+                                     self.n_local, sink=sink, page_idx=self.page_idx, out=self.out,
+                                     lse=self.lse, num_splits=self.step_splits, workspace=self.step_workspace)
         self.select(q, kmin, kmax, ctx_len)
         return self.attend(q, k_cache, v_cache, ctx_len, sink)
 

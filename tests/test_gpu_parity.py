@@ -162,9 +162,11 @@ def check_all_rows(s, host, sel, cnt, out, lse, dw=None):
     return ties
 
 
-# attend kernels: tensor cores fed by tensor-map copies (the default for bf16
-# pages of >= 16 tokens), tensor cores fed by register loads, CUDA cores
-PATHS = {"tma": dict(), "registers": dict(no_tma=True), "cuda_cores": dict(cuda_cores=True)}
+# kernels of a step: the one-launch Quest step (the default for bf16 pages of
+# >= 16 tokens), select + the tensor-map fed attend, select + the register-fed
+# attend, CUDA cores
+PATHS = {"step": dict(), "tma": dict(), "registers": dict(no_tma=True), "cuda_cores": dict(cuda_cores=True)}
+ONE_LAUNCH = {"step": True, "tma": False, "registers": True, "cuda_cores": True}
 
 
 @pytest.mark.parametrize("key", list(SMALL_QUEST))
@@ -173,13 +175,13 @@ def test_quest_step_small(key, path):
     s = quest_case(key)
     host = W.generate(s)
     dw = PT.upload(s, host, **PATHS[path])
-    sel, cnt, out, lse = PT.run_step(dw)
+    sel, cnt, out, lse = PT.run_step(dw, one_launch=ONE_LAUNCH[path])
     ties = check_all_rows(s, host, sel, cnt, out, lse, dw)
     print(f"{key}: boundary ties {ties}")
 
 
 @pytest.mark.parametrize("key", list(SMALL_DELTA))
-@pytest.mark.parametrize("path", ["tma", "registers"])
+@pytest.mark.parametrize("path", ["step", "registers"])
 def test_delta_step_small(key, path):
     s = make(SMALL_DELTA[key])
     host = W.generate(s)
@@ -190,23 +192,52 @@ def test_delta_step_small(key, path):
     print(f"{key}: kept fraction {kept:.3f}, boundary ties {ties}")
 
 
-@pytest.mark.parametrize("key", ["qwen7b_ragged", "gptoss_ragged"])
+@pytest.mark.parametrize("key", ["qwen7b_ragged", "gptoss_ragged", "gptoss_p16"])
 def test_fused_and_separate_combine_agree_and_reuse_workspace(key):
     s = quest_case(key)
     host = W.generate(s)
     dw = PT.upload(s, host)
-    step = PT.H.make_step(dw, fused=True)
-    outs = []
-    for _ in range(3):  # the arrival tickets must be back at zero after every call
-        o, l = step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx, dw.sink)
-        outs.append((o.float().clone(), l.clone()))
+    results = {}
+    for name, kw in (("one_launch", dict(fused=True)), ("two_launch", dict(fused=True, one_launch=False))):
+        step = PT.H.make_step(dw, **kw)
+        outs = []
+        for _ in range(3):  # reused workspaces: the arrival tickets are back at zero after every call
+            o, l = step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx, dw.sink)
+            outs.append((o.float().clone(), l.clone(), step.page_idx.clone()))
+        ops.pipeline_check()
+        for o, l, p in outs:
+            assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1]) and torch.equal(p, outs[0][2])
+        results[name] = outs[0]
     sel, _, out_sep, lse_sep = PT.run_step(dw, fused=False)
-    for o, l in outs:
-        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
-    check_all_rows(s, host, sel, None, outs[0][0].cpu().numpy().astype(np.float64),
-                   outs[0][1].cpu().numpy().astype(np.float64))
+    for name, (o, l, p) in results.items():
+        check_all_rows(s, host, p.cpu().numpy(), None, o.cpu().numpy().astype(np.float64),
+                       l.cpu().numpy().astype(np.float64))
+        assert np.abs(o.cpu().numpy() - out_sep).max() < 2e-2, name
     check_all_rows(s, host, sel, None, out_sep, lse_sep)
-    assert np.abs(outs[0][0].cpu().numpy() - out_sep).max() < 2e-2
+
+
+def test_one_launch_step_long_rows():
+    """Rows of 8192 pages: the row's keys no longer fit the registers of the
+    CTA, the shared-memory selection runs."""
+    s = W.spec("qwen1p5b", batch=1, ctx_len=[131072], capacity=131072)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, _, out, lse = PT.run_step(dw)
+    assert ops.quest_step_splits(dw.desc, s.k_pages) > 0
+    check_all_rows(s, host, sel, None, out, lse)
+
+
+@pytest.mark.parametrize("ctx", [[0, 1, 17, 5000], [16, 2048, 2049, 4095]])
+def test_one_launch_step_edge_contexts(ctx):
+    """Empty rows, single pages, budgets covering every page and just not."""
+    s = W.spec("qwen7b", batch=len(ctx), ctx_len=ctx, capacity=5008)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, _, out, lse = PT.run_step(dw)
+    rows = s.num_kv_heads
+    if ctx[0] == 0:
+        assert np.all(sel[:rows] == -1) and np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    check_all_rows(s, host, sel, None, out, lse)
 
 
 def _bits(x):
