@@ -36,6 +36,28 @@ from sparse_long_context_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak) for select+attend"
 
+# DRAM bytes per launch of the one-launch step kernel, from the committed ncu
+# capture (profiles/quest_step_qwen1p5b_64k_b8_full.md: batch 8 at 64k, read +
+# written; traffic grows with the rows, so x4 for batch 32).  Reported only
+# for that workload and only while the kernel's sources hash to the ones
+# captured; otherwise null.
+STEP_TRAFFIC_B32 = 4 * (50.478592e6 + 0.146944e6)
+STEP_SOURCES = ("quest_step.cu", "attend_tma.cuh", "tma.cuh", "mma.cuh", "attend_common.cuh", "common.cuh")
+STEP_SOURCES_SHA256 = "eeb4c1a55be40a1974af0faf77d763c45ef36de75569af2b1305f806d484ecce"
+
+
+def step_traffic(s: W.Spec):
+    """Per-launch DRAM bytes of the step kernel for the captured workload, else None."""
+    import hashlib
+    if (s.name, s.batch, s.ctx_len[0]) != ("qwen1p5b", 32, 65536):
+        return None
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "sparse_long_context_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in STEP_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return round(STEP_TRAFFIC_B32) if h.hexdigest() == STEP_SOURCES_SHA256 else None
+
 
 # ------------------------------------------------------------------ helpers
 
@@ -329,6 +351,22 @@ def run_ours(args, s: W.Spec):
     elapsed = e0.elapsed_time(e1) / 1e3
     t_max, total_bytes = aggregate(elapsed, float(nbytes["total"] * args.steps), world)
 
+    # per-replay spread: events around single replays (a separate pass, so the
+    # timed loop above has no events inside it)
+    nrep = max(200, min(args.steps, 1000))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+    with torch.cuda.stream(stream):
+        for i, (a, b_) in enumerate(evs):
+            if i % 100 == 0:
+                torch.cuda._sleep(int(2e7))  # keeps the queue ahead of the device
+            a.record(stream)
+            graphs[i % nsets].replay()
+            b_.record(stream)
+    torch.cuda.synchronize()
+    per_rep = sorted(1e3 * a.elapsed_time(b_) for a, b_ in evs)
+    rep_us = {"p10": round(per_rep[nrep // 10], 2), "p50": round(per_rep[nrep // 2], 2),
+              "p90": round(per_rep[nrep * 9 // 10], 2), "replays": nrep}
+
     # per-kernel device time: eager launches bracketed by events on the
     # launching stream, queued behind a sleep so the host stays ahead
     ksteps = max(50, min(args.steps, 400))
@@ -393,7 +431,11 @@ def run_ours(args, s: W.Spec):
         dom_bytes = nbytes[dom]
         dom_name = ("select: quest_score_kernel + topk_kernel" if dom == "select"
                     else "attend: attend_tma_kernel with the cluster combine")
-    achieved = dom_bytes / (kern_us[dom] * 1e-6) / 1e9
+    if one:
+        # the step is this one kernel: its average launch over the timed region
+        achieved = dom_bytes / (t_max / args.steps) / 1e9
+    else:
+        achieved = dom_bytes / (kern_us[dom] * 1e-6) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -408,9 +450,10 @@ def run_ours(args, s: W.Spec):
                    "parallelism": f"weak: {world} GPU(s), {s.batch} sequences each"},
         "bytes_per_step": nbytes["total"], "bytes_select": nbytes["select"], "bytes_attend": nbytes["attend"],
         "kernel_us": {k: round(v, 2) for k, v in kern_us.items()},
+        "replay_us": rep_us,
         "roofline": {"bound": "hbm", "kernel": dom_name,
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": step_traffic(s) if one else None,
                      "peak_kind": f"{peak_kind} (burst copy)"},
         "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4)},
         "gpu_launches": (1 if one else 3) * args.steps,  # one step kernel, or score, top-k, attend
@@ -442,13 +485,19 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="qwen1p5b", choices=("qwen1p5b", "qwen7b"))
     ap.add_argument("--ctx", type=int, default=None, help="context length (default: the workload's)")
+    ap.add_argument("--batch", type=int, default=None, help="sequences per GPU (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=None,
                     help="attend splits per (sequence, KV head) (default: the library's choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    s = W.spec(args.workload, ctx_len=args.ctx) if args.ctx else W.spec(args.workload)
+    kw = {}
+    if args.ctx:
+        kw["ctx_len"] = args.ctx
+    if args.batch:
+        kw["batch"] = args.batch
+    s = W.spec(args.workload, **kw)
     if args.impl == "reference":
         run_reference(args, s)
     else:
