@@ -367,6 +367,39 @@ def run_ours(args, s: W.Spec):
     rep_us = {"p10": round(per_rep[nrep // 10], 2), "p50": round(per_rep[nrep // 2], 2),
               "p90": round(per_rep[nrep * 9 // 10], 2), "replays": nrep}
 
+    # dense decode on the same workload (the sparsity gate forced open: every
+    # row attends its whole context through the same kernel), for the
+    # speedup of the sparse step and dense GB/s against the peak
+    dense = None
+    if not args.no_dense and steps_obj[0].one_launch and ops.quest_step_splits(dw.desc, s.k_pages) > 0:
+        dsteps = [ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, args.splits,
+                                  min_sparsity=1e9) for _ in sets]
+        dgraphs = []
+        with torch.cuda.stream(stream):
+            for st, (K, V, kmin, kmax) in zip(dsteps, sets):
+                st(dw.q, K, V, kmin, kmax, dw.ctx)
+            torch.cuda.synchronize()
+            for st, (K, V, kmin, kmax) in zip(dsteps, sets):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    st(dw.q, K, V, kmin, kmax, dw.ctx)
+                dgraphs.append(g)
+            for i in range(3):
+                dgraphs[i % nsets].replay()
+            torch.cuda.synchronize()
+            nd = max(20, min(args.steps, 200))
+            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            d0.record(stream)
+            for i in range(nd):
+                dgraphs[i % nsets].replay()
+            d1.record(stream)
+        torch.cuda.synchronize()
+        dense_s = d0.elapsed_time(d1) / 1e3 / nd
+        dense_bytes = sum(s.num_kv_heads * n * 2 * s.head_dim * 2 for n in s.ctx_len)
+        dense = {"us_per_step": round(dense_s * 1e6, 2), "GB/s": round(dense_bytes / dense_s / 1e9, 1),
+                 "frac_of_peak": None, "bytes_per_step": int(dense_bytes), "steps": nd}
+        del dgraphs, dsteps
+
     # per-kernel device time: eager launches bracketed by events on the
     # launching stream, queued behind a sleep so the host stays ahead
     ksteps = max(50, min(args.steps, 400))
@@ -420,6 +453,8 @@ def run_ours(args, s: W.Spec):
         return
 
     peak, peak_kind = load_peaks()
+    if dense:
+        dense["frac_of_peak"] = round(dense["GB/s"] / peak, 4)
     value = total_bytes / t_max / 1e9
     ms_step = 1e3 * t_max / args.steps
     # dominant kernel: the one-launch step (all bytes of the step), else the
@@ -456,6 +491,8 @@ def run_ours(args, s: W.Spec):
                      "frac": round(achieved / peak, 4), "traffic": step_traffic(s) if one else None,
                      "peak_kind": f"{peak_kind} (burst copy)"},
         "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4)},
+        "dense": dense,
+        "speedup_vs_dense": round(dense["us_per_step"] / (1e6 * t_max / args.steps), 2) if dense else None,
         "gpu_launches": (1 if one else 3) * args.steps,  # one step kernel, or score, top-k, attend
         "clocks": clk,
         "e2e": {"value": round(e2e_bytes / e2e_max / 1e9, 2), "unit": "GB/s",
@@ -486,6 +523,7 @@ def main():
     ap.add_argument("--workload", default="qwen1p5b", choices=("qwen1p5b", "qwen7b"))
     ap.add_argument("--ctx", type=int, default=None, help="context length (default: the workload's)")
     ap.add_argument("--batch", type=int, default=None, help="sequences per GPU (default: the workload's)")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense-decode comparison")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=None,
                     help="attend splits per (sequence, KV head) (default: the library's choice)")

@@ -362,6 +362,13 @@ int32_t sls_quest_decode_step_splits(const sls_attn_desc* desc, int32_t k);
  *   out, lse    as in sls_combine_splits
  *   num_splits  CTAs per row (0: the library's choice; the one-launch kernel
  *               uses at most 16)
+ *   min_sparsity  sparsity gate ("perf(core): fused sparse-attention decode
+ *               via page indirection", Corrected premise 2): a row whose
+ *               context holds fewer than min_sparsity * k * P tokens is
+ *               attended densely over its whole context, without selection,
+ *               and its page_idx row is left at -1.  0 disables the gate.
+ *               The gate needs the one-launch kernel: on the two-launch path
+ *               a non-zero value returns SLS_EUNSUPPORTED.
  *   workspace   >= sls_quest_decode_step_workspace_size() bytes, zero-filled
  *               before its first use (the one-launch kernel leaves it alone;
  *               the two-launch path keeps its tickets at zero).
@@ -370,8 +377,8 @@ sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const
                                  const void* v_cache, const void* kmin, const void* kmax,
                                  const int32_t* ctx_len, int32_t k, int32_t n_sink_pages,
                                  int32_t n_local_tokens, const float* sink, int32_t* page_idx,
-                                 void* out, float* lse, int32_t num_splits, void* workspace,
-                                 size_t workspace_bytes, void* stream);
+                                 void* out, float* lse, int32_t num_splits, float min_sparsity,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- diagnostics ------------------------------------------------------- */
 

@@ -319,8 +319,8 @@ int32_t sls_quest_decode_step_splits(const sls_attn_desc* desc, int32_t k) {
 sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const void* k_cache, const void* v_cache,
                                  const void* kmin, const void* kmax, const int32_t* ctx_len, int32_t k,
                                  int32_t n_sink_pages, int32_t n_local_tokens, const float* sink, int32_t* page_idx,
-                                 void* out, float* lse, int32_t num_splits, void* workspace, size_t workspace_bytes,
-                                 void* stream) {
+                                 void* out, float* lse, int32_t num_splits, float min_sparsity, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
@@ -334,14 +334,18 @@ sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const
     return fail(SLS_EINVAL, "budget k=%d cannot hold the forced pages (up to %lld)", k, (long long)forced_max);
   if (s.P == 1 && kmin != kmax) return fail(SLS_EINVAL, "page_size 1: pass the key cache as both kmin and kmax");
   if (num_splits < 0 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [0, 1024]", num_splits);
+  if (!(min_sparsity >= 0.f) || std::isinf(min_sparsity))
+    return fail(SLS_EINVAL, "min_sparsity must be finite and >= 0");
   const size_t need = sls_quest_decode_step_workspace_size(desc, k, num_splits);
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
   bool handled = false;
   cudaError_t e = sls::launch_quest_step(s, q, k_cache, v_cache, kmin, kmax, ctx_len, k, n_sink_pages,
-                                         n_local_tokens, sink, page_idx, out, lse, num_splits,
+                                         n_local_tokens, sink, page_idx, out, lse, num_splits, min_sparsity,
                                          (cudaStream_t)stream, &handled);
   if (handled) return cuda_status(e, "sls_quest_decode_step");
+  if (min_sparsity > 0.f)
+    return fail(SLS_EUNSUPPORTED, "min_sparsity needs the one-launch step (bf16, pages of >= 16 tokens)");
   // two launches: select into page_idx (or the workspace), then attend with the fused combine
   const size_t chunk = (size_t)(npcap + sls::select_pages_cluster() - 1) / sls::select_pages_cluster();
   if (chunk * 4 > sls::select_pages_smem_limit())

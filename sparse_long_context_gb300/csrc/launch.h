@@ -94,7 +94,7 @@ int quest_step_splits(const Shape& s, int k);
 cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache, const void* v_cache,
                               const void* kmin, const void* kmax, const int32_t* ctx_len, int k, int n_sink,
                               int n_local, const float* sink, int32_t* page_idx, void* out, float* lse,
-                              int num_splits, cudaStream_t st, bool* handled);
+                              int num_splits, float min_sparsity, cudaStream_t st, bool* handled);
 unsigned int take_step_wait_timeouts();
 int max_auto_splits(const Shape& s);
 cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const void* v,

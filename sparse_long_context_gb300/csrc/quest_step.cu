@@ -49,6 +49,7 @@ struct StepArgs {
   int npcap;  // Cap / P
   size_t keys_bytes;   // shared-memory region of the keys (also the combine inbox)
   int scratch_off;     // top-k scratch in the ring, after the row's keys (all-keys selection)
+  float min_sparsity;  // rows with N < min_sparsity * k * P attend densely (0: never)
   int topk_mode;       // 0: candidates of every CTA, 1: all keys to every CTA
   int cand_cap;        // candidates one CTA may send
 };
@@ -557,6 +558,9 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   const int per = (k + C - 1) / C;  // list entries attended per CTA
   const int e0 = split * per;
   const int nent = max(0, min(per, k - e0));
+  // sparsity gate (mlxcel, "Corrected premise 2"): a context shorter than
+  // min_sparsity times the selected tokens is attended densely
+  const bool dense = sa.min_sparsity > 0.f && (double)N < (double)sa.min_sparsity * k * a.P;
   __syncthreads();
 
   uint32_t seq = 0;  // ring position (identical in every thread)
@@ -569,7 +573,12 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     return use == 0 || mbar_wait(&empty[st], (use - 1) & 1);
   };
 
-  if (NP > k) {
+  if (dense) {
+    // every page of the context, no selection; page_idx stays -1
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // completes the arrive made at entry
+    if (sa.page_idx)
+      for (int e = threadIdx.x; e < nent; e += NT) sa.page_idx[(size_t)row * k + e0 + e] = -1;
+  } else if (NP > k) {
     // ------------------------------------------------------------ 1. score
     const int p0 = split * sa.chunk;
     const int nloc = max(0, min(sa.chunk, NP - p0));
@@ -772,13 +781,18 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   __syncthreads();
 
   // -------------------------------------------------------------- 3. attend
-  const int ngroups = (nent << a.pshift) >> 4;
+  // a sparse row: the CTA's share of the list; a dense row: its share of the
+  // context's 16-token groups
+  const int dper = (((NP << a.pshift) >> 4) + C - 1) / C;
+  const int dg0 = split * dper;
+  const int ngroups = dense ? max(0, min(dper, ((NP << a.pshift) >> 4) - dg0)) : (nent << a.pshift) >> 4;
   auto group_at = [&](int gi, int& lim) -> int {
     const int j0 = gi << 4;
-    const int pg = list[j0 >> a.pshift];
+    const int pg = dense ? ((dg0 + gi) << 4) >> a.pshift : list[j0 >> a.pshift];
+    const int jo = dense ? ((dg0 + gi) << 4) : j0;
     lim = 0;
     if ((unsigned)pg >= (unsigned)(a.Cap >> a.pshift)) return 0;
-    const int base = (pg << a.pshift) + (j0 & (a.P - 1));
+    const int base = (pg << a.pshift) + (jo & (a.P - 1));
     lim = min(N - base, 16);
     return base;
   };
@@ -954,7 +968,7 @@ static cudaError_t step_launch(const Shape& s, const StepArgs& sa0, cudaStream_t
 cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache, const void* v_cache,
                               const void* kmin, const void* kmax, const int32_t* ctx_len, int k, int n_sink,
                               int n_local, const float* sink, int32_t* page_idx, void* out, float* lse,
-                              int num_splits, cudaStream_t st, bool* handled) {
+                              int num_splits, float min_sparsity, cudaStream_t st, bool* handled) {
   *handled = false;
   if (!quest_step_eligible(s, k)) return cudaSuccess;
   if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
@@ -980,6 +994,7 @@ cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache
   sa.n_sink = n_sink;
   sa.n_local = n_local;
   sa.npcap = s.Cap >> s.pshift;
+  sa.min_sparsity = min_sparsity;
   return s.D == 64 ? step_launch<64>(s, sa, st, handled) : step_launch<128>(s, sa, st, handled);
 }
 

@@ -223,7 +223,8 @@ def quest_step_splits(desc: L.AttnDesc, k: int) -> int:
 
 def quest_decode_step(desc: L.AttnDesc, q, k_cache, v_cache, kmin, kmax, ctx_len, k: int,
                       n_sink_pages: int = 0, n_local_tokens: int = 0, sink=None, page_idx=None,
-                      out=None, lse=None, num_splits: int = 0, workspace=None, want_lse: bool = True):
+                      out=None, lse=None, num_splits: int = 0, workspace=None, want_lse: bool = True,
+                      min_sparsity: float = 0.0):
     """The whole Quest step (select + attend + combine), one launch where the
     shape allows; returns (out, lse).  page_idx, if given, receives the list."""
     for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (kmin, "kmin"), (kmax, "kmax")):
@@ -240,7 +241,8 @@ def quest_decode_step(desc: L.AttnDesc, q, k_cache, v_cache, kmin, kmax, ctx_len
     workspace = quest_step_workspace(desc, k, num_splits, q.device) if workspace is None else workspace
     L.call("sls_quest_decode_step", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kmin),
            _ptr(kmax), _ptr(ctx_len), int(k), int(n_sink_pages), int(n_local_tokens), _ptr(sink),
-           _ptr(page_idx), _ptr(out), _ptr(lse), int(num_splits), _ptr(workspace), workspace.numel(), _stream())
+           _ptr(page_idx), _ptr(out), _ptr(lse), int(num_splits), float(min_sparsity), _ptr(workspace),
+           workspace.numel(), _stream())
     return out, lse
 
 
@@ -254,12 +256,13 @@ class QuestDecode:
 
     def __init__(self, desc: L.AttnDesc, k_budget: int, n_sink_pages: int, n_local_tokens: int,
                  num_splits: Optional[int] = None, device="cuda", fused: bool = True,
-                 one_launch: bool = True):
+                 one_launch: bool = True, min_sparsity: float = 0.0):
         self.desc = desc
         self.k = int(k_budget)
         self.n_sink, self.n_local = int(n_sink_pages), int(n_local_tokens)
         self.fused = fused
         self.one_launch = fused and one_launch
+        self.min_sparsity = float(min_sparsity)
         rows = desc.batch * desc.num_kv_heads
         self.S = num_splits or default_splits(desc, self.k)
         self.step_splits = int(num_splits or 0)
@@ -289,7 +292,8 @@ class QuestDecode:
         if self.one_launch:
             return quest_decode_step(self.desc, q, k_cache, v_cache, kmin, kmax, ctx_len, self.k, self.n_sink,
                                      self.n_local, sink=sink, page_idx=self.page_idx, out=self.out,
-                                     lse=self.lse, num_splits=self.step_splits, workspace=self.step_workspace)
+                                     lse=self.lse, num_splits=self.step_splits, workspace=self.step_workspace,
+                                     min_sparsity=self.min_sparsity)
         self.select(q, kmin, kmax, ctx_len)
         return self.attend(q, k_cache, v_cache, ctx_len, sink)
 

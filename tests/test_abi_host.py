@@ -131,6 +131,23 @@ def test_attend_combine_validation(lib):
     assert lib.sls_attend_default_splits(None, 8) == 1
 
 
+def test_quest_step_validation(lib):
+    d = desc()
+    ws = lib.sls_quest_decode_step_workspace_size(ctypes.byref(d), 8, 0)
+    assert ws > 0
+    call = lambda k=8, ms=0.0, wsb=ws, dd=d: lib.sls_quest_decode_step(
+        ctypes.byref(dd), BAD, BAD, BAD, BAD, BAD, BAD, k, 0, 0, None, None, BAD, None, 0, ms, BAD, wsb, None)
+    assert call(k=0) == L.SLS_EINVAL
+    assert call(ms=-1.0) == L.SLS_EINVAL
+    assert call(ms=float("inf")) == L.SLS_EINVAL
+    assert call(wsb=ws - 1) == L.SLS_EWORKSPACE
+    # the gate needs the one-launch kernel, which the CUDA-core flag turns off
+    d2 = desc(flags=L.SLS_FLAG_CUDA_CORES)
+    ws2 = lib.sls_quest_decode_step_workspace_size(ctypes.byref(d2), 8, 0)
+    assert call(ms=8.0, wsb=ws2, dd=d2) == L.SLS_EUNSUPPORTED
+    assert lib.sls_quest_decode_step_splits(ctypes.byref(d2), 8) == 0
+
+
 def test_python_layer_raises_on_status(lib):
     d = desc(head_dim=96)
     with pytest.raises(L.SlsError) as e:

@@ -216,6 +216,32 @@ def test_fused_and_separate_combine_agree_and_reuse_workspace(key):
     check_all_rows(s, host, sel, None, out_sep, lse_sep)
 
 
+def test_sparsity_gate_attends_short_contexts_densely():
+    """mlxcel's gate: rows with fewer than min_sparsity * k * P context tokens
+    skip the selection and attend every token; longer rows stay sparse."""
+    s = W.spec("qwen7b", batch=3, ctx_len=[1000, 5000, 20000], capacity=20000)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    step = ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, min_sparsity=4.0)
+    out, lse = step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx)
+    ops.pipeline_check()
+    out = out.float().cpu().numpy().astype(np.float64)
+    sel = step.page_idx.cpu().numpy()
+    G, H = s.group, s.num_kv_heads
+    for b in (0, 1):  # 1000 and 5000 tokens < 4 * 128 * 16: dense
+        assert np.all(sel[b * H:(b + 1) * H] == -1)
+        n = int(host.ctx_len[b])
+        for h in range(H):
+            q = O.to_f64(host.q[b, h * G:(h + 1) * G], "bf16")
+            ref, _ = O.softmax_attention(q, O.to_f64(host.K[b, h, :n], "bf16"),
+                                         O.to_f64(host.V[b, h, :n], "bf16"), s.scale)
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], ref, f"dense row {(b, h)}")
+    for h in range(H):  # 20000 tokens: sparse, as without the gate
+        orc = PT.oracle_row(s, host, 2, h)
+        PT.check_quest_list(sel[2 * H + h], orc, 20000, 16, s.k_pages)
+        PT.assert_close(s, out[2, h * G:(h + 1) * G], orc.o, f"sparse row {h}")
+
+
 def test_one_launch_step_long_rows():
     """Rows of 8192 pages: the row's keys no longer fit the registers of the
     CTA, the shared-memory selection runs."""
