@@ -361,6 +361,34 @@ def delta_select_row(q, K, n, block, delta, scale):
 
 
 # ----------------------------------------------------------------------------
+# selection quality
+# ----------------------------------------------------------------------------
+
+def attention_mass_recall(q: np.ndarray, K: np.ndarray, pages, n: int, page_size: int,
+                          scale: float) -> np.ndarray:
+    """Share of each query head's full-context softmax mass that falls on the
+    tokens of the selected pages ([haystack] Part three, "attention mass
+    captured": how much of the true attention mass the selected pages hold).
+
+    q [G, D]; K [>= n, D] float64; pages: the row's page list (-1 entries and
+    positions >= n ignored).  recall_g = sum_{t in sel} exp(x_gt - M_g) /
+    sum_{t < n} exp(x_gt - M_g) with x = scale * q.k and M the row max.
+    Reading: the sink (a virtual key) is not a token and takes no part; an
+    empty context misses nothing, so its recall is 1.
+    Returns [G].
+    """
+    q = np.asarray(q, np.float64)
+    G = q.shape[0]
+    if n == 0:
+        return np.ones(G)
+    x = scale * (q @ K[:n].T)
+    m = x.max(axis=1, keepdims=True)
+    w = np.exp(x - m)
+    toks = pages_to_tokens(np.asarray(pages), n, page_size)
+    return w[:, toks].sum(axis=1) / w.sum(axis=1)
+
+
+# ----------------------------------------------------------------------------
 # one decode step of one row
 # ----------------------------------------------------------------------------
 

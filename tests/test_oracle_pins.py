@@ -307,3 +307,40 @@ def test_delta_invariants(n):
     sel, _ = O.delta_select_row(q, K, n, block, 1e9, scale)
     assert sel.tolist() == list(range(-(-n // block)))
     assert set(O.delta_forced_blocks(n, block).tolist()) <= set(sel.tolist())
+
+
+# ------------------------------------------------------- selection quality
+
+@pytest.mark.parametrize("n", [1, 17, 200])
+def test_recall_equals_mass_ratio_of_the_lse(n):
+    """Recall of a page set = exp(lse over the set - lse over the context):
+    a second route through the pinned attention routine, not the same sums."""
+    rng = np.random.default_rng(11 + n)
+    G, D, P = 3, 16, 8
+    q, K = rng.normal(size=(G, D)), rng.normal(size=(n + 5, D))
+    V = rng.normal(size=(n + 5, D))
+    NP = O.num_pages(n, P)
+    pages = rng.choice(NP, size=max(1, NP // 2), replace=False)
+    rec = O.attention_mass_recall(q, K, pages, n, P, 0.3)
+    _, lse_sel = O.sparse_attention_row(q, K, V, pages, n, P, 0.3)
+    _, lse_all = O.softmax_attention(q, K[:n], V[:n], 0.3)
+    np.testing.assert_allclose(rec, np.exp(lse_sel - lse_all), rtol=1e-12)
+
+
+def test_recall_bounds_additivity_and_monotonicity():
+    rng = np.random.default_rng(5)
+    G, D, P, n = 2, 8, 4, 61
+    q, K = rng.normal(size=(G, D)), rng.normal(size=(n, D))
+    NP = O.num_pages(n, P)
+    all_pages = np.arange(NP)
+    np.testing.assert_allclose(O.attention_mass_recall(q, K, all_pages, n, P, 1.0), 1.0, rtol=0, atol=1e-15)
+    assert np.all(O.attention_mass_recall(q, K, np.array([], dtype=np.int64), n, P, 1.0) == 0.0)
+    a, b = all_pages[:5], all_pages[5:9]
+    ra, rb = (O.attention_mass_recall(q, K, x, n, P, 1.0) for x in (a, b))
+    rab = O.attention_mass_recall(q, K, np.concatenate([a, b]), n, P, 1.0)
+    np.testing.assert_allclose(rab, ra + rb, rtol=1e-12)   # disjoint pages add up
+    assert np.all(rab >= ra) and np.all(rab <= 1.0)
+    # -1 padding and empty contexts
+    np.testing.assert_allclose(O.attention_mass_recall(q, K, np.array([-1, 3, -1]), n, P, 1.0),
+                               O.attention_mass_recall(q, K, np.array([3]), n, P, 1.0))
+    assert np.all(O.attention_mass_recall(q, K, a, 0, P, 1.0) == 1.0)
