@@ -380,6 +380,29 @@ sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const
                                  void* out, float* lse, int32_t num_splits, float min_sparsity,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- selection quality ------------------------------------------------- */
+
+/* Bytes of workspace sls_selection_recall needs. */
+size_t sls_selection_recall_workspace_size(const sls_attn_desc* desc);
+
+/*
+ * Attention-mass recall of page lists ("Don't read the haystack", Part
+ * three: how much of the true attention mass the selected pages hold): for
+ * every query head, the share of its full-context softmax mass (scores
+ * scale * q.k over the positions < ctx_len; no sink) that falls on the
+ * tokens of its row's listed pages.  A diagnostic beside the decode step: it
+ * reads every key of the context.
+ *   page_idx, idx_stride, count, k_fixed   as in sls_sparse_decode_attend
+ *               (NULL page_idx: every page, recall 1)
+ *   recall      [B, Hq] float; an empty context gives 1 (no mass missed)
+ *   workspace   >= sls_selection_recall_workspace_size() bytes
+ * Capacities above 262144 pages per row return SLS_EUNSUPPORTED.
+ */
+sls_status sls_selection_recall(const sls_attn_desc* desc, const void* q, const void* k_cache,
+                                const int32_t* page_idx, int32_t idx_stride, const int32_t* count,
+                                int32_t k_fixed, const int32_t* ctx_len, float* recall, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* ---- diagnostics ------------------------------------------------------- */
 
 /* Message of the last failing call on this thread ("" if none). */

@@ -48,6 +48,8 @@ SIGNATURES = {
     "sls_quest_decode_step_splits": (_I, [_D, _I]),
     "sls_quest_decode_step": (_I, [_D, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _I, ctypes.c_float,
                                    _P, ctypes.c_size_t, _P]),
+    "sls_selection_recall_workspace_size": (ctypes.c_size_t, [_D]),
+    "sls_selection_recall": (_I, [_D, _P, _P, _P, _I, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
     "sls_pipeline_check": (_I, []),
     "sls_last_error": (ctypes.c_char_p, []),
     "sls_version": (_I, []),

@@ -376,6 +376,34 @@ sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const
                      "sls_quest_decode_step (attend)");
 }
 
+size_t sls_selection_recall_workspace_size(const sls_attn_desc* desc) {
+  sls::Shape s;
+  if (check_desc(desc, &s)) return 0;
+  return sls::recall_workspace(s);
+}
+
+sls_status sls_selection_recall(const sls_attn_desc* desc, const void* q, const void* k_cache,
+                                const int32_t* page_idx, int32_t idx_stride, const int32_t* count, int32_t k_fixed,
+                                const int32_t* ctx_len, float* recall, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(q); REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(recall);
+  if (page_idx) {
+    if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
+    if (!count && (k_fixed < 0 || k_fixed > idx_stride))
+      return fail(SLS_EINVAL, "k_fixed %d not in [0, idx_stride=%d]", k_fixed, idx_stride);
+  }
+  if (!sls::recall_supported(s)) return fail(SLS_EUNSUPPORTED, "Cap/P above 262144 pages");
+  const size_t need = sls::recall_workspace(s);
+  if (!workspace || workspace_bytes < need)
+    return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  return cuda_status(sls::launch_recall(s, q, k_cache, page_idx, idx_stride, count, k_fixed, ctx_len, recall,
+                                        workspace, (cudaStream_t)stream),
+                     "sls_selection_recall");
+}
+
 sls_status sls_combine_splits(const sls_attn_desc* desc, const float* o_part, const float* m_part,
                               const float* l_part, int32_t num_splits, const float* sink, void* out,
                               float* lse, void* stream) {

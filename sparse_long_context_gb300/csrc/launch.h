@@ -96,6 +96,13 @@ cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache
                               int n_local, const float* sink, int32_t* page_idx, void* out, float* lse,
                               int num_splits, float min_sparsity, cudaStream_t st, bool* handled);
 unsigned int take_step_wait_timeouts();
+
+// Selection quality: attention-mass recall of page lists (a diagnostic).
+size_t recall_workspace(const Shape& s);
+bool recall_supported(const Shape& s);
+cudaError_t launch_recall(const Shape& s, const void* q, const void* k, const int32_t* page_idx, int idx_stride,
+                          const int32_t* count, int k_fixed, const int32_t* ctx_len, float* recall, void* ws,
+                          cudaStream_t st);
 int max_auto_splits(const Shape& s);
 cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const void* v,
                           const int32_t* page_idx, int idx_stride, const int32_t* count,

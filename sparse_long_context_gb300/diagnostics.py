@@ -1,0 +1,94 @@
+"""Selection-quality diagnostics on the synthetic workloads.
+
+For one decode step of a workload this reports, per query head:
+
+* attention-mass recall of the selected pages ("Don't read the haystack",
+  Part three: how much of the true attention mass the selection holds),
+  from ``sls_selection_recall``;
+* the relative L2 error of the sparse output against dense attention over
+  the whole context (the split-K attend kernel with no page list);
+* for the top-delta workload, top-delta against Quest top-k at the same
+  budget (the mean number of blocks top-delta keeps per row): recall of both.
+
+Usage: ``python -m sparse_long_context_gb300.diagnostics --workload qwen1p5b --batch 4``
+prints one JSON object.  Everything runs on the GPU through the C ABI; the
+statistics at the end are host arithmetic on the results.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import numpy as np
+import torch
+
+from . import harness as H
+from . import ops
+from . import workloads as W
+
+
+def _stats(x: np.ndarray) -> dict:
+    x = np.asarray(x, np.float64).ravel()
+    return {"min": float(x.min()), "p10": float(np.percentile(x, 10)), "median": float(np.median(x)),
+            "mean": float(x.mean())}
+
+
+def quest_quality(dw: H.DeviceWorkload) -> dict:
+    """Recall of the Quest selection and the sparse output's error vs dense."""
+    s = dw.spec
+    step = H.make_step(dw)
+    out, _ = step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx, dw.sink)
+    out = out.float().clone()
+    rec = ops.selection_recall(dw.desc, dw.q, dw.K, step.page_idx, dw.ctx)
+    S = ops.default_splits(dw.desc, s.capacity // s.page_size)
+    dense, _ = ops.sparse_decode_attend_combine(dw.desc, dw.q, dw.K, dw.V, None, dw.ctx, S, sink=dw.sink)
+    dense = dense.float()
+    rel = torch.linalg.vector_norm(out - dense, dim=-1) / torch.linalg.vector_norm(dense, dim=-1).clamp_min(1e-30)
+    ops.pipeline_check()
+    return {"selector": "quest", "budget_pages": s.k_pages, "recall": _stats(rec.cpu().numpy()),
+            "rel_l2_vs_dense": _stats(rel.cpu().numpy())}
+
+
+def delta_vs_topk(dw: H.DeviceWorkload) -> dict:
+    """Top-delta's kept blocks against Quest top-k at the same mean budget."""
+    s = dw.spec
+    step = H.make_step(dw)
+    step(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink)
+    cnt = step.count
+    rec_d = ops.selection_recall(dw.desc, dw.q, dw.K, step.block_idx, dw.ctx, count=cnt)
+    k = max(1, int(round(float(cnt.float().mean()))))
+    kmin, kmax = ops.pagemeta_build(dw.desc, dw.K, dw.ctx)
+    page_idx = ops.select_pages(dw.desc, dw.q, kmin, kmax, dw.ctx, k, 1, s.block)
+    rec_q = ops.selection_recall(dw.desc, dw.q, dw.K, page_idx, dw.ctx)
+    ops.pipeline_check()
+    nblk = np.array([-(-int(n) // s.block) for n in s.ctx_len for _ in range(s.num_kv_heads)])
+    return {"selector": "top-delta", "delta": s.delta,
+            "kept_fraction": float(cnt.cpu().numpy().sum() / nblk.sum()),
+            "recall_top_delta": _stats(rec_d.cpu().numpy()),
+            "matched_budget_blocks": k, "recall_quest_topk": _stats(rec_q.cpu().numpy())}
+
+
+def run(name: str, batch=None, ctx=None) -> dict:
+    kw = {}
+    if batch:
+        kw["batch"] = batch
+    if ctx:
+        kw["ctx_len"] = ctx
+    s = W.spec(name, **kw)
+    dw = H.upload(s, W.generate(s))
+    res = {"workload": name, "batch": s.batch, "ctx_len": int(s.ctx_len[0])}
+    res.update(quest_quality(dw) if s.selector == "quest" else delta_vs_topk(dw))
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser(description="selection-quality diagnostics")
+    ap.add_argument("--workload", default="qwen1p5b", choices=W.CONFIG_NAMES)
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--ctx", type=int, default=None)
+    a = ap.parse_args()
+    print(json.dumps(run(a.workload, a.batch, a.ctx)))
+
+
+if __name__ == "__main__":
+    main()

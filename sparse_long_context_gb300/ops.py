@@ -246,6 +246,22 @@ def quest_decode_step(desc: L.AttnDesc, q, k_cache, v_cache, kmin, kmax, ctx_len
     return out, lse
 
 
+def selection_recall(desc: L.AttnDesc, q, k_cache, page_idx, ctx_len, count=None,
+                     k_fixed: Optional[int] = None, recall=None, workspace=None):
+    """Attention-mass recall of each query head's page list: [B, Hq] float32."""
+    _need(q, "q")
+    _need(k_cache, "k_cache")
+    recall = torch.empty((desc.batch, desc.num_q_heads), dtype=torch.float32, device=q.device) \
+        if recall is None else recall
+    n = L.load().sls_selection_recall_workspace_size(ctypes.byref(desc))
+    workspace = torch.empty(max(int(n), 1), dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    stride = int(page_idx.shape[1]) if page_idx is not None else 0
+    kf = stride if k_fixed is None else int(k_fixed)
+    L.call("sls_selection_recall", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(page_idx), stride, _ptr(count),
+           kf, _ptr(ctx_len), _ptr(recall), _ptr(workspace), workspace.numel(), _stream())
+    return recall
+
+
 # ------------------------------------------------------------ decode step
 
 class QuestDecode:

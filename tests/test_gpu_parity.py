@@ -446,3 +446,68 @@ def test_full_size_sampled_rows(name):
             PT.assert_close(s, out[b, h * G:(h + 1) * G], orc.o, f"{name} row {r}")
     print(f"{name}: rows {rows} boundary ties {ties}"
           + (f" kept {cnt.sum() / (s.rows * (s.ctx_len[0] // 64)):.3f}" if cnt is not None else ""))
+
+
+# ------------------------------------------------------- selection quality
+
+RECALL_ATOL = 2e-4  # ratio of fp32 sums of exp over up to 2^17 tokens, scores from bf16 inputs
+
+
+@pytest.mark.parametrize("key", ["qwen7b_ragged", "gptoss_ragged", "gptoss_p16"])
+def test_selection_recall_matches_oracle(key):
+    s = quest_case(key)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, _, _, _ = PT.run_step(dw)
+    rec = ops.selection_recall(dw.desc, dw.q, dw.K, torch.from_numpy(sel).cuda(), dw.ctx).cpu().numpy()
+    G = s.group
+    for b in range(s.batch):
+        n = int(host.ctx_len[b])
+        for h in range(s.num_kv_heads):
+            q = O.to_f64(host.q[b, h * G:(h + 1) * G], s.dtype)
+            ref = O.attention_mass_recall(q, O.to_f64(host.K[b, h], s.dtype), sel[b * s.num_kv_heads + h], n,
+                                          s.page_size, s.scale)
+            np.testing.assert_allclose(rec[b, h * G:(h + 1) * G], ref, rtol=0, atol=RECALL_ATOL)
+
+
+def test_selection_recall_of_delta_lists_and_edge_rows():
+    s = make(SMALL_DELTA["ffd_ragged"])
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    sel, cnt, _, _ = PT.run_step(dw)
+    rec = ops.selection_recall(dw.desc, dw.q, dw.K, torch.from_numpy(sel).cuda(), dw.ctx,
+                               count=torch.from_numpy(cnt).cuda()).cpu().numpy()
+    G = s.group
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            r = b * s.num_kv_heads + h
+            q = O.to_f64(host.q[b, h * G:(h + 1) * G], s.dtype)
+            ref = O.attention_mass_recall(q, O.to_f64(host.K[b, h], s.dtype), sel[r, :cnt[r]],
+                                          int(host.ctx_len[b]), s.block, s.scale)
+            np.testing.assert_allclose(rec[b, h * G:(h + 1) * G], ref, rtol=0, atol=RECALL_ATOL)
+    # every page (no list): 1; an empty context: 1
+    full = ops.selection_recall(dw.desc, dw.q, dw.K, None, dw.ctx).cpu().numpy()
+    np.testing.assert_allclose(full, 1.0, rtol=0, atol=1e-6)
+    s2 = W.spec("qwen7b", batch=2, ctx_len=[0, 300], capacity=320)
+    dw2 = PT.upload(s2, W.generate(s2))
+    idx = torch.full((s2.rows, 4), -1, dtype=torch.int32, device="cuda")
+    rec2 = ops.selection_recall(dw2.desc, dw2.q, dw2.K, idx, dw2.ctx).cpu().numpy()
+    assert np.all(rec2[0] == 1.0) and np.all(rec2[1] == 0.0)
+
+
+def test_diagnostics_report_and_bound_beats_random_pages():
+    from sparse_long_context_gb300 import diagnostics as DG
+    s = W.spec("qwen7b", batch=2, ctx_len=8192, capacity=8192)
+    dw = PT.upload(s, W.generate(s))
+    q = DG.quest_quality(dw)
+    assert 0.0 <= q["recall"]["min"] <= q["recall"]["mean"] <= 1.0
+    assert np.isfinite(q["rel_l2_vs_dense"]["mean"])
+    # a random list of the same size holds less of the mass than the bound's top k
+    rng = np.random.default_rng(0)
+    NP = 8192 // 16
+    rnd = np.stack([np.sort(rng.choice(NP, size=s.k_pages, replace=False)) for _ in range(s.rows)]).astype(np.int32)
+    rec_rand = ops.selection_recall(dw.desc, dw.q, dw.K, torch.from_numpy(rnd).cuda(), dw.ctx).cpu().numpy()
+    assert q["recall"]["mean"] > rec_rand.mean() + 0.1
+    sd = make(SMALL_DELTA["ffd_aligned"])
+    d = DG.delta_vs_topk(PT.upload(sd, W.generate(sd)))
+    assert 0.0 < d["kept_fraction"] <= 1.0 and 0.0 <= d["recall_top_delta"]["min"] <= 1.0
