@@ -132,6 +132,26 @@ sls_status sls_pagemeta_update(const sls_attn_desc* desc, const void* k_cache,
                                const int32_t* pos, void* kmin, void* kmax,
                                void* stream);
 
+/*
+ * Append one decoded token per sequence, entirely on the device, so that a
+ * captured decode step can be replayed step after step: the new key and
+ * value of every KV head are written at position ctx_len[b], the key is
+ * folded into its page's min/max as sls_pagemeta_update does ("Don't read
+ * the haystack", Part two: summaries maintained as tokens append), and
+ * ctx_len[b] advances by one.  A sequence already at capacity is left
+ * unchanged.
+ *   k_new, v_new  [B, Hkv, D] dtype (read)
+ *   k_cache, v_cache  [B, Hkv, Cap, D] dtype (row ctx_len[b] written)
+ *   kmin, kmax    page metadata to keep current, or both NULL (page size 1,
+ *                 or a selector without it)
+ *   ctx_len       [B] int32 (read and advanced)
+ *   pos_out       [B] int32 receiving the written position (-1 at capacity),
+ *                 e.g. for sls_thumb_update; may be NULL
+ */
+sls_status sls_decode_append(const sls_attn_desc* desc, const void* k_new, const void* v_new,
+                             void* k_cache, void* v_cache, void* kmin, void* kmax,
+                             int32_t* ctx_len, int32_t* pos_out, void* stream);
+
 /* ---- metadata: 2-bit key thumbnails ------------------------------------ */
 
 /*

@@ -30,6 +30,7 @@ _D = ctypes.POINTER(AttnDesc)
 SIGNATURES = {
     "sls_pagemeta_build": (_I, [_D, _P, _P, _P, _P, _P]),
     "sls_pagemeta_update": (_I, [_D, _P, _P, _P, _P, _P]),
+    "sls_decode_append": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "sls_thumb_build": (_I, [_D, _P, _P, _I, _P, _P, _P]),
     "sls_thumb_update": (_I, [_D, _P, _P, _I, _P, _P, _P]),
     "sls_select_pages": (_I, [_D, _P, _P, _P, _P, _I, _I, _I, _P, _P, ctypes.c_size_t, _P]),

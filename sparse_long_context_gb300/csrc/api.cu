@@ -136,6 +136,20 @@ static sls_status check_block(const sls::Shape& s, int32_t block) {
   return SLS_OK;
 }
 
+sls_status sls_decode_append(const sls_attn_desc* desc, const void* k_new, const void* v_new, void* k_cache,
+                             void* v_cache, void* kmin, void* kmax, int32_t* ctx_len, int32_t* pos_out,
+                             void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(k_new); REQUIRE(v_new); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(ctx_len);
+  if ((kmin == nullptr) != (kmax == nullptr)) return fail(SLS_EINVAL, "kmin and kmax: both or neither");
+  if (kmin && s.P == 1) return fail(SLS_EINVAL, "page_size 1: the key cache is its own page metadata (pass NULL)");
+  return cuda_status(sls::launch_decode_append(s, k_new, v_new, k_cache, v_cache, kmin, kmax, ctx_len, pos_out,
+                                               (cudaStream_t)stream),
+                     "sls_decode_append");
+}
+
 sls_status sls_thumb_build(const sls_attn_desc* desc, const void* k_cache, const int32_t* ctx_len,
                            int32_t block, uint8_t* codes, void* scales, void* stream) {
   sls::Shape s;

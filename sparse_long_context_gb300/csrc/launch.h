@@ -54,6 +54,8 @@ cudaError_t launch_pagemeta_build(const Shape& s, const void* k, const int32_t* 
                                   void* kmin, void* kmax, cudaStream_t st);
 cudaError_t launch_pagemeta_update(const Shape& s, const void* k, const int32_t* pos,
                                    void* kmin, void* kmax, cudaStream_t st);
+cudaError_t launch_decode_append(const Shape& s, const void* k_new, const void* v_new, void* k, void* v,
+                                 void* kmin, void* kmax, int32_t* ctx_len, int32_t* pos_out, cudaStream_t st);
 cudaError_t launch_thumb_build(const Shape& s, const void* k, const int32_t* ctx_len,
                                int block, uint8_t* codes, void* scales, cudaStream_t st);
 cudaError_t launch_thumb_update(const Shape& s, const void* k, const int32_t* pos,

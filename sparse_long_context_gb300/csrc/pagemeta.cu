@@ -79,6 +79,45 @@ pagemeta_update_kernel(const T* __restrict__ k, const int32_t* __restrict__ pos,
   }
 }
 
+// One CTA per sequence: the new token's key and value of every KV head go to
+// position ctx_len[b] (when below Cap), the key is folded into its page's
+// min/max (the page's first token resets them), the position is reported in
+// pos_out, and ctx_len[b] advances by one.  Every thread reads ctx_len before
+// the barrier; only then does thread 0 advance it.
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+decode_append_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new, T* k, T* v, T* kmin, T* kmax,
+                     int32_t* ctx_len, int32_t* pos_out, int Hkv, int Cap, int P, int pshift) {
+  const int b = blockIdx.x;
+  const int t = ctx_len[b];
+  __syncthreads();
+  const bool ok = t >= 0 && t < Cap;
+  if (ok) {
+    for (int i = threadIdx.x; i < Hkv * D; i += blockDim.x) {
+      const size_t row = (size_t)b * Hkv + i / D;
+      const int c = i % D;
+      const T kx = k_new[row * D + c];
+      k[(row * Cap + t) * D + c] = kx;
+      v[(row * Cap + t) * D + c] = v_new[row * D + c];
+      if (kmin) {
+        const size_t o = (row * (Cap >> pshift) + (t >> pshift)) * D + c;
+        if ((t & (P - 1)) == 0) {
+          kmin[o] = kx;
+          kmax[o] = kx;
+        } else {
+          const float x = to_f32<T>(kx);
+          kmin[o] = from_f32<T>(fminf(to_f32<T>(kmin[o]), x));
+          kmax[o] = from_f32<T>(fmaxf(to_f32<T>(kmax[o]), x));
+        }
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (pos_out) pos_out[b] = ok ? t : -1;
+    if (ok) ctx_len[b] = t + 1;
+  }
+}
+
 // ---------------------------------------------------------------- thumbnails
 
 // Code of one element: 3 if k >= s/2, 2 if 0 <= k < s/2, 1 if -s/2 <= k < 0,
@@ -170,6 +209,24 @@ cudaError_t launch_pagemeta_update(const Shape& s, const void* k, const int32_t*
                      : pm_update<float, 128>(s, k, pos, kmin, kmax, st);
   return s.D == 64 ? pm_update<bf16, 64>(s, k, pos, kmin, kmax, st)
                    : pm_update<bf16, 128>(s, k, pos, kmin, kmax, st);
+}
+
+template <typename T, int D>
+static cudaError_t dec_append(const Shape& s, const void* k_new, const void* v_new, void* k, void* v, void* kmin,
+                              void* kmax, int32_t* ctx_len, int32_t* pos_out, cudaStream_t st) {
+  decode_append_kernel<T, D><<<s.B, 256, 0, st>>>(
+      static_cast<const T*>(k_new), static_cast<const T*>(v_new), static_cast<T*>(k), static_cast<T*>(v),
+      static_cast<T*>(kmin), static_cast<T*>(kmax), ctx_len, pos_out, s.Hkv, s.Cap, s.P, s.pshift);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_append(const Shape& s, const void* k_new, const void* v_new, void* k, void* v,
+                                 void* kmin, void* kmax, int32_t* ctx_len, int32_t* pos_out, cudaStream_t st) {
+  if (s.dtype == 0)
+    return s.D == 64 ? dec_append<float, 64>(s, k_new, v_new, k, v, kmin, kmax, ctx_len, pos_out, st)
+                     : dec_append<float, 128>(s, k_new, v_new, k, v, kmin, kmax, ctx_len, pos_out, st);
+  return s.D == 64 ? dec_append<bf16, 64>(s, k_new, v_new, k, v, kmin, kmax, ctx_len, pos_out, st)
+                   : dec_append<bf16, 128>(s, k_new, v_new, k, v, kmin, kmax, ctx_len, pos_out, st);
 }
 
 template <typename T, int D>

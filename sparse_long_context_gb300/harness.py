@@ -77,3 +77,51 @@ def run_step(dw: DeviceWorkload, num_splits=None, fused: bool = True, one_launch
     ops.pipeline_check()  # synchronises; raises if a pipelined kernel gave up waiting
     return (sel.cpu().numpy(), None if cnt is None else cnt.cpu().numpy(),
             out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64))
+
+
+class DecodeLoop:
+    """A multi-step decode loop resident on the device.  One step appends the
+    new token's key and value at ctx_len (keeping the selector's summaries
+    current: page min/max, or the thumbnail of a block the token completes),
+    advances ctx_len, then runs select + attend + combine on the longer
+    context.  capture() records one step in a CUDA graph; each replay decodes
+    one more token with no host work.  The caller writes the step's q,
+    k_new and v_new into the fixed buffers before a replay."""
+
+    def __init__(self, dw: DeviceWorkload, num_splits=None, min_sparsity: float = 0.0):
+        s = dw.spec
+        self.dw = dw
+        if s.selector == "quest":
+            self.step = ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, num_splits,
+                                        min_sparsity=min_sparsity)
+        else:
+            self.step = make_step(dw, num_splits)
+        dt = dw.K.dtype
+        self.k_new = torch.zeros((s.batch, s.num_kv_heads, s.head_dim), dtype=dt, device=dw.K.device)
+        self.v_new = torch.zeros_like(self.k_new)
+        self.pos = torch.empty(s.batch, dtype=torch.int32, device=dw.K.device)
+        self.graph = None
+
+    def run_once(self):
+        dw, s = self.dw, self.dw.spec
+        if s.selector == "quest":
+            meta = (dw.kmin, dw.kmax) if s.page_size > 1 else (None, None)
+            ops.decode_append(dw.desc, self.k_new, self.v_new, dw.K, dw.V, dw.ctx, *meta, pos_out=self.pos)
+            return self.step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx, dw.sink)
+        ops.decode_append(dw.desc, self.k_new, self.v_new, dw.K, dw.V, dw.ctx, pos_out=self.pos)
+        ops.thumb_update(dw.desc, dw.K, self.pos, s.block, dw.codes, dw.scales)
+        return self.step(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink)
+
+    def capture(self, stream=None):
+        """Records one step (nothing runs until replay())."""
+        stream = stream or torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            self.out, self.lse = self.run_once()
+        torch.cuda.current_stream().wait_stream(stream)
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
+        return self.out, self.lse

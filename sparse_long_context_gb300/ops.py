@@ -210,6 +210,16 @@ def combine_splits(desc: L.AttnDesc, parts, sink=None, out=None, lse=None, want_
     return out, lse
 
 
+def decode_append(desc: L.AttnDesc, k_new, v_new, k_cache, v_cache, ctx_len, kmin=None, kmax=None,
+                  pos_out=None):
+    """Writes one new token per sequence at ctx_len, keeps the page min/max
+    current and advances ctx_len (all on the device)."""
+    for t, nm in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, nm)
+    L.call("sls_decode_append", ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+           _ptr(kmin), _ptr(kmax), _ptr(ctx_len), _ptr(pos_out), _stream())
+
+
 def quest_step_workspace(desc: L.AttnDesc, k: int, num_splits: int = 0, device="cuda"):
     """Zero-filled workspace of quest_decode_step (reusable)."""
     n = L.load().sls_quest_decode_step_workspace_size(ctypes.byref(desc), int(k), int(num_splits))
