@@ -9,9 +9,12 @@ inputs (no real KV cache exists here).
 value = algorithmic bytes of the step (page min/max metadata of every page
 + K and V of the selected tokens) / device time per step, in GB/s.
 
-The timed region replays one CUDA graph per buffer set; NSETS copies of the
-KV cache and metadata rotate so that consecutive steps never find their
-bytes in L2 (NSETS * step bytes >= 4 * L2).  `python bench.py --impl
+The timed region replays CUDA graphs of up to 8 consecutive steps each (a
+decode engine captures a whole iteration in one graph; consecutive step
+kernels overlap launch and tail through programmatic dependent launch).
+NSETS copies of the KV cache and metadata rotate, step i using set
+i % NSETS, so that consecutive steps never find their bytes in L2
+(NSETS * step bytes >= 4 * L2).  `replay_us` times graphs of one step.  `python bench.py --impl
 reference` times the fp64 CPU oracle on the same workload instead.
 """
 from __future__ import annotations
@@ -331,14 +334,28 @@ def run_ours(args, s: W.Spec):
             with torch.cuda.graph(g, stream=stream):
                 st(dw.q, K, V, kmin, kmax, dw.ctx)
             graphs.append(g)
+        # the timed loop's graphs: `spg` consecutive steps each (global step i
+        # uses buffer set i % nsets, continuing across graphs), as a decode
+        # engine captures a whole iteration; consecutive kernels overlap
+        # their launch with the previous one's tail (programmatic launch)
+        spg = next(r for r in (8, 4, 2, 1) if args.steps % r == 0)
+        mgraphs = []
+        for gi in range(nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(spg):
+                    u = (gi * spg + j) % nsets
+                    K, V, kmin, kmax = sets[u]
+                    steps_obj[u](dw.q, K, V, kmin, kmax, dw.ctx)
+            mgraphs.append(g)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % nsets].replay()
+        for i in range(-(-args.warmup // spg)):
+            mgraphs[i % nsets].replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -347,8 +364,8 @@ def run_ours(args, s: W.Spec):
     w0 = time.time()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(args.steps):
-            graphs[i % nsets].replay()
+        for i in range(args.steps // spg):
+            mgraphs[i % nsets].replay()
         e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -526,7 +543,7 @@ def run_ours(args, s: W.Spec):
         "config": {"workload": _workload_name(s), "batch": s.batch, "ctx_len": s.ctx_len[0],
                    "seq_len": s.ctx_len[0], "page_size": s.page_size, "budget_tokens": s.k_pages * s.page_size,
                    "num_splits": ops.quest_step_splits(dw.desc, s.k_pages) if one else S,
-                   "launches_per_step": 1 if one else 2, "buffer_sets": nsets,
+                   "launches_per_step": 1 if one else 3, "buffer_sets": nsets, "steps_per_graph": spg,
                    "l2": f"inputs rotate over {nsets} buffer sets ({nsets * nbytes['total'] / 1e6:.0f} MB >= 4x L2 {l2 / 1e6:.0f} MB)",
                    "parallelism": f"weak: {world} GPU(s), {s.batch} sequences each"},
         "bytes_per_step": nbytes["total"], "bytes_select": nbytes["select"], "bytes_attend": nbytes["attend"],
