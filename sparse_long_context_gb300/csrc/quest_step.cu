@@ -52,6 +52,7 @@ struct StepArgs {
   float min_sparsity;  // rows with N < min_sparsity * k * P attend densely (0: never)
   int topk_mode;       // 0: candidates of every CTA, 1: all keys to every CTA
   int cand_cap;        // candidates one CTA may send
+  int cand_m;          // real keys a CTA sends (about; plus its forced keys)
 };
 
 template <int D>
@@ -455,11 +456,12 @@ __device__ __forceinline__ bool kth_largest_reg(const uint32_t (&kk)[KPT], int k
 
 // Positions in the ascending list of the keys chosen by (T, take): for the
 // key at position i, (#keys > T before i) + min(#T-keys before i, take).
-// Entries that land in [e0, e0 + nent) get share[pos - e0] = value[i]
-// (value = position when `values` is null).
+// Entries that land in [e0, e0 + nent) get share[pos - e0] = values[i *
+// vstride] (the position i when `values` is null).
 template <int NT, int KPT>
 __device__ __forceinline__ void place_chosen(const uint32_t (&kk)[KPT], uint32_t T, int take, int e0, int nent,
-                                             const int32_t* values, int32_t* share, int* scan_tmp) {
+                                             const int32_t* values, int32_t* share, int* scan_tmp,
+                                             int vstride = 1) {
   int gt = 0, eq = 0;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
@@ -477,7 +479,7 @@ __device__ __forceinline__ void place_chosen(const uint32_t (&kk)[KPT], uint32_t
     Gp += g;
     Ep += e;
     const int i = threadIdx.x * KPT + j;
-    if (pos >= e0 && pos < e0 + nent) share[pos - e0] = values ? values[i] : i;
+    if (pos >= e0 && pos < e0 + nent) share[pos - e0] = values ? values[(size_t)i * vstride] : i;
   }
 }
 
@@ -495,18 +497,105 @@ __device__ __forceinline__ bool select_share_reg(const uint32_t* keys, int n, in
   return true;
 }
 
-// Candidate selection: the row's chosen pages from the cluster's candidate
-// lists (cand_key / cand_page, n candidates in page order, n <= NT * KPT).
+// A CTA's candidate threshold: the smallest key tau such that the CTA's real
+// (non-forced) keys >= tau are its m largest plus the rest of their
+// histogram bin (the range-scaled bins of kth_largest_reg); 1 (every key)
+// when the CTA holds at most m real keys.  No exact rank: the cluster's
+// selection checks afterwards that the row's k-th largest is >= every CTA's
+// tau, which makes the candidates a superset of the row's top k.
 template <int NT, int KPT>
-__device__ __forceinline__ bool select_share_cand(const uint32_t* cand_key, const int32_t* cand_page, int n, int k,
-                                                  uint32_t* scratch, int e0, int nent, int32_t* share,
-                                                  int* scan_tmp) {
+__device__ __forceinline__ uint32_t top_bin_threshold(const uint32_t (&kk)[KPT], int m, uint32_t* hist,
+                                                      int* scan_tmp) {
+  __shared__ TopkScalars sc;
+  constexpr int NWp = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t mx = 0, mn = 0xffffffffu;
+  int nr = 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t x = kk[j];
+    const bool real = x != kForcedKey32 && x != 0u;
+    nr += real;
+    mx = max(mx, real ? x : 0u);
+    mn = min(mn, real ? x : 0xffffffffu);
+  }
+  for (int d = threadIdx.x; d < kWinBins + 32; d += NT) hist[d] = 0;
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  nr = __reduce_add_sync(0xffffffffu, nr);
+  if (lane == 0) {
+    sc.red_max[warp] = mx;
+    sc.red_min[warp] = mn;
+    sc.red_n[warp] = nr;
+  }
+  if (threadIdx.x == 0) sc.bin = -1;
+  __syncthreads();
+  const uint32_t top = __reduce_max_sync(0xffffffffu, lane < NWp ? sc.red_max[lane] : 0u);
+  const uint32_t bot = __reduce_min_sync(0xffffffffu, lane < NWp ? sc.red_min[lane] : 0xffffffffu);
+  const int nreal = __reduce_add_sync(0xffffffffu, lane < NWp ? sc.red_n[lane] : 0);
+  if (nreal <= m) return 1u;  // uniform: every thread read the same totals
+  const uint32_t span = top - bot;
+  const int shift = span >= (uint32_t)kWinBins ? 32 - __clz(span >> 11) : 0;
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const uint32_t x = kk[j];
+    const bool real = x != kForcedKey32 && x != 0u;
+    atomicAdd(&hist[real ? (top - x) >> shift : kWinBins + lane], 1u);
+  }
+  __syncthreads();
+  constexpr int BPT = (kWinBins + NT - 1) / NT;
+  const int b0 = threadIdx.x * BPT;
+  int cnt[BPT], sum = 0;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    cnt[i] = b0 + i < kWinBins ? (int)hist[b0 + i] : 0;
+    sum += cnt[i];
+  }
+  int total;
+  int above = block_scan_excl<NT>(sum, scan_tmp, total);
+  int mybin = -1;
+#pragma unroll
+  for (int i = 0; i < BPT; ++i) {
+    mybin = (above < m && above + cnt[i] >= m) ? b0 + i : mybin;
+    above += cnt[i];
+  }
+  if (mybin >= 0) sc.bin = mybin;
+  __syncthreads();
+  // keys x with (top - x) >> shift <= bin
+  const long long lo = (long long)top - ((long long)(sc.bin + 1) << shift) + 1;
+  return (uint32_t)max(lo, 1ll);
+}
+
+// Candidates of the cluster's CTAs in one array of (key, page) pairs, CTA c
+// at slots [c * cap, c * cap + n[c]), slot order = page order.  Thread t
+// holds slots [t * KPT, t * KPT + KPT); slots past a CTA's count hold key 0.
+template <int NT, int KPT>
+__device__ __forceinline__ void load_cand_reg(const uint2* cand, int cap, int C, const int* n, uint32_t (&kk)[KPT]) {
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int i = threadIdx.x * KPT + j;
+    const int c = i / cap;
+    kk[j] = (c < C && i - c * cap < n[c]) ? cand[i].x : 0u;
+  }
+}
+
+// The row's chosen pages from the cluster's candidates into this CTA's share
+// of the list.  False (the same in every CTA of the cluster) when the rank
+// overflows or when the row's k-th largest T falls below some CTA's
+// threshold: that CTA may hold unsent keys >= T.
+template <int NT, int KPT>
+__device__ __forceinline__ bool select_share_cand(const uint2* cand, int cap, int C, const int* n,
+                                                  const uint32_t* tau, int k, uint32_t* scratch, int e0, int nent,
+                                                  int32_t* share, int* scan_tmp) {
   uint32_t kk[KPT];
-  load_keys_reg<NT, KPT>(cand_key, n, kk);
+  load_cand_reg<NT, KPT>(cand, cap, C, n, kk);
   uint32_t T;
   int take;
   if (!kth_largest_reg<NT, KPT>(kk, k, scratch, scan_tmp, T, take)) return false;
-  place_chosen<NT, KPT>(kk, T, take, e0, nent, cand_page, share, scan_tmp);
+  uint32_t tmax = 0u;
+  for (int c = 0; c < C; ++c) tmax = max(tmax, tau[c]);
+  if (T < tmax) return false;
+  place_chosen<NT, KPT>(kk, T, take, e0, nent, reinterpret_cast<const int32_t*>(cand) + 1, share, scan_tmp, 2);
   return true;
 }
 
@@ -531,7 +620,8 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   __shared__ float sM[W][8], sL[W][8], sF[W][8];
   __shared__ float sHm[8], sHl[8];
   __shared__ int scan_tmp[32];
-  __shared__ int s_cand_n[kMaxClusterSplits], s_cand_pre[kMaxClusterSplits], s_cand_tot;
+  __shared__ int s_cand_n[kMaxClusterSplits];
+  __shared__ uint32_t s_cand_tau[kMaxClusterSplits];
 
   cg::cluster_group cl = cg::this_cluster();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -650,32 +740,29 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // completes the arrive made at entry
     bool use_all = sa.topk_mode != 0;
     if (!use_all) {
-      // Candidates: every page of the row's top k is among its own CTA's
-      // top k (ties at the CTA's threshold included), so each CTA sends
-      // only its keys >= its local k-th largest; every CTA then selects
-      // among the cluster's candidates, which stay in page order.
+      // Candidates: each CTA sends its forced keys and about its cand_m
+      // largest real keys (every key >= its threshold tau, with the
+      // threshold itself); every CTA then selects the row's top k among the
+      // cluster's candidates.  That selection is exact when the row's k-th
+      // largest is >= every CTA's tau (nothing unsent can reach it), which
+      // holds unless one CTA holds far more than its share of the row's top
+      // k; otherwise every CTA falls back to the all-keys selection.
       const int cap = sa.cand_cap;
       uint32_t* scratch = reinterpret_cast<uint32_t*>(ring);
-      uint32_t* gkp = reinterpret_cast<uint32_t*>(ring + kTopkScratchBytes);  // [C][cap] (key, page) pairs
-      uint32_t* dk = gkp + 2 * C * cap;                                         // dense keys, page order
-      int32_t* dp = reinterpret_cast<int32_t*>(dk + C * cap);                   // dense pages
+      uint2* cand = reinterpret_cast<uint2*>(ring + kTopkScratchBytes);  // [C][cap] (key, page) pairs
       uint32_t kk[kLocalKeys];
       load_keys_reg<NT, kLocalKeys>(keys, nloc, kk);
-      uint32_t tau = 1u;  // every real key (all are > 0) when the CTA holds at most k pages
-      if (nloc > k) {
-        int tk;
-        if (!kth_largest_reg<NT, kLocalKeys>(kk, k, scratch, scan_tmp, tau, tk)) tau = 1u;
-      }
+      const uint32_t tau = top_bin_threshold<NT, kLocalKeys>(kk, sa.cand_m, scratch, scan_tmp);
       const int j0 = threadIdx.x * kLocalKeys;
       int cnt = 0;
 #pragma unroll
-      for (int j = 0; j < kLocalKeys; ++j) cnt += kk[j] >= tau;  // slots past nloc hold 0
+      for (int j = 0; j < kLocalKeys; ++j) cnt += kk[j] >= tau;  // slots past nloc hold 0 < tau
       int total;
       const int off = block_scan_excl<NT>(cnt, scan_tmp, total);
       const bool ovf = total > cap;
-      cl.sync();  // every CTA has its candidates; every ring is free
+      cl.sync();  // every ring is free
       for (int c = 0; c < C; ++c) {
-        uint2* rkp = reinterpret_cast<uint2*>(cl.map_shared_rank(gkp, c)) + split * cap;
+        uint2* rkp = cl.map_shared_rank(cand, c) + split * cap;
         if (!ovf) {
           int o = off;
 #pragma unroll
@@ -685,34 +772,24 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
             o += in;
           }
         }
-        if (threadIdx.x == 0) cl.map_shared_rank(s_cand_n, c)[split] = ovf ? -1 : total;
+        if (threadIdx.x == 0) {
+          cl.map_shared_rank(s_cand_n, c)[split] = ovf ? -1 : total;
+          cl.map_shared_rank(s_cand_tau, c)[split] = tau;
+        }
       }
       cl.sync();  // the cluster's candidates are delivered
-      if (threadIdx.x == 0) {
-        int t = 0;
-        for (int c = 0; c < C; ++c) {
-          s_cand_pre[c] = t;
-          t = (t < 0 || s_cand_n[c] < 0) ? -1 : t + s_cand_n[c];
-        }
-        s_cand_tot = t;
-      }
-      __syncthreads();
-      const int n = s_cand_tot;
-      if (n < 0 || n > NT * kRegKeys) {
-        use_all = true;  // same decision in every CTA: the counts are the cluster's
+      bool any_ovf = false;
+      for (int c = 0; c < C; ++c) any_ovf |= s_cand_n[c] < 0;
+      if (any_ovf) {
+        use_all = true;  // the same in every CTA: the counts are the cluster's
       } else {
-        for (int c = 0; c < C; ++c)
-          for (int i = threadIdx.x; i < s_cand_n[c]; i += NT) {
-            const uint2 e = reinterpret_cast<const uint2*>(gkp)[c * cap + i];
-            dk[s_cand_pre[c] + i] = e.x;
-            dp[s_cand_pre[c] + i] = (int32_t)e.y;
-          }
-        __syncthreads();
+        const int slots = C * cap;
         bool okc;
-        if (n <= NT * 4) okc = select_share_cand<NT, 4>(dk, dp, n, k, scratch, e0, nent, list, scan_tmp);
-        else if (n <= NT * 8) okc = select_share_cand<NT, 8>(dk, dp, n, k, scratch, e0, nent, list, scan_tmp);
-        else if (n <= NT * 16) okc = select_share_cand<NT, 16>(dk, dp, n, k, scratch, e0, nent, list, scan_tmp);
-        else okc = select_share_cand<NT, 32>(dk, dp, n, k, scratch, e0, nent, list, scan_tmp);
+        if (slots <= NT * 2) okc = select_share_cand<NT, 2>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        else if (slots <= NT * 4) okc = select_share_cand<NT, 4>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        else if (slots <= NT * 8) okc = select_share_cand<NT, 8>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        else if (slots <= NT * 16) okc = select_share_cand<NT, 16>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        else okc = select_share_cand<NT, 32>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
         if (!okc) use_all = true;  // identical candidates everywhere: the same in every CTA
       }
     }
@@ -944,8 +1021,12 @@ static cudaError_t step_launch(const Shape& s, const StepArgs& sa0, cudaStream_t
   sa.keys_bytes = (keys + 15) / 16 * 16;
   sa.scratch_off = (int)(((size_t)sa.npcap * 4 + 15) / 16 * 16);
   // candidate selection when a CTA's keys fit its registers and the lists fit the ring
-  sa.cand_cap = (sa.k + 64 + 15) / 16 * 16;
-  const size_t cand_bytes = (size_t)kTopkScratchBytes + (size_t)16 * C * sa.cand_cap;
+  // a CTA holds about k / C of the row's chosen pages: it sends about twice
+  // that (plus its forced pages), room for the rest of a histogram bin
+  const int forced_max = sa.n_sink + (sa.n_local + s.P - 1) / s.P + 1;
+  sa.cand_m = std::min(sa.k, (2 * sa.k + C - 1) / C + 8);
+  sa.cand_cap = (sa.cand_m + forced_max + 16 + 15) / 16 * 16;
+  const size_t cand_bytes = (size_t)kTopkScratchBytes + (size_t)8 * C * sa.cand_cap;
   sa.topk_mode = (sa.chunk <= (kTmaConsumers + 1) * 32 * kLocalKeys && cand_bytes <= StepLayout<D>::RING_REGION &&
                   C * sa.cand_cap <= (kTmaConsumers + 1) * 32 * kRegKeys)
                      ? 0

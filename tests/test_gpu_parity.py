@@ -308,6 +308,26 @@ def test_topk_scores_spanning_many_octaves():
         assert t <= 2
 
 
+@pytest.mark.parametrize("splits,npg", [(5, 50), (5, 100), (5, 300), (2, 128), (16, 20), (16, 128)])
+def test_topk_with_the_best_pages_in_one_split(splits, npg):
+    """A run of `npg` pages whose keys align with the query holds most of the
+    row's top k: a split may hold more than its share of the chosen pages
+    (its candidates alone then do not decide the selection)."""
+    s = W.spec("qwen7b", batch=1, ctx_len=[8192])
+    host = W.generate(s)
+    K = W.bf16_bits_to_f32(host.K[0]).copy()
+    q = W.bf16_bits_to_f32(host.q[0])
+    p0 = 200
+    for h in range(s.num_kv_heads):
+        sgn = np.sign(q[h * s.group])
+        t0, t1 = p0 * 16, (p0 + npg) * 16
+        K[h, t0:t1] = np.abs(K[h, t0:t1]) * sgn[None, :] * 1.5
+    host.K[0] = _bits(K)
+    dw = PT.upload(s, host)
+    sel, cnt, out, lse = PT.run_step(dw, num_splits=splits)
+    check_all_rows(s, host, sel, cnt, out, lse)
+
+
 # 2..16 splits combine inside a thread-block cluster, more through global memory
 @pytest.mark.parametrize("splits", [1, 2, 3, 8, 13, 16, 17, 64, 1024])
 def test_split_counts_do_not_change_the_result(splits):
