@@ -760,21 +760,30 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       int total;
       const int off = block_scan_excl<NT>(cnt, scan_tmp, total);
       const bool ovf = total > cap;
-      cl.sync();  // every ring is free
-      for (int c = 0; c < C; ++c) {
-        uint2* rkp = cl.map_shared_rank(cand, c) + split * cap;
-        if (!ovf) {
-          int o = off;
+      // compact into this CTA's own slots (its ring is free), then copy the
+      // block to the other CTAs with coalesced 16-byte stores
+      uint2* mine = cand + split * cap;  // 16-byte aligned: cap is even
+      if (!ovf) {
+        int o = off;
 #pragma unroll
-          for (int j = 0; j < kLocalKeys; ++j) {
-            const bool in = kk[j] >= tau;
-            if (in) rkp[o] = make_uint2(kk[j], (uint32_t)(sa.chunk * split + j0 + j));
-            o += in;
-          }
+        for (int j = 0; j < kLocalKeys; ++j) {
+          const bool in = kk[j] >= tau;
+          if (in) mine[o] = make_uint2(kk[j], (uint32_t)(sa.chunk * split + j0 + j));
+          o += in;
         }
-        if (threadIdx.x == 0) {
-          cl.map_shared_rank(s_cand_n, c)[split] = ovf ? -1 : total;
-          cl.map_shared_rank(s_cand_tau, c)[split] = tau;
+      }
+      cl.sync();  // every ring is free; the compacted block is complete
+      if (threadIdx.x < C) {
+        cl.map_shared_rank(s_cand_n, (int)threadIdx.x)[split] = ovf ? -1 : total;
+        cl.map_shared_rank(s_cand_tau, (int)threadIdx.x)[split] = tau;
+      }
+      if (!ovf && C > 1) {
+        const int n2 = (total + 1) >> 1;  // pairs of entries (the odd tail entry is past the count)
+        const uint4* src = reinterpret_cast<const uint4*>(mine);
+        for (int idx = threadIdx.x; idx < (C - 1) * n2; idx += NT) {
+          const int cc = idx / n2, i = idx - cc * n2;
+          const int c = cc + (cc >= split);
+          reinterpret_cast<uint4*>(cl.map_shared_rank(cand, c) + split * cap)[i] = src[i];
         }
       }
       cl.sync();  // the cluster's candidates are delivered
@@ -1025,7 +1034,7 @@ static cudaError_t step_launch(const Shape& s, const StepArgs& sa0, cudaStream_t
   // that (plus its forced pages), room for the rest of a histogram bin
   const int forced_max = sa.n_sink + (sa.n_local + s.P - 1) / s.P + 1;
   sa.cand_m = std::min(sa.k, (2 * sa.k + C - 1) / C + 8);
-  sa.cand_cap = (sa.cand_m + forced_max + 16 + 15) / 16 * 16;
+  sa.cand_cap = (sa.cand_m + forced_max + 16 + 1) / 2 * 2;  // even: 16-byte aligned per-CTA blocks
   const size_t cand_bytes = (size_t)kTopkScratchBytes + (size_t)8 * C * sa.cand_cap;
   sa.topk_mode = (sa.chunk <= (kTmaConsumers + 1) * 32 * kLocalKeys && cand_bytes <= StepLayout<D>::RING_REGION &&
                   C * sa.cand_cap <= (kTmaConsumers + 1) * 32 * kRegKeys)
