@@ -14,7 +14,8 @@ Sources (web pages; cited by title and section):
   sink page and local pages).
 * [ffd]       "Faster Than Flash: Exploiting Attention Sparsity for Efficient
   Long-Context Decoding" (picx.dev summary), Methodology 1 (2-bit mid-rise
-  thumbnails), 2 (top-delta, eqs. 1-3) and 3 (eq. 4 scaling).
+  thumbnails and 8-bit residuals), 2 (top-delta, eqs. 1-3) and 3 (eq. 4:
+  scaling and the refined final scores).
 * [undivided] "Attention: Undivided & Uncompressed" (clintsebastian.com),
   Notation (S = QK^T / sqrt(d)) and Traffic (online softmax, delayed division).
 * [tsd]       "Training-free sparse attention for long-context LLM decode"
@@ -358,6 +359,74 @@ def delta_select_row(q, K, n, block, delta, scale):
     kept = blocks[margins >= -delta]
     sel = np.union1d(delta_forced_blocks(n, block), kept)
     return sel.astype(np.int64), (blocks, margins)
+
+
+# ----------------------------------------------------------------------------
+# FFD 8-bit residuals and the refined scores (eq. 4)
+# ----------------------------------------------------------------------------
+
+RES_DENOM = 508.0  # 4 * 127: residual codes -127..127 span the +-s/4 quantisation error
+
+
+def residual_quantize(Kb: np.ndarray, codes: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """8-bit residual of one complete block ([ffd] Methodology 1: the key is
+    split into the 2-bit thumbnail k_quant and an 8-bit residual k_res that
+    recovers the precision the thumbnail drops).
+
+    Readings (the page gives no encoding): the residual e = k - k^ of a
+    mid-rise 2-bit code lies in [-s/4, s/4] (levels s/2 apart, thresholds
+    half-way), so it is stored on the thumbnail's own block/channel scale s
+    as r = round(e * 508 / s) in [-127, 127], and the refined key is
+    k~ = k^ + r * s / 508.  The integer is decided in float32, the kernel's
+    precision: e = f32(k - k^), x = f32(f32(e * 508) / s), r = rint(x) (ties
+    to even), clamped to [-127, 127]; s = 0 (an all-zero channel) gives 0.
+    k^ is exact in float32 (a bf16 scale times +-0.25 or +-0.75).
+
+    Kb [T, D] float64 (exact bf16 values); codes [T, D]; s [D].
+    Returns r [T, D] int8."""
+    k32 = np.asarray(Kb, np.float64).astype(np.float32)
+    kh32 = thumb_dequant(codes, s).astype(np.float32)
+    e = k32 - kh32                                   # float32 arithmetic
+    x = e * np.float32(RES_DENOM)
+    s32 = np.broadcast_to(np.asarray(s, np.float64).astype(np.float32), x.shape)
+    safe = np.where(s32 > 0, s32, np.float32(1.0))
+    x = np.where(s32 > 0, x / safe, np.float32(0.0)).astype(np.float32)
+    return np.clip(np.rint(x), -127, 127).astype(np.int8)
+
+
+def refined_keys(codes: np.ndarray, s: np.ndarray, r: np.ndarray) -> np.ndarray:
+    """The key the refinement scores with: k~ = k^ + r * s / 508, so that
+    q . k~ = q . k_quant + q . k_res ([ffd] eq. 4 numerator).  float64."""
+    return thumb_dequant(codes, s) + np.asarray(r, np.float64) * (np.asarray(s, np.float64) / RES_DENOM)
+
+
+def residuals_row(K: np.ndarray, n: int, block: int):
+    """Codes, scales and residuals of every complete block of one row
+    (positions < n).  Returns (codes [nfull*block, D], scales [nfull, D],
+    res [nfull*block, D] int8)."""
+    codes, scales = thumbnails_row(K, n, block)
+    res = np.zeros(codes.shape, dtype=np.int8)
+    for j in range(n // block):
+        rows = slice(j * block, (j + 1) * block)
+        res[rows] = residual_quantize(K[rows], codes[rows], scales[j])
+    return codes, scales, res
+
+
+def refined_attention_row(q, K, V, blocks, n, block, scale, sink=None):
+    """Attention over the selected blocks with the refined final scores of
+    [ffd] Methodology 3 step 3, eq. 4: s = (q . k_quant + q . k_res) / sqrt(d)
+    for the tokens of complete blocks.
+
+    Reading: the newest block is partial and has no thumbnail yet, so its
+    tokens are scored with the exact key; values are exact.
+    q [G, D]; K, V [>= n, D] float64; blocks: the row's block list."""
+    codes, scales, res = residuals_row(K, n, block)
+    Kt = np.array(K[:n], dtype=np.float64, copy=True)
+    nfull = n // block
+    if nfull:
+        Kt[:nfull * block] = refined_keys(codes, np.repeat(scales, block, axis=0), res)
+    toks = pages_to_tokens(np.asarray(blocks), n, block)
+    return softmax_attention(q, Kt[toks], V[toks], scale, sink)
 
 
 # ----------------------------------------------------------------------------

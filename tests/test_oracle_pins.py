@@ -344,3 +344,105 @@ def test_recall_bounds_additivity_and_monotonicity():
     np.testing.assert_allclose(O.attention_mass_recall(q, K, np.array([-1, 3, -1]), n, P, 1.0),
                                O.attention_mass_recall(q, K, np.array([3]), n, P, 1.0))
     assert np.all(O.attention_mass_recall(q, K, a, 0, P, 1.0) == 1.0)
+
+
+# ------------------------------------------------------- ffd 8-bit residuals
+
+def _bf16_exact(x):
+    """Round float64 values to the nearest bf16 (ties to even), as float64."""
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def test_residual_golden():
+    d = golden("ffd_residual_example.json")
+    K = np.array(d["K"])
+    codes, s = O.thumb_quantize(K)
+    assert codes.tolist() == d["codes"] and s.tolist() == d["scale"]
+    r = O.residual_quantize(K, codes, s)
+    assert r.tolist() == d["res"]
+    kt = O.refined_keys(codes, s, r)
+    np.testing.assert_allclose(kt, d["refined"], rtol=0, atol=1e-15)
+    assert abs(float(np.dot(d["q"], kt[1])) - d["score_token1"]) < 1e-15
+
+
+def test_residual_error_bound():
+    """The refined key is within s/1016 of the key (half a residual step of
+    s/508) up to float32 rounding of the code decision; codes stay in range;
+    an all-zero channel gets 0."""
+    K = _bf16_exact(rnd(40, 64, 128) * np.exp(2 * rnd(41, 1, 128)))
+    codes, s = O.thumb_quantize(K)
+    r = O.residual_quantize(K, codes, s)
+    assert r.dtype == np.int8 and np.abs(r.astype(int)).max() <= 127
+    err = np.abs(K - O.refined_keys(codes, s, r))
+    assert np.all(err <= s / 1016 * (1 + 1e-5) + 1e-30)
+    assert np.max(err / s) > 0.9 / 1016      # the bound is met, not slack
+    K[:, 5] = 0
+    codes, s = O.thumb_quantize(K)
+    assert np.all(O.residual_quantize(K, codes, s)[:, 5] == 0)
+
+
+def test_residual_is_the_nearest_level_brute_force():
+    """Exact rational arithmetic: r is the integer j in [-127, 127] nearest to
+    (k - k^) * 508 / s (ties to the even j), except where float32 rounding of
+    that quotient could move it across a half-integer."""
+    from fractions import Fraction
+    K = _bf16_exact(rnd(42, 64, 16) * np.exp(rnd(43, 1, 16)))
+    K[3, :] = 0.0
+    codes, s = O.thumb_quantize(K)
+    r = O.residual_quantize(K, codes, s)
+    near = 0
+    for t in range(K.shape[0]):
+        for c in range(K.shape[1]):
+            sc = Fraction(float(s[c]))
+            kh = (Fraction(int(codes[t, c])) - Fraction(3, 2)) * sc / 2
+            x = (Fraction(float(K[t, c])) - kh) * 508 / sc
+            lo = math.floor(x)
+            frac = x - lo
+            if abs(frac - Fraction(1, 2)) < Fraction(1, 10**5) and frac != Fraction(1, 2):
+                near += 1
+                continue
+            j = lo + 1 if frac > Fraction(1, 2) else lo
+            if frac == Fraction(1, 2) and lo % 2 != 0:
+                j = lo + 1
+            assert int(r[t, c]) == max(-127, min(127, j)), (t, c, x)
+    assert near < 10
+
+
+def test_refined_attention_brute_force():
+    """Refined attention over a block list: complete blocks scored with the
+    brute-force nearest-level keys, the partial newest block with the exact
+    key, against explicit loops."""
+    block, D, G = 64, 8, 2
+    n = 3 * block + 10
+    K = _bf16_exact(rnd(44, 4 * block, D) * 1.5)
+    V = rnd(45, 4 * block, D)
+    q = rnd(46, G, D)
+    scale = 1 / math.sqrt(D)
+    blocks = np.array([0, 2, 3])
+    o, lse = O.refined_attention_row(q, K, V, blocks, n, block, scale)
+    Kt = []
+    toks = []
+    for b in blocks.tolist():
+        for t in range(b * block, min((b + 1) * block, n)):
+            toks.append(t)
+            if t >= (n // block) * block:
+                Kt.append(K[t].tolist())       # partial block: exact key
+                continue
+            blk = K[b * block:(b + 1) * block]
+            row = []
+            for c in range(D):
+                sc = max(abs(v) for v in blk[:, c])
+                k = K[t, c]
+                code = 3 if k >= sc / 2 else (2 if k >= 0 else (1 if k >= -sc / 2 else 0))
+                kh = (code - 1.5) * sc / 2
+                best = min(range(-127, 128), key=lambda j: (abs(k - (kh + j * sc / 508)), j % 2))
+                row.append(kh + best * sc / 508 if sc > 0 else 0.0)
+            Kt.append(row)
+    ob, lb = brute_attention(q.tolist(), Kt, V[toks].tolist(), scale)
+    np.testing.assert_allclose(o, ob, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(lse, lb, rtol=1e-12, atol=1e-12)
+    # close to exact attention: k~ is within s/1016 of k
+    oe, _ = O.sparse_attention_row(q, K, V, blocks, n, block, scale)
+    assert np.max(np.abs(o - oe)) < 2e-2
