@@ -181,6 +181,26 @@ sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache,
                             const int32_t* pos, int32_t block,
                             uint8_t* codes, void* scales, void* stream);
 
+/*
+ * Thumbnails plus 8-bit residuals ("Faster Than Flash", Methodology 1: the
+ * key splits into the 2-bit thumbnail and an 8-bit residual that recovers
+ * the precision the thumbnail drops).  The codes and scales are those of
+ * sls_thumb_build; the residual of element (t, c) is
+ *   r = clamp(rint(((k - k^) * 508) / s), -127, 127),   0 when s == 0,
+ * each step one IEEE float32 operation (k^ = (code - 1.5) * s / 2 exactly),
+ * so that the refined key k~ = k^ + r * s / 508 is within s / 1016 of k.
+ *   res  [B, Hkv, Cap, D] int8 (written for complete blocks only)
+ * The _update form quantises the block that position pos[b] completes, as
+ * sls_thumb_update does.  Errors: SLS_EINVAL for a null pointer or a block
+ * that is not a power of two in [16, 256] dividing Cap.
+ */
+sls_status sls_thumb_residual_build(const sls_attn_desc* desc, const void* k_cache,
+                                    const int32_t* ctx_len, int32_t block, uint8_t* codes,
+                                    void* scales, int8_t* res, void* stream);
+sls_status sls_thumb_residual_update(const sls_attn_desc* desc, const void* k_cache,
+                                     const int32_t* pos, int32_t block, uint8_t* codes,
+                                     void* scales, int8_t* res, void* stream);
+
 /* ---- selection --------------------------------------------------------- */
 
 /*
@@ -353,6 +373,34 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
                                             const float* sink, void* out, float* lse,
                                             void* workspace, size_t workspace_bytes,
                                             void* stream);
+
+/*
+ * Refined top-delta attention ("Faster Than Flash", Methodology 3 step 3,
+ * eq. 4): attention over each row's kept blocks in which the tokens of
+ * complete blocks are scored with the refined key
+ *   k~ = (code - 1.5) * s / 2 + r * s / 508
+ * (thumbnail level plus 8-bit residual, sls_thumb_residual_build) instead
+ * of the bf16 key; tokens of the newest, partial block are scored with the
+ * bf16 key.  Values are the bf16 V.  The combine (sink, lse) is fused as in
+ * sls_sparse_decode_attend_combine, with the same workspace.
+ *   desc.page_size  the thumbnail block (>= 16); bf16, G <= 8, D 64 or 128
+ *   codes, scales, res  as written by sls_thumb_residual_build/_update
+ *   block_idx [B*Hkv, idx_stride] int32, count [B*Hkv] int32: the kept
+ *             blocks of each row (sls_select_delta's output); -1 entries
+ *             and blocks past the context are skipped
+ *   |q * s| must stay below 65504 (the products run in fp16 hi/lo parts).
+ * Errors: SLS_EUNSUPPORTED for another dtype, G > 8 or blocks < 16 tokens;
+ * SLS_EINVAL for null pointers or bad sizes; SLS_EWORKSPACE.
+ */
+sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const void* q,
+                                             const void* k_cache, const void* v_cache,
+                                             const uint8_t* codes, const void* scales,
+                                             const int8_t* res, const int32_t* block_idx,
+                                             int32_t idx_stride, const int32_t* count,
+                                             const int32_t* ctx_len, int32_t num_splits,
+                                             const float* sink, void* out, float* lse,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream);
 
 /* ---- the whole Quest decode step ---------------------------------------- */
 

@@ -157,8 +157,20 @@ sls_status sls_thumb_build(const sls_attn_desc* desc, const void* k_cache, const
   if (r) return r;
   if ((r = check_block(s, block))) return r;
   REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(codes); REQUIRE(scales);
-  return cuda_status(sls::launch_thumb_build(s, k_cache, ctx_len, block, codes, scales, (cudaStream_t)stream),
+  return cuda_status(sls::launch_thumb_build(s, k_cache, ctx_len, block, codes, scales, nullptr,
+                                             (cudaStream_t)stream),
                      "sls_thumb_build");
+}
+
+sls_status sls_thumb_residual_build(const sls_attn_desc* desc, const void* k_cache, const int32_t* ctx_len,
+                                    int32_t block, uint8_t* codes, void* scales, int8_t* res, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  if ((r = check_block(s, block))) return r;
+  REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(codes); REQUIRE(scales); REQUIRE(res);
+  return cuda_status(sls::launch_thumb_build(s, k_cache, ctx_len, block, codes, scales, res, (cudaStream_t)stream),
+                     "sls_thumb_residual_build");
 }
 
 sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache, const int32_t* pos,
@@ -168,8 +180,20 @@ sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache, cons
   if (r) return r;
   if ((r = check_block(s, block))) return r;
   REQUIRE(k_cache); REQUIRE(pos); REQUIRE(codes); REQUIRE(scales);
-  return cuda_status(sls::launch_thumb_update(s, k_cache, pos, block, codes, scales, (cudaStream_t)stream),
+  return cuda_status(sls::launch_thumb_update(s, k_cache, pos, block, codes, scales, nullptr,
+                                              (cudaStream_t)stream),
                      "sls_thumb_update");
+}
+
+sls_status sls_thumb_residual_update(const sls_attn_desc* desc, const void* k_cache, const int32_t* pos,
+                                     int32_t block, uint8_t* codes, void* scales, int8_t* res, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  if ((r = check_block(s, block))) return r;
+  REQUIRE(k_cache); REQUIRE(pos); REQUIRE(codes); REQUIRE(scales); REQUIRE(res);
+  return cuda_status(sls::launch_thumb_update(s, k_cache, pos, block, codes, scales, res, (cudaStream_t)stream),
+                     "sls_thumb_residual_update");
 }
 
 size_t sls_select_pages_workspace_size(const sls_attn_desc* desc) {
@@ -314,6 +338,47 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
   return cuda_status(sls::launch_attend(s, q, k_cache, v_cache, page_idx, idx_stride, count, k_fixed, ctx_len,
                                         num_splits, o_part, m_part, l_part, (cudaStream_t)stream, &f),
                      "sls_sparse_decode_attend_combine");
+}
+
+sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const void* q, const void* k_cache,
+                                             const void* v_cache, const uint8_t* codes, const void* scales,
+                                             const int8_t* res, const int32_t* block_idx, int32_t idx_stride,
+                                             const int32_t* count, const int32_t* ctx_len, int32_t num_splits,
+                                             const float* sink, void* out, float* lse, void* workspace,
+                                             size_t workspace_bytes, void* stream) {
+  sls::Shape s;
+  sls_status r = check_desc(desc, &s);
+  if (r) return r;
+  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(codes); REQUIRE(scales); REQUIRE(res);
+  REQUIRE(block_idx); REQUIRE(count); REQUIRE(ctx_len); REQUIRE(out);
+  if (!sls::refined_supported(s))
+    return fail(SLS_EUNSUPPORTED, "refined attend needs bf16, G <= 8 and blocks (page_size) of >= 16 tokens");
+  if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
+  if (num_splits < 0 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [0, 1024]", num_splits);
+  int64_t ctas;
+  if (!checked_mul((int64_t)s.B * s.Hkv, num_splits ? num_splits : sls::max_auto_splits(s), &ctas) ||
+      ctas > INT32_MAX)
+    return fail(SLS_EOVERFLOW, "grid too large");
+  const size_t need = sls_attend_combine_workspace_size(desc, num_splits);
+  if (!workspace || workspace_bytes < need)
+    return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  char* w = static_cast<char*>(workspace);
+  const size_t heads = (size_t)s.B * s.Hq * (num_splits ? num_splits : sls::max_auto_splits(s));
+  sls::FusedCombine f;
+  f.tickets = reinterpret_cast<int32_t*>(w);
+  w += align256((size_t)s.B * s.Hkv * 4);
+  float* o_part = reinterpret_cast<float*>(w);
+  w += align256(heads * s.D * 4);
+  float* m_part = reinterpret_cast<float*>(w);
+  w += align256(heads * 4);
+  float* l_part = reinterpret_cast<float*>(w);
+  f.sink = sink;
+  f.out = out;
+  f.lse = lse;
+  return cuda_status(sls::launch_attend_refined(s, q, k_cache, v_cache, codes, scales, res, block_idx, idx_stride,
+                                                count, ctx_len, num_splits, o_part, m_part, l_part, f,
+                                                (cudaStream_t)stream),
+                     "sls_refined_decode_attend_combine");
 }
 
 size_t sls_quest_decode_step_workspace_size(const sls_attn_desc* desc, int32_t k, int32_t num_splits) {

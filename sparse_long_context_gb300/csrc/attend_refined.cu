@@ -1,0 +1,367 @@
+// Refined top-delta attention for bf16 caches ("Faster Than Flash",
+// Methodology 3 step 3, eq. 4): split-K online-softmax attention over a
+// row's kept blocks in which every token of a complete block is scored with
+// its refined key k~ = k^ + r s / 508 (the 2-bit thumbnail level plus the
+// 8-bit residual on the thumbnail's block/channel scale s) instead of the
+// bf16 key.  Tokens of the newest, partial block have no thumbnail yet and
+// use the bf16 key.  Values are bf16.
+//
+// One CTA per (row, split) with 8 warps; a warp walks 16-token groups of its
+// slice with two groups in flight in registers (the shape of the register-
+// fed attend).  Lane (r, m) owns the channels [m D/4, (m+1) D/4) of the
+// score product and loads, for tokens r and r + 8 of a group, either D/16
+// bytes of codes and D/4 bytes of residuals (a refined group) or D/2 bytes
+// of bf16 key (a group of the partial block).
+//
+// Refined scores run on the tensor cores in fp16:
+//   n = 254 code - 381 + r   is an integer in [-508, 508], exact in fp16,
+//   q s                      is exact in fp32 (bf16 x bf16) and splits into
+//                            fp16 hi + lo (q s - hi is exact in fp32),
+//   S^T = (Q s)_hi N + (Q s)_lo N   accumulated in fp32,
+// which is 508 q . k~ to about 2^-22 relative (|q s| < 65504 assumed).
+// Softmax and O^T += V^T P^T follow the register-fed attend.
+#include <cuda_fp16.h>
+
+#include "attend_common.cuh"
+#include "launch.h"
+#include "mma.cuh"
+
+namespace sls {
+
+constexpr int kRefWarps = 8;
+constexpr int kRefStaged = 1024;  // block-list entries staged in shared memory
+
+struct RefinedArgs {
+  AttendArgs a;         // q, k, v, block list (page_idx with P = block), count, ctx_len, partials, combine
+  const uint8_t* codes; // [rows, Cap, D/4]
+  const bf16* scales;   // [rows, Cap/P, D]
+  const int8_t* res;    // [rows, Cap, D]
+};
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 ldg_stream2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ldg_stream1(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// n of channel pair p (channels 2p, 2p+1 of an 8-channel step) as fp16x2:
+// 16 code bits of the step and the two residual words of the step.
+__device__ __forceinline__ uint32_t refined_pair(uint32_t c16, uint32_t w0, uint32_t w1, int p) {
+  const uint32_t cb = c16 >> (4 * p);
+  // (1024 + code_a, 1024 + code_b): a 10-bit exponent field of 25 leaves unit steps
+  const uint32_t ch = (cb & 3u) | ((cb & 0xcu) << 14) | 0x64006400u;
+  // (1152 + r_a, 1152 + r_b): the signed byte plus 128 under the same exponent
+  const uint32_t w = ((p >> 1) ? w1 : w0) ^ 0x80808080u;
+  const uint32_t rh = __byte_perm(w, 0x64646464u, (p & 1) ? 0x4342u : 0x4140u);
+  const __half2 c = __hsub2(bits_h2(ch), __float2half2_rn(1024.f));
+  const __half2 t = __hfma2(c, __float2half2_rn(254.f), bits_h2(rh));  // 254 c + 1152 + r <= 2041: exact
+  return h2_bits(__hsub2(t, __float2half2_rn(1533.f)));               // 254 c - 381 + r
+}
+
+template <int D>
+struct RGroup {
+  static constexpr int NS = D / 32, VL = D / 64;
+  uint4 kc[2][NS];  // exact: bf16 key chunks; refined: [0] codes, [1..] residual bytes
+  uint4 vc[4][VL];
+  int pv[4];
+  int pg;           // the group's block, -1 when the group is empty
+  bool refined;
+};
+
+struct RSeg {
+  int N, nent, ntok;
+};
+
+template <int D>
+__device__ __forceinline__ void load_rgroup(RGroup<D>& g, const RefinedArgs& ra, const RSeg& sl, const int* s_pg,
+                                            const int32_t* plist, int gi, int row) {
+  constexpr int NS = RGroup<D>::NS, VL = RGroup<D>::VL;
+  constexpr int CPR = D / 8;
+  const AttendArgs& a = ra.a;
+  const int lane = threadIdx.x & 31, r = lane >> 2, m = lane & 3;
+  const int j0 = gi << 4;  // 16 tokens inside one block (P >= 16)
+  int base = -1, lim = 0, pg = -1;
+  if (j0 < sl.ntok) {
+    const int e = j0 >> a.pshift;
+    pg = e < kRefStaged ? s_pg[e] : __ldg(plist + e);
+    if ((unsigned)pg < (unsigned)(a.Cap >> a.pshift)) {
+      base = (pg << a.pshift) + (j0 & (a.P - 1));
+      lim = min(sl.N - base, 16);
+    } else {
+      pg = -1;
+    }
+  }
+  g.pg = pg;
+  g.refined = pg >= 0 && ((pg + 1) << a.pshift) <= sl.N;  // a complete block has its thumbnail
+  auto at = [&](int t) { return (base >= 0 && t < lim) ? base + t : -1; };
+  const int pk[2] = {at(r), at(r + 8)};
+  g.pv[0] = at(2 * m);
+  g.pv[1] = at(2 * m + 1);
+  g.pv[2] = at(2 * m + 8);
+  g.pv[3] = at(2 * m + 9);
+  const size_t rbase = (size_t)row * a.Cap;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const size_t tok = rbase + (size_t)max(pk[t], 0);
+    const bool ok = pk[t] >= 0;
+    if (g.refined) {
+      if constexpr (D == 128) {
+        const uint2 c = ok ? ldg_stream2(ra.codes + tok * (D / 4) + m * (D / 16)) : make_uint2(0u, 0u);
+        g.kc[t][0] = make_uint4(c.x, c.y, 0u, 0u);
+      } else {
+        g.kc[t][0] = make_uint4(ok ? ldg_stream1(ra.codes + tok * (D / 4) + m * (D / 16)) : 0u, 0u, 0u, 0u);
+      }
+      const int8_t* rp = ra.res + tok * D + m * (D / 4);
+#pragma unroll
+      for (int u = 0; u < D / 64; ++u) g.kc[t][1 + u] = ok ? ldg_stream(rp + 16 * u) : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      const bf16* kp = static_cast<const bf16*>(a.k) + tok * D + m * (D / 4);
+#pragma unroll
+      for (int s = 0; s < NS; ++s) g.kc[t][s] = ok ? ldg_stream(kp + 8 * s) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  const bf16* vl = static_cast<const bf16*>(a.v) + rbase * D + r * CPR;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const bf16* v = vl + (size_t)max(g.pv[t], 0) * D;
+#pragma unroll
+    for (int u = 0; u < VL; ++u) g.vc[t][u] = g.pv[t] >= 0 ? ldg_stream(v + 8 * u) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void compute_rgroup(const RGroup<D>& g, const RefinedArgs& ra, int row,
+                                               const uint32_t (&qa)[D / 32][4], float (&o)[D / 16][4],
+                                               float& m_run, float& l_run) {
+  constexpr int NS = RGroup<D>::NS, MT = D / 16;
+  const AttendArgs& a = ra.a;
+  const int lane = threadIdx.x & 31, m = lane & 3;
+  float sc[2][2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) sc[nt][c][0] = sc[nt][c][1] = sc[nt][c][2] = sc[nt][c][3] = 0.f;
+  float mul = a.qscale;
+  if (g.refined) {
+    mul = a.qscale * (1.f / 508.f);
+    const bf16* sp = ra.scales + ((size_t)row * (a.Cap >> a.pshift) + g.pg) * D + m * (D / 4);
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(sp + 8 * s));
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t sw = (&s8.x)[p];
+        const float xa = bf16_lo_f(qa[s][p]) * bf16_lo_f(sw);  // exact
+        const float xb = bf16_hi_f(qa[s][p]) * bf16_hi_f(sw);
+        const __half2 h = __floats2half2_rn(xa, xb);
+        hi[p] = h2_bits(h);
+        lo[p] = h2_bits(__floats2half2_rn(xa - __low2float(h), xb - __high2float(h)));
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t c16 = (&g.kc[nt][0].x)[s >> 1] >> (16 * (s & 1));
+        const uint32_t* rw = &g.kc[nt][1].x;
+        const uint32_t w0 = rw[2 * s], w1 = rw[2 * s + 1];
+        const uint32_t n0 = refined_pair(c16, w0, w1, 0), n1 = refined_pair(c16, w0, w1, 1);
+        const uint32_t n2 = refined_pair(c16, w0, w1, 2), n3 = refined_pair(c16, w0, w1, 3);
+        mma_f16(sc[nt][0], hi[0], 0u, hi[1], 0u, n0, n1);
+        mma_f16(sc[nt][1], hi[2], 0u, hi[3], 0u, n2, n3);
+        mma_f16(sc[nt][0], lo[0], 0u, lo[1], 0u, n0, n1);
+        mma_f16(sc[nt][1], lo[2], 0u, lo[3], 0u, n2, n3);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        mma_bf16(sc[nt][0], qa[s][0], 0u, qa[s][1], 0u, g.kc[nt][s].x, g.kc[nt][s].y);
+        mma_bf16(sc[nt][1], qa[s][2], 0u, qa[s][3], 0u, g.kc[nt][s].z, g.kc[nt][s].w);
+      }
+    }
+  }
+  // head r, tokens 2m, 2m+1, 2m+8, 2m+9 (base-2 units)
+  float s4[4];
+  s4[0] = g.pv[0] >= 0 ? (sc[0][0][0] + sc[0][1][0]) * mul : kNegInf;
+  s4[1] = g.pv[1] >= 0 ? (sc[0][0][1] + sc[0][1][1]) * mul : kNegInf;
+  s4[2] = g.pv[2] >= 0 ? (sc[1][0][0] + sc[1][1][0]) * mul : kNegInf;
+  s4[3] = g.pv[3] >= 0 ? (sc[1][0][1] + sc[1][1][1]) * mul : kNegInf;
+  float gm = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
+  gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
+  gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+  const float mn = fmaxf(m_run, gm);
+  const bool live = mn != kNegInf;
+  const float alpha = live ? exp2f(m_run - mn) : 1.f;
+  m_run = mn;
+  float p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = live ? exp2f(s4[i] - mn) : 0.f;
+  l_run = fmaf(l_run, alpha, (p[0] + p[1]) + (p[2] + p[3]));
+  const uint32_t pb0 = pack_bf16(p[0], p[1]), pb1 = pack_bf16(p[2], p[3]);
+  const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * m);
+  const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * m + 4);
+#pragma unroll
+  for (int t = 0; t < MT; ++t) {
+    o[t][0] *= a_lo; o[t][1] *= a_hi; o[t][2] *= a_lo; o[t][3] *= a_hi;
+  }
+#pragma unroll
+  for (int t = 0; t < MT; ++t) {
+    const int u = t >> 2, wsel = t & 3;
+    const uint32_t w0 = (&g.vc[0][u].x)[wsel], w1 = (&g.vc[1][u].x)[wsel];
+    const uint32_t w2 = (&g.vc[2][u].x)[wsel], w3 = (&g.vc[3][u].x)[wsel];
+    mma_bf16(o[t], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
+             __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kRefWarps * 32, 1) attend_refined_kernel(const RefinedArgs ra) {
+  pdl_wait_then_release();
+  constexpr int NW = kRefWarps, NS = D / 32, MT = D / 16, CPR = D / 8;
+  extern __shared__ float sO[];  // [NW][8][D]
+  __shared__ float sM[NW][8], sL[NW][8];
+  __shared__ int s_pg[kRefStaged];
+  const AttendArgs& a = ra.a;
+  const int row = blockIdx.x / a.S, split = blockIdx.x % a.S;
+  const Slice slc = attend_slice(a, row, split);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, m = lane & 3;
+  const int b = row / a.Hkv, h = row % a.Hkv;
+  const int G = a.G;
+  const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + slc.e0;
+  RSeg sl;
+  sl.N = slc.N;
+  sl.nent = slc.nent;
+  sl.ntok = slc.nent << a.pshift;
+  for (int i = threadIdx.x; i < min(sl.nent, kRefStaged); i += NW * 32) s_pg[i] = __ldg(plist + i);
+
+  // Q as the A operand, head r (rows 8..15 zero), the lane's channel range
+  uint32_t qa[NS][4];
+  {
+    const bf16* qp = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G + r) * D + m * (D / 4);
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+      const uint4 c = r < G ? ldg_stream(qp + 8 * s) : make_uint4(0, 0, 0, 0);
+      qa[s][0] = c.x; qa[s][1] = c.y; qa[s][2] = c.z; qa[s][3] = c.w;
+    }
+  }
+  float o[MT][4];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  float m_run = kNegInf, l_run = 0.f;
+  __syncthreads();
+
+  const int ngroups = (sl.ntok + 15) >> 4;
+  RGroup<D> ga, gb;
+  int gi = warp;
+  if (gi < ngroups) load_rgroup<D>(ga, ra, sl, s_pg, plist, gi, row);
+  while (gi < ngroups) {
+    if (gi + NW < ngroups) load_rgroup<D>(gb, ra, sl, s_pg, plist, gi + NW, row);
+    compute_rgroup<D>(ga, ra, row, qa, o, m_run, l_run);
+    gi += NW;
+    if (gi >= ngroups) break;
+    if (gi + NW < ngroups) load_rgroup<D>(ga, ra, sl, s_pg, plist, gi + NW, row);
+    compute_rgroup<D>(gb, ra, row, qa, o, m_run, l_run);
+    gi += NW;
+  }
+
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  if (m == 0) {
+    sM[warp][r] = m_run;
+    sL[warp][r] = l_run;
+  }
+#pragma unroll
+  for (int t = 0; t < MT; ++t) {
+    const int ch = CPR * r + 2 * t;
+    sO[(warp * 8 + 2 * m) * D + ch] = o[t][0];
+    sO[(warp * 8 + 2 * m + 1) * D + ch] = o[t][1];
+    sO[(warp * 8 + 2 * m) * D + ch + 1] = o[t][2];
+    sO[(warp * 8 + 2 * m + 1) * D + ch + 1] = o[t][3];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D; i += NW * 32) {
+    const int g = i / D, d = i % D;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sM[w][g]);
+    float av = 0.f, lv = 0.f;
+    if (M != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        if (sM[w][g] == kNegInf) continue;
+        const float f = exp2f(sM[w][g] - M);
+        av += sO[(w * 8 + g) * D + d] * f;
+        lv += sL[w][g] * f;
+      }
+    }
+    const size_t hq = (size_t)b * a.Hq + (size_t)h * G + g;
+    a.o_part[(hq * a.S + split) * D + d] = av;
+    if (d == 0) {
+      a.m_part[hq * a.S + split] = M == kNegInf ? kNegInf : M * kLn2;
+      a.l_part[hq * a.S + split] = lv;
+    }
+  }
+  if (a.tickets) combine_row_if_last<bf16, D, NW * 32>(a, row, a.S);
+}
+
+bool refined_supported(const Shape& s) { return s.dtype == 1 && s.G <= 8 && s.P >= 16 && (s.D == 64 || s.D == 128); }
+
+template <int D>
+static cudaError_t refined_launch(const RefinedArgs& ra, int grid, cudaStream_t st) {
+  constexpr size_t smem = (size_t)kRefWarps * 8 * D * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(attend_refined_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(attend_refined_kernel<D>, dim3(grid), dim3(kRefWarps * 32), smem, st, ra);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attend_refined(const Shape& s, const void* q, const void* k, const void* v, const uint8_t* codes,
+                                  const void* scales, const int8_t* res, const int32_t* block_idx, int idx_stride,
+                                  const int32_t* count, const int32_t* ctx_len, int num_splits, float* o_part,
+                                  float* m_part, float* l_part, const FusedCombine& fused, cudaStream_t st) {
+  RefinedArgs ra;
+  AttendArgs& a = ra.a;
+  a = AttendArgs{};
+  a.tickets = fused.tickets;
+  a.sink = fused.sink;
+  a.out = fused.out;
+  a.lse = fused.lse;
+  a.q = q; a.k = k; a.v = v;
+  a.page_idx = block_idx; a.count = count; a.ctx_len = ctx_len;
+  a.o_part = o_part; a.m_part = m_part; a.l_part = l_part;
+  a.idx_stride = idx_stride; a.k_fixed = idx_stride; a.S = num_splits;
+  a.cluster = 0;
+  if (num_splits == 0) {
+    a.S = attend_default_splits(s, idx_stride);
+    if (a.S > max_auto_splits(s)) a.S = max_auto_splits(s);
+  }
+  a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.G; a.Cap = s.Cap; a.P = s.P; a.pshift = s.pshift;
+  a.qscale = s.scale * kLog2e;
+  ra.codes = codes;
+  ra.scales = static_cast<const bf16*>(scales);
+  ra.res = res;
+  const int grid = s.B * s.Hkv * a.S;
+  return s.D == 128 ? refined_launch<128>(ra, grid, st) : refined_launch<64>(ra, grid, st);
+}
+
+}  // namespace sls

@@ -57,9 +57,16 @@ cudaError_t launch_pagemeta_update(const Shape& s, const void* k, const int32_t*
 cudaError_t launch_decode_append(const Shape& s, const void* k_new, const void* v_new, void* k, void* v,
                                  void* kmin, void* kmax, int32_t* ctx_len, int32_t* pos_out, cudaStream_t st);
 cudaError_t launch_thumb_build(const Shape& s, const void* k, const int32_t* ctx_len,
-                               int block, uint8_t* codes, void* scales, cudaStream_t st);
+                               int block, uint8_t* codes, void* scales, int8_t* res, cudaStream_t st);
 cudaError_t launch_thumb_update(const Shape& s, const void* k, const int32_t* pos,
-                                int block, uint8_t* codes, void* scales, cudaStream_t st);
+                                int block, uint8_t* codes, void* scales, int8_t* res, cudaStream_t st);
+
+bool refined_supported(const Shape& s);
+struct FusedCombine;
+cudaError_t launch_attend_refined(const Shape& s, const void* q, const void* k, const void* v, const uint8_t* codes,
+                                  const void* scales, const int8_t* res, const int32_t* block_idx, int idx_stride,
+                                  const int32_t* count, const int32_t* ctx_len, int num_splits, float* o_part,
+                                  float* m_part, float* l_part, const FusedCombine& fused, cudaStream_t st);
 
 size_t select_pages_workspace(const Shape& s);
 cudaError_t launch_select_pages(const Shape& s, const void* q, const void* kmin,

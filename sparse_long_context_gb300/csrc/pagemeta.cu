@@ -126,10 +126,24 @@ __device__ __forceinline__ uint32_t thumb_code(float x, float half) {
   return x >= half ? 3u : (x >= 0.f ? 2u : (x >= -half ? 1u : 0u));
 }
 
-// Quantise block j of `row` (block tokens, all valid).  blockDim.x == D.
+// 8-bit residual of one element ("Faster Than Flash", Methodology 1: the
+// key splits into the 2-bit thumbnail and an 8-bit residual): the error
+// e = k - k^ of the mid-rise code lies in [-s/4, s/4] and is stored as
+// r = rint(e * 508 / s) in [-127, 127] on the thumbnail's scale s (0 when
+// s = 0).  Every step is one IEEE float32 operation, so the integer does not
+// depend on contraction or on the division's implementation.
+__device__ __forceinline__ int8_t residual_code(float x, float s, uint32_t code) {
+  if (!(s > 0.f)) return 0;
+  const float kh = __fmul_rn((float)code - 1.5f, s) * 0.5f;  // exact: a level of the thumbnail
+  const float q = __fdiv_rn(__fmul_rn(__fsub_rn(x, kh), 508.f), s);
+  return (int8_t)fminf(fmaxf(rintf(q), -127.f), 127.f);
+}
+
+// Quantise block j of `row` (block tokens, all valid), and its residuals
+// when `res` is given.  blockDim.x == D.
 template <typename T, int D>
 __device__ __forceinline__ void quantise_block(const T* __restrict__ k, uint8_t* codes, T* scales,
-                                               int row, int j, int Cap, int block, int nblk_cap) {
+                                               int8_t* res, int row, int j, int Cap, int block, int nblk_cap) {
   __shared__ float s_half[D];
   const int c = threadIdx.x;
   const T* src = k + ((size_t)row * Cap + (size_t)j * block) * D;
@@ -148,26 +162,34 @@ __device__ __forceinline__ void quantise_block(const T* __restrict__ k, uint8_t*
     for (int u = 0; u < 4; ++u) v |= thumb_code(to_f32<T>(x[u]), s_half[by * 4 + u]) << (2 * u);
     dst[i] = (uint8_t)v;
   }
+  if (res) {
+    // thread c walks channel c: the scale is its own
+    int8_t* rd = res + ((size_t)row * Cap + (size_t)j * block) * D + c;
+    for (int t = 0; t < block; ++t) {
+      const float x = to_f32<T>(src[(size_t)t * D + c]);
+      rd[(size_t)t * D] = residual_code(x, s, thumb_code(x, s_half[c]));
+    }
+  }
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(D)
 thumb_build_kernel(const T* __restrict__ k, const int32_t* __restrict__ ctx_len, uint8_t* codes,
-                   T* scales, int Hkv, int Cap, int block, int nblk_cap) {
+                   T* scales, int8_t* res, int Hkv, int Cap, int block, int nblk_cap) {
   const int row = blockIdx.y, j = blockIdx.x;
   const int N = clamp_len(ctx_len[row / Hkv], Cap);
   if ((j + 1) * block > N) return;
-  quantise_block<T, D>(k, codes, scales, row, j, Cap, block, nblk_cap);
+  quantise_block<T, D>(k, codes, scales, res, row, j, Cap, block, nblk_cap);
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(D)
 thumb_update_kernel(const T* __restrict__ k, const int32_t* __restrict__ pos, uint8_t* codes,
-                    T* scales, int Hkv, int Cap, int block, int nblk_cap) {
+                    T* scales, int8_t* res, int Hkv, int Cap, int block, int nblk_cap) {
   const int row = blockIdx.x;
   const int t = pos[row / Hkv];
   if (t < 0 || t >= Cap || (t + 1) % block != 0) return;
-  quantise_block<T, D>(k, codes, scales, row, t / block, Cap, block, nblk_cap);
+  quantise_block<T, D>(k, codes, scales, res, row, t / block, Cap, block, nblk_cap);
 }
 
 // ---------------------------------------------------------------- launches
@@ -231,39 +253,39 @@ cudaError_t launch_decode_append(const Shape& s, const void* k_new, const void* 
 
 template <typename T, int D>
 static cudaError_t th_build(const Shape& s, const void* k, const int32_t* ctx, int block,
-                            uint8_t* codes, void* scales, cudaStream_t st) {
+                            uint8_t* codes, void* scales, int8_t* res, cudaStream_t st) {
   const int nblk = s.Cap / block;
   dim3 grid(nblk, s.B * s.Hkv);
   thumb_build_kernel<T, D><<<grid, D, 0, st>>>(static_cast<const T*>(k), ctx, codes, static_cast<T*>(scales),
-                                               s.Hkv, s.Cap, block, nblk);
+                                               res, s.Hkv, s.Cap, block, nblk);
   return cudaGetLastError();
 }
 
 cudaError_t launch_thumb_build(const Shape& s, const void* k, const int32_t* ctx_len, int block,
-                               uint8_t* codes, void* scales, cudaStream_t st) {
+                               uint8_t* codes, void* scales, int8_t* res, cudaStream_t st) {
   if (s.dtype == 0)
-    return s.D == 64 ? th_build<float, 64>(s, k, ctx_len, block, codes, scales, st)
-                     : th_build<float, 128>(s, k, ctx_len, block, codes, scales, st);
-  return s.D == 64 ? th_build<bf16, 64>(s, k, ctx_len, block, codes, scales, st)
-                   : th_build<bf16, 128>(s, k, ctx_len, block, codes, scales, st);
+    return s.D == 64 ? th_build<float, 64>(s, k, ctx_len, block, codes, scales, res, st)
+                     : th_build<float, 128>(s, k, ctx_len, block, codes, scales, res, st);
+  return s.D == 64 ? th_build<bf16, 64>(s, k, ctx_len, block, codes, scales, res, st)
+                   : th_build<bf16, 128>(s, k, ctx_len, block, codes, scales, res, st);
 }
 
 template <typename T, int D>
 static cudaError_t th_update(const Shape& s, const void* k, const int32_t* pos, int block,
-                             uint8_t* codes, void* scales, cudaStream_t st) {
+                             uint8_t* codes, void* scales, int8_t* res, cudaStream_t st) {
   thumb_update_kernel<T, D><<<s.B * s.Hkv, D, 0, st>>>(static_cast<const T*>(k), pos, codes,
-                                                        static_cast<T*>(scales), s.Hkv, s.Cap, block,
+                                                        static_cast<T*>(scales), res, s.Hkv, s.Cap, block,
                                                         s.Cap / block);
   return cudaGetLastError();
 }
 
 cudaError_t launch_thumb_update(const Shape& s, const void* k, const int32_t* pos, int block,
-                                uint8_t* codes, void* scales, cudaStream_t st) {
+                                uint8_t* codes, void* scales, int8_t* res, cudaStream_t st) {
   if (s.dtype == 0)
-    return s.D == 64 ? th_update<float, 64>(s, k, pos, block, codes, scales, st)
-                     : th_update<float, 128>(s, k, pos, block, codes, scales, st);
-  return s.D == 64 ? th_update<bf16, 64>(s, k, pos, block, codes, scales, st)
-                   : th_update<bf16, 128>(s, k, pos, block, codes, scales, st);
+    return s.D == 64 ? th_update<float, 64>(s, k, pos, block, codes, scales, res, st)
+                     : th_update<float, 128>(s, k, pos, block, codes, scales, res, st);
+  return s.D == 64 ? th_update<bf16, 64>(s, k, pos, block, codes, scales, res, st)
+                   : th_update<bf16, 128>(s, k, pos, block, codes, scales, res, st);
 }
 
 }  // namespace sls

@@ -103,6 +103,24 @@ def thumb_update(desc: L.AttnDesc, k_cache, pos, block: int, codes, scales):
            _ptr(codes), _ptr(scales), _stream())
 
 
+def thumb_residual_build(desc: L.AttnDesc, k_cache, ctx_len, block: int, codes=None, scales=None, res=None):
+    """Thumbnails plus 8-bit residuals of every complete block."""
+    B, H, Cap, D = desc.batch, desc.num_kv_heads, desc.capacity, desc.head_dim
+    dev = k_cache.device
+    codes = torch.zeros((B, H, Cap, D // 4), dtype=torch.uint8, device=dev) if codes is None else codes
+    scales = torch.zeros((B, H, Cap // block, D), dtype=k_cache.dtype, device=dev) if scales is None else scales
+    res = torch.zeros((B, H, Cap, D), dtype=torch.int8, device=dev) if res is None else res
+    L.call("sls_thumb_residual_build", ctypes.byref(desc), _ptr(k_cache), _ptr(ctx_len), int(block), _ptr(codes),
+           _ptr(scales), _ptr(res), _stream())
+    return codes, scales, res
+
+
+def thumb_residual_update(desc: L.AttnDesc, k_cache, pos, block: int, codes, scales, res):
+    _need(pos, "pos", torch.int32)
+    L.call("sls_thumb_residual_update", ctypes.byref(desc), _ptr(k_cache), _ptr(pos), int(block), _ptr(codes),
+           _ptr(scales), _ptr(res), _stream())
+
+
 # ---------------------------------------------------------------- selection
 
 def select_pages_workspace(desc: L.AttnDesc, device="cuda"):
@@ -193,6 +211,28 @@ def sparse_decode_attend_combine(desc: L.AttnDesc, q, k_cache, v_cache, page_idx
     L.call("sls_sparse_decode_attend_combine", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
            _ptr(page_idx), stride, _ptr(count), kf, _ptr(ctx_len), int(num_splits), _ptr(sink),
            _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream())
+    return out, lse
+
+
+def refined_decode_attend_combine(desc: L.AttnDesc, q, k_cache, v_cache, codes, scales, res, block_idx, count,
+                                  ctx_len, num_splits: int = 0, sink=None, out=None, lse=None, workspace=None,
+                                  want_lse: bool = True):
+    """Attention over the kept blocks with the refined (2-bit + 8-bit) keys
+    of complete blocks, combine fused; returns (out, lse)."""
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (codes, "codes"), (scales, "scales"),
+                  (res, "res"), (block_idx, "block_idx"), (count, "count")):
+        _need(t, nm)
+    B, Hq, D = desc.batch, desc.num_q_heads, desc.head_dim
+    out = torch.empty((B, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, (Hq,))
+    workspace = attend_combine_workspace(desc, num_splits, q.device) if workspace is None else workspace
+    L.call("sls_refined_decode_attend_combine", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+           _ptr(codes), _ptr(scales), _ptr(res), _ptr(block_idx), int(block_idx.shape[-1]), _ptr(count),
+           _ptr(ctx_len), int(num_splits), _ptr(sink), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+           _stream())
     return out, lse
 
 
@@ -325,14 +365,18 @@ class QuestDecode:
 
 
 class DeltaDecode:
-    """One top-delta decode step (select_delta + attend + combine)."""
+    """One top-delta decode step (select_delta + attend + combine).  With
+    refined=True the attend scores complete blocks with the refined keys
+    (2-bit thumbnail + 8-bit residual, "Faster Than Flash" eq. 4): the call
+    then takes the residuals as well."""
 
     def __init__(self, desc: L.AttnDesc, block: int, delta: float, num_splits: Optional[int] = None,
-                 device="cuda", fused: bool = True):
+                 device="cuda", fused: bool = True, refined: bool = False):
         if desc.page_size != block:
             raise ValueError("attend page_size must equal the thumbnail block")
         self.desc, self.block, self.delta = desc, int(block), float(delta)
         self.fused = fused
+        self.refined = refined
         rows = desc.batch * desc.num_kv_heads
         nblk = desc.capacity // block
         self.S = num_splits or default_splits(desc, nblk)
@@ -358,6 +402,15 @@ class DeltaDecode:
                              count=self.count, parts=self.parts)
         return combine_splits(self.desc, self.parts, sink, out=self.out, lse=self.lse)
 
-    def __call__(self, q, k_cache, v_cache, codes, scales, ctx_len, sink=None):
+    def attend_refined(self, q, k_cache, v_cache, codes, scales, res, ctx_len, sink=None):
+        return refined_decode_attend_combine(self.desc, q, k_cache, v_cache, codes, scales, res, self.block_idx,
+                                             self.count, ctx_len, self.S, sink=sink, out=self.out, lse=self.lse,
+                                             workspace=self.ac_workspace)
+
+    def __call__(self, q, k_cache, v_cache, codes, scales, ctx_len, sink=None, res=None):
         self.select(q, k_cache, codes, scales, ctx_len)
+        if self.refined:
+            if res is None:
+                raise ValueError("the refined step needs the residuals")
+            return self.attend_refined(q, k_cache, v_cache, codes, scales, res, ctx_len, sink)
         return self.attend(q, k_cache, v_cache, ctx_len, sink)

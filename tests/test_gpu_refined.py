@@ -1,0 +1,173 @@
+"""FFD 8-bit residuals and the refined attention ("Faster Than Flash",
+Methodology 1 and eq. 4) through the C ABI against the fp64 oracle.
+
+Residual codes are integers decided in float32 on both sides: bit-exact.
+The refined step (top-delta selection, then attention whose complete blocks
+are scored with k~ = thumbnail level + residual) is compared with the
+oracle's refined attention on the same block sets, within the bf16 output
+tolerance."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import sls_oracle as O
+from sparse_long_context_gb300 import ops
+from sparse_long_context_gb300 import workloads as W
+
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def _row_inputs(s, host, b, h):
+    G = s.group
+    q = O.to_f64(host.q[b, h * G:(h + 1) * G], s.dtype)
+    K = O.to_f64(host.K[b, h], s.dtype)
+    V = O.to_f64(host.V[b, h], s.dtype)
+    sink = None if host.sink is None else host.sink[h * G:(h + 1) * G].astype(np.float64)
+    return q, K, V, sink
+
+
+def _check_residuals(s, host, codes, scales, res, ctx):
+    codes, scales, res = codes.cpu().numpy(), scales.float().cpu().numpy(), res.cpu().numpy()
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            n = int(ctx[b])
+            oc, osc, ores = O.residuals_row(O.to_f64(host.K[b, h], s.dtype), n, s.block)
+            nfull = n // s.block
+            np.testing.assert_array_equal(codes[b, h, :nfull * s.block], O.pack_codes(oc))
+            np.testing.assert_array_equal(scales[b, h, :nfull], osc)
+            np.testing.assert_array_equal(res[b, h, :nfull * s.block], ores)
+
+
+@pytest.mark.parametrize("ctx", [[64 * 9 + 5, 64 * 3], [64 * 40]])
+def test_residuals_are_bit_exact(ctx):
+    s = W.spec("ffd", ctx_len=ctx, capacity=64 * 40)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block)
+    torch.cuda.synchronize()
+    _check_residuals(s, host, codes, scales, res, host.ctx_len)
+    # the plain thumbnail call writes the same codes and scales
+    c2, s2 = ops.thumb_build(dw.desc, dw.K, dw.ctx, s.block)
+    assert torch.equal(c2, codes) and torch.equal(s2, scales)
+
+
+def test_residual_update_completes_blocks():
+    s = W.spec("ffd", batch=2, ctx_len=[64 * 5, 64 * 7], capacity=64 * 8)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    start = torch.tensor([64 * 3 + 10, 64 * 6 + 60], dtype=torch.int32, device="cuda")
+    codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, start, 64)
+    cur = start.cpu().numpy().copy()
+    end = host.ctx_len
+    while np.any(cur < end):
+        pos = np.where(cur < end, cur, -1).astype(np.int32)
+        ops.thumb_residual_update(dw.desc, dw.K, torch.from_numpy(pos).cuda(), 64, codes, scales, res)
+        cur = np.minimum(cur + 1, end)
+    torch.cuda.synchronize()
+    _check_residuals(s, host, codes, scales, res, end)
+
+
+SMALL = {
+    "ffd_ragged": dict(ctx_len=[65536 + 100, 20000], capacity=65536 + 128),
+    "ffd_aligned": dict(batch=1, ctx_len=8192),
+    "ffd_short": dict(batch=3, ctx_len=[64, 100, 1], capacity=256),
+}
+
+
+def _refined_step(s, host):
+    dw = PT.upload(s, host)
+    codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block)
+    step = ops.DeltaDecode(dw.desc, s.block, s.delta, refined=True)
+    out, lse = step(dw.q, dw.K, dw.V, codes, scales, dw.ctx, dw.sink, res=res)
+    ops.pipeline_check()
+    return dw, (codes, scales, res), step, out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy()
+
+
+def _refined_oracle(s, host, b, h, blocks):
+    q, K, V, sink = _row_inputs(s, host, b, h)
+    return O.refined_attention_row(q, K, V, blocks, int(host.ctx_len[b]), s.block, s.scale, sink)
+
+
+@pytest.mark.parametrize("key", list(SMALL))
+def test_refined_step_matches_oracle(key):
+    s = W.spec("ffd", **SMALL[key])
+    host = W.generate(s)
+    dw, (codes, scales, res), step, out, lse = _refined_step(s, host)
+    sel, cnt = step.block_idx.cpu().numpy(), step.count.cpu().numpy()
+    G = s.group
+    ties = 0
+    sets = []
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            r = b * s.num_kv_heads + h
+            orc = PT.oracle_row(s, host, b, h)
+            sets.append(orc.pages)
+            t = PT.check_delta_list(int(cnt[r]), sel[r], orc, s.delta)
+            ties += t
+            if t:
+                continue
+            o_ref, lse_ref = _refined_oracle(s, host, b, h, orc.pages)
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"refined row {(b, h)}")
+            fin = np.isfinite(lse_ref)
+            np.testing.assert_allclose(lse[b, h * G:(h + 1) * G][fin], lse_ref[fin], rtol=1e-4, atol=1e-4)
+    # the attend alone on the oracle's own block sets
+    width = max(1, max(len(p) for p in sets))
+    idx = np.full((s.rows, width), -1, dtype=np.int32)
+    count = np.array([len(p) for p in sets], dtype=np.int32)
+    for r, p in enumerate(sets):
+        idx[r, :len(p)] = p
+    o2, _ = ops.refined_decode_attend_combine(dw.desc, dw.q, dw.K, dw.V, codes, scales, res,
+                                              torch.from_numpy(idx).cuda(), torch.from_numpy(count).cuda(),
+                                              dw.ctx, 3, sink=dw.sink)
+    o2 = o2.float().cpu().numpy().astype(np.float64)
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            o_ref, _ = _refined_oracle(s, host, b, h, sets[b * s.num_kv_heads + h])
+            PT.assert_close(s, o2[b, h * G:(h + 1) * G], o_ref, f"refined attend on oracle set {(b, h)}")
+    print(f"{key}: boundary ties {ties}")
+
+
+def test_refined_scores_differ_from_exact_ones():
+    """The refined path really scores with k~: against the exact-key step on
+    the same selection the outputs differ (slightly), and both stay within
+    tolerance of their own oracle."""
+    s = W.spec("ffd", **SMALL["ffd_aligned"])
+    host = W.generate(s)
+    dw, _, step, out_ref, _ = _refined_step(s, host)
+    exact = ops.DeltaDecode(dw.desc, s.block, s.delta)
+    out_ex, _ = exact(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink)
+    out_ex = out_ex.float().cpu().numpy().astype(np.float64)
+    assert np.abs(out_ref - out_ex).max() > 0
+    q, K, V, sink = _row_inputs(s, host, 0, 0)
+    blocks = step.block_idx.cpu().numpy()[0, :int(step.count.cpu().numpy()[0])]
+    o_ex, _ = O.sparse_attention_row(q, K, V, blocks, int(host.ctx_len[0]), s.block, s.scale, sink)
+    o_rf, _ = O.refined_attention_row(q, K, V, blocks, int(host.ctx_len[0]), s.block, s.scale, sink)
+    assert np.abs(o_ex - o_rf).max() > 0
+
+
+def test_refined_full_size_sampled_rows():
+    """The full-size top-delta workload (2 sequences of 256k tokens), in the
+    launch configuration of the step, on two sampled rows."""
+    s = W.spec("ffd")
+    host = W.generate(s)
+    _, _, step, out, lse = _refined_step(s, host)
+    sel, cnt = step.block_idx.cpu().numpy(), step.count.cpu().numpy()
+    G = s.group
+    for b, h in [(0, 0), (s.batch - 1, s.num_kv_heads - 1)]:
+        r = b * s.num_kv_heads + h
+        orc = PT.oracle_row(s, host, b, h)
+        if PT.check_delta_list(int(cnt[r]), sel[r], orc, s.delta):
+            continue
+        o_ref, _ = _refined_oracle(s, host, b, h, orc.pages)
+        PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"full-size refined row {(b, h)}")
+    assert math.isfinite(float(np.abs(out).max()))
