@@ -580,13 +580,126 @@ def run_ours(args, s: W.Spec):
         dist.destroy_process_group()
 
 
+def delta_bytes(s: W.Spec, ctx, count, block_idx) -> dict:
+    """Algorithmic bytes of one top-delta step: the scan (codes, scales, the
+    pseudo-max keys) plus the kept blocks' keys and values, and the same
+    with the refined attend, which reads codes + residuals + the block's
+    scales instead of the bf16 key of every complete block."""
+    D, esz, blk = s.head_dim, 2, s.block
+    scan = algorithmic_bytes(s)["select"]
+    kv_exact = kv_refined = 0
+    for r in range(s.rows):
+        n = int(ctx[r // s.num_kv_heads])
+        nfull = n // blk
+        for j in block_idx[r, :int(count[r])].tolist():
+            ntok = max(0, min(blk, n - j * blk))
+            kv_exact += ntok * 2 * D * esz
+            if j < nfull:
+                kv_refined += ntok * (D // 4 + D + D * esz) + D * esz
+            else:
+                kv_refined += ntok * 2 * D * esz
+    return {"scan": int(scan), "attend_exact": int(kv_exact), "attend_refined": int(kv_refined)}
+
+
+def run_delta(args, s: W.Spec):
+    """The top-delta step on the FFD workload, with the exact-key attend and
+    with the refined (2-bit + 8-bit residual) attend."""
+    import torch
+    from sparse_long_context_gb300 import _lib
+    from sparse_long_context_gb300 import harness as H
+    from sparse_long_context_gb300 import ops
+
+    torch.cuda.set_device(0)
+    _lib.load()
+    host = W.generate(s)
+    dw = H.upload(s, host)
+    codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block)
+    exact = ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits)
+    refined = ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits, refined=True)
+    stream = torch.cuda.Stream()
+    spg = next(r for r in (8, 4, 2, 1) if args.steps % r == 0)
+    graphs = {}
+    with torch.cuda.stream(stream):
+        exact(dw.q, dw.K, dw.V, codes, scales, dw.ctx, dw.sink)
+        refined(dw.q, dw.K, dw.V, codes, scales, dw.ctx, dw.sink, res=res)
+        torch.cuda.synchronize()
+        for name, st in (("exact", exact), ("refined", refined)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(spg):
+                    st(dw.q, dw.K, dw.V, codes, scales, dw.ctx, dw.sink, res=res)
+            graphs[name] = g
+    ops.pipeline_check()
+    nb = delta_bytes(s, host.ctx_len, refined.count.cpu().numpy(), refined.block_idx.cpu().numpy())
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    us = {}
+    with torch.cuda.stream(stream):
+        for name, g in graphs.items():
+            for _ in range(-(-args.warmup // spg)):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps // spg):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us[name] = 1e3 * e0.elapsed_time(e1) / args.steps
+        # per-stage device time, eager launches between events
+        ev = {k: [] for k in ("select", "attend_exact", "attend_refined")}
+        for i in range(50):
+            if i % 10 == 0:
+                torch.cuda._sleep(int(2e7))
+            for name, fn in (("select", lambda: refined.select(dw.q, dw.K, codes, scales, dw.ctx)),
+                             ("attend_exact", lambda: exact.attend(dw.q, dw.K, dw.V, dw.ctx, dw.sink)),
+                             ("attend_refined", lambda: refined.attend_refined(dw.q, dw.K, dw.V, codes, scales,
+                                                                               res, dw.ctx, dw.sink))):
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b_.record(stream)
+                ev[name].append((a, b_))
+    torch.cuda.synchronize()
+    ops.pipeline_check()
+    clk = clocks.stop()
+    kus = {k: 1e3 * statistics.mean(a.elapsed_time(b_) for a, b_ in v) for k, v in ev.items()}
+    peak, peak_kind = load_peaks()
+    tot_ref = nb["scan"] + nb["attend_refined"]
+    value = tot_ref / (us["refined"] * 1e-6) / 1e9
+    achieved = nb["attend_refined"] / (kus["attend_refined"] * 1e-6) / 1e9
+    kept = int(refined.count.sum().item())
+    nblk = sum(-(-n // s.block) for n in s.ctx_len) * s.num_kv_heads
+    line = {
+        "metric": "top-delta decode step us and achieved HBM GB/s, refined attend", "value": round(value, 2),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us["refined"] / 1e3, 5), "us_per_step": round(us["refined"], 2),
+        "us_per_step_exact_attend": round(us["exact"], 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy, see workloads.py)",
+        "config": {"workload": f"{s.name}: B={s.batch} Hq={s.num_q_heads} Hkv={s.num_kv_heads} D={s.head_dim} "
+                               f"ctx={s.ctx_len[0]} block={s.block} delta={s.delta} bf16",
+                   "kept_blocks": kept, "kept_fraction": round(kept / nblk, 4), "steps_per_graph": spg,
+                   "l2": f"one buffer set of {(tot_ref) / 1e6:.0f} MB per step (> L2)"},
+        "bytes_per_step": tot_ref, "bytes": nb,
+        "kernel_us": {k: round(v, 2) for k, v in kus.items()},
+        "roofline": {"bound": "hbm", "kernel": "attend_refined_kernel (combine fused)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "peak_kind": f"{peak_kind} (burst copy)"},
+        "gpu_launches": 3 * args.steps,  # delta scan, compaction, refined attend
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="qwen1p5b", choices=("qwen1p5b", "qwen7b"))
+    ap.add_argument("--workload", default="qwen1p5b", choices=("qwen1p5b", "qwen7b", "ffd"),
+                    help="ffd: the top-delta step with exact and refined attends (a study line)")
     ap.add_argument("--ctx", type=int, default=None, help="context length (default: the workload's)")
     ap.add_argument("--batch", type=int, default=None, help="sequences per GPU (default: the workload's)")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-decode comparison")
@@ -605,6 +718,8 @@ def main():
     s = W.spec(args.workload, **kw)
     if args.impl == "reference":
         run_reference(args, s)
+    elif s.selector != "quest":
+        run_delta(args, s)
     else:
         run_ours(args, s)
 
