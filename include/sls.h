@@ -381,26 +381,33 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
  *   k~ = (code - 1.5) * s / 2 + r * s / 508
  * (thumbnail level plus 8-bit residual, sls_thumb_residual_build) instead
  * of the bf16 key; tokens of the newest, partial block are scored with the
- * bf16 key.  Values are the bf16 V.  The combine (sink, lse) is fused as in
- * sls_sparse_decode_attend_combine, with the same workspace.
- *   desc.page_size  the thumbnail block (>= 16); bf16, G <= 8, D 64 or 128
+ * bf16 key.  Values are the bf16 V.  With codes, scales and res all NULL
+ * every token is scored with its bf16 key (plain attention over the lists).
+ * The rows' lists, of different lengths, are cut into work items of equal
+ * length spread over the GPU; each row's last item merges the row (sink,
+ * lse as in sls_combine_splits).
+ *   desc.page_size  the thumbnail block (>= 16); bf16, G <= 8, D 64 or 128,
+ *                   B*Hkv <= 4096
  *   codes, scales, res  as written by sls_thumb_residual_build/_update
  *   block_idx [B*Hkv, idx_stride] int32, count [B*Hkv] int32: the kept
  *             blocks of each row (sls_select_delta's output); -1 entries
  *             and blocks past the context are skipped
+ *   workspace >= sls_refined_decode_attend_workspace_size() bytes, zero-
+ *             filled before its first use (every call leaves its arrival
+ *             counters at zero); calls sharing it must not run concurrently
  *   |q * s| must stay below 65504 (the products run in fp16 hi/lo parts).
- * Errors: SLS_EUNSUPPORTED for another dtype, G > 8 or blocks < 16 tokens;
- * SLS_EINVAL for null pointers or bad sizes; SLS_EWORKSPACE.
+ * Errors: SLS_EUNSUPPORTED for another dtype, G > 8, blocks < 16 tokens or
+ * more rows; SLS_EINVAL for null pointers or bad sizes; SLS_EWORKSPACE.
  */
+size_t sls_refined_decode_attend_workspace_size(const sls_attn_desc* desc);
 sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const void* q,
                                              const void* k_cache, const void* v_cache,
                                              const uint8_t* codes, const void* scales,
                                              const int8_t* res, const int32_t* block_idx,
                                              int32_t idx_stride, const int32_t* count,
-                                             const int32_t* ctx_len, int32_t num_splits,
-                                             const float* sink, void* out, float* lse,
-                                             void* workspace, size_t workspace_bytes,
-                                             void* stream);
+                                             const int32_t* ctx_len, const float* sink,
+                                             void* out, float* lse, void* workspace,
+                                             size_t workspace_bytes, void* stream);
 
 /* ---- the whole Quest decode step ---------------------------------------- */
 

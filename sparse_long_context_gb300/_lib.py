@@ -47,7 +47,8 @@ SIGNATURES = {
     "sls_attend_combine_workspace_size": (ctypes.c_size_t, [_D, _I]),
     "sls_sparse_decode_attend_combine": (_I, [_D, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P,
                                               ctypes.c_size_t, _P]),
-    "sls_refined_decode_attend_combine": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _P, _P, _P,
+    "sls_refined_decode_attend_workspace_size": (ctypes.c_size_t, [_D]),
+    "sls_refined_decode_attend_combine": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
                                                _P, ctypes.c_size_t, _P]),
     "sls_quest_decode_step_workspace_size": (ctypes.c_size_t, [_D, _I, _I]),
     "sls_quest_decode_step_splits": (_I, [_D, _I]),

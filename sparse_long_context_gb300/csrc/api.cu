@@ -340,44 +340,34 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
                      "sls_sparse_decode_attend_combine");
 }
 
+size_t sls_refined_decode_attend_workspace_size(const sls_attn_desc* desc) {
+  sls::Shape s;
+  if (check_desc(desc, &s)) return 0;
+  return sls::refined_workspace(s);
+}
+
 sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const void* q, const void* k_cache,
                                              const void* v_cache, const uint8_t* codes, const void* scales,
                                              const int8_t* res, const int32_t* block_idx, int32_t idx_stride,
-                                             const int32_t* count, const int32_t* ctx_len, int32_t num_splits,
-                                             const float* sink, void* out, float* lse, void* workspace,
-                                             size_t workspace_bytes, void* stream) {
+                                             const int32_t* count, const int32_t* ctx_len, const float* sink,
+                                             void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                             void* stream) {
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(codes); REQUIRE(scales); REQUIRE(res);
-  REQUIRE(block_idx); REQUIRE(count); REQUIRE(ctx_len); REQUIRE(out);
+  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(block_idx); REQUIRE(count); REQUIRE(ctx_len);
+  REQUIRE(out);
+  if ((codes == nullptr) != (res == nullptr) || (codes == nullptr) != (scales == nullptr))
+    return fail(SLS_EINVAL, "codes, scales and res: all or none");
   if (!sls::refined_supported(s))
-    return fail(SLS_EUNSUPPORTED, "refined attend needs bf16, G <= 8 and blocks (page_size) of >= 16 tokens");
+    return fail(SLS_EUNSUPPORTED,
+                "needs bf16, G <= 8, blocks (page_size) of >= 16 tokens and at most 4096 rows (B*Hkv)");
   if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
-  if (num_splits < 0 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [0, 1024]", num_splits);
-  int64_t ctas;
-  if (!checked_mul((int64_t)s.B * s.Hkv, num_splits ? num_splits : sls::max_auto_splits(s), &ctas) ||
-      ctas > INT32_MAX)
-    return fail(SLS_EOVERFLOW, "grid too large");
-  const size_t need = sls_attend_combine_workspace_size(desc, num_splits);
+  const size_t need = sls::refined_workspace(s);
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
-  char* w = static_cast<char*>(workspace);
-  const size_t heads = (size_t)s.B * s.Hq * (num_splits ? num_splits : sls::max_auto_splits(s));
-  sls::FusedCombine f;
-  f.tickets = reinterpret_cast<int32_t*>(w);
-  w += align256((size_t)s.B * s.Hkv * 4);
-  float* o_part = reinterpret_cast<float*>(w);
-  w += align256(heads * s.D * 4);
-  float* m_part = reinterpret_cast<float*>(w);
-  w += align256(heads * 4);
-  float* l_part = reinterpret_cast<float*>(w);
-  f.sink = sink;
-  f.out = out;
-  f.lse = lse;
   return cuda_status(sls::launch_attend_refined(s, q, k_cache, v_cache, codes, scales, res, block_idx, idx_stride,
-                                                count, ctx_len, num_splits, o_part, m_part, l_part, f,
-                                                (cudaStream_t)stream),
+                                                count, ctx_len, sink, out, lse, workspace, (cudaStream_t)stream),
                      "sls_refined_decode_attend_combine");
 }
 

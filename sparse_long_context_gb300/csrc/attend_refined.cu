@@ -6,12 +6,19 @@
 // bf16 key.  Tokens of the newest, partial block have no thumbnail yet and
 // use the bf16 key.  Values are bf16.
 //
-// One CTA per (row, split) with 8 warps; a warp walks 16-token groups of its
-// slice with two groups in flight in registers (the shape of the register-
-// fed attend).  Lane (r, m) owns the channels [m D/4, (m+1) D/4) of the
-// score product and loads, for tokens r and r + 8 of a group, either D/16
-// bytes of codes and D/4 bytes of residuals (a refined group) or D/2 bytes
-// of bf16 key (a group of the partial block).
+// Top-delta keeps a different number of blocks in every row (a few percent
+// in one head, most of the context in another), so a fixed split count per
+// row leaves the kernel as slow as its longest row.  Here the rows' lists,
+// concatenated, are cut into one equal range of entries per CTA (one 8-warp
+// CTA per SM, stream-K style; attend_balanced_kernel).  Without codes the
+// same kernel attends with the bf16 keys everywhere.
+//
+// Within an item a warp walks 16-token groups with two groups in flight in
+// registers (the shape of the register-fed attend).  Lane (r, m) owns the
+// channels [m D/4, (m+1) D/4) of the score product and loads, for tokens r
+// and r + 8 of a group, either D/16 bytes of codes and D/4 bytes of
+// residuals (a refined group) or D/2 bytes of bf16 key (a group of the
+// partial block, or every group without codes).
 //
 // Refined scores run on the tensor cores in fp16:
 //   n = 254 code - 381 + r   is an integer in [-508, 508], exact in fp16,
@@ -21,6 +28,8 @@
 // which is 508 q . k~ to about 2^-22 relative (|q s| < 65504 assumed).
 // Softmax and O^T += V^T P^T follow the register-fed attend.
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "attend_common.cuh"
 #include "launch.h"
@@ -32,10 +41,14 @@ constexpr int kRefWarps = 8;
 constexpr int kRefStaged = 1024;  // block-list entries staged in shared memory
 
 struct RefinedArgs {
-  AttendArgs a;         // q, k, v, block list (page_idx with P = block), count, ctx_len, partials, combine
-  const uint8_t* codes; // [rows, Cap, D/4]
+  AttendArgs a;         // q, k, v, block list (page_idx with P = block), count, ctx_len, combine
+  const uint8_t* codes; // [rows, Cap, D/4], or null: every token scored with its bf16 key
   const bf16* scales;   // [rows, Cap/P, D]
   const int8_t* res;    // [rows, Cap, D]
+  int rows;
+  float* po;            // [slot][G][D] partial accumulators (two slots per CTA)
+  float* pm;            // [slot][G] running max (natural-log units)
+  float* pl;            // [slot][G] normaliser
 };
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -108,7 +121,7 @@ __device__ __forceinline__ void load_rgroup(RGroup<D>& g, const RefinedArgs& ra,
     }
   }
   g.pg = pg;
-  g.refined = pg >= 0 && ((pg + 1) << a.pshift) <= sl.N;  // a complete block has its thumbnail
+  g.refined = ra.codes && pg >= 0 && ((pg + 1) << a.pshift) <= sl.N;  // a complete block has its thumbnail
   auto at = [&](int t) { return (base >= 0 && t < lim) ? base + t : -1; };
   const int pk[2] = {at(r), at(r + 8)};
   g.pv[0] = at(2 * m);
@@ -231,137 +244,363 @@ __device__ __forceinline__ void compute_rgroup(const RGroup<D>& g, const Refined
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kRefWarps * 32, 1) attend_refined_kernel(const RefinedArgs ra) {
-  pdl_wait_then_release();
-  constexpr int NW = kRefWarps, NS = D / 32, MT = D / 16, CPR = D / 8;
-  extern __shared__ float sO[];  // [NW][8][D]
-  __shared__ float sM[NW][8], sL[NW][8];
-  __shared__ int s_pg[kRefStaged];
-  const AttendArgs& a = ra.a;
-  const int row = blockIdx.x / a.S, split = blockIdx.x % a.S;
-  const Slice slc = attend_slice(a, row, split);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = lane >> 2, m = lane & 3;
-  const int b = row / a.Hkv, h = row % a.Hkv;
-  const int G = a.G;
-  const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + slc.e0;
-  RSeg sl;
-  sl.N = slc.N;
-  sl.nent = slc.nent;
-  sl.ntok = slc.nent << a.pshift;
-  for (int i = threadIdx.x; i < min(sl.nent, kRefStaged); i += NW * 32) s_pg[i] = __ldg(plist + i);
+constexpr int kRefMaxRows = 4096;  // rows whose list prefix one CTA keeps in shared memory
 
-  // Q as the A operand, head r (rows 8..15 zero), the lane's channel range
-  uint32_t qa[NS][4];
-  {
-    const bf16* qp = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G + r) * D + m * (D / 4);
+constexpr int kRefMaxContrib = 1024;  // CTAs sharing one row (one CTA per SM)
+
+struct RefSmem {
+  float sM[kRefWarps][8], sL[kRefWarps][8];
+  int s_pg[kRefStaged];
+  int s_tmp[kRefWarps];
+  int s_slot[kRefMaxContrib];
+  int s_ncontrib;
+  int s_last;
+  float s_w[8][64], s_m[8], s_inv[8];
+};
+
+// Exclusive scan of one int per thread (256 threads); `total` gets the sum.
+__device__ __forceinline__ int ref_scan(int v, int* tmp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
 #pragma unroll
-    for (int s = 0; s < NS; ++s) {
-      const uint4 c = r < G ? ldg_stream(qp + 8 * s) : make_uint4(0, 0, 0, 0);
-      qa[s][0] = c.x; qa[s][1] = c.y; qa[s][2] = c.z; qa[s][3] = c.w;
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  float o[MT][4];
-#pragma unroll
-  for (int t = 0; t < MT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-  float m_run = kNegInf, l_run = 0.f;
+  if (lane == 31) tmp[warp] = x;
   __syncthreads();
-
-  const int ngroups = (sl.ntok + 15) >> 4;
-  RGroup<D> ga, gb;
-  int gi = warp;
-  if (gi < ngroups) load_rgroup<D>(ga, ra, sl, s_pg, plist, gi, row);
-  while (gi < ngroups) {
-    if (gi + NW < ngroups) load_rgroup<D>(gb, ra, sl, s_pg, plist, gi + NW, row);
-    compute_rgroup<D>(ga, ra, row, qa, o, m_run, l_run);
-    gi += NW;
-    if (gi >= ngroups) break;
-    if (gi + NW < ngroups) load_rgroup<D>(ga, ra, sl, s_pg, plist, gi + NW, row);
-    compute_rgroup<D>(gb, ra, row, qa, o, m_run, l_run);
-    gi += NW;
-  }
-
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  if (m == 0) {
-    sM[warp][r] = m_run;
-    sL[warp][r] = l_run;
-  }
+  int before = 0;
+  total = 0;
 #pragma unroll
-  for (int t = 0; t < MT; ++t) {
-    const int ch = CPR * r + 2 * t;
-    sO[(warp * 8 + 2 * m) * D + ch] = o[t][0];
-    sO[(warp * 8 + 2 * m + 1) * D + ch] = o[t][1];
-    sO[(warp * 8 + 2 * m) * D + ch + 1] = o[t][2];
-    sO[(warp * 8 + 2 * m + 1) * D + ch + 1] = o[t][3];
+  for (int w = 0; w < kRefWarps; ++w) {
+    const int t = tmp[w];
+    before += w < warp ? t : 0;
+    total += t;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < G * D; i += NW * 32) {
-    const int g = i / D, d = i % D;
-    float M = kNegInf;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, sM[w][g]);
-    float av = 0.f, lv = 0.f;
-    if (M != kNegInf) {
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        if (sM[w][g] == kNegInf) continue;
-        const float f = exp2f(sM[w][g] - M);
-        av += sO[(w * 8 + g) * D + d] * f;
-        lv += sL[w][g] * f;
-      }
-    }
-    const size_t hq = (size_t)b * a.Hq + (size_t)h * G + g;
-    a.o_part[(hq * a.S + split) * D + d] = av;
-    if (d == 0) {
-      a.m_part[hq * a.S + split] = M == kNegInf ? kNegInf : M * kLn2;
-      a.l_part[hq * a.S + split] = lv;
-    }
-  }
-  if (a.tickets) combine_row_if_last<bf16, D, NW * 32>(a, row, a.S);
+  return before + x - v;
 }
 
-bool refined_supported(const Shape& s) { return s.dtype == 1 && s.G <= 8 && s.P >= 16 && (s.D == 64 || s.D == 128); }
+__device__ __forceinline__ long long range_lo(long long T, int c, int grid) { return T * c / grid; }
+
+// The CTA whose entry range [T c / grid, T (c+1) / grid) holds entry x < T.
+__device__ __forceinline__ int cta_of(long long x, long long T, int grid) {
+  int c = (int)min((long long)grid - 1, x * grid / T);
+  while (c + 1 < grid && range_lo(T, c + 1, grid) <= x) ++c;
+  while (c > 0 && range_lo(T, c, grid) > x) --c;
+  return c;
+}
+
+// Writes the finished output of one head: accumulator sum `av` and
+// normaliser `lv` relative to exp(M) (natural log units), the sink joining
+// the normaliser.
+__device__ __forceinline__ void finish_head(const AttendArgs& a, size_t hq, int h, int g, float M, float lv,
+                                            float av, int d, int D) {
+  const float sk = a.sink ? a.sink[h * a.G + g] : kNegInf;
+  const float Mx = fmaxf(M, sk);
+  float f = 0.f, L = 0.f;
+  if (Mx != kNegInf) {
+    f = M == kNegInf ? 0.f : expf(M - Mx);
+    L = lv * f + (a.sink ? expf(sk - Mx) : 0.f);
+  }
+  static_cast<bf16*>(a.out)[hq * D + d] = __float2bfloat16(L > 0.f ? av * f / L : 0.f);
+  if (d == 0 && a.lse) a.lse[hq] = L > 0.f ? Mx + logf(L) : kNegInf;
+}
+
+// Stream-K over the rows' lists (top-delta keeps a different number of
+// blocks in every row): the lists, concatenated row after row (T entries),
+// are cut into one equal range of entries per CTA.  A CTA attends the row
+// segments of its range; a row entirely inside the range is finished in
+// place, a row shared with neighbouring CTAs gets a partial from each of
+// them (slot 2c for the segment a CTA's range starts in, 2c + 1 for the one
+// it ends in) and the row's last contributor to arrive merges them in CTA
+// order, so the result does not depend on timing.  Rows with an empty list
+// are written by CTA row % grid.
+template <int D>
+__global__ void __launch_bounds__(kRefWarps * 32, 1) attend_balanced_kernel(const RefinedArgs ra) {
+  pdl_wait_then_release();
+  constexpr int NW = kRefWarps, NT = NW * 32, NS = D / 32, MT = D / 16, CPR = D / 8;
+  extern __shared__ float smem_f[];
+  float* sO = smem_f;                                         // [NW][8][D]
+  int* s_pref = reinterpret_cast<int*>(smem_f + NW * 8 * D);  // [rows + 1] first entry of each row
+  __shared__ RefSmem sh;
+  const AttendArgs& a = ra.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, m = lane & 3;
+  const int G = a.G, rows = ra.rows, grid = gridDim.x, c = blockIdx.x;
+
+  // 1. prefix of the rows' list lengths
+  const int RPT = (rows + NT - 1) / NT;
+  const int r0 = threadIdx.x * RPT;
+  int csum = 0;
+  for (int i = 0; i < RPT; ++i) {
+    const int row = r0 + i;
+    if (row < rows) csum += min(max(a.count[row], 0), a.idx_stride);
+  }
+  int T;
+  int acc = ref_scan(csum, sh.s_tmp, T);
+  for (int i = 0; i < RPT; ++i) {
+    const int row = r0 + i;
+    if (row < rows) {
+      s_pref[row] = acc;
+      acc += min(max(a.count[row], 0), a.idx_stride);
+    }
+  }
+  if (threadIdx.x == 0) s_pref[rows] = T;
+  __syncthreads();
+
+  // rows with an empty list: output 0, lse -inf (or the sink alone)
+  for (int row = c; row < rows; row += grid) {
+    if (s_pref[row + 1] != s_pref[row]) continue;
+    const int b = row / a.Hkv, h = row % a.Hkv;
+    for (int i = threadIdx.x; i < G * D; i += NT)
+      finish_head(a, (size_t)b * a.Hq + (size_t)h * G + i / D, h, i / D, kNegInf, 0.f, 0.f, i % D, D);
+  }
+  if (T == 0) return;
+  const long long lo = range_lo(T, c, grid), hi = range_lo(T, c + 1, grid);
+  if (lo >= hi) return;
+  // the row holding entry lo: the last row whose first entry is <= lo
+  int row;
+  {
+    int l = 0, u = rows - 1;
+    while (l < u) {
+      const int mid = (l + u + 1) >> 1;
+      if (s_pref[mid] <= lo) l = mid;
+      else u = mid - 1;
+    }
+    row = l;
+  }
+  long long e = lo;
+  while (e < hi) {
+    const long long seg_end = min(hi, (long long)s_pref[row + 1]);
+    const int b = row / a.Hkv, h = row % a.Hkv;
+    const int e0 = (int)(e - s_pref[row]);
+    RSeg sl;
+    sl.N = clamp_len(a.ctx_len[b], a.Cap);
+    sl.nent = (int)(seg_end - e);
+    sl.ntok = sl.nent << a.pshift;
+    const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + e0;
+    for (int i = threadIdx.x; i < min(sl.nent, kRefStaged); i += NT) sh.s_pg[i] = __ldg(plist + i);
+
+    uint32_t qa[NS][4];
+    {
+      const bf16* qp = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G + r) * D + m * (D / 4);
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        const uint4 cq = r < G ? ldg_stream(qp + 8 * s) : make_uint4(0, 0, 0, 0);
+        qa[s][0] = cq.x; qa[s][1] = cq.y; qa[s][2] = cq.z; qa[s][3] = cq.w;
+      }
+    }
+    float o[MT][4];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    float m_run = kNegInf, l_run = 0.f;
+    __syncthreads();
+
+    const int ngroups = (sl.ntok + 15) >> 4;
+    RGroup<D> ga, gb;
+    int gi = warp;
+    if (gi < ngroups) load_rgroup<D>(ga, ra, sl, sh.s_pg, plist, gi, row);
+    while (gi < ngroups) {
+      if (gi + NW < ngroups) load_rgroup<D>(gb, ra, sl, sh.s_pg, plist, gi + NW, row);
+      compute_rgroup<D>(ga, ra, row, qa, o, m_run, l_run);
+      gi += NW;
+      if (gi >= ngroups) break;
+      if (gi + NW < ngroups) load_rgroup<D>(ga, ra, sl, sh.s_pg, plist, gi + NW, row);
+      compute_rgroup<D>(gb, ra, row, qa, o, m_run, l_run);
+      gi += NW;
+    }
+
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (m == 0) {
+      sh.sM[warp][r] = m_run;
+      sh.sL[warp][r] = l_run;
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      const int ch = CPR * r + 2 * t;
+      sO[(warp * 8 + 2 * m) * D + ch] = o[t][0];
+      sO[(warp * 8 + 2 * m + 1) * D + ch] = o[t][1];
+      sO[(warp * 8 + 2 * m) * D + ch + 1] = o[t][2];
+      sO[(warp * 8 + 2 * m + 1) * D + ch + 1] = o[t][3];
+    }
+    __syncthreads();
+    const bool whole = e == s_pref[row] && seg_end == s_pref[row + 1];
+    const int slot = e == lo ? 2 * c : 2 * c + 1;
+    const size_t hq0 = (size_t)b * a.Hq + (size_t)h * G;
+    for (int i = threadIdx.x; i < G * D; i += NT) {
+      const int g = i / D, d = i % D;
+      float M = kNegInf;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, sh.sM[w][g]);
+      float av = 0.f, lv = 0.f;
+      if (M != kNegInf) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          if (sh.sM[w][g] == kNegInf) continue;
+          const float f = exp2f(sh.sM[w][g] - M);
+          av += sO[(w * 8 + g) * D + d] * f;
+          lv += sh.sL[w][g] * f;
+        }
+      }
+      const float Mn = M == kNegInf ? kNegInf : M * kLn2;
+      if (whole) {
+        finish_head(a, hq0 + g, h, g, Mn, lv, av, d, D);
+      } else {
+        const size_t sg = (size_t)slot * G + g;
+        ra.po[sg * D + d] = av;
+        if (d == 0) {
+          ra.pm[sg] = Mn;
+          ra.pl[sg] = lv;
+        }
+      }
+    }
+    if (!whole) {
+      // the row's contributors are the CTAs from the one holding its first
+      // entry to the one holding its last; the last to arrive merges
+      // (skipping CTAs with empty ranges, which exist when T < grid); CTA k
+      // wrote slot 2k when its range starts inside the row, else 2k + 1
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const int cf = cta_of(s_pref[row], T, grid), cl = cta_of((long long)s_pref[row + 1] - 1, T, grid);
+        int n = 0;
+        for (int k = cf; k <= cl && n < kRefMaxContrib; ++k) {
+          const long long klo = range_lo(T, k, grid);
+          if (klo < range_lo(T, k + 1, grid)) sh.s_slot[n++] = klo >= s_pref[row] ? 2 * k : 2 * k + 1;
+        }
+        sh.s_ncontrib = n;
+        sh.s_last = atomicAdd(a.tickets + row, 1) == n - 1;
+      }
+      __syncthreads();
+      const int ncontrib = sh.s_ncontrib;
+      if (sh.s_last) {
+        __threadfence();
+        auto slot_of = [&](int j) -> size_t { return (size_t)sh.s_slot[j]; };
+        for (int g = warp; g < G; g += NW) {
+          float M = kNegInf;
+          for (int j = lane; j < ncontrib; j += 32) M = fmaxf(M, __ldcg(ra.pm + slot_of(j) * G + g));
+          M = warp_max(M);
+          const float sk = a.sink ? a.sink[h * G + g] : kNegInf;
+          M = fmaxf(M, sk);
+          float Ls = 0.f;
+          for (int j = lane; j < ncontrib; j += 32) {
+            const float ms = __ldcg(ra.pm + slot_of(j) * G + g);
+            const float w = (ms == kNegInf || M == kNegInf) ? 0.f : expf(ms - M);
+            Ls += __ldcg(ra.pl + slot_of(j) * G + g) * w;
+            if (j < 64) sh.s_w[g][j] = w;
+          }
+          Ls = warp_sum(Ls);
+          if (a.sink && M != kNegInf) Ls += expf(sk - M);
+          if (lane == 0) {
+            sh.s_m[g] = M;
+            sh.s_inv[g] = Ls > 0.f ? 1.f / Ls : 0.f;
+            if (a.lse) a.lse[hq0 + g] = Ls > 0.f ? M + logf(Ls) : kNegInf;
+          }
+        }
+        __syncthreads();
+        constexpr int C4 = D / 4;
+        for (int i = threadIdx.x; i < G * C4; i += NT) {
+          const int g = i / C4, cc = i % C4;
+          const float M = sh.s_m[g];
+          float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j0 = 0; j0 < ncontrib; j0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              v[u] = j0 + u < ncontrib
+                         ? __ldcg(reinterpret_cast<const float4*>(ra.po + (slot_of(j0 + u) * G + g) * D) + cc)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = j0 + u;
+              if (j >= ncontrib) break;
+              float w;
+              if (j < 64) {
+                w = sh.s_w[g][j];
+              } else {
+                const float ms = __ldcg(ra.pm + slot_of(j) * G + g);
+                w = (ms == kNegInf || M == kNegInf) ? 0.f : expf(ms - M);
+              }
+              accv.x = fmaf(v[u].x, w, accv.x);
+              accv.y = fmaf(v[u].y, w, accv.y);
+              accv.z = fmaf(v[u].z, w, accv.z);
+              accv.w = fmaf(v[u].w, w, accv.w);
+            }
+          }
+          const float inv = sh.s_inv[g];
+          bf16* op = static_cast<bf16*>(a.out) + (hq0 + g) * D + 4 * cc;
+          op[0] = __float2bfloat16(accv.x * inv);
+          op[1] = __float2bfloat16(accv.y * inv);
+          op[2] = __float2bfloat16(accv.z * inv);
+          op[3] = __float2bfloat16(accv.w * inv);
+        }
+        if (threadIdx.x == 0) a.tickets[row] = 0;  // ready for the next call
+      }
+    }
+    __syncthreads();  // shared memory is reused by the next segment
+    e = seg_end;
+    ++row;
+    while (row < rows && s_pref[row + 1] == s_pref[row]) ++row;  // empty rows hold no entries
+  }
+}
+
+bool refined_supported(const Shape& s) {
+  return s.dtype == 1 && s.G <= 8 && s.P >= 16 && (s.D == 64 || s.D == 128) && s.B * s.Hkv <= kRefMaxRows;
+}
+
+// one 8-warp CTA per SM (the register budget)
+static int balanced_grid() { return std::min(sm_count(), kRefMaxContrib); }
+
+size_t refined_workspace(const Shape& s) {
+  const size_t rows = (size_t)s.B * s.Hkv;
+  const size_t slots = 2 * (size_t)balanced_grid();
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  return al(rows * 4) + al(slots * s.G * s.D * 4) + 2 * al(slots * s.G * 4);
+}
 
 template <int D>
-static cudaError_t refined_launch(const RefinedArgs& ra, int grid, cudaStream_t st) {
-  constexpr size_t smem = (size_t)kRefWarps * 8 * D * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(attend_refined_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+static cudaError_t balanced_launch(const RefinedArgs& ra, cudaStream_t st) {
+  const size_t smem = (size_t)kRefWarps * 8 * D * sizeof(float) + (size_t)(ra.rows + 1) * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(attend_balanced_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(attend_refined_kernel<D>, dim3(grid), dim3(kRefWarps * 32), smem, st, ra);
+  e = launch_pdl(attend_balanced_kernel<D>, dim3(balanced_grid()), dim3(kRefWarps * 32), smem, st, ra);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_attend_refined(const Shape& s, const void* q, const void* k, const void* v, const uint8_t* codes,
                                   const void* scales, const int8_t* res, const int32_t* block_idx, int idx_stride,
-                                  const int32_t* count, const int32_t* ctx_len, int num_splits, float* o_part,
-                                  float* m_part, float* l_part, const FusedCombine& fused, cudaStream_t st) {
+                                  const int32_t* count, const int32_t* ctx_len, const float* sink, void* out,
+                                  float* lse, void* ws, cudaStream_t st) {
   RefinedArgs ra;
   AttendArgs& a = ra.a;
   a = AttendArgs{};
-  a.tickets = fused.tickets;
-  a.sink = fused.sink;
-  a.out = fused.out;
-  a.lse = fused.lse;
+  ra.rows = s.B * s.Hkv;
+  const size_t items = 2 * (size_t)balanced_grid();  // partial slots
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  char* w = static_cast<char*>(ws);
+  a.tickets = reinterpret_cast<int32_t*>(w);
+  w += al((size_t)ra.rows * 4);
+  ra.po = reinterpret_cast<float*>(w);
+  w += al(items * s.G * s.D * 4);
+  ra.pm = reinterpret_cast<float*>(w);
+  w += al(items * s.G * 4);
+  ra.pl = reinterpret_cast<float*>(w);
+  a.sink = sink;
+  a.out = out;
+  a.lse = lse;
   a.q = q; a.k = k; a.v = v;
   a.page_idx = block_idx; a.count = count; a.ctx_len = ctx_len;
-  a.o_part = o_part; a.m_part = m_part; a.l_part = l_part;
-  a.idx_stride = idx_stride; a.k_fixed = idx_stride; a.S = num_splits;
-  a.cluster = 0;
-  if (num_splits == 0) {
-    a.S = attend_default_splits(s, idx_stride);
-    if (a.S > max_auto_splits(s)) a.S = max_auto_splits(s);
-  }
+  a.idx_stride = idx_stride; a.k_fixed = idx_stride; a.S = 1;
   a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.G; a.Cap = s.Cap; a.P = s.P; a.pshift = s.pshift;
   a.qscale = s.scale * kLog2e;
   ra.codes = codes;
   ra.scales = static_cast<const bf16*>(scales);
   ra.res = res;
-  const int grid = s.B * s.Hkv * a.S;
-  return s.D == 128 ? refined_launch<128>(ra, grid, st) : refined_launch<64>(ra, grid, st);
+  return s.D == 128 ? balanced_launch<128>(ra, st) : balanced_launch<64>(ra, st);
 }
 
 }  // namespace sls

@@ -62,11 +62,11 @@ cudaError_t launch_thumb_update(const Shape& s, const void* k, const int32_t* po
                                 int block, uint8_t* codes, void* scales, int8_t* res, cudaStream_t st);
 
 bool refined_supported(const Shape& s);
-struct FusedCombine;
+size_t refined_workspace(const Shape& s);
 cudaError_t launch_attend_refined(const Shape& s, const void* q, const void* k, const void* v, const uint8_t* codes,
                                   const void* scales, const int8_t* res, const int32_t* block_idx, int idx_stride,
-                                  const int32_t* count, const int32_t* ctx_len, int num_splits, float* o_part,
-                                  float* m_part, float* l_part, const FusedCombine& fused, cudaStream_t st);
+                                  const int32_t* count, const int32_t* ctx_len, const float* sink, void* out,
+                                  float* lse, void* ws, cudaStream_t st);
 
 size_t select_pages_workspace(const Shape& s);
 cudaError_t launch_select_pages(const Shape& s, const void* q, const void* kmin,

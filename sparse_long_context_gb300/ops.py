@@ -214,13 +214,20 @@ def sparse_decode_attend_combine(desc: L.AttnDesc, q, k_cache, v_cache, page_idx
     return out, lse
 
 
+def refined_workspace(desc: L.AttnDesc, device="cuda"):
+    """Zero-filled workspace of refined_decode_attend_combine (reusable)."""
+    n = L.load().sls_refined_decode_attend_workspace_size(ctypes.byref(desc))
+    return torch.zeros(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
 def refined_decode_attend_combine(desc: L.AttnDesc, q, k_cache, v_cache, codes, scales, res, block_idx, count,
-                                  ctx_len, num_splits: int = 0, sink=None, out=None, lse=None, workspace=None,
-                                  want_lse: bool = True):
-    """Attention over the kept blocks with the refined (2-bit + 8-bit) keys
-    of complete blocks, combine fused; returns (out, lse)."""
-    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (codes, "codes"), (scales, "scales"),
-                  (res, "res"), (block_idx, "block_idx"), (count, "count")):
+                                  ctx_len, sink=None, out=None, lse=None, workspace=None, want_lse: bool = True):
+    """Attention over the kept blocks of every row, the rows' lists cut into
+    equal work items, combine fused; complete blocks are scored with the
+    refined (2-bit + 8-bit) keys, or with the bf16 keys when codes, scales
+    and res are None.  Returns (out, lse)."""
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (block_idx, "block_idx"),
+                  (count, "count")):
         _need(t, nm)
     B, Hq, D = desc.batch, desc.num_q_heads, desc.head_dim
     out = torch.empty((B, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
@@ -228,11 +235,10 @@ def refined_decode_attend_combine(desc: L.AttnDesc, q, k_cache, v_cache, codes, 
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     if sink is not None:
         _need(sink, "sink", torch.float32, (Hq,))
-    workspace = attend_combine_workspace(desc, num_splits, q.device) if workspace is None else workspace
+    workspace = refined_workspace(desc, q.device) if workspace is None else workspace
     L.call("sls_refined_decode_attend_combine", ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache),
            _ptr(codes), _ptr(scales), _ptr(res), _ptr(block_idx), int(block_idx.shape[-1]), _ptr(count),
-           _ptr(ctx_len), int(num_splits), _ptr(sink), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-           _stream())
+           _ptr(ctx_len), _ptr(sink), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream())
     return out, lse
 
 
@@ -365,18 +371,29 @@ class QuestDecode:
 
 
 class DeltaDecode:
-    """One top-delta decode step (select_delta + attend + combine).  With
-    refined=True the attend scores complete blocks with the refined keys
-    (2-bit thumbnail + 8-bit residual, "Faster Than Flash" eq. 4): the call
-    then takes the residuals as well."""
+    """One top-delta decode step (select_delta + attend + combine).
+
+    balanced=True (the default where the shape allows: bf16, G <= 8, no path
+    flag in the descriptor) attends
+    with the work-item kernel, which spreads rows of very different list
+    lengths evenly over the GPU; otherwise the split-K attend with num_splits
+    per row.  With refined=True the attend scores complete blocks with the
+    refined keys (2-bit thumbnail + 8-bit residual, "Faster Than Flash"
+    eq. 4): the call then takes the residuals as well."""
 
     def __init__(self, desc: L.AttnDesc, block: int, delta: float, num_splits: Optional[int] = None,
-                 device="cuda", fused: bool = True, refined: bool = False):
+                 device="cuda", fused: bool = True, refined: bool = False, balanced: Optional[bool] = None):
         if desc.page_size != block:
             raise ValueError("attend page_size must equal the thumbnail block")
         self.desc, self.block, self.delta = desc, int(block), float(delta)
         self.fused = fused
         self.refined = refined
+        ok = desc.dtype == L.SLS_DTYPE_BF16 and desc.num_q_heads // desc.num_kv_heads <= 8
+        # the default for the fast path only: the descriptor's path flags select the split-K attends
+        self.balanced = (fused and ok and desc.flags == 0) if balanced is None else balanced
+        if refined and not ok:
+            raise ValueError("the refined attend needs bf16 and G <= 8")
+        self.bal_workspace = refined_workspace(desc, device) if (self.balanced or refined) else None
         rows = desc.batch * desc.num_kv_heads
         nblk = desc.capacity // block
         self.S = num_splits or default_splits(desc, nblk)
@@ -394,6 +411,10 @@ class DeltaDecode:
                             count=self.count, block_idx=self.block_idx, workspace=self.workspace)
 
     def attend(self, q, k_cache, v_cache, ctx_len, sink=None):
+        if self.balanced:
+            return refined_decode_attend_combine(self.desc, q, k_cache, v_cache, None, None, None, self.block_idx,
+                                                 self.count, ctx_len, sink=sink, out=self.out, lse=self.lse,
+                                                 workspace=self.bal_workspace)
         if self.fused:
             return sparse_decode_attend_combine(self.desc, q, k_cache, v_cache, self.block_idx, ctx_len,
                                                 self.S, count=self.count, sink=sink, out=self.out,
@@ -404,8 +425,8 @@ class DeltaDecode:
 
     def attend_refined(self, q, k_cache, v_cache, codes, scales, res, ctx_len, sink=None):
         return refined_decode_attend_combine(self.desc, q, k_cache, v_cache, codes, scales, res, self.block_idx,
-                                             self.count, ctx_len, self.S, sink=sink, out=self.out, lse=self.lse,
-                                             workspace=self.ac_workspace)
+                                             self.count, ctx_len, sink=sink, out=self.out, lse=self.lse,
+                                             workspace=self.bal_workspace)
 
     def __call__(self, q, k_cache, v_cache, codes, scales, ctx_len, sink=None, res=None):
         self.select(q, k_cache, codes, scales, ctx_len)

@@ -128,7 +128,7 @@ def test_refined_step_matches_oracle(key):
         idx[r, :len(p)] = p
     o2, _ = ops.refined_decode_attend_combine(dw.desc, dw.q, dw.K, dw.V, codes, scales, res,
                                               torch.from_numpy(idx).cuda(), torch.from_numpy(count).cuda(),
-                                              dw.ctx, 3, sink=dw.sink)
+                                              dw.ctx, sink=dw.sink)
     o2 = o2.float().cpu().numpy().astype(np.float64)
     for b in range(s.batch):
         for h in range(s.num_kv_heads):
@@ -171,3 +171,53 @@ def test_refined_full_size_sampled_rows():
         o_ref, _ = _refined_oracle(s, host, b, h, orc.pages)
         PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"full-size refined row {(b, h)}")
     assert math.isfinite(float(np.abs(out).max()))
+
+
+@pytest.mark.parametrize("ctx", [[5000, 3000, 10], [100, 37, 16]])
+def test_balanced_attend_uneven_lists_and_sink(ctx):
+    """The stream-K attend (bf16 keys) on lists of very different lengths:
+    empty rows, one page, every page, padded entries, a sink, against the
+    oracle's attention over the same pages; with few entries in all (the
+    second case) most CTAs get an empty range."""
+    s = W.spec("qwen7b", batch=3, ctx_len=ctx, capacity=5008)
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    rng = np.random.default_rng(7)
+    npg = [-(-int(n) // s.page_size) for n in host.ctx_len]
+    width = max(npg) + 3
+    idx = np.full((s.rows, width), -1, dtype=np.int32)
+    count = np.zeros(s.rows, dtype=np.int32)
+    lists = []
+    for r in range(s.rows):
+        n = npg[r // s.num_kv_heads]
+        kind = r % 4
+        if kind == 0:
+            pages = np.zeros(0, dtype=np.int64)
+        elif kind == 1:
+            pages = np.array([n - 1])
+        elif kind == 2:
+            pages = np.arange(n)
+        else:
+            pages = np.sort(rng.choice(n, size=min(n, 37), replace=False))
+        lists.append(pages)
+        idx[r, :len(pages)] = pages
+        count[r] = len(pages) + (2 if kind == 3 else 0)  # two -1 entries counted in: skipped
+    sink = torch.from_numpy(rng.standard_normal(s.num_q_heads).astype(np.float32)).cuda()
+    out, lse = ops.refined_decode_attend_combine(dw.desc, dw.q, dw.K, dw.V, None, None, None,
+                                                 torch.from_numpy(idx).cuda(), torch.from_numpy(count).cuda(),
+                                                 dw.ctx, sink=sink)
+    ops.pipeline_check()
+    out = out.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy()
+    G = s.group
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            r = b * s.num_kv_heads + h
+            q = O.to_f64(host.q[b, h * G:(h + 1) * G], s.dtype)
+            K = O.to_f64(host.K[b, h], s.dtype)
+            V = O.to_f64(host.V[b, h], s.dtype)
+            sk = sink.cpu().numpy()[h * G:(h + 1) * G].astype(np.float64)
+            o_ref, l_ref = O.sparse_attention_row(q, K, V, lists[r], int(host.ctx_len[b]), s.page_size,
+                                                  s.scale, sk)
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"row {r}")
+            np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], l_ref, rtol=1e-4, atol=1e-4)
