@@ -6,6 +6,10 @@
 // compaction of the kept blocks into a per-row list with a device-side
 // count (the list length is data dependent, so the attend kernel derives
 // its split boundaries on the device).
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -13,6 +17,7 @@ namespace sls {
 
 constexpr int kDeltaThreads = 256;
 constexpr int kDeltaWarps = kDeltaThreads / 32;
+constexpr int kMaxScanTiles = 4;  // 16-token tiles of a block in the tensor-core scan (block <= 64)
 
 struct DeltaArgs {
   const void* q;
@@ -36,6 +41,82 @@ __device__ __forceinline__ void delta_layout(int N, int bshift, int block, int& 
   jend = (N & (block - 1)) == 0 ? nfull - 1 : nfull;
 }
 
+// The row's pseudo-max m~ ("Faster Than Flash", eq. 3): the best exact
+// score of each head over block 0 and the newest block, into s_m (every CTA
+// of a row recomputes it: at most two blocks of keys, L2-resident).
+template <typename T, int D, int GM>
+__device__ __forceinline__ void pseudo_max_cta(const DeltaArgs& a, const T* qrow, const T* krow, int N, int last,
+                                               float (*s_mt)[GM], float* s_m) {
+  constexpr int EPL = Vec16<T>::N;
+  constexpr int L = D / EPL;  // lanes per exact key
+  constexpr int TPW = 32 / L;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = a.G;
+  const int grp = lane / L, sub = lane % L;
+  float qv[GM][EPL];
+#pragma unroll
+  for (int g = 0; g < GM; ++g) {
+    float t[EPL];
+    if (g < G) load_vec(qrow + (size_t)g * D + sub * EPL, t);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) qv[g][e] = g < G ? t[e] * a.scale : 0.f;
+  }
+  const int nb0 = min(a.block, N);
+  const int lb0 = max(last << a.bshift, nb0);
+  const int ntk = nb0 + (N - lb0);
+  float mx[GM];
+#pragma unroll
+  for (int g = 0; g < GM; ++g) mx[g] = kNegInf;
+  // the keys of up to kPmRounds rounds are requested together (the scan waits on this)
+  constexpr int kPmRounds = 8;
+  const int step = kDeltaWarps * TPW;
+  for (int i00 = warp * TPW; i00 < ntk; i00 += kPmRounds * step) {
+    uint4 kraw[kPmRounds];
+#pragma unroll
+    for (int u = 0; u < kPmRounds; ++u) {
+      const int i = i00 + u * step + grp;
+      const int t = i < nb0 ? i : lb0 + (i - nb0);
+      kraw[u] = i < ntk ? ldg_stream(krow + (size_t)t * D + sub * EPL) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kPmRounds; ++u) {
+      const int i = i00 + u * step + grp;
+      const bool ok = i < ntk;
+      float kf[EPL];
+      unpack_vec(kraw[u], kf);
+      float s[GM];
+#pragma unroll
+      for (int g = 0; g < GM; ++g) {
+        s[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) s[g] = fmaf(qv[g][e], kf[e], s[g]);
+      }
+#pragma unroll
+      for (int o = L / 2; o > 0; o >>= 1) {
+#pragma unroll
+        for (int g = 0; g < GM; ++g) s[g] += __shfl_xor_sync(0xffffffffu, s[g], o);
+      }
+      if (ok) {
+#pragma unroll
+        for (int g = 0; g < GM; ++g) mx[g] = fmaxf(mx[g], s[g]);
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < GM; ++g) {
+    const float w = warp_max(mx[g]);
+    if (lane == 0) s_mt[warp][g] = w;
+  }
+  __syncthreads();
+  if (threadIdx.x < GM) {
+    float w = kNegInf;
+#pragma unroll
+    for (int i = 0; i < kDeltaWarps; ++i) w = fmaxf(w, s_mt[i][threadIdx.x]);
+    s_m[threadIdx.x] = w;
+  }
+  __syncthreads();
+}
+
 // One CTA per (row, part of the row's blocks).  Every CTA recomputes the
 // row's pseudo-max (at most two blocks of exact keys, L2-resident).
 template <typename T, int D, int GM>
@@ -43,8 +124,6 @@ __global__ void __launch_bounds__(kDeltaThreads)
 delta_scan_kernel(const DeltaArgs a) {
   pdl_wait_then_release();
   constexpr int EPL = Vec16<T>::N;
-  constexpr int L = D / EPL;       // lanes per exact key
-  constexpr int TPW = 32 / L;
   constexpr int CPL = 16;          // channels per lane in the scan (one 32-bit code word)
   constexpr int LC = D / CPL;      // lanes per thumbnail token
   constexpr int TPS = 32 / LC;     // tokens per warp step in the scan
@@ -66,64 +145,7 @@ delta_scan_kernel(const DeltaArgs a) {
   const T* qrow = static_cast<const T*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G) * D;
   const T* krow = static_cast<const T*>(a.k) + (size_t)row * a.Cap * D;
 
-  // ---- pseudo-max over block 0 and the newest block (exact keys)
-  {
-    const int grp = lane / L, sub = lane % L;
-    float qv[GM][EPL];
-#pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      float t[EPL];
-      if (g < G) load_vec(qrow + (size_t)g * D + sub * EPL, t);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) qv[g][e] = g < G ? t[e] * a.scale : 0.f;
-    }
-    const int nb0 = min(a.block, N);
-    const int lb0 = max(last << a.bshift, nb0);
-    const int ntk = nb0 + (N - lb0);
-    float mx[GM];
-#pragma unroll
-    for (int g = 0; g < GM; ++g) mx[g] = kNegInf;
-    for (int i0 = warp * TPW; i0 < ntk; i0 += kDeltaWarps * TPW) {
-      const int i = i0 + grp;
-      const bool ok = i < ntk;
-      const int t = i < nb0 ? i : lb0 + (i - nb0);
-      float kf[EPL];
-      if (ok) load_vec(krow + (size_t)t * D + sub * EPL, kf);
-      else {
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) kf[e] = 0.f;
-      }
-      float s[GM];
-#pragma unroll
-      for (int g = 0; g < GM; ++g) {
-        s[g] = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) s[g] = fmaf(qv[g][e], kf[e], s[g]);
-      }
-#pragma unroll
-      for (int o = L / 2; o > 0; o >>= 1) {
-#pragma unroll
-        for (int g = 0; g < GM; ++g) s[g] += __shfl_xor_sync(0xffffffffu, s[g], o);
-      }
-      if (ok) {
-#pragma unroll
-        for (int g = 0; g < GM; ++g) mx[g] = fmaxf(mx[g], s[g]);
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < GM; ++g) {
-      const float w = warp_max(mx[g]);
-      if (lane == 0) s_mt[warp][g] = w;
-    }
-    __syncthreads();
-    if (threadIdx.x < GM) {
-      float w = kNegInf;
-#pragma unroll
-      for (int i = 0; i < kDeltaWarps; ++i) w = fmaxf(w, s_mt[i][threadIdx.x]);
-      s_m[threadIdx.x] = w;
-    }
-    __syncthreads();
-  }
+  pseudo_max_cta<T, D, GM>(a, qrow, krow, N, last, s_mt, s_m);
 
   // ---- scan: one warp per block, LC lanes per token, 16 channels per lane
   const int grp = lane / LC, sub = lane % LC;
@@ -202,6 +224,159 @@ delta_scan_kernel(const DeltaArgs a) {
   }
 }
 
+// The same scan on the tensor cores (bf16 keys, any G <= 8).  Per complete
+// block the tentative scores of all its tokens and heads are one product
+//   S[t][g] = sum_c code[t][c] * w[g][c]  -  1.5 * sum_c w[g][c],
+//   w[g][c] = scale * q[g][c] * s[c] / 2   (the level is (code - 1.5) s / 2),
+// with A = the codes (16 tokens x 16 channels per m16n8k16, exact small
+// integers in fp16) and B = w split into fp16 hi + lo parts (w - hi is
+// exact in fp32), accumulated in fp32: the same scores as the CUDA-core
+// scan to about 2^-22 relative.  Lane (r, m) owns channels
+// [m D/4, (m+1) D/4) (k-step ks: its 4 channels m D/4 + 4 ks .. + 3, one
+// code byte), tokens r and r + 8 of each 16-token tile, head r of B.  A warp
+// takes one block at a time and loads the codes of its next block before
+// scoring the current one.
+__device__ __forceinline__ uint32_t code_pair_h2(uint32_t b) {
+  // (code of bits 0-1, code of bits 2-3) as fp16x2: 1024 + code under a
+  // 10-bit exponent field of 25, then minus 1024 (exact)
+  const uint32_t h = (b & 3u) | ((b & 0xcu) << 14) | 0x64006400u;
+  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __float2half2_rn(1024.f));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void mma_f16_d(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int D>
+struct ScanCodes {
+  static constexpr int W = D / 64;  // 32-bit code words per token and lane (D/4 channels)
+  uint32_t c[kMaxScanTiles][2][W];  // [m-tile][token r, r + 8][word]
+  uint4 sv[D / 32];                 // the block's scales of the lane's D/4 channels (bf16)
+};
+
+template <int D>
+__device__ __forceinline__ void load_scan_codes(ScanCodes<D>& sc, const uint8_t* cblk, const bf16* sblk, int ntile,
+                                                int lane) {
+  constexpr int W = ScanCodes<D>::W;
+  const int r = lane >> 2, m = lane & 3;
+#pragma unroll
+  for (int v = 0; v < D / 32; ++v) sc.sv[v] = __ldg(reinterpret_cast<const uint4*>(sblk + m * (D / 4) + 8 * v));
+#pragma unroll
+  for (int mt = 0; mt < kMaxScanTiles; ++mt) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint8_t* p = cblk + (size_t)(16 * mt + 8 * t + r) * (D / 4) + m * (D / 16);
+      if (mt < ntile) {
+        if constexpr (W == 2) {
+          const uint2 v = *reinterpret_cast<const uint2*>(p);
+          sc.c[mt][t][0] = v.x;
+          sc.c[mt][t][1] = v.y;
+        } else {
+          sc.c[mt][t][0] = *reinterpret_cast<const uint32_t*>(p);
+        }
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDeltaThreads, 2)
+delta_scan_mma_kernel(const DeltaArgs a) {
+  pdl_wait_then_release();
+  constexpr int KS = D / 16;      // k-steps
+  constexpr int CPL = D / 4;      // channels per lane
+  __shared__ float s_mt[kDeltaWarps][8];
+  __shared__ float s_m[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, m = lane & 3;
+  const int row = blockIdx.x / a.SPL, part = blockIdx.x % a.SPL;
+  const int b = row / a.Hkv, h = row % a.Hkv;
+  const int G = a.G;
+  const int N = clamp_len(a.ctx_len[b], a.Cap);
+  int nfull, last, jend;
+  delta_layout(N, a.bshift, a.block, nfull, last, jend);
+  const int nscan = jend > 1 ? jend - 1 : 0;
+  const int per = (nscan + a.SPL - 1) / a.SPL;
+  const int j0 = 1 + part * per, j1 = 1 + min(nscan, (part + 1) * per);
+  if (j0 >= j1) return;
+  const bf16* qrow = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G) * D;
+  const bf16* krow = static_cast<const bf16*>(a.k) + (size_t)row * a.Cap * D;
+  pseudo_max_cta<bf16, D, 8>(a, qrow, krow, N, last, s_mt, s_m);
+
+  // q * scale / 2 of head r on the lane's channels
+  float qh[CPL];
+#pragma unroll
+  for (int v = 0; v < CPL / 8; ++v) {
+    float t[8];
+    if (r < G) load_vec(qrow + (size_t)r * D + m * CPL + 8 * v, t);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qh[8 * v + e] = r < G ? t[e] * a.scale * 0.5f : 0.f;
+  }
+  // the pseudo-max of the lane's two output heads 2m, 2m + 1
+  const bool hv0 = 2 * m < G, hv1 = 2 * m + 1 < G;
+  const float mt0 = hv0 ? s_m[2 * m] : 0.f, mt1 = hv1 ? s_m[2 * m + 1] : 0.f;
+  const int ntile = a.block >> 4;
+  const bf16* srow = static_cast<const bf16*>(a.scales) + (size_t)row * a.nblk_cap * D;
+  const uint8_t* crow = a.codes + (size_t)row * a.Cap * (D / 4);
+
+  ScanCodes<D> cur, nxt;
+  int j = j0 + warp;
+  if (j < j1) load_scan_codes<D>(cur, crow + (size_t)j * a.block * (D / 4), srow + (size_t)j * D, ntile, lane);
+  while (j < j1) {
+    const int jn = j + kDeltaWarps;
+    if (jn < j1) load_scan_codes<D>(nxt, crow + (size_t)jn * a.block * (D / 4), srow + (size_t)jn * D, ntile, lane);
+    // weights of the block: hi/lo fp16 pairs per k-step, and their fp32 sum
+    uint32_t whi[KS][2], wlo[KS][2];
+    float wsum = 0.f;
+#pragma unroll
+    for (int v = 0; v < CPL / 8; ++v) {
+      float sv[8];
+      unpack_vec(cur.sv[v], sv);
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const int c = 8 * v + e;
+        const float w0 = qh[c] * sv[e], w1 = qh[c + 1] * sv[e + 1];
+        wsum += w0 + w1;
+        const __half2 hi = __floats2half2_rn(w0, w1);
+        const __half2 lo = __floats2half2_rn(w0 - __low2float(hi), w1 - __high2float(hi));
+        whi[c / 4][(c / 2) & 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        wlo[c / 4][(c / 2) & 1] = *reinterpret_cast<const uint32_t*>(&lo);
+      }
+    }
+    wsum += __shfl_xor_sync(0xffffffffu, wsum, 1);
+    wsum += __shfl_xor_sync(0xffffffffu, wsum, 2);  // head r's sum over all channels
+    const float ws0 = __shfl_sync(0xffffffffu, wsum, 8 * m), ws1 = __shfl_sync(0xffffffffu, wsum, 8 * m + 4);
+    const float off0 = -1.5f * ws0 - mt0, off1 = -1.5f * ws1 - mt1;
+    float best = kNegInf;
+#pragma unroll
+    for (int mt = 0; mt < kMaxScanTiles; ++mt) {
+      if (mt >= ntile) break;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint32_t b0 = (cur.c[mt][0][ks >> 2] >> (8 * (ks & 3))) & 0xffu;
+        const uint32_t b1 = (cur.c[mt][1][ks >> 2] >> (8 * (ks & 3))) & 0xffu;
+        const uint32_t a0 = code_pair_h2(b0), a2 = code_pair_h2(b0 >> 4);
+        const uint32_t a1 = code_pair_h2(b1), a3 = code_pair_h2(b1 >> 4);
+        mma_f16_d(acc, a0, a1, a2, a3, whi[ks][0], whi[ks][1]);
+        mma_f16_d(acc, a0, a1, a2, a3, wlo[ks][0], wlo[ks][1]);
+      }
+      // acc: tokens r (0, 1) and r + 8 (2, 3), heads 2m (0, 2) and 2m + 1 (1, 3)
+      if (hv0) best = fmaxf(best, fmaxf(acc[0], acc[2]) + off0);
+      if (hv1) best = fmaxf(best, fmaxf(acc[1], acc[3]) + off1);
+    }
+    best = warp_max(best);
+    if (lane == 0) a.flags[(size_t)row * a.nblk_cap + j] = best >= -a.delta ? 1 : 0;
+    cur = nxt;
+    j = jn;
+  }
+}
+
 // One CTA per row: ordered list of the kept blocks and its length.
 __global__ void __launch_bounds__(1024)
 delta_compact_kernel(const DeltaArgs a) {
@@ -260,6 +435,15 @@ static cudaError_t delta_launch(const DeltaArgs& a, int rows, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t delta_mma_launch(const DeltaArgs& a, int rows, cudaStream_t st) {
+  cudaError_t e = launch_pdl(delta_scan_mma_kernel<D>, dim3(rows * a.SPL), dim3(kDeltaThreads), 0, st, a);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(delta_compact_kernel, dim3(rows), dim3(1024), 0, st, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <typename T, int D>
 static cudaError_t delta_g(const DeltaArgs& a, int rows, cudaStream_t st) {
   if (a.G <= 1) return delta_launch<T, D, 1>(a, rows, st);
@@ -283,13 +467,18 @@ cudaError_t launch_select_delta(const Shape& s, const void* q, const void* k,
   a.scale = s.scale; a.delta = delta;
   const int rows = s.B * s.Hkv;
   // parts per row: enough CTAs to cover the SMs a few times over
-  int spl = (4 * 152 + rows - 1) / rows;
+  int spl = (4 * sm_count() + rows - 1) / rows;
   const int maxblk = a.nblk_cap;
   spl = spl < 1 ? 1 : spl;
   spl = spl > maxblk ? maxblk : spl;
   a.SPL = spl;
   if (s.dtype == 0)
     return s.D == 64 ? delta_g<float, 64>(a, rows, st) : delta_g<float, 128>(a, rows, st);
+  if (!(s.flags & 1) && s.G <= 8 && block <= 16 * kMaxScanTiles) {  // tensor cores unless asked for CUDA cores
+    // one wave of two CTAs per SM (each recomputes the row's pseudo-max once)
+    a.SPL = std::max(1, std::min(maxblk, (2 * sm_count()) / rows));
+    return s.D == 64 ? delta_mma_launch<64>(a, rows, st) : delta_mma_launch<128>(a, rows, st);
+  }
   return s.D == 64 ? delta_g<bf16, 64>(a, rows, st) : delta_g<bf16, 128>(a, rows, st);
 }
 

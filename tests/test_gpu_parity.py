@@ -181,7 +181,7 @@ def test_quest_step_small(key, path):
 
 
 @pytest.mark.parametrize("key", list(SMALL_DELTA))
-@pytest.mark.parametrize("path", ["step", "registers"])
+@pytest.mark.parametrize("path", ["step", "registers", "cuda_cores"])
 def test_delta_step_small(key, path):
     s = make(SMALL_DELTA[key])
     host = W.generate(s)
