@@ -73,18 +73,27 @@ __device__ __forceinline__ uint32_t ldg_stream1(const void* p) {
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// n of channel pair p (channels 2p, 2p+1 of an 8-channel step) as fp16x2:
-// 16 code bits of the step and the two residual words of the step.
-__device__ __forceinline__ uint32_t refined_pair(uint32_t c16, uint32_t w0, uint32_t w1, int p) {
-  const uint32_t cb = c16 >> (4 * p);
-  // (1024 + code_a, 1024 + code_b): a 10-bit exponent field of 25 leaves unit steps
-  const uint32_t ch = (cb & 3u) | ((cb & 0xcu) << 14) | 0x64006400u;
-  // (1152 + r_a, 1152 + r_b): the signed byte plus 128 under the same exponent
-  const uint32_t w = ((p >> 1) ? w1 : w0) ^ 0x80808080u;
-  const uint32_t rh = __byte_perm(w, 0x64646464u, (p & 1) ? 0x4342u : 0x4140u);
-  const __half2 c = __hsub2(bits_h2(ch), __float2half2_rn(1024.f));
-  const __half2 t = __hfma2(c, __float2half2_rn(254.f), bits_h2(rh));  // 254 c + 1152 + r <= 2041: exact
-  return h2_bits(__hsub2(t, __float2half2_rn(1533.f)));               // 254 c - 381 + r
+// n = 254 code - 381 + r of the 8 channels of one step as four fp16x2
+// (channel pairs 0-1, 2-3, 4-5, 6-7): c16 holds the step's 16 code bits,
+// w0 and w1 its 8 residual bytes.  Codes: x = b * 0x4001 places a code byte
+// at bit 0 and again at bit 14, so the fields at bits 0-1 and 16-17 of x
+// (of x >> 4) are the byte's codes 0 and 1 (2 and 3), and under the
+// exponent field 0x6400 each reads as 1024 + code.  Residuals: the signed
+// byte plus 128 (xor 0x80) under the same exponent reads as 1152 + r.
+// Then 254 (c' - 1024) + (1152 + r) <= 2041 and the final - 1533 are exact.
+__device__ __forceinline__ void refined_step(uint32_t c16, uint32_t w0, uint32_t w1, uint32_t (&n)[4]) {
+  const __half2 k1024 = __float2half2_rn(1024.f), k254 = __float2half2_rn(254.f), k1533 = __float2half2_rn(1533.f);
+  const uint32_t x0 = (c16 & 0xffu) * 0x4001u, x1 = ((c16 >> 8) & 0xffu) * 0x4001u;
+  const uint32_t ch[4] = {(x0 & 0x00030003u) | 0x64006400u, ((x0 >> 4) & 0x00030003u) | 0x64006400u,
+                          (x1 & 0x00030003u) | 0x64006400u, ((x1 >> 4) & 0x00030003u) | 0x64006400u};
+  const uint32_t v0 = w0 ^ 0x80808080u, v1 = w1 ^ 0x80808080u;
+  const uint32_t rh[4] = {__byte_perm(v0, 0x64646464u, 0x4140u), __byte_perm(v0, 0x64646464u, 0x4342u),
+                          __byte_perm(v1, 0x64646464u, 0x4140u), __byte_perm(v1, 0x64646464u, 0x4342u)};
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const __half2 t = __hfma2(__hsub2(bits_h2(ch[p]), k1024), k254, bits_h2(rh[p]));
+    n[p] = h2_bits(__hsub2(t, k1533));
+  }
 }
 
 template <int D>
@@ -192,12 +201,12 @@ __device__ __forceinline__ void compute_rgroup(const RGroup<D>& g, const Refined
         const uint32_t c16 = (&g.kc[nt][0].x)[s >> 1] >> (16 * (s & 1));
         const uint32_t* rw = &g.kc[nt][1].x;
         const uint32_t w0 = rw[2 * s], w1 = rw[2 * s + 1];
-        const uint32_t n0 = refined_pair(c16, w0, w1, 0), n1 = refined_pair(c16, w0, w1, 1);
-        const uint32_t n2 = refined_pair(c16, w0, w1, 2), n3 = refined_pair(c16, w0, w1, 3);
-        mma_f16(sc[nt][0], hi[0], 0u, hi[1], 0u, n0, n1);
-        mma_f16(sc[nt][1], hi[2], 0u, hi[3], 0u, n2, n3);
-        mma_f16(sc[nt][0], lo[0], 0u, lo[1], 0u, n0, n1);
-        mma_f16(sc[nt][1], lo[2], 0u, lo[3], 0u, n2, n3);
+        uint32_t n[4];
+        refined_step(c16, w0, w1, n);
+        mma_f16(sc[nt][0], hi[0], 0u, hi[1], 0u, n[0], n[1]);
+        mma_f16(sc[nt][1], hi[2], 0u, hi[3], 0u, n[2], n[3]);
+        mma_f16(sc[nt][0], lo[0], 0u, lo[1], 0u, n[0], n[1]);
+        mma_f16(sc[nt][1], lo[2], 0u, lo[3], 0u, n[2], n[3]);
       }
     }
   } else {

@@ -236,12 +236,20 @@ delta_scan_kernel(const DeltaArgs a) {
 // code byte), tokens r and r + 8 of each 16-token tile, head r of B.  A warp
 // takes one block at a time and loads the codes of its next block before
 // scoring the current one.
-__device__ __forceinline__ uint32_t code_pair_h2(uint32_t b) {
-  // (code of bits 0-1, code of bits 2-3) as fp16x2: 1024 + code under a
-  // 10-bit exponent field of 25, then minus 1024 (exact)
-  const uint32_t h = (b & 3u) | ((b & 0xcu) << 14) | 0x64006400u;
-  const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __float2half2_rn(1024.f));
-  return *reinterpret_cast<const uint32_t*>(&v);
+// The four 2-bit codes of one byte b as two fp16x2 values (channels 0, 1
+// and 2, 3): x = b * 0x4001 places b at bit 0 and again at bit 14, so the
+// fields at bits 0-1 and 16-17 of x (of x >> 4) are codes 0 and 1 (2 and
+// 3); under the exponent field 0x6400 each reads as 1024 + code, and one
+// subtraction of 1024 leaves the code (all exact).
+__device__ __forceinline__ void code_quad_h2(uint32_t b, uint32_t& h01, uint32_t& h23) {
+  const uint32_t x = b * 0x4001u;
+  const uint32_t u01 = (x & 0x00030003u) | 0x64006400u;
+  const uint32_t u23 = ((x >> 4) & 0x00030003u) | 0x64006400u;
+  const __half2 k1024 = __float2half2_rn(1024.f);
+  const __half2 v01 = __hsub2(*reinterpret_cast<const __half2*>(&u01), k1024);
+  const __half2 v23 = __hsub2(*reinterpret_cast<const __half2*>(&u23), k1024);
+  h01 = *reinterpret_cast<const uint32_t*>(&v01);
+  h23 = *reinterpret_cast<const uint32_t*>(&v23);
 }
 
 __device__ __forceinline__ void mma_f16_d(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -359,10 +367,12 @@ delta_scan_mma_kernel(const DeltaArgs a) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const uint32_t b0 = (cur.c[mt][0][ks >> 2] >> (8 * (ks & 3))) & 0xffu;
-        const uint32_t b1 = (cur.c[mt][1][ks >> 2] >> (8 * (ks & 3))) & 0xffu;
-        const uint32_t a0 = code_pair_h2(b0), a2 = code_pair_h2(b0 >> 4);
-        const uint32_t a1 = code_pair_h2(b1), a3 = code_pair_h2(b1 >> 4);
+        const uint32_t sel = 0x4440u + (ks & 3);  // byte ks & 3 of the word, zeros above
+        const uint32_t b0 = __byte_perm(cur.c[mt][0][ks >> 2], 0u, sel);
+        const uint32_t b1 = __byte_perm(cur.c[mt][1][ks >> 2], 0u, sel);
+        uint32_t a0, a1, a2, a3;
+        code_quad_h2(b0, a0, a2);
+        code_quad_h2(b1, a1, a3);
         mma_f16_d(acc, a0, a1, a2, a3, whi[ks][0], whi[ks][1]);
         mma_f16_d(acc, a0, a1, a2, a3, wlo[ks][0], wlo[ks][1]);
       }
