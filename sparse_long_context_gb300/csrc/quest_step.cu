@@ -327,15 +327,17 @@ __device__ __forceinline__ void load_keys_reg(const uint32_t* keys, int n, uint3
 // exactly (by counting, or a radix select when the bin is crowded).  Forced
 // keys (the largest value) are counted first.  Returns false when the bin
 // holds more than kCandMax keys (T and take are then undefined).
-template <int NT, int KPT>
+template <int NT, int KPT, int NB = kWinBins>
 __device__ __forceinline__ bool kth_largest_reg(const uint32_t (&kk)[KPT], int k, uint32_t* scratch, int* scan_tmp,
                                                 uint32_t& T, int& take) {
   // Loops over the keys are branch-free (selects, a spill bin, one slot
   // reservation per warp): divergent branches per key cost far more here
   // than the work they guard.
   __shared__ TopkScalars sc;
-  uint32_t* hist = scratch;                  // [kWinBins + 32]: the last 32 bins absorb excluded keys
-  uint32_t* cand = scratch + kWinBins + 32;  // [kCandMax]
+  static_assert((NB & (NB - 1)) == 0 && NB <= kWinBins, "bins: a power of two");
+  constexpr int LB = __builtin_ctz(NB);
+  uint32_t* hist = scratch;            // [NB + 32]: the last 32 bins absorb excluded keys
+  uint32_t* cand = scratch + NB + 32;  // [kCandMax]
   uint32_t* h256 = cand + kCandMax;          // [256]
   constexpr int NWp = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -350,7 +352,7 @@ __device__ __forceinline__ bool kth_largest_reg(const uint32_t (&kk)[KPT], int k
     mx = max(mx, real ? x : 0u);
     mn = min(mn, real ? x : 0xffffffffu);
   }
-  for (int d = threadIdx.x; d < kWinBins + 32; d += NT) hist[d] = 0;
+  for (int d = threadIdx.x; d < NB + 32; d += NT) hist[d] = 0;
   mx = __reduce_max_sync(0xffffffffu, mx);
   mn = __reduce_min_sync(0xffffffffu, mn);
   nf = __reduce_add_sync(0xffffffffu, nf);
@@ -373,21 +375,21 @@ __device__ __forceinline__ bool kth_largest_reg(const uint32_t (&kk)[KPT], int k
   if (need <= 0) return true;  // the first k forced keys
   // 2. histogram of (top - key) >> shift, the smallest shift fitting the range
   const uint32_t span = top - bot;
-  const int shift = span >= (uint32_t)kWinBins ? 32 - __clz(span >> 11) : 0;
+  const int shift = span >= (uint32_t)NB ? 32 - __clz(span >> LB) : 0;  // (span >> shift) < NB
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     const uint32_t x = kk[j];
     const bool real = x != kForcedKey32 && x != 0u;
-    atomicAdd(&hist[real ? (top - x) >> shift : kWinBins + lane], 1u);
+    atomicAdd(&hist[real ? (top - x) >> shift : NB + lane], 1u);
   }
   __syncthreads();
   // 3. the bin of the need-th largest
-  constexpr int BPT = (kWinBins + NT - 1) / NT;
+  constexpr int BPT = (NB + NT - 1) / NT;
   const int b0 = threadIdx.x * BPT;
   int cnt[BPT], sum = 0;
 #pragma unroll
   for (int i = 0; i < BPT; ++i) {
-    cnt[i] = b0 + i < kWinBins ? (int)hist[b0 + i] : 0;
+    cnt[i] = b0 + i < NB ? (int)hist[b0 + i] : 0;
     sum += cnt[i];
   }
   int total;
@@ -567,15 +569,15 @@ __device__ __forceinline__ uint32_t top_bin_threshold(const uint32_t (&kk)[KPT],
 }
 
 // Candidates of the cluster's CTAs in one array of (key, page) pairs, CTA c
-// at slots [c * cap, c * cap + n[c]), slot order = page order.  Thread t
-// holds slots [t * KPT, t * KPT + KPT); slots past a CTA's count hold key 0.
+// at slots [c * cap, c * cap + n[c]), slot order = page order; the other
+// slots hold key 0 (below every key).  Thread t holds slots
+// [t * KPT, t * KPT + KPT).
 template <int NT, int KPT>
-__device__ __forceinline__ void load_cand_reg(const uint2* cand, int cap, int C, const int* n, uint32_t (&kk)[KPT]) {
+__device__ __forceinline__ void load_cand_reg(const uint2* cand, int slots, uint32_t (&kk)[KPT]) {
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     const int i = threadIdx.x * KPT + j;
-    const int c = i / cap;
-    kk[j] = (c < C && i - c * cap < n[c]) ? cand[i].x : 0u;
+    kk[j] = i < slots ? cand[i].x : 0u;
   }
 }
 
@@ -584,14 +586,16 @@ __device__ __forceinline__ void load_cand_reg(const uint2* cand, int cap, int C,
 // overflows or when the row's k-th largest T falls below some CTA's
 // threshold: that CTA may hold unsent keys >= T.
 template <int NT, int KPT>
-__device__ __forceinline__ bool select_share_cand(const uint2* cand, int cap, int C, const int* n,
-                                                  const uint32_t* tau, int k, uint32_t* scratch, int e0, int nent,
-                                                  int32_t* share, int* scan_tmp) {
+__device__ __forceinline__ bool select_share_cand(const uint2* cand, int slots, int C, const uint32_t* tau, int k,
+                                                  uint32_t* scratch, int e0, int nent, int32_t* share,
+                                                  int* scan_tmp) {
   uint32_t kk[KPT];
-  load_cand_reg<NT, KPT>(cand, cap, C, n, kk);
+  load_cand_reg<NT, KPT>(cand, slots, kk);
   uint32_t T;
   int take;
-  if (!kth_largest_reg<NT, KPT>(kk, k, scratch, scan_tmp, T, take)) return false;
+  // a few hundred candidates: 512 range-scaled bins leave about one key per bin
+  constexpr int NB = KPT <= 4 ? 512 : kWinBins;
+  if (!kth_largest_reg<NT, KPT, NB>(kk, k, scratch, scan_tmp, T, take)) return false;
   uint32_t tmax = 0u;
   for (int c = 0; c < C; ++c) tmax = max(tmax, tau[c]);
   if (T < tmax) return false;
@@ -757,6 +761,8 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       int cnt = 0;
 #pragma unroll
       for (int j = 0; j < kLocalKeys; ++j) cnt += kk[j] >= tau;  // slots past nloc hold 0 < tau
+      // empty candidate slots read as key 0 (the scan's barrier orders this before the compaction)
+      for (int i = threadIdx.x; i < C * cap / 2; i += NT) reinterpret_cast<uint4*>(cand)[i] = make_uint4(0u, 0u, 0u, 0u);
       int total;
       const int off = block_scan_excl<NT>(cnt, scan_tmp, total);
       const bool ovf = total > cap;
@@ -794,11 +800,11 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       } else {
         const int slots = C * cap;
         bool okc;
-        if (slots <= NT * 2) okc = select_share_cand<NT, 2>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
-        else if (slots <= NT * 4) okc = select_share_cand<NT, 4>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
-        else if (slots <= NT * 8) okc = select_share_cand<NT, 8>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
-        else if (slots <= NT * 16) okc = select_share_cand<NT, 16>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
-        else okc = select_share_cand<NT, 32>(cand, cap, C, s_cand_n, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        if (slots <= NT * 2) okc = select_share_cand<NT, 2>(cand, slots, C, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        else if (slots <= NT * 4) okc = select_share_cand<NT, 4>(cand, slots, C, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        else if (slots <= NT * 8) okc = select_share_cand<NT, 8>(cand, slots, C, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        else if (slots <= NT * 16) okc = select_share_cand<NT, 16>(cand, slots, C, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
+        else okc = select_share_cand<NT, 32>(cand, slots, C, s_cand_tau, k, scratch, e0, nent, list, scan_tmp);
         if (!okc) use_all = true;  // identical candidates everywhere: the same in every CTA
       }
     }
