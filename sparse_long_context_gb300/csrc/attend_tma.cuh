@@ -151,9 +151,11 @@ __device__ __forceinline__ void merge_warps(const float (&o)[D / 16][4], int G, 
 }
 
 // Receive buffers of the cluster combine (in the owner CTA's shared memory).
+// 16-byte aligned: the combine moves its values as float4 (a static
+// __shared__ instance would otherwise only be 4-byte aligned).
 template <int D>
-struct ClusterInbox {
-  float o[8 * D + kMaxClusterSplits];
+struct __align__(16) ClusterInbox {
+  float o[8 * D + 4 * kMaxClusterSplits];  // S shares of round4(ceil(G D / S)) values
   float m[kMaxClusterSplits * 8];
   float l[kMaxClusterSplits * 8];
 };
@@ -175,15 +177,24 @@ __device__ __forceinline__ void cluster_push_combine(const AttendArgs& a, int ro
   cg::cluster_group cl = cg::this_cluster();
   const int S = a.S, G = a.G, GD = G * D;
   const int b = row / a.Hkv, h = row % a.Hkv;
-  const int chunk = (GD + S - 1) / S;
+  // owner r holds the values [r chunk, (r + 1) chunk): a multiple of 4, so
+  // that every float4 below stays inside one head and one owner (D % 4 == 0)
+  const int chunk = ((GD + S - 1) / S + 3) & ~3;
   if (wait_first) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  for (int it = threadIdx.x; it < GD; it += NT) {
+  for (int it = 4 * threadIdx.x; it < GD; it += 4 * NT) {
     const int g = it / D, d = it % D;
-    float av = 0.f;
+    float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < W; ++w) av = fmaf(sO[(w * 8 + g) * D + d], sF[w][g], av);
+    for (int w = 0; w < W; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(sO + (w * 8 + g) * D + d);
+      const float f = sF[w][g];
+      av.x = fmaf(x.x, f, av.x);
+      av.y = fmaf(x.y, f, av.y);
+      av.z = fmaf(x.z, f, av.z);
+      av.w = fmaf(x.w, f, av.w);
+    }
     const int owner = it / chunk;
-    cl.map_shared_rank(inbox->o, owner)[split * chunk + (it - owner * chunk)] = av;
+    *reinterpret_cast<float4*>(cl.map_shared_rank(inbox->o, owner) + split * chunk + (it - owner * chunk)) = av;
   }
   if (threadIdx.x < S * G) {
     const int owner = threadIdx.x / G, g = threadIdx.x % G;
@@ -193,22 +204,30 @@ __device__ __forceinline__ void cluster_push_combine(const AttendArgs& a, int ro
   cl.sync();
   const size_t hq0 = (size_t)b * a.Hq + (size_t)h * G;
   const int i0 = split * chunk, i1 = min(GD, i0 + chunk);
-  for (int it = i0 + threadIdx.x; it < i1; it += NT) {
+  for (int it = i0 + 4 * threadIdx.x; it < i1; it += 4 * NT) {
     const int g = it / D, d = it % D;
     float M = kNegInf;
     for (int s = 0; s < S; ++s) M = fmaxf(M, inbox->m[s * 8 + g]);
     const float sk = a.sink ? a.sink[h * G + g] : kNegInf;
     M = fmaxf(M, sk);
-    float Ls = 0.f, acc = 0.f;
+    float Ls = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < S; ++s) {
       const float ms = inbox->m[s * 8 + g];
       if (ms == kNegInf || M == kNegInf) continue;
       const float w = expf(ms - M);
       Ls = fmaf(inbox->l[s * 8 + g], w, Ls);
-      acc = fmaf(inbox->o[s * chunk + (it - i0)], w, acc);
+      const float4 x = *reinterpret_cast<const float4*>(inbox->o + s * chunk + (it - i0));
+      acc.x = fmaf(x.x, w, acc.x);
+      acc.y = fmaf(x.y, w, acc.y);
+      acc.z = fmaf(x.z, w, acc.z);
+      acc.w = fmaf(x.w, w, acc.w);
     }
     if (a.sink && M != kNegInf) Ls += expf(sk - M);
-    static_cast<bf16*>(a.out)[(hq0 + g) * D + d] = __float2bfloat16_rn(Ls > 0.f ? acc / Ls : 0.f);
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(static_cast<bf16*>(a.out) + (hq0 + g) * D + d);
+    op[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    op[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     if (d == 0 && a.lse) a.lse[hq0 + g] = Ls > 0.f ? M + logf(Ls) : kNegInf;
   }
 }

@@ -501,11 +501,11 @@ __device__ __forceinline__ bool select_share_reg(const uint32_t* keys, int n, in
 
 // A CTA's candidate threshold: the smallest key tau such that the CTA's real
 // (non-forced) keys >= tau are its m largest plus the rest of their
-// histogram bin (the range-scaled bins of kth_largest_reg); 1 (every key)
+// histogram bin (NB range-scaled bins, as in kth_largest_reg); 1 (every key)
 // when the CTA holds at most m real keys.  No exact rank: the cluster's
 // selection checks afterwards that the row's k-th largest is >= every CTA's
 // tau, which makes the candidates a superset of the row's top k.
-template <int NT, int KPT>
+template <int NT, int KPT, int NB = 1024>
 __device__ __forceinline__ uint32_t top_bin_threshold(const uint32_t (&kk)[KPT], int m, uint32_t* hist,
                                                       int* scan_tmp) {
   __shared__ TopkScalars sc;
@@ -521,7 +521,9 @@ __device__ __forceinline__ uint32_t top_bin_threshold(const uint32_t (&kk)[KPT],
     mx = max(mx, real ? x : 0u);
     mn = min(mn, real ? x : 0xffffffffu);
   }
-  for (int d = threadIdx.x; d < kWinBins + 32; d += NT) hist[d] = 0;
+  static_assert((NB & (NB - 1)) == 0 && NB <= kWinBins, "bins: a power of two");
+  constexpr int LB = __builtin_ctz(NB);
+  for (int d = threadIdx.x; d < NB + 32; d += NT) hist[d] = 0;
   mx = __reduce_max_sync(0xffffffffu, mx);
   mn = __reduce_min_sync(0xffffffffu, mn);
   nr = __reduce_add_sync(0xffffffffu, nr);
@@ -537,20 +539,20 @@ __device__ __forceinline__ uint32_t top_bin_threshold(const uint32_t (&kk)[KPT],
   const int nreal = __reduce_add_sync(0xffffffffu, lane < NWp ? sc.red_n[lane] : 0);
   if (nreal <= m) return 1u;  // uniform: every thread read the same totals
   const uint32_t span = top - bot;
-  const int shift = span >= (uint32_t)kWinBins ? 32 - __clz(span >> 11) : 0;
+  const int shift = span >= (uint32_t)NB ? 32 - __clz(span >> LB) : 0;  // (span >> shift) < NB
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     const uint32_t x = kk[j];
     const bool real = x != kForcedKey32 && x != 0u;
-    atomicAdd(&hist[real ? (top - x) >> shift : kWinBins + lane], 1u);
+    atomicAdd(&hist[real ? (top - x) >> shift : NB + lane], 1u);
   }
   __syncthreads();
-  constexpr int BPT = (kWinBins + NT - 1) / NT;
+  constexpr int BPT = (NB + NT - 1) / NT;
   const int b0 = threadIdx.x * BPT;
   int cnt[BPT], sum = 0;
 #pragma unroll
   for (int i = 0; i < BPT; ++i) {
-    cnt[i] = b0 + i < kWinBins ? (int)hist[b0 + i] : 0;
+    cnt[i] = b0 + i < NB ? (int)hist[b0 + i] : 0;
     sum += cnt[i];
   }
   int total;
