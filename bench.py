@@ -45,9 +45,9 @@ METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak) for select+att
 # written; traffic grows with the rows, so x4 for batch 32).  Reported only
 # for that workload and only while the kernel's sources hash to the ones
 # captured; otherwise null.
-STEP_TRAFFIC_B32 = 4 * (50.475776e6 + 0.143104e6)
+STEP_TRAFFIC_B32 = 4 * (50.472960e6 + 0.105984e6)
 STEP_SOURCES = ("quest_step.cu", "attend_tma.cuh", "tma.cuh", "mma.cuh", "attend_common.cuh", "common.cuh")
-STEP_SOURCES_SHA256 = "29d4ff35fcd20a211e6aa047eddd4436b5facfef38137f25741e05495d3f57c9"
+STEP_SOURCES_SHA256 = "c472bbc9d6d425b9af9a80fa93d615edf1e419210bc0874488b4494d2f6038bd"
 
 
 def step_traffic(s: W.Spec):
