@@ -39,44 +39,31 @@ struct TmaLayout {
   static constexpr size_t SMEM = (RING > MERGE ? RING : MERGE) + 1024;  // + alignment slack
 };
 
-// One group from the stage at shared address `stage`.  Lane (r, m) supplies
-// ldmatrix row addresses for matrix j = lane / 8, row i = lane % 8: token
-// 8 * (j / 2) + i and 8-channel chunk 2 * step + (j % 2), which makes the
-// four matrices the two n-tiles' (or the k-halves') fragments in the order
-// the mma wants.
+// The 16-token group's softmax and P.V once its raw scores are known: sc
+// holds the QK sums of lane (r, m) (head r; n-tile nt, chain c: tokens
+// 8 nt + 2m, +1), mul turns them into base-2 logits, and the group's V sits
+// at shared address `vstage` in the swizzled layout.  Tokens at or past
+// `lim` are masked (score -inf, V zero).
 template <int D>
-__device__ __forceinline__ void tma_group(uint32_t stage, int lim, const uint32_t (&qa)[D / 16][2],
-                                          float (&o)[D / 16][4], float& m_run, float& l_run, float sl2,
-                                          int lane) {
+__device__ __forceinline__ void tma_softmax_pv(const float (&sc)[2][2][4], uint32_t vstage, int lim,
+                                               float (&o)[D / 16][4], float& m_run, float& l_run, float mul,
+                                               int lane) {
   using L = TmaLayout<D>;
   constexpr int KS = D / 16;
   const int m = lane & 3;
   const int j = lane >> 3, i = lane & 7;
   const int tok = 8 * (j >> 1) + i;
-  // 128-byte swizzle: 16-byte chunk c of the row of token t sits at chunk c ^ (t % 8)
   auto row_addr = [&](uint32_t half_base, int c16) -> uint32_t {
     const int bx = c16 >> 3, c = c16 & 7;
     return half_base + bx * L::BOX + tok * 128 + ((c ^ i) << 4);
   };
-  float sc[2][2][4];
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int c = 0; c < 2; ++c) sc[nt][c][0] = sc[nt][c][1] = sc[nt][c][2] = sc[nt][c][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    uint32_t b00, b01, b10, b11;
-    ldsm_x4(row_addr(stage, 2 * ks + (j & 1)), b00, b01, b10, b11);
-    mma_bf16(sc[0][ks & 1], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
-    mma_bf16(sc[1][ks & 1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
-  }
   // lane (r, m): head r, tokens 2m, 2m+1 (n-tile 0) and 8+2m, 9+2m (n-tile 1)
   const int t0 = 2 * m;
   float s4[4];
-  s4[0] = t0 < lim ? (sc[0][0][0] + sc[0][1][0]) * sl2 : kNegInf;
-  s4[1] = t0 + 1 < lim ? (sc[0][0][1] + sc[0][1][1]) * sl2 : kNegInf;
-  s4[2] = t0 + 8 < lim ? (sc[1][0][0] + sc[1][1][0]) * sl2 : kNegInf;
-  s4[3] = t0 + 9 < lim ? (sc[1][0][1] + sc[1][1][1]) * sl2 : kNegInf;
+  s4[0] = t0 < lim ? (sc[0][0][0] + sc[0][1][0]) * mul : kNegInf;
+  s4[1] = t0 + 1 < lim ? (sc[0][0][1] + sc[0][1][1]) * mul : kNegInf;
+  s4[2] = t0 + 8 < lim ? (sc[1][0][0] + sc[1][1][0]) * mul : kNegInf;
+  s4[3] = t0 + 9 < lim ? (sc[1][0][1] + sc[1][1][1]) * mul : kNegInf;
   float gm = fmaxf(fmaxf(s4[0], s4[1]), fmaxf(s4[2], s4[3]));
   gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
   gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
@@ -101,7 +88,6 @@ __device__ __forceinline__ void tma_group(uint32_t stage, int lim, const uint32_
   // V values of tokens past the context may be anything (even NaN): zero them
   const uint32_t mlo = (t0 < lim ? 0x0000ffffu : 0u) | (t0 + 1 < lim ? 0xffff0000u : 0u);
   const uint32_t mhi = (t0 + 8 < lim ? 0x0000ffffu : 0u) | (t0 + 9 < lim ? 0xffff0000u : 0u);
-  const uint32_t vstage = stage + L::GROUP;
 #pragma unroll
   for (int t = 0; t < KS; ++t) {
     uint32_t a0, a1, a2, a3;
@@ -111,6 +97,39 @@ __device__ __forceinline__ void tma_group(uint32_t stage, int lim, const uint32_
     }
     mma_bf16(o[t], a0, a1, a2, a3, pb0, pb1);
   }
+}
+
+// One group from the stage at shared address `stage` (K, then V at +GROUP).
+// Lane (r, m) supplies ldmatrix row addresses for matrix j = lane / 8, row
+// i = lane % 8: token 8 * (j / 2) + i and 8-channel chunk 2 * step + (j % 2),
+// which makes the four matrices the two n-tiles' (or the k-halves')
+// fragments in the order the mma wants.
+template <int D>
+__device__ __forceinline__ void tma_group(uint32_t stage, int lim, const uint32_t (&qa)[D / 16][2],
+                                          float (&o)[D / 16][4], float& m_run, float& l_run, float sl2,
+                                          int lane) {
+  using L = TmaLayout<D>;
+  constexpr int KS = D / 16;
+  const int j = lane >> 3, i = lane & 7;
+  const int tok = 8 * (j >> 1) + i;
+  // 128-byte swizzle: 16-byte chunk c of the row of token t sits at chunk c ^ (t % 8)
+  auto row_addr = [&](uint32_t half_base, int c16) -> uint32_t {
+    const int bx = c16 >> 3, c = c16 & 7;
+    return half_base + bx * L::BOX + tok * 128 + ((c ^ i) << 4);
+  };
+  float sc[2][2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) sc[nt][c][0] = sc[nt][c][1] = sc[nt][c][2] = sc[nt][c][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t b00, b01, b10, b11;
+    ldsm_x4(row_addr(stage, 2 * ks + (j & 1)), b00, b01, b10, b11);
+    mma_bf16(sc[0][ks & 1], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
+    mma_bf16(sc[1][ks & 1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
+  }
+  tma_softmax_pv<D>(sc, stage + L::GROUP, lim, o, m_run, l_run, sl2, lane);
 }
 
 // Merge of the consumer warps' online-softmax states (after the last

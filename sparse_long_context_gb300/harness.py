@@ -86,16 +86,24 @@ class DecodeLoop:
     advances ctx_len, then runs select + attend + combine on the longer
     context.  capture() records one step in a CUDA graph; each replay decodes
     one more token with no host work.  The caller writes the step's q,
-    k_new and v_new into the fixed buffers before a replay."""
+    k_new and v_new into the fixed buffers before a replay.  refined=True
+    (top-delta only) keeps the 8-bit residuals current as well and attends
+    with the refined keys; `res` is then the residual tensor matching
+    dw.codes and dw.scales."""
 
-    def __init__(self, dw: DeviceWorkload, num_splits=None, min_sparsity: float = 0.0):
+    def __init__(self, dw: DeviceWorkload, num_splits=None, min_sparsity: float = 0.0, refined: bool = False,
+                 res=None):
         s = dw.spec
         self.dw = dw
+        self.refined = refined
+        self.res = res
+        if refined and (s.selector == "quest" or res is None):
+            raise ValueError("the refined loop is a top-delta loop and needs the residuals")
         if s.selector == "quest":
             self.step = ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, num_splits,
                                         min_sparsity=min_sparsity)
         else:
-            self.step = make_step(dw, num_splits)
+            self.step = ops.DeltaDecode(dw.desc, s.block, s.delta, num_splits, refined=refined)
         dt = dw.K.dtype
         self.k_new = torch.zeros((s.batch, s.num_kv_heads, s.head_dim), dtype=dt, device=dw.K.device)
         self.v_new = torch.zeros_like(self.k_new)
@@ -109,6 +117,9 @@ class DecodeLoop:
             ops.decode_append(dw.desc, self.k_new, self.v_new, dw.K, dw.V, dw.ctx, *meta, pos_out=self.pos)
             return self.step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx, dw.sink)
         ops.decode_append(dw.desc, self.k_new, self.v_new, dw.K, dw.V, dw.ctx, pos_out=self.pos)
+        if self.refined:
+            ops.thumb_residual_update(dw.desc, dw.K, self.pos, s.block, dw.codes, dw.scales, self.res)
+            return self.step(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink, res=self.res)
         ops.thumb_update(dw.desc, dw.K, self.pos, s.block, dw.codes, dw.scales)
         return self.step(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink)
 

@@ -158,6 +158,56 @@ def test_graph_replays_equal_eager_steps(key):
     _check_state(dg, host)
 
 
+def test_refined_decode_loop_matches_oracle():
+    """The top-delta loop with 8-bit residuals kept current (f2 inside f3):
+    after the appends the codes, scales and residuals equal the oracle's on
+    the full context, graph replays equal eager steps, and the last step's
+    output matches the oracle's refined attention."""
+    s, L = _spec("ffd")
+    host = W.generate(s)
+    n0 = host.ctx_len - L
+    outs = []
+    for graph in (False, True):
+        dw = PT.upload(s, host)
+        _rewind(dw, n0)
+        _, _, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block, dw.codes, dw.scales)
+        loop = H.DecodeLoop(dw, refined=True, res=res)
+        if graph:
+            loop.capture()
+        for i in range(L):
+            k_new, v_new = _token(host, s, n0 + i)
+            loop.k_new.copy_(k_new)
+            loop.v_new.copy_(v_new)
+            out, lse = loop.replay() if graph else loop.run_once()
+            outs.append((graph, i, out.clone(), lse.clone()))
+        ops.pipeline_check()
+        _check_state(dw, host)
+        rr = res.cpu().numpy()
+        for b in range(s.batch):
+            for h in range(s.num_kv_heads):
+                n = int(host.ctx_len[b])
+                _, _, ores = O.residuals_row(O.to_f64(host.K[b, h], s.dtype), n, s.block)
+                np.testing.assert_array_equal(rr[b, h, :(n // s.block) * s.block], ores)
+    eager = {i: (o, l) for g, i, o, l in outs if not g}
+    for g, i, o, l in outs:
+        if g:
+            assert torch.equal(o, eager[i][0]) and torch.equal(l, eager[i][1]), f"step {i}"
+    sel, cnt = _selection(loop)
+    out = outs[-1][2].float().cpu().numpy().astype(np.float64)
+    G = s.group
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            r = b * s.num_kv_heads + h
+            orc = PT.oracle_row(s, host, b, h)
+            if PT.check_delta_list(int(cnt[r]), sel[r], orc, s.delta):
+                continue
+            q = O.to_f64(host.q[b, h * G:(h + 1) * G], s.dtype)
+            K = O.to_f64(host.K[b, h], s.dtype)
+            V = O.to_f64(host.V[b, h], s.dtype)
+            o_ref, _ = O.refined_attention_row(q, K, V, orc.pages, int(host.ctx_len[b]), s.block, s.scale)
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"refined loop row {(b, h)}")
+
+
 def test_append_at_capacity_changes_nothing():
     s = W.spec("qwen7b", batch=2, ctx_len=[2304, 2288], capacity=2304)
     host = W.generate(s)
