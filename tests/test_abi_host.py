@@ -153,3 +153,40 @@ def test_python_layer_raises_on_status(lib):
     with pytest.raises(L.SlsError) as e:
         L.call("sls_pagemeta_build", ctypes.byref(d), BAD, BAD, BAD, BAD, None)
     assert e.value.code == L.SLS_EUNSUPPORTED
+
+
+def test_decode_append_validation(lib):
+    d = desc()
+    call = lambda kmin=BAD, kmax=BAD, ctx=BAD, dd=d: lib.sls_decode_append(
+        ctypes.byref(dd), BAD, BAD, BAD, BAD, kmin, kmax, ctx, None, None)
+    assert call(ctx=None) == L.SLS_EINVAL
+    assert call(kmax=None) == L.SLS_EINVAL          # both summaries or neither
+    assert "both or neither" in err(lib)
+    assert call(dd=desc(page_size=1)) == L.SLS_EINVAL  # page size 1: the cache is its own metadata
+
+
+def test_thumb_residual_validation(lib):
+    d = desc(page_size=64)
+    build = lambda block=64, res=BAD: lib.sls_thumb_residual_build(ctypes.byref(d), BAD, BAD, block, BAD, BAD, res,
+                                                                   None)
+    update = lambda block=64, res=BAD: lib.sls_thumb_residual_update(ctypes.byref(d), BAD, BAD, block, BAD, BAD, res,
+                                                                     None)
+    for f in (build, update):
+        assert f(res=None) == L.SLS_EINVAL
+        assert f(block=48) == L.SLS_EINVAL   # not a power of two
+        assert f(block=8) == L.SLS_EINVAL    # below 16
+
+
+def test_refined_attend_validation(lib):
+    d = desc(page_size=64)
+    ws = lib.sls_refined_decode_attend_workspace_size(ctypes.byref(d))
+    assert ws > 0
+    call = lambda dd=d, codes=BAD, res=BAD, stride=8, wsb=ws, out=BAD: lib.sls_refined_decode_attend_combine(
+        ctypes.byref(dd), BAD, BAD, BAD, codes, BAD, res, BAD, stride, BAD, BAD, None, out, None, BAD, wsb, None)
+    assert call(out=None) == L.SLS_EINVAL
+    assert call(res=None) == L.SLS_EINVAL               # codes, scales and res: all or none
+    assert call(stride=0) == L.SLS_EINVAL
+    assert call(wsb=ws - 1) == L.SLS_EWORKSPACE
+    assert call(dd=desc(page_size=64, dtype=L.SLS_DTYPE_F32)) == L.SLS_EUNSUPPORTED
+    assert call(dd=desc(page_size=64, num_q_heads=32, num_kv_heads=2)) == L.SLS_EUNSUPPORTED  # G = 16
+    assert call(dd=desc(page_size=1)) == L.SLS_EUNSUPPORTED

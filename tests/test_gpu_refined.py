@@ -221,3 +221,24 @@ def test_balanced_attend_uneven_lists_and_sink(ctx):
                                                   s.scale, sk)
             PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"row {r}")
             np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], l_ref, rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,sink", [(64, 16, 2, True), (128, 4, 4, False), (64, 3, 1, True)])
+def test_refined_other_head_shapes(D, Hq, Hkv, sink):
+    """The refined step at D = 64 and at group sizes 8, 1 and 3 (padded head
+    rows), with and without a sink, against the oracle's refined attention."""
+    s = W.spec("ffd", batch=2, ctx_len=[64 * 37 + 5, 64 * 12], capacity=64 * 38)
+    s.head_dim, s.num_q_heads, s.num_kv_heads, s.has_sink = D, Hq, Hkv, sink
+    host = W.generate(s)
+    dw, _, step, out, lse = _refined_step(s, host)
+    sel, cnt = step.block_idx.cpu().numpy(), step.count.cpu().numpy()
+    G = s.group
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            r = b * s.num_kv_heads + h
+            orc = PT.oracle_row(s, host, b, h)
+            if PT.check_delta_list(int(cnt[r]), sel[r], orc, s.delta):
+                continue
+            o_ref, lse_ref = _refined_oracle(s, host, b, h, orc.pages)
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"row {(b, h)}")
+            np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], lse_ref, rtol=1e-4, atol=1e-4)
