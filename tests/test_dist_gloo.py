@@ -58,3 +58,23 @@ def test_algorithmic_bytes_of_the_benchmark_workload():
     assert nb["select"] == 32 * 2 * 4096 * 2 * 128 * 2          # 134.2 MB of page min/max
     assert nb["attend"] == 32 * 2 * 2048 * 2 * 128 * 2          # 67.1 MB of selected K+V
     assert abs(nb["total"] / 1e6 - 201.3) < 0.1
+
+
+def test_delta_bytes_counts_refined_and_partial_blocks():
+    """Top-delta step bytes: bf16 K + V of every kept token; with residuals a
+    complete block reads codes (D/4) + residuals (D) + V (2D) per token and
+    its scales (2D) once, the partial newest block stays on bf16 keys."""
+    import numpy as np
+    from sparse_long_context_gb300 import workloads as W
+    s = W.spec("ffd", batch=1, ctx_len=[64 * 3 + 10], capacity=64 * 4)
+    D = s.head_dim
+    count = np.zeros(s.rows, dtype=np.int32)
+    idx = np.full((s.rows, 4), -1, dtype=np.int32)
+    count[0], idx[0, :3] = 3, [0, 2, 3]          # two complete blocks, the partial one (10 tokens)
+    count[1], idx[1, :1] = 1, [1]
+    nb = bench.delta_bytes(s, s.ctx_len, count, idx)
+    assert nb["scan"] == bench.algorithmic_bytes(s)["select"]
+    assert nb["attend_exact"] == (64 + 64 + 10 + 64) * 2 * D * 2
+    refined_block = 64 * (D // 4 + D + 2 * D) + 2 * D
+    assert nb["attend_refined"] == 3 * refined_block + 10 * 2 * D * 2
+    assert bench.step_traffic(W.spec("qwen1p5b", batch=8)) is None   # only the captured workload
