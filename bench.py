@@ -349,6 +349,9 @@ def run_ours(args, s: W.Spec):
                     steps_obj[u](dw.q, K, V, kmin, kmax, dw.ctx)
             mgraphs.append(g)
     torch.cuda.synchronize()
+    # kernels the library picked while the graphs were captured (the replays
+    # make no host calls); the device-side row counters restart here
+    paths_capture = {k: v for k, v in ops.get_stats(reset=True).items() if v}
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -374,6 +377,7 @@ def run_ours(args, s: W.Spec):
     w1 = time.time()
     clocks.window(w0, w1)
     elapsed = e0.elapsed_time(e1) / 1e3
+    timed_rows = ops.get_stats(reset=True)  # rows the one-launch step handled off its fast path
     t_max, total_bytes = aggregate(elapsed, float(nbytes["total"] * args.steps), world)
 
     # per-replay spread: events around single replays (a separate pass, so the
@@ -582,6 +586,9 @@ def run_ours(args, s: W.Spec):
         "decode_loop": loop_rec,
         "speedup_vs_dense": round(dense["us_per_step"] / (1e6 * t_max / args.steps), 2) if dense else None,
         "gpu_launches": (1 if one else 3) * args.steps,  # one step kernel, or score, top-k, attend
+        "paths": {"at_capture": paths_capture,
+                  "timed_rows_dense": timed_rows["step_rows_dense"],
+                  "timed_rows_all_keys": timed_rows["step_rows_all_keys"]},
         "clocks": clk,
         "e2e": {"value": round(e2e_bytes / e2e_max / 1e9, 2), "unit": "GB/s",
                 "us_per_step": round(1e6 * e2e_max / esteps, 2),

@@ -493,6 +493,36 @@ const char* sls_last_error(void);
  */
 sls_status sls_pipeline_check(void);
 
+/*
+ * Which paths the library took ("perf(core): fused sparse-attention decode
+ * via page indirection", Proving which path a benchmark arm took: a
+ * benchmark must be able to show which kernel it measured).  Host counters
+ * count launches by the kernel the library picked; the two row counters are
+ * kept on the device by the one-launch step.
+ */
+typedef struct sls_stats {
+  uint64_t quest_step_one_launch;     /* sls_quest_decode_step calls run as one kernel */
+  uint64_t quest_step_two_launch;     /* ... run as select + attend (shape outside the kernel) */
+  uint64_t step_rows_dense;           /* rows the sparsity gate sent to dense attention */
+  uint64_t step_rows_all_keys;        /* rows whose cluster selected from all of the row's keys
+                                         (long rows, or the candidate check failed) */
+  uint64_t select_pages;              /* sls_select_pages(_static) launches */
+  uint64_t select_delta_tensor_cores; /* top-delta scans on the tensor cores */
+  uint64_t select_delta_cuda_cores;   /* ... on the CUDA cores (fp32, or the CUDA-core flag) */
+  uint64_t attend_tma;                /* split-K attends by kernel: tensor-map fed, */
+  uint64_t attend_mma;                /* register-fed tensor cores, */
+  uint64_t attend_cuda_cores;         /* CUDA cores */
+  uint64_t attend_stream_k;           /* stream-K attends over block lists with bf16 keys */
+  uint64_t attend_refined;            /* ... with the refined (2-bit + 8-bit) keys */
+  uint64_t combine;                   /* separate combine launches */
+  uint64_t metadata;                  /* page min/max, thumbnail, residual and append launches */
+  uint64_t recall;                    /* selection-recall launches */
+} sls_stats;
+
+/* Fills *out with the counters (synchronising the device to read the row
+ * counters); reset != 0 zeroes them.  SLS_EINVAL for a NULL out. */
+sls_status sls_get_stats(sls_stats* out, int32_t reset);
+
 /* Library ABI version (major*10000 + minor*100 + patch). */
 int32_t sls_version(void);
 

@@ -24,6 +24,14 @@ class AttnDesc(ctypes.Structure):
                 ("scale", ctypes.c_float)]
 
 
+class Stats(ctypes.Structure):
+    """sls_stats: which paths the library took (include/sls.h)."""
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "quest_step_one_launch", "quest_step_two_launch", "step_rows_dense", "step_rows_all_keys",
+        "select_pages", "select_delta_tensor_cores", "select_delta_cuda_cores", "attend_tma", "attend_mma",
+        "attend_cuda_cores", "attend_stream_k", "attend_refined", "combine", "metadata", "recall")]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
 _D = ctypes.POINTER(AttnDesc)
@@ -48,6 +56,7 @@ SIGNATURES = {
     "sls_sparse_decode_attend_combine": (_I, [_D, _P, _P, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P, _P,
                                               ctypes.c_size_t, _P]),
     "sls_refined_decode_attend_workspace_size": (ctypes.c_size_t, [_D]),
+    "sls_get_stats": (_I, [ctypes.POINTER(Stats), _I]),
     "sls_refined_decode_attend_combine": (_I, [_D, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P,
                                                _P, ctypes.c_size_t, _P]),
     "sls_quest_decode_step_workspace_size": (ctypes.c_size_t, [_D, _I, _I]),

@@ -1,5 +1,6 @@
 // C ABI of libsls: host-side validation, then launch.  Nothing here touches
 // device memory or synchronises; a failed check returns before any launch.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -11,6 +12,7 @@
 namespace {
 
 thread_local char g_err[512] = "";
+std::atomic<unsigned long long> g_stats[sls::kStatCount];
 
 sls_status fail(sls_status code, const char* fmt, ...) {
   va_list ap;
@@ -85,6 +87,10 @@ sls_status check_desc(const sls_attn_desc* d, sls::Shape* s) {
 }  // namespace
 
 namespace sls {
+void stat_add(StatId id) { g_stats[id].fetch_add(1, std::memory_order_relaxed); }
+}  // namespace sls
+
+namespace sls {
 // Records a failure message for sls_last_error() from another translation unit.
 sls_status record_error(sls_status code, const char* msg) { return fail(code, "%s", msg); }
 }  // namespace sls
@@ -102,6 +108,33 @@ const char* sls_last_error(void) { return g_err; }
 
 int32_t sls_version(void) { return 10000; }
 
+sls_status sls_get_stats(sls_stats* out, int32_t reset) {
+  if (!out) return fail(SLS_EINVAL, "out is NULL");
+  std::memset(out, 0, sizeof(*out));
+  auto take = [&](sls::StatId id) -> uint64_t {
+    return reset ? g_stats[id].exchange(0) : g_stats[id].load();
+  };
+  out->quest_step_one_launch = take(sls::kStatStepOneLaunch);
+  out->quest_step_two_launch = take(sls::kStatStepTwoLaunch);
+  out->select_pages = take(sls::kStatSelectPages);
+  out->select_delta_tensor_cores = take(sls::kStatDeltaTensorCores);
+  out->select_delta_cuda_cores = take(sls::kStatDeltaCudaCores);
+  out->attend_tma = take(sls::kStatAttendTma);
+  out->attend_mma = take(sls::kStatAttendMma);
+  out->attend_cuda_cores = take(sls::kStatAttendCudaCores);
+  out->attend_stream_k = take(sls::kStatAttendStreamK);
+  out->attend_refined = take(sls::kStatAttendRefined);
+  out->combine = take(sls::kStatCombine);
+  out->metadata = take(sls::kStatMetadata);
+  out->recall = take(sls::kStatRecall);
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(SLS_ECUDA, "device synchronisation failed");
+  unsigned long long dense = 0, all_keys = 0;
+  sls::take_step_row_stats(&dense, &all_keys, reset != 0);
+  out->step_rows_dense = dense;
+  out->step_rows_all_keys = all_keys;
+  return ok();
+}
+
 sls_status sls_pipeline_check(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(SLS_ECUDA, "device synchronisation failed");
   const unsigned int n = sls::take_attend_wait_timeouts() + sls::take_step_wait_timeouts();
@@ -115,6 +148,7 @@ sls_status sls_pagemeta_build(const sls_attn_desc* desc, const void* k_cache, co
   sls_status r = check_desc(desc, &s);
   if (r) return r;
   REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(kmin); REQUIRE(kmax);
+  sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_pagemeta_build(s, k_cache, ctx_len, kmin, kmax, (cudaStream_t)stream),
                      "sls_pagemeta_build");
 }
@@ -125,6 +159,7 @@ sls_status sls_pagemeta_update(const sls_attn_desc* desc, const void* k_cache, c
   sls_status r = check_desc(desc, &s);
   if (r) return r;
   REQUIRE(k_cache); REQUIRE(pos); REQUIRE(kmin); REQUIRE(kmax);
+  sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_pagemeta_update(s, k_cache, pos, kmin, kmax, (cudaStream_t)stream),
                      "sls_pagemeta_update");
 }
@@ -145,6 +180,7 @@ sls_status sls_decode_append(const sls_attn_desc* desc, const void* k_new, const
   REQUIRE(k_new); REQUIRE(v_new); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(ctx_len);
   if ((kmin == nullptr) != (kmax == nullptr)) return fail(SLS_EINVAL, "kmin and kmax: both or neither");
   if (kmin && s.P == 1) return fail(SLS_EINVAL, "page_size 1: the key cache is its own page metadata (pass NULL)");
+  sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_decode_append(s, k_new, v_new, k_cache, v_cache, kmin, kmax, ctx_len, pos_out,
                                                (cudaStream_t)stream),
                      "sls_decode_append");
@@ -157,6 +193,7 @@ sls_status sls_thumb_build(const sls_attn_desc* desc, const void* k_cache, const
   if (r) return r;
   if ((r = check_block(s, block))) return r;
   REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(codes); REQUIRE(scales);
+  sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_thumb_build(s, k_cache, ctx_len, block, codes, scales, nullptr,
                                              (cudaStream_t)stream),
                      "sls_thumb_build");
@@ -169,6 +206,7 @@ sls_status sls_thumb_residual_build(const sls_attn_desc* desc, const void* k_cac
   if (r) return r;
   if ((r = check_block(s, block))) return r;
   REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(codes); REQUIRE(scales); REQUIRE(res);
+  sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_thumb_build(s, k_cache, ctx_len, block, codes, scales, res, (cudaStream_t)stream),
                      "sls_thumb_residual_build");
 }
@@ -180,6 +218,7 @@ sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache, cons
   if (r) return r;
   if ((r = check_block(s, block))) return r;
   REQUIRE(k_cache); REQUIRE(pos); REQUIRE(codes); REQUIRE(scales);
+  sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_thumb_update(s, k_cache, pos, block, codes, scales, nullptr,
                                               (cudaStream_t)stream),
                      "sls_thumb_update");
@@ -192,6 +231,7 @@ sls_status sls_thumb_residual_update(const sls_attn_desc* desc, const void* k_ca
   if (r) return r;
   if ((r = check_block(s, block))) return r;
   REQUIRE(k_cache); REQUIRE(pos); REQUIRE(codes); REQUIRE(scales); REQUIRE(res);
+  sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_thumb_update(s, k_cache, pos, block, codes, scales, res, (cudaStream_t)stream),
                      "sls_thumb_residual_update");
 }
@@ -228,6 +268,7 @@ sls_status sls_select_pages(const sls_attn_desc* desc, const void* q, const void
   const size_t need = sls::select_pages_workspace(s);
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  sls::stat_add(sls::kStatSelectPages);
   return cuda_status(sls::launch_select_pages(s, q, kmin, kmax, ctx_len, k, n_sink_pages, n_local_tokens,
                                               page_idx, workspace, (cudaStream_t)stream),
                      "sls_select_pages");
@@ -366,6 +407,7 @@ sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const vo
   const size_t need = sls::refined_workspace(s);
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  sls::stat_add(codes ? sls::kStatAttendRefined : sls::kStatAttendStreamK);
   return cuda_status(sls::launch_attend_refined(s, q, k_cache, v_cache, codes, scales, res, block_idx, idx_stride,
                                                 count, ctx_len, sink, out, lse, workspace, (cudaStream_t)stream),
                      "sls_refined_decode_attend_combine");
@@ -412,10 +454,14 @@ sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const
   cudaError_t e = sls::launch_quest_step(s, q, k_cache, v_cache, kmin, kmax, ctx_len, k, n_sink_pages,
                                          n_local_tokens, sink, page_idx, out, lse, num_splits, min_sparsity,
                                          (cudaStream_t)stream, &handled);
-  if (handled) return cuda_status(e, "sls_quest_decode_step");
+  if (handled) {
+    sls::stat_add(sls::kStatStepOneLaunch);
+    return cuda_status(e, "sls_quest_decode_step");
+  }
   if (min_sparsity > 0.f)
     return fail(SLS_EUNSUPPORTED, "min_sparsity needs the one-launch step (bf16, pages of >= 16 tokens)");
   // two launches: select into page_idx (or the workspace), then attend with the fused combine
+  sls::stat_add(sls::kStatStepTwoLaunch);
   const size_t chunk = (size_t)(npcap + sls::select_pages_cluster() - 1) / sls::select_pages_cluster();
   if (chunk * 4 > sls::select_pages_smem_limit())
     return fail(SLS_EUNSUPPORTED, "Cap/P=%d pages per row exceeds the supported %zu", npcap,
@@ -468,6 +514,7 @@ sls_status sls_selection_recall(const sls_attn_desc* desc, const void* q, const 
   const size_t need = sls::recall_workspace(s);
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  sls::stat_add(sls::kStatRecall);
   return cuda_status(sls::launch_recall(s, q, k_cache, page_idx, idx_stride, count, k_fixed, ctx_len, recall,
                                         workspace, (cudaStream_t)stream),
                      "sls_selection_recall");

@@ -338,10 +338,17 @@ cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const vo
   if (!(s.flags & 1)) {
     bool handled = false;
     cudaError_t e = launch_attend_tma(s, a, st, &handled);
-    if (handled) return e;
+    if (handled) {
+      stat_add(kStatAttendTma);
+      return e;
+    }
     e = launch_attend_mma(s, a, st, &handled);
-    if (handled) return e;
+    if (handled) {
+      stat_add(kStatAttendMma);
+      return e;
+    }
   }
+  stat_add(kStatAttendCudaCores);
   if (s.dtype == 0) {
     return s.D == 64 ? attend_cc_g<float, 64>(a, rows, st) : attend_cc_g<float, 128>(a, rows, st);
   }
@@ -353,6 +360,7 @@ cudaError_t launch_combine(const Shape& s, const float* o_part, const float* m_p
                            void* out, float* lse, cudaStream_t st) {
   const int total = s.B * s.Hq;
   const int grid = (total + 3) / 4;
+  stat_add(kStatCombine);
   cudaError_t e;
   if (s.dtype == 0) {
     if (s.D == 64)

@@ -124,6 +124,18 @@ cudaError_t launch_combine(const Shape& s, const float* o_part, const float* m_p
                            void* out, float* lse, cudaStream_t st);
 
 // Streaming multiprocessors of the current device (cached per device).
+// Which paths the library took (read back by sls_get_stats): host counters
+// bumped where a launch picks its kernel.
+enum StatId {
+  kStatStepOneLaunch, kStatStepTwoLaunch, kStatSelectPages, kStatDeltaTensorCores, kStatDeltaCudaCores,
+  kStatAttendTma, kStatAttendMma, kStatAttendCudaCores, kStatAttendStreamK, kStatAttendRefined, kStatCombine,
+  kStatMetadata, kStatRecall, kStatCount
+};
+void stat_add(StatId id);
+// Rows the one-launch step attended densely (sparsity gate) and rows whose
+// cluster selected from all of the row's keys, counted on the device.
+void take_step_row_stats(unsigned long long* dense, unsigned long long* all_keys, bool reset);
+
 inline int sm_count() {
   static int cache[64] = {0};
   int dev = 0;

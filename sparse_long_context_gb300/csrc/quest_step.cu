@@ -38,6 +38,8 @@ constexpr int kStepMaxK = 4096;      // page budget (the row's list sits in shar
 constexpr uint32_t kForcedKey32 = 0xffffffffu;
 
 __device__ unsigned int g_step_wait_timeouts = 0;
+__device__ unsigned long long g_step_rows_dense = 0;     // rows attended densely (sparsity gate)
+__device__ unsigned long long g_step_rows_all_keys = 0;  // rows selected from all keys
 
 struct StepArgs {
   AttendArgs a;  // q, k, v, ctx_len, sink, out, lse, shapes, qscale; S = C; cluster = 1
@@ -672,6 +674,7 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   if (dense) {
     // every page of the context, no selection; page_idx stays -1
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // completes the arrive made at entry
+    if (split == 0 && threadIdx.x == 0) atomicAdd(&g_step_rows_dense, 1ull);
     if (sa.page_idx)
       for (int e = threadIdx.x; e < nent; e += NT) sa.page_idx[(size_t)row * k + e0 + e] = -1;
   } else if (NP > k) {
@@ -812,6 +815,7 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     }
     if (use_all) {
       // every CTA receives the row's keys in its ring and selects locally
+      if (split == 0 && threadIdx.x == 0) atomicAdd(&g_step_rows_all_keys, 1ull);
       cl.sync();  // every ring is free (and every candidate list read)
       uint32_t* allk = reinterpret_cast<uint32_t*>(ring);  // [NP] keys of the row, by page
       {
@@ -1094,6 +1098,20 @@ cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache
   sa.npcap = s.Cap >> s.pshift;
   sa.min_sparsity = min_sparsity;
   return s.D == 64 ? step_launch<64>(s, sa, st, handled) : step_launch<128>(s, sa, st, handled);
+}
+
+void take_step_row_stats(unsigned long long* dense, unsigned long long* all_keys, bool reset) {
+  *dense = *all_keys = 0;
+  if (cudaMemcpyFromSymbol(dense, g_step_rows_dense, sizeof(*dense)) != cudaSuccess ||
+      cudaMemcpyFromSymbol(all_keys, g_step_rows_all_keys, sizeof(*all_keys)) != cudaSuccess) {
+    *dense = *all_keys = 0;
+    return;
+  }
+  if (reset) {
+    const unsigned long long zero = 0;
+    cudaMemcpyToSymbol(g_step_rows_dense, &zero, sizeof(zero));
+    cudaMemcpyToSymbol(g_step_rows_all_keys, &zero, sizeof(zero));
+  }
 }
 
 unsigned int take_step_wait_timeouts() {

@@ -482,13 +482,17 @@ cudaError_t launch_select_delta(const Shape& s, const void* q, const void* k,
   spl = spl < 1 ? 1 : spl;
   spl = spl > maxblk ? maxblk : spl;
   a.SPL = spl;
-  if (s.dtype == 0)
+  if (s.dtype == 0) {
+    stat_add(kStatDeltaCudaCores);
     return s.D == 64 ? delta_g<float, 64>(a, rows, st) : delta_g<float, 128>(a, rows, st);
+  }
   if (!(s.flags & 1) && s.G <= 8 && block <= 16 * kMaxScanTiles) {  // tensor cores unless asked for CUDA cores
     // one wave of two CTAs per SM (each recomputes the row's pseudo-max once)
     a.SPL = std::max(1, std::min(maxblk, (2 * sm_count()) / rows));
+    stat_add(kStatDeltaTensorCores);
     return s.D == 64 ? delta_mma_launch<64>(a, rows, st) : delta_mma_launch<128>(a, rows, st);
   }
+  stat_add(kStatDeltaCudaCores);
   return s.D == 64 ? delta_g<bf16, 64>(a, rows, st) : delta_g<bf16, 128>(a, rows, st);
 }
 

@@ -43,6 +43,13 @@ def make_desc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, d
                       flags, float(scale))
 
 
+def get_stats(reset: bool = False) -> dict:
+    """Counters of the paths the library took (synchronises the device)."""
+    st = L.Stats()
+    L.call("sls_get_stats", ctypes.byref(st), int(bool(reset)))
+    return {name: int(getattr(st, name)) for name, _ in L.Stats._fields_}
+
+
 def pipeline_check() -> None:
     """Synchronises the device; raises SlsError if a pipelined kernel gave up
     waiting for its copies since the last check."""

@@ -190,3 +190,15 @@ def test_refined_attend_validation(lib):
     assert call(dd=desc(page_size=64, dtype=L.SLS_DTYPE_F32)) == L.SLS_EUNSUPPORTED
     assert call(dd=desc(page_size=64, num_q_heads=32, num_kv_heads=2)) == L.SLS_EUNSUPPORTED  # G = 16
     assert call(dd=desc(page_size=1)) == L.SLS_EUNSUPPORTED
+
+
+def test_stats_counters_without_a_launch(lib):
+    """Calls that fail validation launch nothing and count nothing; the
+    counters read back and reset without a GPU."""
+    st = L.Stats()
+    assert lib.sls_get_stats(None, 0) == L.SLS_EINVAL
+    d = desc()
+    lib.sls_pagemeta_build(ctypes.byref(d), None, BAD, BAD, BAD, None)   # fails validation
+    rc = lib.sls_get_stats(ctypes.byref(st), 1)
+    assert rc in (L.SLS_OK, L.SLS_ECUDA)          # no device here: the row counters cannot be read
+    assert st.metadata == 0 and st.quest_step_one_launch == 0

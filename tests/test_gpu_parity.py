@@ -223,8 +223,11 @@ def test_sparsity_gate_attends_short_contexts_densely():
     host = W.generate(s)
     dw = PT.upload(s, host)
     step = ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, min_sparsity=4.0)
+    ops.get_stats(reset=True)
     out, lse = step(dw.q, dw.K, dw.V, dw.kmin, dw.kmax, dw.ctx)
     ops.pipeline_check()
+    st = ops.get_stats(reset=True)
+    assert st["step_rows_dense"] == 2 * s.num_kv_heads and st["quest_step_one_launch"] == 1, st
     out = out.float().cpu().numpy().astype(np.float64)
     sel = step.page_idx.cpu().numpy()
     G, H = s.group, s.num_kv_heads
@@ -324,8 +327,19 @@ def test_topk_with_the_best_pages_in_one_split(splits, npg):
         K[h, t0:t1] = np.abs(K[h, t0:t1]) * sgn[None, :] * 1.5
     host.K[0] = _bits(K)
     dw = PT.upload(s, host)
+    ops.get_stats(reset=True)
     sel, cnt, out, lse = PT.run_step(dw, num_splits=splits)
+    st = ops.get_stats(reset=True)
     check_all_rows(s, host, sel, cnt, out, lse)
+    assert st["quest_step_one_launch"] == 1 and st["quest_step_two_launch"] == 0
+    # a split holding more of the row's top k than it sends forces the all-keys selection:
+    # with 5 splits of 112 pages the run 200-299 puts 76 of the top 128 into split 2 (it
+    # sends about 60); with 16 splits of 32 pages, the run 200-327 fills splits 7-9 (each
+    # sends about 24).  With 2 splits each sends its whole top k, so the candidates decide.
+    if (splits, npg) in ((5, 100), (16, 128)):
+        assert st["step_rows_all_keys"] >= 1, st
+    if splits == 2:
+        assert st["step_rows_all_keys"] == 0, st
 
 
 # 2..16 splits combine inside a thread-block cluster, more through global memory

@@ -140,12 +140,16 @@ def test_refined_step_matches_oracle(key):
 def test_refined_scores_differ_from_exact_ones():
     """The refined path really scores with k~: against the exact-key step on
     the same selection the outputs differ (slightly), and both stay within
-    tolerance of their own oracle."""
+    tolerance of their own oracle; the path counters name the kernels."""
     s = W.spec("ffd", **SMALL["ffd_aligned"])
     host = W.generate(s)
+    ops.get_stats(reset=True)
     dw, _, step, out_ref, _ = _refined_step(s, host)
     exact = ops.DeltaDecode(dw.desc, s.block, s.delta)
     out_ex, _ = exact(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink)
+    st = ops.get_stats(reset=True)
+    assert st["attend_refined"] == 1 and st["attend_stream_k"] == 1, st
+    assert st["select_delta_tensor_cores"] == 2 and st["select_delta_cuda_cores"] == 0, st
     out_ex = out_ex.float().cpu().numpy().astype(np.float64)
     assert np.abs(out_ref - out_ex).max() > 0
     q, K, V, sink = _row_inputs(s, host, 0, 0)
