@@ -236,15 +236,18 @@ delta_scan_kernel(const DeltaArgs a) {
 // code byte), tokens r and r + 8 of each 16-token tile, head r of B.  A warp
 // takes one block at a time and loads the codes of its next block before
 // scoring the current one.
-// The four 2-bit codes of one byte b as two fp16x2 values (channels 0, 1
-// and 2, 3): x = b * 0x4001 places b at bit 0 and again at bit 14, so the
-// fields at bits 0-1 and 16-17 of x (of x >> 4) are codes 0 and 1 (2 and
-// 3); under the exponent field 0x6400 each reads as 1024 + code, and one
-// subtraction of 1024 leaves the code (all exact).
-__device__ __forceinline__ void code_quad_h2(uint32_t b, uint32_t& h01, uint32_t& h23) {
-  const uint32_t x = b * 0x4001u;
-  const uint32_t u01 = (x & 0x00030003u) | 0x64006400u;
-  const uint32_t u23 = ((x >> 4) & 0x00030003u) | 0x64006400u;
+
+// The four 2-bit codes of code byte k of word w as two fp16x2 values
+// (channels 0, 1 and 2, 3), each code scaled by 1, 4, 16 and 64: a byte
+// permute puts the byte into both 16-bit halves, and masking keeps bits
+// 0-1 and 2-3 (4-5 and 6-7) in place under the exponent field 0x6400, where
+// the half reads as 1024 + f * code; one subtraction of 1024 leaves f *
+// code (all exact).  The weights carry 64 / f, so every product is 64 times
+// the level's.
+__device__ __forceinline__ void code_quad_h2(uint32_t w, int k, uint32_t& h01, uint32_t& h23) {
+  const uint32_t h = __byte_perm(w, 0u, 0x4040u + 0x0101u * (uint32_t)k);  // [byte k, 0, byte k, 0]
+  const uint32_t u01 = (h & 0x000C0003u) | 0x64006400u;
+  const uint32_t u23 = (h & 0x00C00030u) | 0x64006400u;
   const __half2 k1024 = __float2half2_rn(1024.f);
   const __half2 v01 = __hsub2(*reinterpret_cast<const __half2*>(&u01), k1024);
   const __half2 v23 = __hsub2(*reinterpret_cast<const __half2*>(&u23), k1024);
@@ -316,14 +319,15 @@ delta_scan_mma_kernel(const DeltaArgs a) {
   const bf16* krow = static_cast<const bf16*>(a.k) + (size_t)row * a.Cap * D;
   pseudo_max_cta<bf16, D, 8>(a, qrow, krow, N, last, s_mt, s_m);
 
-  // q * scale / 2 of head r on the lane's channels
+  // q * scale / 2 of head r on the lane's channels, times 64 / f for the
+  // code scaling f = 1, 4, 16, 64 of the channel's place in its code byte
   float qh[CPL];
 #pragma unroll
   for (int v = 0; v < CPL / 8; ++v) {
     float t[8];
     if (r < G) load_vec(qrow + (size_t)r * D + m * CPL + 8 * v, t);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qh[8 * v + e] = r < G ? t[e] * a.scale * 0.5f : 0.f;
+    for (int e = 0; e < 8; ++e) qh[8 * v + e] = r < G ? t[e] * a.scale * (0.5f * (64 >> (2 * (e & 3)))) : 0.f;
   }
   // the pseudo-max of the lane's two output heads 2m, 2m + 1
   const bool hv0 = 2 * m < G, hv1 = 2 * m + 1 < G;
@@ -349,7 +353,8 @@ delta_scan_mma_kernel(const DeltaArgs a) {
       for (int e = 0; e < 8; e += 2) {
         const int c = 8 * v + e;
         const float w0 = qh[c] * sv[e], w1 = qh[c + 1] * sv[e + 1];
-        wsum += w0 + w1;
+        // the level sum takes the unscaled weights (exact: powers of two)
+        wsum += w0 * (1.f / (64 >> (2 * (e & 3)))) + w1 * (1.f / (64 >> (2 * ((e + 1) & 3))));
         const __half2 hi = __floats2half2_rn(w0, w1);
         const __half2 lo = __floats2half2_rn(w0 - __low2float(hi), w1 - __high2float(hi));
         whi[c / 4][(c / 2) & 1] = *reinterpret_cast<const uint32_t*>(&hi);
@@ -367,18 +372,15 @@ delta_scan_mma_kernel(const DeltaArgs a) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const uint32_t sel = 0x4440u + (ks & 3);  // byte ks & 3 of the word, zeros above
-        const uint32_t b0 = __byte_perm(cur.c[mt][0][ks >> 2], 0u, sel);
-        const uint32_t b1 = __byte_perm(cur.c[mt][1][ks >> 2], 0u, sel);
         uint32_t a0, a1, a2, a3;
-        code_quad_h2(b0, a0, a2);
-        code_quad_h2(b1, a1, a3);
+        code_quad_h2(cur.c[mt][0][ks >> 2], ks & 3, a0, a2);
+        code_quad_h2(cur.c[mt][1][ks >> 2], ks & 3, a1, a3);
         mma_f16_d(acc, a0, a1, a2, a3, whi[ks][0], whi[ks][1]);
         mma_f16_d(acc, a0, a1, a2, a3, wlo[ks][0], wlo[ks][1]);
       }
-      // acc: tokens r (0, 1) and r + 8 (2, 3), heads 2m (0, 2) and 2m + 1 (1, 3)
-      if (hv0) best = fmaxf(best, fmaxf(acc[0], acc[2]) + off0);
-      if (hv1) best = fmaxf(best, fmaxf(acc[1], acc[3]) + off1);
+      // acc (64 times the level sums): tokens r (0, 1) and r + 8 (2, 3), heads 2m (0, 2) and 2m + 1 (1, 3)
+      if (hv0) best = fmaxf(best, fmaxf(acc[0], acc[2]) * (1.f / 64.f) + off0);
+      if (hv1) best = fmaxf(best, fmaxf(acc[1], acc[3]) * (1.f / 64.f) + off1);
     }
     best = warp_max(best);
     if (lane == 0) a.flags[(size_t)row * a.nblk_cap + j] = best >= -a.delta ? 1 : 0;
