@@ -395,7 +395,8 @@ class DeltaDecode:
         self.desc, self.block, self.delta = desc, int(block), float(delta)
         self.fused = fused
         self.refined = refined
-        ok = desc.dtype == L.SLS_DTYPE_BF16 and desc.num_q_heads // desc.num_kv_heads <= 8
+        ok = (desc.dtype == L.SLS_DTYPE_BF16 and desc.num_q_heads // desc.num_kv_heads <= 8
+              and desc.batch * desc.num_kv_heads <= 4096)  # the work-item kernel's row limit
         # the default for the fast path only: the descriptor's path flags select the split-K attends
         self.balanced = (fused and ok and desc.flags == 0) if balanced is None else balanced
         if refined and not ok:
