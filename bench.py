@@ -45,9 +45,9 @@ METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak) for select+att
 # written; traffic grows with the rows, so x4 for batch 32).  Reported only
 # for that workload and only while the kernel's sources hash to the ones
 # captured; otherwise null.
-STEP_TRAFFIC_B32 = 4 * (50.472960e6 + 0.103424e6)
+STEP_TRAFFIC_B32 = 4 * (50.475264e6 + 0.102912e6)
 STEP_SOURCES = ("quest_step.cu", "attend_tma.cuh", "tma.cuh", "mma.cuh", "attend_common.cuh", "common.cuh")
-STEP_SOURCES_SHA256 = "62f8315aa2c04b72987e6391a2d3c4bf2f14936e779b9ddcc2c362e4d073fc09"
+STEP_SOURCES_SHA256 = "47e78991e4c5f32f831eb2f0adca24a306946651ca07f62fdb6ea567eb81491a"
 
 
 def step_traffic(s: W.Spec):
