@@ -397,7 +397,9 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
  *             counters at zero); calls sharing it must not run concurrently
  *   |q * s| must stay below 65504 (the products run in fp16 hi/lo parts).
  * Errors: SLS_EUNSUPPORTED for another dtype, G > 8, blocks < 16 tokens or
- * more rows; SLS_EINVAL for null pointers or bad sizes; SLS_EWORKSPACE.
+ * more rows; SLS_EINVAL for null pointers, bad sizes or a q, k_cache,
+ * v_cache, codes, scales or res pointer that is not 16-byte aligned;
+ * SLS_EWORKSPACE.
  */
 size_t sls_refined_decode_attend_workspace_size(const sls_attn_desc* desc);
 sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const void* q,

@@ -404,6 +404,10 @@ sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const vo
     return fail(SLS_EUNSUPPORTED,
                 "needs bf16, G <= 8, blocks (page_size) of >= 16 tokens and at most 4096 rows (B*Hkv)");
   if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+       reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales) | reinterpret_cast<uintptr_t>(res)) &
+      15)
+    return fail(SLS_EINVAL, "q, the caches, codes, scales and res must be 16-byte aligned");
   const size_t need = sls::refined_workspace(s);
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);

@@ -186,6 +186,7 @@ def test_refined_attend_validation(lib):
     assert call(out=None) == L.SLS_EINVAL
     assert call(res=None) == L.SLS_EINVAL               # codes, scales and res: all or none
     assert call(stride=0) == L.SLS_EINVAL
+    assert call(res=ctypes.c_void_p(0x1008)) == L.SLS_EINVAL  # 16-byte alignment
     assert call(wsb=ws - 1) == L.SLS_EWORKSPACE
     assert call(dd=desc(page_size=64, dtype=L.SLS_DTYPE_F32)) == L.SLS_EUNSUPPORTED
     assert call(dd=desc(page_size=64, num_q_heads=32, num_kv_heads=2)) == L.SLS_EUNSUPPORTED  # G = 16
