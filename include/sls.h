@@ -18,6 +18,10 @@
  * - Every pointer argument is a DEVICE pointer owned by the caller, unless
  *   stated otherwise.  The library allocates no memory; scratch comes from a
  *   caller buffer whose size a *_workspace_size() call reports.
+ * - Queries, K/V caches, page metadata (kmin/kmax), thumbnail codes, scales
+ *   and residuals, appended keys/values and split partials (o_part) are read
+ *   in 16-byte vectors: their pointers must be 16-byte aligned, or the call
+ *   fails with SLS_EINVAL before launching anything.
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *   stream).  Calls only enqueue work: they never synchronise the device
  *   and never read device memory from the host, so they can be captured in
@@ -397,8 +401,7 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
  *             counters at zero); calls sharing it must not run concurrently
  *   |q * s| must stay below 65504 (the products run in fp16 hi/lo parts).
  * Errors: SLS_EUNSUPPORTED for another dtype, G > 8, blocks < 16 tokens or
- * more rows; SLS_EINVAL for null pointers, bad sizes or a q, k_cache,
- * v_cache, codes, scales or res pointer that is not 16-byte aligned;
+ * more rows; SLS_EINVAL for null or misaligned pointers or bad sizes;
  * SLS_EWORKSPACE.
  */
 size_t sls_refined_decode_attend_workspace_size(const sls_attn_desc* desc);
@@ -427,8 +430,8 @@ int32_t sls_quest_decode_step_splits(const sls_attn_desc* desc, int32_t k);
  * sparse attention with the combine of sls_sparse_decode_attend_combine
  * over the chosen pages ("Don't read the haystack", Part two).
  *
- * For bf16 caches with pages of >= 16 tokens (k <= 4096, Cap/P <= 131072,
- * 16-byte aligned cache and metadata pointers) this is ONE kernel launch: a
+ * For bf16 caches with pages of >= 16 tokens (k <= 4096, Cap/P <= 131072)
+ * this is ONE kernel launch: a
  * thread-block cluster per (sequence, KV head) scores its row's pages from
  * the min/max metadata, selects the top k inside the cluster and attends to
  * them; the scores and the page list never leave shared memory.  Otherwise

@@ -100,6 +100,12 @@ namespace {
 #define REQUIRE(ptr) \
   if (!(ptr)) return fail(SLS_EINVAL, "%s is NULL", #ptr)
 
+// Tensors the kernels read or write in 16-byte vectors.
+#define REQUIRE16(ptr)                                                         \
+  REQUIRE(ptr);                                                                \
+  if (reinterpret_cast<uintptr_t>(ptr) & 15)                                   \
+  return fail(SLS_EINVAL, "%s is not 16-byte aligned", #ptr)
+
 }  // namespace
 
 extern "C" {
@@ -147,7 +153,7 @@ sls_status sls_pagemeta_build(const sls_attn_desc* desc, const void* k_cache, co
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(kmin); REQUIRE(kmax);
+  REQUIRE16(k_cache); REQUIRE(ctx_len); REQUIRE16(kmin); REQUIRE16(kmax);
   sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_pagemeta_build(s, k_cache, ctx_len, kmin, kmax, (cudaStream_t)stream),
                      "sls_pagemeta_build");
@@ -158,7 +164,7 @@ sls_status sls_pagemeta_update(const sls_attn_desc* desc, const void* k_cache, c
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(k_cache); REQUIRE(pos); REQUIRE(kmin); REQUIRE(kmax);
+  REQUIRE16(k_cache); REQUIRE(pos); REQUIRE16(kmin); REQUIRE16(kmax);
   sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_pagemeta_update(s, k_cache, pos, kmin, kmax, (cudaStream_t)stream),
                      "sls_pagemeta_update");
@@ -177,7 +183,7 @@ sls_status sls_decode_append(const sls_attn_desc* desc, const void* k_new, const
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(k_new); REQUIRE(v_new); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(ctx_len);
+  REQUIRE16(k_new); REQUIRE16(v_new); REQUIRE16(k_cache); REQUIRE16(v_cache); REQUIRE(ctx_len);
   if ((kmin == nullptr) != (kmax == nullptr)) return fail(SLS_EINVAL, "kmin and kmax: both or neither");
   if (kmin && s.P == 1) return fail(SLS_EINVAL, "page_size 1: the key cache is its own page metadata (pass NULL)");
   sls::stat_add(sls::kStatMetadata);
@@ -192,7 +198,7 @@ sls_status sls_thumb_build(const sls_attn_desc* desc, const void* k_cache, const
   sls_status r = check_desc(desc, &s);
   if (r) return r;
   if ((r = check_block(s, block))) return r;
-  REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(codes); REQUIRE(scales);
+  REQUIRE16(k_cache); REQUIRE(ctx_len); REQUIRE16(codes); REQUIRE16(scales);
   sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_thumb_build(s, k_cache, ctx_len, block, codes, scales, nullptr,
                                              (cudaStream_t)stream),
@@ -205,7 +211,7 @@ sls_status sls_thumb_residual_build(const sls_attn_desc* desc, const void* k_cac
   sls_status r = check_desc(desc, &s);
   if (r) return r;
   if ((r = check_block(s, block))) return r;
-  REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(codes); REQUIRE(scales); REQUIRE(res);
+  REQUIRE16(k_cache); REQUIRE(ctx_len); REQUIRE16(codes); REQUIRE16(scales); REQUIRE16(res);
   sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_thumb_build(s, k_cache, ctx_len, block, codes, scales, res, (cudaStream_t)stream),
                      "sls_thumb_residual_build");
@@ -217,7 +223,7 @@ sls_status sls_thumb_update(const sls_attn_desc* desc, const void* k_cache, cons
   sls_status r = check_desc(desc, &s);
   if (r) return r;
   if ((r = check_block(s, block))) return r;
-  REQUIRE(k_cache); REQUIRE(pos); REQUIRE(codes); REQUIRE(scales);
+  REQUIRE16(k_cache); REQUIRE(pos); REQUIRE16(codes); REQUIRE16(scales);
   sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_thumb_update(s, k_cache, pos, block, codes, scales, nullptr,
                                               (cudaStream_t)stream),
@@ -230,7 +236,7 @@ sls_status sls_thumb_residual_update(const sls_attn_desc* desc, const void* k_ca
   sls_status r = check_desc(desc, &s);
   if (r) return r;
   if ((r = check_block(s, block))) return r;
-  REQUIRE(k_cache); REQUIRE(pos); REQUIRE(codes); REQUIRE(scales); REQUIRE(res);
+  REQUIRE16(k_cache); REQUIRE(pos); REQUIRE16(codes); REQUIRE16(scales); REQUIRE16(res);
   sls::stat_add(sls::kStatMetadata);
   return cuda_status(sls::launch_thumb_update(s, k_cache, pos, block, codes, scales, res, (cudaStream_t)stream),
                      "sls_thumb_residual_update");
@@ -249,7 +255,7 @@ sls_status sls_select_pages(const sls_attn_desc* desc, const void* q, const void
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(q); REQUIRE(kmin); REQUIRE(kmax); REQUIRE(ctx_len); REQUIRE(page_idx);
+  REQUIRE16(q); REQUIRE16(kmin); REQUIRE16(kmax); REQUIRE(ctx_len); REQUIRE(page_idx);
   const int npcap = s.Cap >> s.pshift;
   if (k < 1 || k > npcap) return fail(SLS_EINVAL, "k=%d must be in [1, Cap/P=%d]", k, npcap);
   if (n_sink_pages < 0 || n_local_tokens < 0)
@@ -289,7 +295,7 @@ sls_status sls_select_delta(const sls_attn_desc* desc, const void* q, const void
   sls_status r = check_desc(desc, &s);
   if (r) return r;
   if ((r = check_block(s, block))) return r;
-  REQUIRE(q); REQUIRE(k_cache); REQUIRE(codes); REQUIRE(scales); REQUIRE(ctx_len);
+  REQUIRE16(q); REQUIRE16(k_cache); REQUIRE16(codes); REQUIRE16(scales); REQUIRE(ctx_len);
   REQUIRE(count); REQUIRE(block_idx);
   if (!(delta >= 0.f) || std::isinf(delta)) return fail(SLS_EINVAL, "delta must be finite and >= 0");
   if (idx_stride < s.Cap / block)
@@ -310,8 +316,8 @@ sls_status sls_sparse_decode_attend(const sls_attn_desc* desc, const void* q, co
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(ctx_len);
-  REQUIRE(o_part); REQUIRE(m_part); REQUIRE(l_part);
+  REQUIRE16(q); REQUIRE16(k_cache); REQUIRE16(v_cache); REQUIRE(ctx_len);
+  REQUIRE16(o_part); REQUIRE(m_part); REQUIRE(l_part);
   if (num_splits < 1 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [1, 1024]", num_splits);
   if (page_idx) {
     if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
@@ -350,7 +356,7 @@ sls_status sls_sparse_decode_attend_combine(const sls_attn_desc* desc, const voi
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(ctx_len); REQUIRE(out);
+  REQUIRE16(q); REQUIRE16(k_cache); REQUIRE16(v_cache); REQUIRE(ctx_len); REQUIRE(out);
   if (num_splits < 0 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [0, 1024]", num_splits);
   if (page_idx) {
     if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
@@ -396,7 +402,7 @@ sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const vo
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(block_idx); REQUIRE(count); REQUIRE(ctx_len);
+  REQUIRE16(q); REQUIRE16(k_cache); REQUIRE16(v_cache); REQUIRE(block_idx); REQUIRE(count); REQUIRE(ctx_len);
   REQUIRE(out);
   if ((codes == nullptr) != (res == nullptr) || (codes == nullptr) != (scales == nullptr))
     return fail(SLS_EINVAL, "codes, scales and res: all or none");
@@ -404,10 +410,9 @@ sls_status sls_refined_decode_attend_combine(const sls_attn_desc* desc, const vo
     return fail(SLS_EUNSUPPORTED,
                 "needs bf16, G <= 8, blocks (page_size) of >= 16 tokens and at most 4096 rows (B*Hkv)");
   if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
-       reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(scales) | reinterpret_cast<uintptr_t>(res)) &
-      15)
-    return fail(SLS_EINVAL, "q, the caches, codes, scales and res must be 16-byte aligned");
+  if (codes) {
+    REQUIRE16(codes); REQUIRE16(scales); REQUIRE16(res);
+  }
   const size_t need = sls::refined_workspace(s);
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
@@ -439,7 +444,7 @@ sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(q); REQUIRE(k_cache); REQUIRE(v_cache); REQUIRE(kmin); REQUIRE(kmax); REQUIRE(ctx_len); REQUIRE(out);
+  REQUIRE16(q); REQUIRE16(k_cache); REQUIRE16(v_cache); REQUIRE16(kmin); REQUIRE16(kmax); REQUIRE(ctx_len); REQUIRE(out);
   const int npcap = s.Cap >> s.pshift;
   if (k < 1 || k > npcap) return fail(SLS_EINVAL, "k=%d must be in [1, Cap/P=%d]", k, npcap);
   if (n_sink_pages < 0 || n_local_tokens < 0) return fail(SLS_EINVAL, "n_sink_pages and n_local_tokens must be >= 0");
@@ -508,7 +513,7 @@ sls_status sls_selection_recall(const sls_attn_desc* desc, const void* q, const 
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(q); REQUIRE(k_cache); REQUIRE(ctx_len); REQUIRE(recall);
+  REQUIRE16(q); REQUIRE16(k_cache); REQUIRE(ctx_len); REQUIRE(recall);
   if (page_idx) {
     if (idx_stride < 1) return fail(SLS_EINVAL, "idx_stride %d < 1", idx_stride);
     if (!count && (k_fixed < 0 || k_fixed > idx_stride))
@@ -530,7 +535,7 @@ sls_status sls_combine_splits(const sls_attn_desc* desc, const float* o_part, co
   sls::Shape s;
   sls_status r = check_desc(desc, &s);
   if (r) return r;
-  REQUIRE(o_part); REQUIRE(m_part); REQUIRE(l_part); REQUIRE(out);
+  REQUIRE16(o_part); REQUIRE(m_part); REQUIRE(l_part); REQUIRE(out);
   if (num_splits < 1 || num_splits > 1024) return fail(SLS_EINVAL, "num_splits %d not in [1, 1024]", num_splits);
   return cuda_status(sls::launch_combine(s, o_part, m_part, l_part, num_splits, sink, out, lse, (cudaStream_t)stream),
                      "sls_combine_splits");

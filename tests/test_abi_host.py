@@ -187,6 +187,7 @@ def test_refined_attend_validation(lib):
     assert call(res=None) == L.SLS_EINVAL               # codes, scales and res: all or none
     assert call(stride=0) == L.SLS_EINVAL
     assert call(res=ctypes.c_void_p(0x1008)) == L.SLS_EINVAL  # 16-byte alignment
+    assert call(codes=ctypes.c_void_p(0x1004)) == L.SLS_EINVAL
     assert call(wsb=ws - 1) == L.SLS_EWORKSPACE
     assert call(dd=desc(page_size=64, dtype=L.SLS_DTYPE_F32)) == L.SLS_EUNSUPPORTED
     assert call(dd=desc(page_size=64, num_q_heads=32, num_kv_heads=2)) == L.SLS_EUNSUPPORTED  # G = 16
@@ -203,3 +204,26 @@ def test_stats_counters_without_a_launch(lib):
     rc = lib.sls_get_stats(ctypes.byref(st), 1)
     assert rc in (L.SLS_OK, L.SLS_ECUDA)          # no device here: the row counters cannot be read
     assert st.metadata == 0 and st.quest_step_one_launch == 0
+
+
+def test_misaligned_tensors_are_rejected(lib):
+    """Tensors read in 16-byte vectors must be 16-byte aligned; a misaligned
+    pointer is an argument error, reported before anything launches."""
+    d = desc()
+    M = ctypes.c_void_p(0x1002)   # a bf16 element past an aligned address
+    ws = lib.sls_quest_decode_step_workspace_size(ctypes.byref(d), 8, 0)
+    cases = {
+        "k_cache": lambda: lib.sls_pagemeta_build(ctypes.byref(d), M, BAD, BAD, BAD, None),
+        "kmax": lambda: lib.sls_pagemeta_update(ctypes.byref(d), BAD, BAD, BAD, M, None),
+        "q": lambda: lib.sls_select_pages(ctypes.byref(d), M, BAD, BAD, BAD, 8, 0, 0, BAD, BAD, 1 << 40, None),
+        "v_cache": lambda: lib.sls_sparse_decode_attend(ctypes.byref(d), BAD, BAD, M, BAD, 8, None, 8, BAD, 4,
+                                                        BAD, BAD, BAD, None),
+        "o_part": lambda: lib.sls_combine_splits(ctypes.byref(d), M, BAD, BAD, 4, None, BAD, None, None),
+        "kmin": lambda: lib.sls_quest_decode_step(ctypes.byref(d), BAD, BAD, BAD, M, BAD, BAD, 8, 0, 0, None,
+                                                  None, BAD, None, 0, 0.0, BAD, ws, None),
+        "k_new": lambda: lib.sls_decode_append(ctypes.byref(d), M, BAD, BAD, BAD, None, None, BAD, None, None),
+        "scales": lambda: lib.sls_thumb_build(ctypes.byref(desc(page_size=64)), BAD, BAD, 64, BAD, M, None),
+    }
+    for name, call in cases.items():
+        assert call() == L.SLS_EINVAL, name
+        assert name in err(lib) and "aligned" in err(lib), (name, err(lib))
