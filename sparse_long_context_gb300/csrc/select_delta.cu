@@ -228,31 +228,28 @@ delta_scan_kernel(const DeltaArgs a) {
 // block the tentative scores of all its tokens and heads are one product
 //   S[t][g] = sum_c code[t][c] * w[g][c]  -  1.5 * sum_c w[g][c],
 //   w[g][c] = scale * q[g][c] * s[c] / 2   (the level is (code - 1.5) s / 2),
-// with A = the codes (16 tokens x 16 channels per m16n8k16, exact small
-// integers in fp16) and B = w split into fp16 hi + lo parts (w - hi is
-// exact in fp32), accumulated in fp32: the same scores as the CUDA-core
-// scan to about 2^-22 relative.  Lane (r, m) owns channels
-// [m D/4, (m+1) D/4) (k-step ks: its 4 channels m D/4 + 4 ks .. + 3, one
-// code byte), tokens r and r + 8 of each 16-token tile, head r of B.  A warp
-// takes one block at a time and loads the codes of its next block before
-// scoring the current one.
-
-// The four 2-bit codes of code byte k of word w as two fp16x2 values
-// (channels 0, 1 and 2, 3), each code scaled by 1, 4, 16 and 64: a byte
-// permute puts the byte into both 16-bit halves, and masking keeps bits
-// 0-1 and 2-3 (4-5 and 6-7) in place under the exponent field 0x6400, where
-// the half reads as 1024 + f * code; one subtraction of 1024 leaves f *
-// code (all exact).  The weights carry 64 / f, so every product is 64 times
-// the level's.
-__device__ __forceinline__ void code_quad_h2(uint32_t w, int k, uint32_t& h01, uint32_t& h23) {
-  const uint32_t h = __byte_perm(w, 0u, 0x4040u + 0x0101u * (uint32_t)k);  // [byte k, 0, byte k, 0]
-  const uint32_t u01 = (h & 0x000C0003u) | 0x64006400u;
-  const uint32_t u23 = (h & 0x00C00030u) | 0x64006400u;
-  const __half2 k1024 = __float2half2_rn(1024.f);
-  const __half2 v01 = __hsub2(*reinterpret_cast<const __half2*>(&u01), k1024);
-  const __half2 v23 = __hsub2(*reinterpret_cast<const __half2*>(&u23), k1024);
-  h01 = *reinterpret_cast<const uint32_t*>(&v01);
-  h23 = *reinterpret_cast<const uint32_t*>(&v23);
+// with A = the codes (16 tokens x 16 channels per m16n8k16, exact in fp16)
+// and B = w split into fp16 hi + lo parts (w - hi is exact in fp32),
+// accumulated in fp32: the same scores as the CUDA-core scan to about 2^-22
+// relative.  Lane (r, m) owns channels [m D/4, (m+1) D/4), tokens r and
+// r + 8 of each 16-token tile and head r of B.  A warp takes one block at a
+// time and loads the codes of its next block before scoring the current one.
+//
+// Codes go to the tensor cores as fp16 subnormals, decoded by one AND each:
+// a 32-bit code word holds the 16 codes of 16 consecutive channels (channel
+// i at bits 2i), and the mask 3 << 2j applied to both 16-bit halves keeps
+// the codes of channels j and 8 + j (j < 4) in place, where the half reads
+// as 4^j code 2^-24 (all below 2^-14: subnormal, exact); the word shifted
+// right by 8 gives channels 4 + j and 12 + j the same way.  Register i
+// (0..7) of a word thus pairs channels (i, i + 8) with the factor 4^(i & 3);
+// k-step ks of the lane uses registers 2u and 2u + 1 (u = ks & 3) of word
+// ks >> 2 for the k-slots {2m, 2m + 1} and {8 + 2m, 9 + 2m}.  Any channel
+// order works as long as A and B agree on it: every lane pairs its k-slots
+// with channels by the same rule.  The weights carry 64 / 4^(c & 3), so
+// every product is 64 2^-24 times the level's.
+template <int I>
+__device__ __forceinline__ uint32_t code_pair_sub(uint32_t w, uint32_t w8) {
+  return (I < 4 ? w : w8) & (0x00030003u << (2 * (I & 3)));
 }
 
 __device__ __forceinline__ void mma_f16_d(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -345,20 +342,27 @@ delta_scan_mma_kernel(const DeltaArgs a) {
     // weights of the block: hi/lo fp16 pairs per k-step, and their fp32 sum
     uint32_t whi[KS][2], wlo[KS][2];
     float wsum = 0.f;
+    float wc[CPL];
 #pragma unroll
     for (int v = 0; v < CPL / 8; ++v) {
       float sv[8];
       unpack_vec(cur.sv[v], sv);
 #pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const int c = 8 * v + e;
-        const float w0 = qh[c] * sv[e], w1 = qh[c + 1] * sv[e + 1];
+      for (int e = 0; e < 8; ++e) {
+        wc[8 * v + e] = qh[8 * v + e] * sv[e];
         // the level sum takes the unscaled weights (exact: powers of two)
-        wsum += w0 * (1.f / (64 >> (2 * (e & 3)))) + w1 * (1.f / (64 >> (2 * ((e + 1) & 3))));
+        wsum += wc[8 * v + e] * (1.f / (64 >> (2 * (e & 3))));
+      }
+    }
+#pragma unroll
+    for (int wd = 0; wd < CPL / 16; ++wd) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // register i of word wd: channels (i, i + 8)
+        const float w0 = wc[16 * wd + i], w1 = wc[16 * wd + i + 8];
         const __half2 hi = __floats2half2_rn(w0, w1);
         const __half2 lo = __floats2half2_rn(w0 - __low2float(hi), w1 - __high2float(hi));
-        whi[c / 4][(c / 2) & 1] = *reinterpret_cast<const uint32_t*>(&hi);
-        wlo[c / 4][(c / 2) & 1] = *reinterpret_cast<const uint32_t*>(&lo);
+        whi[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        wlo[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&lo);
       }
     }
     wsum += __shfl_xor_sync(0xffffffffu, wsum, 1);
@@ -371,16 +375,30 @@ delta_scan_mma_kernel(const DeltaArgs a) {
       if (mt >= ntile) break;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        code_quad_h2(cur.c[mt][0][ks >> 2], ks & 3, a0, a2);
-        code_quad_h2(cur.c[mt][1][ks >> 2], ks & 3, a1, a3);
-        mma_f16_d(acc, a0, a1, a2, a3, whi[ks][0], whi[ks][1]);
-        mma_f16_d(acc, a0, a1, a2, a3, wlo[ks][0], wlo[ks][1]);
+      for (int wd = 0; wd < CPL / 16; ++wd) {
+        const uint32_t x = cur.c[mt][0][wd], y = cur.c[mt][1][wd];  // tokens r and r + 8
+        const uint32_t x8 = x >> 8, y8 = y >> 8;
+        mma_f16_d(acc, code_pair_sub<0>(x, x8), code_pair_sub<0>(y, y8), code_pair_sub<1>(x, x8),
+                  code_pair_sub<1>(y, y8), whi[4 * wd][0], whi[4 * wd][1]);
+        mma_f16_d(acc, code_pair_sub<0>(x, x8), code_pair_sub<0>(y, y8), code_pair_sub<1>(x, x8),
+                  code_pair_sub<1>(y, y8), wlo[4 * wd][0], wlo[4 * wd][1]);
+        mma_f16_d(acc, code_pair_sub<2>(x, x8), code_pair_sub<2>(y, y8), code_pair_sub<3>(x, x8),
+                  code_pair_sub<3>(y, y8), whi[4 * wd + 1][0], whi[4 * wd + 1][1]);
+        mma_f16_d(acc, code_pair_sub<2>(x, x8), code_pair_sub<2>(y, y8), code_pair_sub<3>(x, x8),
+                  code_pair_sub<3>(y, y8), wlo[4 * wd + 1][0], wlo[4 * wd + 1][1]);
+        mma_f16_d(acc, code_pair_sub<4>(x, x8), code_pair_sub<4>(y, y8), code_pair_sub<5>(x, x8),
+                  code_pair_sub<5>(y, y8), whi[4 * wd + 2][0], whi[4 * wd + 2][1]);
+        mma_f16_d(acc, code_pair_sub<4>(x, x8), code_pair_sub<4>(y, y8), code_pair_sub<5>(x, x8),
+                  code_pair_sub<5>(y, y8), wlo[4 * wd + 2][0], wlo[4 * wd + 2][1]);
+        mma_f16_d(acc, code_pair_sub<6>(x, x8), code_pair_sub<6>(y, y8), code_pair_sub<7>(x, x8),
+                  code_pair_sub<7>(y, y8), whi[4 * wd + 3][0], whi[4 * wd + 3][1]);
+        mma_f16_d(acc, code_pair_sub<6>(x, x8), code_pair_sub<6>(y, y8), code_pair_sub<7>(x, x8),
+                  code_pair_sub<7>(y, y8), wlo[4 * wd + 3][0], wlo[4 * wd + 3][1]);
       }
-      // acc (64 times the level sums): tokens r (0, 1) and r + 8 (2, 3), heads 2m (0, 2) and 2m + 1 (1, 3)
-      if (hv0) best = fmaxf(best, fmaxf(acc[0], acc[2]) * (1.f / 64.f) + off0);
-      if (hv1) best = fmaxf(best, fmaxf(acc[1], acc[3]) * (1.f / 64.f) + off1);
+      // acc (64 2^-24 times the level sums): tokens r (0, 1) and r + 8 (2, 3), heads 2m (0, 2) and 2m + 1 (1, 3)
+      constexpr float kUnscale = 262144.f;  // 2^24 / 64
+      if (hv0) best = fmaxf(best, fmaxf(acc[0], acc[2]) * kUnscale + off0);
+      if (hv1) best = fmaxf(best, fmaxf(acc[1], acc[3]) * kUnscale + off1);
     }
     best = warp_max(best);
     if (lane == 0) a.flags[(size_t)row * a.nblk_cap + j] = best >= -a.delta ? 1 : 0;
