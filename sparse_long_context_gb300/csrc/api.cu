@@ -97,14 +97,17 @@ sls_status record_error(sls_status code, const char* msg) { return fail(code, "%
 
 namespace {
 
-#define REQUIRE(ptr) \
-  if (!(ptr)) return fail(SLS_EINVAL, "%s is NULL", #ptr)
+#define REQUIRE(ptr)                                     \
+  do {                                                   \
+    if (!(ptr)) return fail(SLS_EINVAL, "%s is NULL", #ptr); \
+  } while (0)
 
 // Tensors the kernels read or write in 16-byte vectors.
-#define REQUIRE16(ptr)                                                         \
-  REQUIRE(ptr);                                                                \
-  if (reinterpret_cast<uintptr_t>(ptr) & 15)                                   \
-  return fail(SLS_EINVAL, "%s is not 16-byte aligned", #ptr)
+#define REQUIRE16(ptr)                                                                      \
+  do {                                                                                      \
+    if (!(ptr)) return fail(SLS_EINVAL, "%s is NULL", #ptr);                                \
+    if (reinterpret_cast<uintptr_t>(ptr) & 15) return fail(SLS_EINVAL, "%s is not 16-byte aligned", #ptr); \
+  } while (0)
 
 }  // namespace
 
