@@ -167,10 +167,14 @@ __device__ __forceinline__ void load_rgroup(RGroup<D>& g, const RefinedArgs& ra,
   }
 }
 
+// wq: the warp's cache of the fp16 hi/lo parts of q s for the block being
+// scored ([step][hi, lo][lane], 32 D bytes), or null.  fresh: compute them
+// from the block's scales (and fill the cache), else read the cache; a warp
+// that scores a block's groups one after the other computes them once.
 template <int D>
 __device__ __forceinline__ void compute_rgroup(const RGroup<D>& g, const RefinedArgs& ra, int row,
                                                const uint32_t (&qa)[D / 32][4], float (&o)[D / 16][4],
-                                               float& m_run, float& l_run) {
+                                               float& m_run, float& l_run, uint4* wq, bool fresh) {
   constexpr int NS = RGroup<D>::NS, MT = D / 16;
   const AttendArgs& a = ra.a;
   const int lane = threadIdx.x & 31, m = lane & 3;
@@ -183,18 +187,29 @@ __device__ __forceinline__ void compute_rgroup(const RGroup<D>& g, const Refined
   if (g.refined) {
     mul = a.qscale * (1.f / 508.f);
     const bf16* sp = ra.scales + ((size_t)row * (a.Cap >> a.pshift) + g.pg) * D + m * (D / 4);
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
-      const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(sp + 8 * s));
       uint32_t hi[4], lo[4];
+      if (fresh) {
+        const uint4 s8 = __ldg(reinterpret_cast<const uint4*>(sp + 8 * s));
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const uint32_t sw = (&s8.x)[p];
-        const float xa = bf16_lo_f(qa[s][p]) * bf16_lo_f(sw);  // exact
-        const float xb = bf16_hi_f(qa[s][p]) * bf16_hi_f(sw);
-        const __half2 h = __floats2half2_rn(xa, xb);
-        hi[p] = h2_bits(h);
-        lo[p] = h2_bits(__floats2half2_rn(xa - __low2float(h), xb - __high2float(h)));
+        for (int p = 0; p < 4; ++p) {
+          const uint32_t sw = (&s8.x)[p];
+          const float xa = bf16_lo_f(qa[s][p]) * bf16_lo_f(sw);  // exact
+          const float xb = bf16_hi_f(qa[s][p]) * bf16_hi_f(sw);
+          const __half2 h = __floats2half2_rn(xa, xb);
+          hi[p] = h2_bits(h);
+          lo[p] = h2_bits(__floats2half2_rn(xa - __low2float(h), xb - __high2float(h)));
+        }
+        if (wq) {
+          wq[(2 * s) * 32 + lane] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          wq[(2 * s + 1) * 32 + lane] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      } else {
+        const uint4 h4 = wq[(2 * s) * 32 + lane], l4 = wq[(2 * s + 1) * 32 + lane];
+        hi[0] = h4.x; hi[1] = h4.y; hi[2] = h4.z; hi[3] = h4.w;
+        lo[0] = l4.x; lo[1] = l4.y; lo[2] = l4.z; lo[3] = l4.w;
       }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -406,18 +421,32 @@ __global__ void __launch_bounds__(kRefWarps * 32, 1) attend_balanced_kernel(cons
     float m_run = kNegInf, l_run = 0.f;
     __syncthreads();
 
-    const int ngroups = (sl.ntok + 15) >> 4;
+    const int ngroups = (sl.ntok + 15) >> 4;  // whole blocks: P / 16 groups each
+    // With codes, a warp takes whole blocks (entries warp, warp + NW, ...)
+    // and scores a block's groups one after the other, so the hi/lo parts of
+    // q s are computed once per block and cached in the warp's slice of sO
+    // (free until the warp's own partial is written there).  Without codes
+    // the warps interleave 16-token groups.
+    const int gpb = a.P >> 4;
+    const bool bmajor = ra.codes != nullptr && gpb > 1;
+    uint4* wq = bmajor ? reinterpret_cast<uint4*>(sO + warp * 8 * D) : nullptr;
+    auto next_group = [&](int g) {
+      return bmajor ? (((g + 1) & (gpb - 1)) ? g + 1 : g + 1 + (NW - 1) * gpb) : g + NW;
+    };
+    auto fresh = [&](int g) { return !bmajor || (g & (gpb - 1)) == 0; };
     RGroup<D> ga, gb;
-    int gi = warp;
+    int gi = bmajor ? warp * gpb : warp;
     if (gi < ngroups) load_rgroup<D>(ga, ra, sl, sh.s_pg, plist, gi, row);
     while (gi < ngroups) {
-      if (gi + NW < ngroups) load_rgroup<D>(gb, ra, sl, sh.s_pg, plist, gi + NW, row);
-      compute_rgroup<D>(ga, ra, row, qa, o, m_run, l_run);
-      gi += NW;
+      int gn = next_group(gi);
+      if (gn < ngroups) load_rgroup<D>(gb, ra, sl, sh.s_pg, plist, gn, row);
+      compute_rgroup<D>(ga, ra, row, qa, o, m_run, l_run, wq, fresh(gi));
+      gi = gn;
       if (gi >= ngroups) break;
-      if (gi + NW < ngroups) load_rgroup<D>(ga, ra, sl, sh.s_pg, plist, gi + NW, row);
-      compute_rgroup<D>(gb, ra, row, qa, o, m_run, l_run);
-      gi += NW;
+      gn = next_group(gi);
+      if (gn < ngroups) load_rgroup<D>(ga, ra, sl, sh.s_pg, plist, gn, row);
+      compute_rgroup<D>(gb, ra, row, qa, o, m_run, l_run, wq, fresh(gi));
+      gi = gn;
     }
 
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);

@@ -246,3 +246,29 @@ def test_refined_other_head_shapes(D, Hq, Hkv, sink):
             o_ref, lse_ref = _refined_oracle(s, host, b, h, orc.pages)
             PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"row {(b, h)}")
             np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], lse_ref, rtol=1e-4, atol=1e-4)
+
+
+@pytest.mark.parametrize("block", [16, 32, 128])
+def test_refined_other_block_sizes(block):
+    """The refined step with thumbnail blocks of 16, 32 and 128 tokens (one,
+    two and eight 16-token groups per block: the attend scores a block's
+    groups in one warp and reuses the block's q s parts) against the oracle's
+    refined attention."""
+    s = W.spec("ffd", batch=2, ctx_len=[block * 45 + 7, block * 20], capacity=block * 46)
+    s.block = s.page_size = block
+    host = W.generate(s)
+    dw, _, step, out, lse = _refined_step(s, host)
+    sel, cnt = step.block_idx.cpu().numpy(), step.count.cpu().numpy()
+    G = s.group
+    checked = 0
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            r = b * s.num_kv_heads + h
+            orc = PT.oracle_row(s, host, b, h)
+            if PT.check_delta_list(int(cnt[r]), sel[r], orc, s.delta):
+                continue
+            o_ref, lse_ref = _refined_oracle(s, host, b, h, orc.pages)
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"block {block} row {(b, h)}")
+            np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], lse_ref, rtol=1e-4, atol=1e-4)
+            checked += 1
+    assert checked >= s.rows // 2
