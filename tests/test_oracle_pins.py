@@ -179,6 +179,22 @@ def test_topk_brute_force(seed):
     assert got == brute_topk(score.tolist(), k, forced)
 
 
+def test_topk_ties_at_the_budget_boundary():
+    """Ties that straddle the budget: among equal scores the lower page index
+    is admitted.  A hand-worked case, then tie-heavy random rows (scores in
+    {0, 1}, budgets below the page count) against the brute force."""
+    assert O.select_topk(np.array([1.0, 2.0, 2.0, 2.0, 0.0]), 2, np.zeros(0, np.int64)).tolist() == [1, 2]
+    assert O.select_topk(np.array([5.0, 1.0, 1.0, 1.0]), 3, np.array([0])).tolist() == [0, 1, 2]
+    for seed in range(40):
+        rng = np.random.default_rng(200 + seed)
+        NP = int(rng.integers(6, 12))
+        score = rng.integers(0, 2, NP).astype(float)
+        forced = sorted(rng.choice(NP, size=int(rng.integers(0, 3)), replace=False).tolist())
+        k = int(rng.integers(len(forced) + 1, NP))
+        got = O.select_topk(score, k, np.array(forced, dtype=np.int64)).tolist()
+        assert got == brute_topk(score.tolist(), k, forced), (seed, score, k, forced)
+
+
 def test_forced_pages():
     assert O.forced_pages(32768, 16, 1, 64).tolist() == [0, 2044, 2045, 2046, 2047]
     assert O.forced_pages(1000, 16, 1, 64).tolist() == [0, 58, 59, 60, 61, 62]
@@ -277,6 +293,23 @@ def test_delta_golden():
     np.testing.assert_allclose(margins, [d["margin_block1"]])
     assert O.delta_select_row(q, K, d["n"], d["block"], 5.0, d["scale"])[0].tolist() == d["kept_delta5"]
     assert O.delta_select_row(q, K, d["n"], d["block"], 2.0, d["scale"])[0].tolist() == d["kept_delta2"]
+
+
+@pytest.mark.parametrize("n", [5, 64, 65, 640, 1000])
+def test_pseudo_max_covers_sink_and_local_blocks(n):
+    """FFD eq. 3: m~ is the max exact score over S_global (block 0) and
+    S_local (the newest block, complete or partial), by explicit loops; a key
+    planted in the newest block, and one in block 0, each set it."""
+    G, D, block = 3, 8, 64
+    q, K = rnd(49, G, D), rnd(50, 1100, D)
+    scale = 1 / math.sqrt(D)
+    last = (n - 1) // block
+    toks = sorted(set(range(0, min(block, n))) | set(range(last * block, n)))
+    for planted in (n - 1, 0):
+        Kp = K.copy()
+        Kp[planted] = 6.0 * q[1] / np.linalg.norm(q[1])
+        want = [max(scale * sum(q[g, c] * Kp[t, c] for c in range(D)) for t in toks) for g in range(G)]
+        np.testing.assert_allclose(O.pseudo_max(q, Kp, n, block, scale), want, rtol=1e-12)
 
 
 @pytest.mark.parametrize("n", [64, 640, 1000, 1024 + 63])
@@ -446,3 +479,52 @@ def test_refined_attention_brute_force():
     # close to exact attention: k~ is within s/1016 of k
     oe, _ = O.sparse_attention_row(q, K, V, blocks, n, block, scale)
     assert np.max(np.abs(o - oe)) < 2e-2
+
+
+# ------------------------------------------------------- input decoding, ties
+
+def test_to_f64_decodes_bf16_bit_patterns():
+    """bf16 is the top half of an IEEE float32: sign, 8 exponent bits, 7
+    mantissa bits.  Patterns worked by hand: 0x3F80 = 1, 0xC040 = -3,
+    0x4049 = 3.140625, 0x0001 = 2^-133 (smallest subnormal), 0x7F7F = the
+    largest finite value (2 - 2^-7) * 2^127, 0xFF80 = -inf; fp32 input
+    passes through unchanged."""
+    bits = np.array([0x3F80, 0xC040, 0x4049, 0x0001, 0x7F7F, 0xFF80, 0x0000, 0x8000], dtype=np.uint16)
+    got = O.to_f64(bits, "bf16")
+    want = [1.0, -3.0, 3.140625, 2.0 ** -133, (2 - 2 ** -7) * 2.0 ** 127, -math.inf, 0.0, -0.0]
+    assert got.dtype == np.float64
+    assert got.tolist() == want
+    assert math.copysign(1.0, got[7]) == -1.0
+    x = np.array([0.1, -2.5, 1e-40], dtype=np.float32)
+    assert O.to_f64(x, "f32").tolist() == [float(v) for v in x]
+
+
+def test_kth_score_is_the_last_admitted_score():
+    """The k-th ranked free page's score is the smallest score among the
+    chosen free pages (brute force over the same tie rule), -inf when every
+    page fits and +inf when the forced pages fill the budget."""
+    for seed in range(8):
+        rng = np.random.default_rng(300 + seed)
+        NP = int(rng.integers(4, 12))
+        score = rng.integers(-3, 4, NP).astype(float)
+        forced = sorted(rng.choice(NP, size=int(rng.integers(0, 3)), replace=False).tolist())
+        k = int(rng.integers(len(forced) + 1, NP))
+        chosen = [p for p in brute_topk(score.tolist(), k, forced) if p not in forced]
+        assert O.kth_score(score, k, np.array(forced, dtype=np.int64)) == min(score[p] for p in chosen)
+    assert O.kth_score(np.zeros(3), 5, np.zeros(0, np.int64)) == -math.inf
+    assert O.kth_score(np.zeros(6), 2, np.array([0, 5])) == math.inf
+
+
+def test_delta_keep_rule_at_the_boundary():
+    """FFD eqs. 1-2 keep a block when s~ - m~ + delta >= 0: a block whose
+    margin is exactly -delta is kept, and one a hair below is not."""
+    G, D, block, n = 2, 16, 64, 64 * 6 + 5
+    q, K = rnd(47, G, D) * 2, rnd(48, n, D)
+    scale = 1 / math.sqrt(D)
+    blocks, margins = O.delta_block_margin(q, K, n, block, scale)
+    i = int(np.argmin(np.abs(margins)))
+    j = int(blocks[i])
+    delta = -float(margins[i])
+    assert j in O.delta_select_row(q, K, n, block, delta, scale)[0].tolist()
+    below = float(np.nextafter(delta, -math.inf))
+    assert j not in O.delta_select_row(q, K, n, block, below, scale)[0].tolist()
