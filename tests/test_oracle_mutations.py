@@ -230,6 +230,35 @@ def _to_f64_low_half(x, dtype):
     return np.asarray(x, dtype=np.float32).astype(np.float64)
 
 
+def _split_empty_as_one(q, K, V, scale, bounds):
+    G, D = q.shape[0], V.shape[1]
+    out = []
+    for a, b in bounds:
+        if b <= a:
+            out.append((np.zeros(G), np.ones(G), np.zeros((G, D))))   # an empty slice as a unit weight at 0
+            continue
+        out.extend(O.split_partials(q, K, V, scale, [(a, b)]))
+    return out
+
+
+def _thumbnails_with_partial(K, n, block):
+    nb = -(-n // block)                                  # the partial block quantised too
+    D = K.shape[1]
+    codes = np.zeros((nb * block, D), dtype=np.uint8)
+    scales = np.zeros((nb, D))
+    for j in range(nb):
+        c, sc = O.thumb_quantize(K[j * block:min((j + 1) * block, n)])
+        codes[j * block:j * block + c.shape[0]] = c
+        scales[j] = sc
+    return codes, scales
+
+
+def _unpack_reversed(packed):
+    T, W = packed.shape
+    p = packed.astype(np.uint32)
+    return np.stack([(p >> (2 * (3 - j))) & 3 for j in range(4)], axis=2).reshape(T, W * 4).astype(np.uint8)
+
+
 MUTATIONS = {
     # name: (oracle attribute, replacement built from the original, pins expected to catch it)
     "sink multiplied by the softmax scale": (
@@ -308,6 +337,17 @@ MUTATIONS = {
         "attention_mass_recall",
         lambda f: lambda q, K, pages, n, P, scale: np.zeros(q.shape[0]) if n == 0 else f(q, K, pages, n, P, scale),
         ["test_recall_bounds_additivity_and_monotonicity"]),
+    "empty split counted as a unit weight": ("split_partials", lambda f: _split_empty_as_one,
+                                             ["test_split_combine_equals_dense"]),
+    "thumbnails of the partial block too": ("thumbnails_row", lambda f: _thumbnails_with_partial,
+                                            ["test_refined_attention_brute_force"]),
+    "codes unpacked high bits first": ("unpack_codes", lambda f: _unpack_reversed,
+                                       ["test_thumbnail_error_bound_and_packing"]),
+    "empty attention gives the mean of nothing": (
+        "softmax_attention",
+        lambda f: lambda q, K, V, scale, sink=None: (np.full((q.shape[0], q.shape[1]), np.nan), np.zeros(q.shape[0]))
+        if K.shape[0] == 0 else f(q, K, V, scale, sink),
+        ["test_empty_attention"]),
     "sparse attention ignores the page list": (
         "sparse_attention_row",
         lambda f: lambda q, K, V, pages, n, P, scale, sink=None: O.softmax_attention(q, K[:n], V[:n], scale, sink),
