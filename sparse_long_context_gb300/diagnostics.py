@@ -8,7 +8,10 @@ For one decode step of a workload this reports, per query head:
 * the relative L2 error of the sparse output against dense attention over
   the whole context (the split-K attend kernel with no page list);
 * for the top-delta workload, top-delta against Quest top-k at the same
-  budget (the mean number of blocks top-delta keeps per row): recall of both.
+  budget (the mean number of blocks top-delta keeps per row): recall of both;
+* needle recall: the share of each row's planted needle pages (blocks) that
+  its list holds (the synthetic queries are built to look for the needles,
+  so this checks the generator as much as the selection).
 
 Usage: ``python -m sparse_long_context_gb300.diagnostics --workload qwen1p5b --batch 4``
 prints one JSON object.  Everything runs on the GPU through the C ABI; the
@@ -33,6 +36,23 @@ def _stats(x: np.ndarray) -> dict:
             "mean": float(x.mean())}
 
 
+def needle_recall(lists: np.ndarray, counts, needles, unit: int, num_kv_heads: int) -> np.ndarray:
+    """Per row r = b * Hkv + h: the fraction of the pages (blocks) of ``unit``
+    tokens holding row r's needle tokens that appear in the row's list
+    (``lists[r, :counts[r]]``, or the whole row when counts is None).  Rows
+    without needles are left out."""
+    out = []
+    for r in range(lists.shape[0]):
+        b, h = divmod(r, num_kv_heads)
+        nd = needles[b][h] if b < len(needles) else None
+        if nd is None or np.asarray(nd).size == 0:
+            continue
+        pages = np.unique(np.asarray(nd, dtype=np.int64) // unit)
+        sel = lists[r] if counts is None else lists[r, :int(counts[r])]
+        out.append(float(np.isin(pages, sel).mean()))
+    return np.asarray(out, np.float64)
+
+
 def quest_quality(dw: H.DeviceWorkload) -> dict:
     """Recall of the Quest selection and the sparse output's error vs dense."""
     s = dw.spec
@@ -45,8 +65,9 @@ def quest_quality(dw: H.DeviceWorkload) -> dict:
     dense = dense.float()
     rel = torch.linalg.vector_norm(out - dense, dim=-1) / torch.linalg.vector_norm(dense, dim=-1).clamp_min(1e-30)
     ops.pipeline_check()
+    nr = needle_recall(step.page_idx.cpu().numpy(), None, dw.host.needles, s.page_size, s.num_kv_heads)
     return {"selector": "quest", "budget_pages": s.k_pages, "recall": _stats(rec.cpu().numpy()),
-            "rel_l2_vs_dense": _stats(rel.cpu().numpy())}
+            "rel_l2_vs_dense": _stats(rel.cpu().numpy()), "needle_recall": _stats(nr) if nr.size else None}
 
 
 def delta_vs_topk(dw: H.DeviceWorkload) -> dict:
@@ -61,11 +82,13 @@ def delta_vs_topk(dw: H.DeviceWorkload) -> dict:
     page_idx = ops.select_pages(dw.desc, dw.q, kmin, kmax, dw.ctx, k, 1, s.block)
     rec_q = ops.selection_recall(dw.desc, dw.q, dw.K, page_idx, dw.ctx)
     ops.pipeline_check()
+    nr = needle_recall(step.block_idx.cpu().numpy(), cnt.cpu().numpy(), dw.host.needles, s.block, s.num_kv_heads)
     nblk = np.array([-(-int(n) // s.block) for n in s.ctx_len for _ in range(s.num_kv_heads)])
     return {"selector": "top-delta", "delta": s.delta,
             "kept_fraction": float(cnt.cpu().numpy().sum() / nblk.sum()),
             "recall_top_delta": _stats(rec_d.cpu().numpy()),
-            "matched_budget_blocks": k, "recall_quest_topk": _stats(rec_q.cpu().numpy())}
+            "matched_budget_blocks": k, "recall_quest_topk": _stats(rec_q.cpu().numpy()),
+            "needle_recall_top_delta": _stats(nr) if nr.size else None}
 
 
 def run(name: str, batch=None, ctx=None) -> dict:

@@ -545,3 +545,5 @@ def test_diagnostics_report_and_bound_beats_random_pages():
     sd = make(SMALL_DELTA["ffd_aligned"])
     d = DG.delta_vs_topk(PT.upload(sd, W.generate(sd)))
     assert 0.0 < d["kept_fraction"] <= 1.0 and 0.0 <= d["recall_top_delta"]["min"] <= 1.0
+    for nr in (q["needle_recall"], d["needle_recall_top_delta"]):
+        assert 0.0 <= nr["min"] <= nr["mean"] <= 1.0

@@ -45,3 +45,29 @@ def test_bf16_rounding_is_nearest_even():
     x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 0.0], dtype=np.float32)
     got = W.bf16_bits_to_f32(W.round_to_bf16_bits(x))
     assert got.tolist() == [1.0, 1.0, 1.0 + 2 ** -6, -2.5, 0.0]
+
+
+def test_planted_pages_are_what_the_tiny_queries_select():
+    """Generator diagnostic: the tiny workload's query is the sum of its
+    three planted pages' keys plus noise, so the oracle's top-8 pages hold
+    all three.  On the outlier workloads the needle recall is reported by
+    the diagnostics module, not asserted."""
+    from oracle import sls_oracle as O
+    from sparse_long_context_gb300 import diagnostics as DG
+    s = W.spec("tiny")
+    host = W.generate(s)
+    G = s.group
+    lists = []
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            q = O.to_f64(host.q[b, h * G:(h + 1) * G], s.dtype)
+            K = O.to_f64(host.K[b, h], s.dtype)
+            pages, _, _ = O.quest_select_row(q, K, int(host.ctx_len[b]), s.page_size, s.k_pages,
+                                             s.n_sink_pages, s.n_local_tokens)
+            lists.append(pages)
+    nr = DG.needle_recall(np.stack(lists), None, host.needles, s.page_size, s.num_kv_heads)
+    assert nr.size == s.rows and np.all(nr == 1.0)
+    # the helper itself: counts bound each row's list, rows without needles are skipped
+    lists = np.array([[3, 9, -1], [0, 1, 2]])
+    needles = [[np.array([48, 49, 150]), None]]
+    np.testing.assert_array_equal(DG.needle_recall(lists, np.array([1, 3]), needles, 16, 2), [0.5])
