@@ -17,6 +17,7 @@ SLS_FLAG_NO_TMA = 2
 
 
 class AttnDesc(ctypes.Structure):
+    """ctypes mirror of sls_attn_desc."""
     _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("capacity", ctypes.c_int32),
@@ -75,6 +76,7 @@ _lib = None
 
 
 class SlsError(RuntimeError):
+    """A non-zero sls_status, with the library's sls_last_error() message."""
     def __init__(self, fn, code, msg):
         super().__init__(f"{fn} failed with status {code}: {msg}")
         self.code = code
@@ -102,11 +104,13 @@ def load(build_if_missing: bool = False):
 
 
 def check(fn_name: str, status: int) -> None:
+    """Raises SlsError when a C call returned a non-zero status."""
     if status != SLS_OK:
         msg = _lib.sls_last_error().decode() if _lib is not None else ""
         raise SlsError(fn_name, status, msg)
 
 
 def call(name: str, *args) -> None:
+    """Calls the named C entry point and raises SlsError on a non-zero status."""
     lib = load()
     check(name, getattr(lib, name)(*args))

@@ -21,6 +21,8 @@ def to_device(arr: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
 
 @dataclasses.dataclass
 class DeviceWorkload:
+    """A workload's tensors on the device with its descriptor and selector
+    metadata (page min/max for Quest, thumbnails for top-delta)."""
     spec: W.Spec
     host: W.Tensors
     K: torch.Tensor
@@ -37,6 +39,8 @@ class DeviceWorkload:
 
 def upload(spec: W.Spec, host: W.Tensors, cuda_cores: bool = False, device="cuda",
            no_tma: bool = False) -> DeviceWorkload:
+    """Copies a generated workload to the device and builds its selector
+    metadata through the library."""
     K = to_device(host.K, spec.dtype, device)
     V = to_device(host.V, spec.dtype, device)
     q = to_device(host.q, spec.dtype, device)
@@ -56,6 +60,7 @@ def upload(spec: W.Spec, host: W.Tensors, cuda_cores: bool = False, device="cuda
 
 
 def make_step(dw: DeviceWorkload, num_splits=None, fused: bool = True, one_launch: bool = True):
+    """The decode step object (QuestDecode or DeltaDecode) for a workload."""
     s = dw.spec
     if s.selector == "quest":
         return ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, num_splits,

@@ -37,6 +37,8 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
 
 def make_desc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, dtype,
               scale: float = 0.0, cuda_cores: bool = False, no_tma: bool = False) -> L.AttnDesc:
+    """Descriptor of one layer's decode shapes (the C ABI's sls_attn_desc); dtype is a torch dtype
+    or an SLS_DTYPE_* code, scale 0 means 1/sqrt(head_dim)."""
     code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     flags = (L.SLS_FLAG_CUDA_CORES if cuda_cores else 0) | (L.SLS_FLAG_NO_TMA if no_tma else 0)
     return L.AttnDesc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, code,
@@ -58,6 +60,7 @@ def pipeline_check() -> None:
 
 def desc_for(k_cache: torch.Tensor, num_q_heads: int, page_size: int, scale: float = 0.0,
              cuda_cores: bool = False) -> L.AttnDesc:
+    """Descriptor read off a [B, Hkv, Cap, D] key cache."""
     B, Hkv, Cap, D = k_cache.shape
     return make_desc(B, num_q_heads, Hkv, D, page_size, Cap, k_cache.dtype, scale, cuda_cores)
 
@@ -70,6 +73,8 @@ def default_splits(desc: L.AttnDesc, max_entries: int) -> int:
 # ----------------------------------------------------------------- metadata
 
 def pagemeta_build(desc: L.AttnDesc, k_cache, ctx_len, kmin=None, kmax=None):
+    """Per-page min and max of the valid keys (sls_pagemeta_build); allocates
+    kmin/kmax [B, Hkv, Cap/P, D] when not given.  Returns (kmin, kmax)."""
     _need(k_cache, "k_cache")
     _need(ctx_len, "ctx_len", torch.int32)
     B, Hkv, Cap, D = k_cache.shape
@@ -84,12 +89,17 @@ def pagemeta_build(desc: L.AttnDesc, k_cache, ctx_len, kmin=None, kmax=None):
 
 
 def pagemeta_update(desc: L.AttnDesc, k_cache, pos, kmin, kmax):
+    """Folds the key at pos[b] of every sequence into its page's min/max
+    (sls_pagemeta_update)."""
     _need(pos, "pos", torch.int32)
     L.call("sls_pagemeta_update", ctypes.byref(desc), _ptr(k_cache), _ptr(pos), _ptr(kmin),
            _ptr(kmax), _stream())
 
 
 def thumb_build(desc: L.AttnDesc, k_cache, ctx_len, block: int, codes=None, scales=None):
+    """2-bit thumbnails of every complete block (sls_thumb_build); allocates
+    codes [B, Hkv, Cap, D/4] u8 and scales [B, Hkv, Cap/block, D] when not given.
+    Returns (codes, scales)."""
     _need(k_cache, "k_cache")
     _need(ctx_len, "ctx_len", torch.int32)
     B, Hkv, Cap, D = k_cache.shape
@@ -105,6 +115,7 @@ def thumb_build(desc: L.AttnDesc, k_cache, ctx_len, block: int, codes=None, scal
 
 
 def thumb_update(desc: L.AttnDesc, k_cache, pos, block: int, codes, scales):
+    """Quantises the block that the key at pos[b] completes (sls_thumb_update)."""
     _need(pos, "pos", torch.int32)
     L.call("sls_thumb_update", ctypes.byref(desc), _ptr(k_cache), _ptr(pos), int(block),
            _ptr(codes), _ptr(scales), _stream())
@@ -123,6 +134,8 @@ def thumb_residual_build(desc: L.AttnDesc, k_cache, ctx_len, block: int, codes=N
 
 
 def thumb_residual_update(desc: L.AttnDesc, k_cache, pos, block: int, codes, scales, res):
+    """Thumbnail and 8-bit residuals of the block that the key at pos[b]
+    completes (sls_thumb_residual_update)."""
     _need(pos, "pos", torch.int32)
     L.call("sls_thumb_residual_update", ctypes.byref(desc), _ptr(k_cache), _ptr(pos), int(block), _ptr(codes),
            _ptr(scales), _ptr(res), _stream())
@@ -131,12 +144,16 @@ def thumb_residual_update(desc: L.AttnDesc, k_cache, pos, block: int, codes, sca
 # ---------------------------------------------------------------- selection
 
 def select_pages_workspace(desc: L.AttnDesc, device="cuda"):
+    """Scratch buffer of select_pages (sls_select_pages_workspace_size bytes)."""
     n = L.load().sls_select_pages_workspace_size(ctypes.byref(desc))
     return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
 
 
 def select_pages(desc: L.AttnDesc, q, kmin, kmax, ctx_len, k: int, n_sink_pages: int = 0,
                  n_local_tokens: int = 0, out=None, workspace=None):
+    """Quest selection (sls_select_pages): per (sequence, KV head) the k pages
+    with the highest min/max bound, forced sink and local pages included,
+    ascending, -1 padded.  Returns page_idx [B*Hkv, k] int32."""
     _need(q, "q")
     rows = desc.batch * desc.num_kv_heads
     out = torch.empty((rows, k), dtype=torch.int32, device=q.device) if out is None else out
@@ -149,12 +166,16 @@ def select_pages(desc: L.AttnDesc, q, kmin, kmax, ctx_len, k: int, n_sink_pages:
 
 
 def select_delta_workspace(desc: L.AttnDesc, block: int, device="cuda"):
+    """Scratch buffer of select_delta (sls_select_delta_workspace_size bytes)."""
     n = L.load().sls_select_delta_workspace_size(ctypes.byref(desc), int(block))
     return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
 
 
 def select_delta(desc: L.AttnDesc, q, k_cache, codes, scales, ctx_len, block: int, delta: float,
                  count=None, block_idx=None, workspace=None):
+    """Top-delta selection (sls_select_delta): the blocks whose thumbnail
+    scores come within delta of the pseudo-max, plus the first and newest
+    block.  Returns (count [B*Hkv], block_idx [B*Hkv, Cap/block])."""
     rows = desc.batch * desc.num_kv_heads
     nblk = desc.capacity // block
     count = torch.empty(rows, dtype=torch.int32, device=q.device) if count is None else count
@@ -170,6 +191,8 @@ def select_delta(desc: L.AttnDesc, q, k_cache, codes, scales, ctx_len, block: in
 # ---------------------------------------------------------------- attention
 
 def partials(desc: L.AttnDesc, num_splits: int, device="cuda"):
+    """Split partials (o [B, Hq, S, D], m and l [B, Hq, S], fp32) for
+    sparse_decode_attend and combine_splits."""
     B, Hq, D = desc.batch, desc.num_q_heads, desc.head_dim
     return (torch.empty((B, Hq, num_splits, D), dtype=torch.float32, device=device),
             torch.empty((B, Hq, num_splits), dtype=torch.float32, device=device),
@@ -250,6 +273,8 @@ def refined_decode_attend_combine(desc: L.AttnDesc, q, k_cache, v_cache, codes, 
 
 
 def combine_splits(desc: L.AttnDesc, parts, sink=None, out=None, lse=None, want_lse: bool = True):
+    """Log-sum-exp merge of the split partials with the optional sink
+    (sls_combine_splits).  Returns (out [B, Hq, D], lse [B, Hq] or None)."""
     o, m, l = parts
     B, Hq, S, D = o.shape
     dtype = torch.bfloat16 if desc.dtype == L.SLS_DTYPE_BF16 else torch.float32
