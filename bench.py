@@ -23,7 +23,6 @@ import argparse
 import dataclasses
 import json
 import math
-import multiprocessing as mp
 import os
 import statistics
 import subprocess
@@ -176,34 +175,44 @@ def aggregate(elapsed_s: float, units: float, world: int):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def _oracle_row_task(args):
-    """Time the oracle's select + sparse attention on one row (inputs and
-    page summaries are prepared outside the timed part)."""
-    spec_kw, b, h, pages_limit = args[:4]
-    min_busy = args[4] if len(args) > 4 else 0.0  # repeat the row until this much CPU time
-    os.environ.setdefault("OMP_NUM_THREADS", "1")
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_oracle(s: W.Spec, host, rows, threads: int, min_busy: float = 0.0, refined: bool = False):
+    """The C++ fp64 oracle's decode step over the listed (b, h) rows of the
+    host workload on `threads` std::threads, each row repeated until it has
+    run `min_busy` seconds (its page summaries or thumbnails are prepared
+    before the timed part).  Returns (GB/s, threads, wall s, bytes,
+    repetitions); wall = the rows' summed busy time / threads."""
     from oracle import sls_oracle as O
-    s = W.spec(**spec_kw)
-    row = W.gen_row(s, b, h)
-    G = s.group
-    q = O.to_f64(row.q, s.dtype)
-    K = O.to_f64(row.K, s.dtype)
-    V = O.to_f64(row.V, s.dtype)
-    n = s.ctx_len[b]
-    if pages_limit:  # a bounded sample: the first pages of the row
-        n = min(n, pages_limit * s.page_size)
-    kmin, kmax = O.page_minmax(K, n, s.page_size)
-    dt, reps = 0.0, 0
-    while reps == 0 or dt < min_busy:
-        t0 = time.perf_counter()
-        score = O.group_score(O.quest_bound(q, kmin, kmax))
-        pages = O.select_topk(score, s.k_pages, O.forced_pages(n, s.page_size, s.n_sink_pages, s.n_local_tokens))
-        O.sparse_attention_row(q, K, V, pages, n, s.page_size, s.scale)
-        dt += time.perf_counter() - t0
-        reps += 1
-    esz = 2
-    nbytes = kmin.shape[0] * 2 * s.head_dim * esz + len(O.pages_to_tokens(pages, n, s.page_size)) * 2 * s.head_dim * esz
-    return dt, nbytes * reps, reps
+    ids = [b * s.num_kv_heads + h for b, h in rows]
+    if s.selector == "quest":
+        *_, busy, nbytes, reps = O.quest_step(host.q, host.K, host.V, host.ctx_len, s.num_q_heads, s.page_size,
+                                              s.k_pages, s.n_sink_pages, s.n_local_tokens, s.scale, host.sink, ids,
+                                              threads=threads, min_busy=min_busy)
+    else:
+        *_, busy, nbytes, reps = O.delta_step(host.q, host.K, host.V, host.ctx_len, s.num_q_heads, s.block,
+                                              s.delta, s.scale, host.sink, ids, refined=refined, threads=threads,
+                                              min_busy=min_busy)
+    wall = busy / max(threads, 1)
+    return nbytes / wall / 1e9, threads, wall, nbytes, reps
 
 
 def parity_check(s: W.Spec, host, sel, out):
@@ -223,55 +232,37 @@ def parity_check(s: W.Spec, host, sel, out):
     return res
 
 
-def cpu_oracle(s: W.Spec, rows, pages_limit=0, cores=None, min_busy=0.0):
-    """Oracle throughput over `rows` on `cores` processes; each row repeats
-    until it has taken `min_busy` seconds.  Returns (GB/s, cores, wall s,
-    bytes, repetitions)."""
-    cores = cores or min(os.cpu_count() or 1, max(len(rows), 1))
-    spec_kw = dict(name=s.name, batch=s.batch, ctx_len=list(s.ctx_len), capacity=s.capacity)
-    tasks = [(spec_kw, b, h, pages_limit, min_busy) for b, h in rows]
-    ctx = mp.get_context("spawn")
-    with ctx.Pool(cores, initializer=_pin_threads) as pool:
-        res = pool.map(_oracle_row_task, tasks)
-    busy = sum(r[0] for r in res)
-    nbytes = sum(r[1] for r in res)
-    wall = busy / cores  # rows run `cores` at a time
-    return nbytes / wall / 1e9, cores, wall, nbytes, sum(r[2] for r in res)
-
-
-def _pin_threads():
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[k] = "1"
-
-
 # ----------------------------------------------------------------- reference
 
 def run_reference(args, s: W.Spec):
-    """The fp64 oracle as the reference arm, on the host cores."""
+    """The C++ fp64 oracle as the reference arm, on one host core."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    # each step: one row of the workload restricted to its first `pl` pages,
-    # sized so that warmup + steps finish within about two minutes
+    # each step: one (b, kv head) row of the workload on one core, its page
+    # summaries (or thumbnails) prepared outside the timed part; rows whose
+    # whole context would take too long are cut to their first `pl` pages so
+    # that warmup + steps finish within about two minutes
     total = args.steps + args.warmup
-    budget = 120.0
-    per_step = budget / max(total, 1)
+    per_step = 90.0 / max(total, 1)
     full_pages = -(-s.ctx_len[0] // s.page_size)
-    est_per_page = 25e-6  # seconds of oracle work per page (bound + top-k + attend share)
-    pl = int(max(s.k_pages + 8, min(full_pages, per_step / est_per_page)))
-    rows = [(i % s.batch, (i // s.batch) % s.num_kv_heads) for i in range(total)]
-    cores = 1
-    spec_kw = dict(name=s.name, batch=s.batch, ctx_len=list(s.ctx_len), capacity=s.capacity)
-    _pin_threads()
+    est_per_page = 2e-6 if s.selector == "quest" else 40e-6  # seconds per page or block (prep + step)
+    pl = int(min(full_pages, max(s.k_pages + 8, per_step / est_per_page)))
+    n_cut = min(s.ctx_len[0], pl * s.page_size)
+    host = W.generate(s, rows=[(i % s.batch, (i // s.batch) % s.num_kv_heads) for i in range(min(total, s.rows))])
+    host.ctx_len = np.minimum(host.ctx_len, n_cut).astype(np.int32)
     times, nbytes = [], []
-    for i, (b, h) in enumerate(rows):
-        dt, nb, _ = _oracle_row_task((spec_kw, b, h, pl))
+    for i in range(total):
+        r = i % min(total, s.rows)
+        b, h = r % s.batch, (r // s.batch) % s.num_kv_heads
+        _, _, wall, nb, _ = cpu_oracle(s, host, [(b, h)], threads=1)
         if i >= args.warmup:
-            times.append(dt)
+            times.append(wall)
             nbytes.append(nb)
     t = sum(times)
     value = sum(nbytes) / t / 1e9
-    sample = f"one (b, kv head) row per step, first {pl} of {full_pages} pages, fp64 numpy"
+    sample = (f"one (b, kv head) row per step, first {pl} of {full_pages} pages, fp64 C++ oracle, "
+              f"1 thread on {cpu_model()} ({os.cpu_count()} cores)")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -279,7 +270,7 @@ def run_reference(args, s: W.Spec):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": _workload_name(s), "batch": s.batch, "ctx_len": s.ctx_len[0],
                    "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -600,14 +591,15 @@ def run_ours(args, s: W.Spec):
     if world == 1 and not args.no_cpu_baseline:
         line["parity"] = parity_check(s, host, first_sel, first_out)
         rows = [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
-        ncore = min(os.cpu_count() or 1, 16)
+        ncore = os.cpu_count() or 1
         take = rows[:max(ncore, 1) * 4]
         # about 16 core-seconds: each row repeats until it has run 0.25 s
-        gbs, cores, wall, nb, reps = cpu_oracle(s, take, cores=ncore, min_busy=0.25)
+        gbs, cores, wall, nb, reps = cpu_oracle(s, host, take, threads=ncore, min_busy=0.25)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                "sample": f"{len(take)} of {s.rows} rows of one step (full rows), "
-                                          f"{reps} row evaluations, {nb / 1e6:.0f} MB in {wall:.1f} s "
-                                          f"on {cores} cores ({wall * cores:.0f} core-s)"}
+                                "cpu": cpu_model(),
+                                "sample": f"{len(take)} of {s.rows} rows of one step (full rows), fp64 C++ oracle "
+                                          f"on {cores} std::threads, {reps} row evaluations, {nb / 1e6:.0f} MB "
+                                          f"in {wall:.1f} s ({wall * cores:.0f} core-s)"}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

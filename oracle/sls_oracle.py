@@ -1,468 +1,425 @@
-"""fp64 CPU oracle for sparse decode attention (select + attend).
+"""The fp64 CPU oracle: Python binding of the plain C++ oracle.
 
-TEST INFRASTRUCTURE ONLY.  Nothing in the library imports, links or calls this
-module; only the test suite, the smoke check and the benchmark's CPU-baseline
-leg do.  It shares no code with the CUDA path: it decodes bf16 itself, builds
-its own page summaries and thumbnails from the keys, and indexes the cache
-layout itself.  Everything is computed in float64 from the exact values of
-the bf16/fp32 inputs.
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()``
+and the benchmark's CPU-baseline leg import this module; the library never
+does.  Every computation happens in ``sls_oracle.cpp`` (C++17, double
+precision, plain loops over the pages' definitions; the sources and readings
+are cited there, function by function).  This module only marshals numpy
+arrays into pointers and sizes and the results back into arrays, with the
+same function names and signatures as the numpy implementation in
+``numpy_oracle.py`` (a second oracle, cross-checked against this one).
 
-Sources (web pages; cited by title and section):
-
-* [haystack]  "Don't read the haystack" (hareesh.pages.dev), Part one
-  (two-stage flash-decoding) and Part two (per-page min/max bound, top-k,
-  sink page and local pages).
-* [ffd]       "Faster Than Flash: Exploiting Attention Sparsity for Efficient
-  Long-Context Decoding" (picx.dev summary), Methodology 1 (2-bit mid-rise
-  thumbnails and 8-bit residuals), 2 (top-delta, eqs. 1-3) and 3 (eq. 4:
-  scaling and the refined final scores).
-* [undivided] "Attention: Undivided & Uncompressed" (clintsebastian.com),
-  Notation (S = QK^T / sqrt(d)) and Traffic (online softmax, delayed division).
-* [tsd]       "Training-free sparse attention for long-context LLM decode"
-  (joeddav/triton-sparse-decode), section 1 (sink as a virtual key, V=0).
-* [mlxcel]    "perf(core): fused sparse-attention decode via page
-  indirection" (lablup/mlxcel #1005), "The reduction" (contiguous cache as a
-  page_size=1 pool) and "Corrected premise 1" (one page list per KV head).
-
-Readings where the pages are silent are listed in the functions that take
-them.  Parity status: every function here is pinned by tests under
-``tests/test_oracle_*.py`` (brute force, closed forms, invariants, hand-worked
-fixtures); none is "parity unpinned".
+``Oracle(path)`` binds any build of the source (the mutation check binds
+planted-mistake builds); the module-level functions are bound to the
+default build, ``oracle/libslsoracle.so``, which is compiled from the source
+on first import when it is missing or older than the source.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 from typing import Optional
 
 import numpy as np
 
+from . import build_oracle
+
 NEG_INF = -math.inf
-
-
-# ----------------------------------------------------------------------------
-# input decoding
-# ----------------------------------------------------------------------------
-
-def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Exact float64 value of an fp32 array or of bf16 bit patterns (uint16)."""
-    if dtype == "bf16":
-        bits = np.asarray(x, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-        return bits.view(np.float32).astype(np.float64)
-    return np.asarray(x, dtype=np.float32).astype(np.float64)
-
-
-# ----------------------------------------------------------------------------
-# attention: the plain definitions
-# ----------------------------------------------------------------------------
-
-def softmax_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float,
-                      sink: Optional[np.ndarray] = None):
-    """Exact softmax attention of G query rows over T keys.
-
-    [undivided] Notation: scores S = q K^T * scale (scale = 1/sqrt(d)), P is
-    the row softmax of S, O = P V.  [tsd] section 1: a learned per-head sink is
-    a scalar logit that joins only the softmax denominator, i.e. a virtual key
-    whose value is zero.  Reading: the sink is a raw logit (not multiplied by
-    ``scale``).
-
-    q [G, D], K [T, D], V [T, D] float64; sink [G] or None.
-    Returns (o [G, D], lse [G]).  With T = 0 the output is 0 and the lse is
-    the sink (or -inf without one).
-    """
-    q = np.asarray(q, np.float64)
-    G = q.shape[0]
-    D = V.shape[1] if V.ndim == 2 else q.shape[1]
-    T = K.shape[0]
-    x = scale * (q @ K.T) if T else np.zeros((G, 0))
-    m = x.max(axis=1) if T else np.full(G, NEG_INF)
-    if sink is not None:
-        m = np.maximum(m, np.asarray(sink, np.float64))
-    o = np.zeros((G, D))
-    lse = np.full(G, NEG_INF)
-    for g in range(G):
-        if m[g] == NEG_INF:
-            continue
-        w = np.exp(x[g] - m[g])
-        z = w.sum()
-        if sink is not None:
-            z += math.exp(float(sink[g]) - m[g])
-        if T:
-            o[g] = (w @ V) / z
-        lse[g] = m[g] + math.log(z)
-    return o, lse
-
-
-def split_partials(q, K, V, scale, bounds):
-    """Stage one of two-stage flash-decoding ([haystack] Part one): for each
-    slice [a, b) of the keys, the slice max m, the normaliser l = sum
-    exp(x - m) and the unnormalised accumulator acc = sum exp(x - m) v.
-    Empty slices give m = -inf, l = 0, acc = 0."""
-    G, D = q.shape[0], V.shape[1]
-    out = []
-    for a, b in bounds:
-        if b <= a:
-            out.append((np.full(G, NEG_INF), np.zeros(G), np.zeros((G, D))))
-            continue
-        x = scale * (q @ K[a:b].T)
-        m = x.max(axis=1)
-        w = np.exp(x - m[:, None])
-        out.append((m, w.sum(axis=1), w @ V[a:b]))
-    return out
-
-
-def combine_partials(parts, sink=None):
-    """Stage two ([haystack] Part one; [undivided] Traffic): rescale every
-    partial by exp(m_s - M) with M the overall max (including the sink), sum,
-    and divide once at the end.  The sink joins the denominator only, once.
-    Returns (o [G, D], lse [G])."""
-    G, D = parts[0][2].shape
-    M = np.full(G, NEG_INF)
-    for m, _, _ in parts:
-        M = np.maximum(M, m)
-    if sink is not None:
-        M = np.maximum(M, np.asarray(sink, np.float64))
-    o = np.zeros((G, D))
-    lse = np.full(G, NEG_INF)
-    for g in range(G):
-        if M[g] == NEG_INF:
-            continue
-        L, acc = 0.0, np.zeros(D)
-        for m, l, a in parts:
-            if m[g] == NEG_INF:
-                continue
-            f = math.exp(m[g] - M[g])
-            L += l[g] * f
-            acc += a[g] * f
-        if sink is not None:
-            L += math.exp(float(sink[g]) - M[g])
-        o[g] = acc / L
-        lse[g] = M[g] + math.log(L)
-    return o, lse
-
-
-# ----------------------------------------------------------------------------
-# Quest page selection
-# ----------------------------------------------------------------------------
-
-def num_pages(n: int, page_size: int) -> int:
-    return -(-int(n) // int(page_size))
-
-
-def page_minmax(K: np.ndarray, n: int, page_size: int):
-    """Per-page, per-channel min and max of the keys of one (b, kv head) row
-    ([haystack] Part two: "the elementwise min and max of its keys").  Only
-    positions < n count, so a partial last page summarises its valid tokens.
-    K [Cap, D] float64.  Returns (kmin, kmax), each [NP, D]."""
-    NP = num_pages(n, page_size)
-    D = K.shape[1]
-    kmin = np.empty((NP, D))
-    kmax = np.empty((NP, D))
-    for p in range(NP):
-        blk = K[p * page_size:min((p + 1) * page_size, n)]
-        kmin[p] = blk.min(axis=0)
-        kmax[p] = blk.max(axis=0)
-    return kmin, kmax
-
-
-def quest_bound(q: np.ndarray, kmin: np.ndarray, kmax: np.ndarray, chunk: int = 4096):
-    """Upper bound of every page's attention score for every query head
-    ([haystack] Part two): U[g, p] = sum_c max(q[g,c] * kmin[p,c],
-    q[g,c] * kmax[p,c]).  Unscaled (ranking is invariant to the positive
-    softmax scale).  q [G, D]; kmin, kmax [NP, D].  Returns U [G, NP]."""
-    G = q.shape[0]
-    NP = kmin.shape[0]
-    U = np.empty((G, NP))
-    for a in range(0, NP, chunk):
-        lo = q[:, None, :] * kmin[None, a:a + chunk, :]
-        hi = q[:, None, :] * kmax[None, a:a + chunk, :]
-        U[:, a:a + chunk] = np.maximum(lo, hi).sum(axis=2)
-    return U
-
-
-def group_score(U: np.ndarray) -> np.ndarray:
-    """One page list per (batch, KV head), shared by the query heads of the
-    group ([mlxcel] "Corrected premise 1": a request shares one page list
-    across the query heads under its KV head).  Reading: the group's score of
-    a page is the max over its heads, which keeps the bound admissible for
-    every head."""
-    return U.max(axis=0)
-
-
-def forced_pages(n: int, page_size: int, n_sink_pages: int, n_local_tokens: int) -> np.ndarray:
-    """Pages kept regardless of score ([haystack] Part two: "plus the
-    attention-sink page and the last few local pages"): the first
-    ``n_sink_pages`` pages and every page holding one of the last
-    ``n_local_tokens`` positions.  Sorted ascending."""
-    NP = num_pages(n, page_size)
-    f = set(range(min(n_sink_pages, NP)))
-    if n_local_tokens > 0 and n > 0:
-        first = max(n - n_local_tokens, 0) // page_size
-        f.update(range(first, NP))
-    return np.array(sorted(f), dtype=np.int64)
-
-
-def select_topk(score: np.ndarray, k: int, forced: np.ndarray) -> np.ndarray:
-    """Top-k selection with forced pages ([haystack] Part two: rank pages by
-    the bound, keep the top k plus the forced pages).
-
-    Readings: the budget k counts the forced pages (the page list has a fixed
-    cardinality of min(k, NP)); among equal scores the lower page index wins;
-    the result is sorted ascending.  score [NP].  Returns page indices."""
-    NP = score.shape[0]
-    if NP <= k:
-        return np.arange(NP, dtype=np.int64)
-    forced = np.asarray(forced, dtype=np.int64)
-    if forced.size > k:
-        raise ValueError("budget smaller than the forced pages")
-    cand = np.setdiff1d(np.arange(NP), forced)
-    kk = k - forced.size
-    order = np.lexsort((cand, -score[cand]))   # by score desc, then index asc
-    chosen = cand[order[:kk]]
-    return np.sort(np.concatenate([forced, chosen]))
-
-
-def kth_score(score: np.ndarray, k: int, forced: np.ndarray) -> float:
-    """Score of the last candidate admitted by ``select_topk`` (the k-th
-    ranked non-forced page), used to recognise boundary ties."""
-    NP = score.shape[0]
-    if NP <= k:
-        return NEG_INF
-    cand = np.setdiff1d(np.arange(NP), np.asarray(forced, dtype=np.int64))
-    kk = k - len(forced)
-    if kk <= 0:
-        return math.inf
-    order = np.lexsort((cand, -score[cand]))
-    return float(score[cand[order[kk - 1]]])
-
-
-def pages_to_tokens(pages: np.ndarray, n: int, page_size: int) -> np.ndarray:
-    """Token positions of the given pages, restricted to positions < n
-    ([mlxcel] "The reduction": a token is reached as page * page_size + i)."""
-    toks = [np.arange(p * page_size, min((p + 1) * page_size, n)) for p in pages if p >= 0]
-    return np.concatenate(toks) if toks else np.zeros(0, dtype=np.int64)
-
-
-def quest_select_row(q, K, n, page_size, k, n_sink_pages, n_local_tokens):
-    """Selection of one row: page summaries -> bound -> group max -> top-k.
-    q [G, D], K [Cap, D] float64.  Returns (pages, group_score, kth)."""
-    if page_size == 1:
-        # A one-token page has kmin = kmax = k_t; the bound is then the exact
-        # score q . k_t.
-        kmin = kmax = K[:n]
-    else:
-        kmin, kmax = page_minmax(K, n, page_size)
-    s = group_score(quest_bound(q, kmin, kmax))
-    f = forced_pages(n, page_size, n_sink_pages, n_local_tokens)
-    return select_topk(s, k, f), s, kth_score(s, k, f)
-
-
-# ----------------------------------------------------------------------------
-# FFD thumbnails and top-delta
-# ----------------------------------------------------------------------------
-
-def thumb_quantize(Kb: np.ndarray):
-    """2-bit symmetric zero-free (mid-rise) thumbnail of one block of keys
-    ([ffd] Methodology 1).  s[c] = max_t |k[t,c]|; levels -0.75s, -0.25s,
-    +0.25s, +0.75s with decision thresholds -s/2, 0, +s/2.
-
-    Readings: a value on a threshold takes the upper level (k = 0 maps to
-    +0.25s, k = s/2 to +0.75s; an all-zero channel, s = 0, takes code 3,
-    whose level is 0); codes 0..3 name the levels in increasing order.  Kb [T, D] float64.  Returns (codes [T, D] uint8, s [D])."""
-    s = np.abs(Kb).max(axis=0)
-    h = s / 2.0
-    codes = np.where(Kb >= h, 3, np.where(Kb >= 0, 2, np.where(Kb >= -h, 1, 0)))
-    return codes.astype(np.uint8), s
-
-
-def thumb_dequant(codes: np.ndarray, s: np.ndarray) -> np.ndarray:
-    """Level value of each code: (code - 1.5) * s / 2."""
-    return (codes.astype(np.float64) - 1.5) * (s / 2.0)
-
-
-def pack_codes(codes: np.ndarray) -> np.ndarray:
-    """Storage format of the thumbnails: four 2-bit codes per byte, channel c
-    in bits 2*(c % 4) of byte c // 4.  codes [T, D] -> [T, D/4] uint8."""
-    T, D = codes.shape
-    c = codes.reshape(T, D // 4, 4).astype(np.uint32)
-    b = c[:, :, 0] | (c[:, :, 1] << 2) | (c[:, :, 2] << 4) | (c[:, :, 3] << 6)
-    return b.astype(np.uint8)
-
-
-def unpack_codes(packed: np.ndarray) -> np.ndarray:
-    T, W = packed.shape
-    p = packed.astype(np.uint32)
-    out = np.stack([(p >> (2 * j)) & 3 for j in range(4)], axis=2)
-    return out.reshape(T, W * 4).astype(np.uint8)
-
-
-def thumbnails_row(K: np.ndarray, n: int, block: int):
-    """Thumbnails of every complete block of one row (positions < n).
-    Returns (codes [nfull*block, D] uint8 unpacked, scales [nfull, D])."""
-    nfull = n // block
-    D = K.shape[1]
-    codes = np.zeros((nfull * block, D), dtype=np.uint8)
-    scales = np.zeros((nfull, D))
-    for j in range(nfull):
-        c, s = thumb_quantize(K[j * block:(j + 1) * block])
-        codes[j * block:(j + 1) * block] = c
-        scales[j] = s
-    return codes, scales
-
-
-def delta_forced_blocks(n: int, block: int) -> np.ndarray:
-    """Blocks always kept by top-delta: block 0 (the sink tokens, S_global)
-    and the block of the newest position (S_local, possibly partial).
-
-    Reading: [ffd] eq. 3 names S_global and S_local without sizes; here they
-    are the first and the last block."""
-    if n <= 0:
-        return np.zeros(0, dtype=np.int64)
-    last = (n - 1) // block
-    return np.array(sorted({0, last}), dtype=np.int64)
-
-
-def pseudo_max(q: np.ndarray, K: np.ndarray, n: int, block: int, scale: float) -> np.ndarray:
-    """[ffd] eq. 3: m~ = max of the exact scores s = scale * q . k over the
-    sink and local tokens (blocks returned by ``delta_forced_blocks``).
-    q [G, D], K [Cap, D].  Returns m~ [G]."""
-    toks = pages_to_tokens(delta_forced_blocks(n, block), n, block)
-    return (scale * (q @ K[toks].T)).max(axis=1)
-
-
-def delta_block_margin(q, K, n, block, scale):
-    """For every complete, non-forced block b of the row: the block margin
-    max_g max_{t in b} (s~[g,t] - m~[g]) where s~ = scale * q . k^ uses the
-    2-bit thumbnail k^ ([ffd] Methodology 2, eq. 1 with the pseudo-max of
-    eq. 3 in place of m; eq. 4 fixes the 1/sqrt(d) scaling).
-
-    Readings: a block's score is the max over its tokens; a GQA group keeps
-    the union over its heads (max over g).  Returns (blocks, margin)."""
-    nfull = n // block
-    forced = set(delta_forced_blocks(n, block).tolist())
-    mt = pseudo_max(q, K, n, block, scale)
-    blocks, margins = [], []
-    for j in range(nfull):
-        if j in forced:
-            continue
-        c, s = thumb_quantize(K[j * block:(j + 1) * block])
-        st = scale * (q @ thumb_dequant(c, s).T)      # [G, block]
-        blocks.append(j)
-        margins.append(float((st - mt[:, None]).max()))
-    return np.array(blocks, dtype=np.int64), np.array(margins)
-
-
-def delta_select_row(q, K, n, block, delta, scale):
-    """Top-delta selection of one row ([ffd] eqs. 1-3): keep a complete block
-    when its margin is >= -delta; the forced blocks are always kept.
-    Returns (sorted kept blocks, (scanned blocks, margins))."""
-    blocks, margins = delta_block_margin(q, K, n, block, scale)
-    kept = blocks[margins >= -delta]
-    sel = np.union1d(delta_forced_blocks(n, block), kept)
-    return sel.astype(np.int64), (blocks, margins)
-
-
-# ----------------------------------------------------------------------------
-# FFD 8-bit residuals and the refined scores (eq. 4)
-# ----------------------------------------------------------------------------
-
-RES_DENOM = 508.0  # 4 * 127: residual codes -127..127 span the +-s/4 quantisation error
-
-
-def residual_quantize(Kb: np.ndarray, codes: np.ndarray, s: np.ndarray) -> np.ndarray:
-    """8-bit residual of one complete block ([ffd] Methodology 1: the key is
-    split into the 2-bit thumbnail k_quant and an 8-bit residual k_res that
-    recovers the precision the thumbnail drops).
-
-    Readings (the page gives no encoding): the residual e = k - k^ of a
-    mid-rise 2-bit code lies in [-s/4, s/4] (levels s/2 apart, thresholds
-    half-way), so it is stored on the thumbnail's own block/channel scale s
-    as r = round(e * 508 / s) in [-127, 127], and the refined key is
-    k~ = k^ + r * s / 508.  The integer is decided in float32, the kernel's
-    precision: e = f32(k - k^), x = f32(f32(e * 508) / s), r = rint(x) (ties
-    to even), clamped to [-127, 127]; s = 0 (an all-zero channel) gives 0.
-    k^ is exact in float32 (a bf16 scale times +-0.25 or +-0.75).
-
-    Kb [T, D] float64 (exact bf16 values); codes [T, D]; s [D].
-    Returns r [T, D] int8."""
-    k32 = np.asarray(Kb, np.float64).astype(np.float32)
-    kh32 = thumb_dequant(codes, s).astype(np.float32)
-    e = k32 - kh32                                   # float32 arithmetic
-    x = e * np.float32(RES_DENOM)
-    s32 = np.broadcast_to(np.asarray(s, np.float64).astype(np.float32), x.shape)
-    safe = np.where(s32 > 0, s32, np.float32(1.0))
-    x = np.where(s32 > 0, x / safe, np.float32(0.0)).astype(np.float32)
-    return np.clip(np.rint(x), -127, 127).astype(np.int8)
-
-
-def refined_keys(codes: np.ndarray, s: np.ndarray, r: np.ndarray) -> np.ndarray:
-    """The key the refinement scores with: k~ = k^ + r * s / 508, so that
-    q . k~ = q . k_quant + q . k_res ([ffd] eq. 4 numerator).  float64."""
-    return thumb_dequant(codes, s) + np.asarray(r, np.float64) * (np.asarray(s, np.float64) / RES_DENOM)
-
-
-def residuals_row(K: np.ndarray, n: int, block: int):
-    """Codes, scales and residuals of every complete block of one row
-    (positions < n).  Returns (codes [nfull*block, D], scales [nfull, D],
-    res [nfull*block, D] int8)."""
-    codes, scales = thumbnails_row(K, n, block)
-    res = np.zeros(codes.shape, dtype=np.int8)
-    for j in range(n // block):
-        rows = slice(j * block, (j + 1) * block)
-        res[rows] = residual_quantize(K[rows], codes[rows], scales[j])
-    return codes, scales, res
-
-
-def refined_attention_row(q, K, V, blocks, n, block, scale, sink=None):
-    """Attention over the selected blocks with the refined final scores of
-    [ffd] Methodology 3 step 3, eq. 4: s = (q . k_quant + q . k_res) / sqrt(d)
-    for the tokens of complete blocks.
-
-    Reading: the newest block is partial and has no thumbnail yet, so its
-    tokens are scored with the exact key; values are exact.
-    q [G, D]; K, V [>= n, D] float64; blocks: the row's block list."""
-    codes, scales, res = residuals_row(K, n, block)
-    Kt = np.array(K[:n], dtype=np.float64, copy=True)
-    nfull = n // block
-    if nfull:
-        Kt[:nfull * block] = refined_keys(codes, np.repeat(scales, block, axis=0), res)
-    toks = pages_to_tokens(np.asarray(blocks), n, block)
-    return softmax_attention(q, Kt[toks], V[toks], scale, sink)
-
-
-# ----------------------------------------------------------------------------
-# selection quality
-# ----------------------------------------------------------------------------
-
-def attention_mass_recall(q: np.ndarray, K: np.ndarray, pages, n: int, page_size: int,
-                          scale: float) -> np.ndarray:
-    """Share of each query head's full-context softmax mass that falls on the
-    tokens of the selected pages ([haystack] Part three, "attention mass
-    captured": how much of the true attention mass the selected pages hold).
-
-    q [G, D]; K [>= n, D] float64; pages: the row's page list (-1 entries and
-    positions >= n ignored).  recall_g = sum_{t in sel} exp(x_gt - M_g) /
-    sum_{t < n} exp(x_gt - M_g) with x = scale * q.k and M the row max.
-    Reading: the sink (a virtual key) is not a token and takes no part; an
-    empty context misses nothing, so its recall is 1.
-    Returns [G].
-    """
-    q = np.asarray(q, np.float64)
-    G = q.shape[0]
-    if n == 0:
-        return np.ones(G)
-    x = scale * (q @ K[:n].T)
-    m = x.max(axis=1, keepdims=True)
-    w = np.exp(x - m)
-    toks = pages_to_tokens(np.asarray(pages), n, page_size)
-    return w[:, toks].sum(axis=1) / w.sum(axis=1)
-
-
-# ----------------------------------------------------------------------------
-# one decode step of one row
-# ----------------------------------------------------------------------------
-
-def sparse_attention_row(q, K, V, pages, n, page_size, scale, sink=None):
-    """Attention restricted to the tokens of the selected pages
-    ([haystack] Part two: the sparse twin walks the selected indices)."""
-    toks = pages_to_tokens(np.asarray(pages), n, page_size)
-    return softmax_attention(q, K[toks], V[toks], scale, sink)
+RES_DENOM = 508.0
+
+_c_i64 = ctypes.c_longlong
+_c_int = ctypes.c_int
+_c_dbl = ctypes.c_double
+_vp = ctypes.c_void_p
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _i64(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int64).reshape(-1))
+
+
+def _u8(x) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.uint8)
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(_vp)
+
+
+def _mat(x) -> np.ndarray:
+    """A 2-D float64 array (a [0, D] array stays 2-D)."""
+    a = _f64(x)
+    return a.reshape(1, -1) if a.ndim == 1 else a
+
+
+class Oracle:
+    """One build of the C++ oracle, with the oracle's functions as methods."""
+
+    _SIGS = {
+        "orc_bf16_to_f64": (None, [_vp, _c_i64, _vp]),
+        "orc_f32_to_f64": (None, [_vp, _c_i64, _vp]),
+        "orc_softmax_attention": (None, [_vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_int, _c_dbl, _vp, _vp, _vp]),
+        "orc_split_partials": (None, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _c_dbl, _vp, _c_int, _vp, _vp, _vp]),
+        "orc_combine_partials": (None, [_c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp]),
+        "orc_num_pages": (_c_i64, [_c_i64, _c_i64]),
+        "orc_page_minmax": (None, [_vp, _c_int, _c_i64, _c_int, _vp, _vp]),
+        "orc_quest_bound": (None, [_vp, _c_int, _c_int, _vp, _vp, _c_i64, _vp]),
+        "orc_group_score": (None, [_vp, _c_int, _c_i64, _vp]),
+        "orc_forced_pages": (_c_i64, [_c_i64, _c_int, _c_int, _c_int, _vp]),
+        "orc_select_topk": (_c_i64, [_vp, _c_i64, _c_i64, _vp, _c_i64, _vp]),
+        "orc_kth_score": (_c_dbl, [_vp, _c_i64, _c_i64, _vp, _c_i64]),
+        "orc_pages_to_tokens": (_c_i64, [_vp, _c_i64, _c_i64, _c_int, _vp]),
+        "orc_quest_select_row": (_c_i64, [_vp, _c_int, _c_int, _vp, _c_i64, _c_int, _c_i64, _c_int, _c_int,
+                                          _vp, _vp, _vp]),
+        "orc_thumb_quantize": (None, [_vp, _c_int, _c_int, _vp, _vp]),
+        "orc_thumb_dequant": (None, [_vp, _vp, _c_int, _c_int, _c_int, _vp]),
+        "orc_pack_codes": (None, [_vp, _c_int, _c_int, _vp]),
+        "orc_unpack_codes": (None, [_vp, _c_int, _c_int, _vp]),
+        "orc_thumbnails_row": (None, [_vp, _c_int, _c_i64, _c_int, _vp, _vp]),
+        "orc_delta_forced_blocks": (_c_i64, [_c_i64, _c_int, _vp]),
+        "orc_pseudo_max": (None, [_vp, _c_int, _c_int, _vp, _c_i64, _c_int, _c_dbl, _vp]),
+        "orc_delta_block_margin": (_c_i64, [_vp, _c_int, _c_int, _vp, _c_i64, _c_int, _c_dbl, _vp, _vp]),
+        "orc_delta_select_row": (_c_i64, [_vp, _c_int, _c_int, _vp, _c_i64, _c_int, _c_dbl, _c_dbl, _vp, _vp,
+                                          _vp, _vp]),
+        "orc_residual_quantize": (None, [_vp, _vp, _vp, _c_int, _c_int, _vp]),
+        "orc_refined_keys": (None, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp]),
+        "orc_residuals_row": (None, [_vp, _c_int, _c_i64, _c_int, _vp, _vp, _vp]),
+        "orc_refined_attention_row": (None, [_vp, _c_int, _c_int, _vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_dbl,
+                                             _vp, _vp, _vp]),
+        "orc_attention_mass_recall": (None, [_vp, _c_int, _c_int, _vp, _vp, _c_i64, _c_i64, _c_int, _c_dbl, _vp]),
+        "orc_sparse_attention_row": (None, [_vp, _c_int, _c_int, _vp, _vp, _vp, _c_i64, _c_i64, _c_int, _c_dbl,
+                                            _vp, _vp, _vp]),
+        "orc_quest_step": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int,
+                                         _c_int, _c_int, _c_int, _c_dbl, _vp, _vp, _c_int, _c_int, _c_dbl,
+                                         _vp, _vp, _vp, _vp]),
+        "orc_delta_step": (_c_int, [_vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int,
+                                         _c_dbl, _c_dbl, _vp, _c_int, _vp, _c_int, _c_int, _c_dbl, _vp, _vp,
+                                         _vp, _vp, _vp]),
+    }
+
+    NEG_INF = NEG_INF
+    RES_DENOM = RES_DENOM
+
+    def __init__(self, path: Optional[str] = None):
+        self.path = path or build_oracle.build()
+        self.lib = ctypes.CDLL(self.path)
+        for name, (res, args) in self._SIGS.items():
+            fn = getattr(self.lib, name)
+            fn.restype = res
+            fn.argtypes = args
+
+    # ------------------------------------------------------------ decoding
+
+    def to_f64(self, x, dtype: str) -> np.ndarray:
+        """Exact float64 value of an fp32 array or of bf16 bit patterns (uint16)."""
+        if dtype == "bf16":
+            a = np.ascontiguousarray(x, dtype=np.uint16)
+            out = np.empty(a.shape, np.float64)
+            self.lib.orc_bf16_to_f64(_p(a), a.size, _p(out))
+            return out
+        a = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(a.shape, np.float64)
+        self.lib.orc_f32_to_f64(_p(a), a.size, _p(out))
+        return out
+
+    # ----------------------------------------------------------- attention
+
+    def softmax_attention(self, q, K, V, scale: float, sink=None):
+        """(o [G, Dv], lse [G]) of G query rows over the rows of K and V."""
+        q = _mat(q)
+        G, Dq = q.shape
+        K = _f64(K).reshape(-1, Dq)
+        V = _f64(V)
+        Dv = V.shape[1] if V.ndim == 2 else Dq
+        sk = None if sink is None else _f64(sink).reshape(-1)
+        o, lse = np.empty((G, Dv)), np.empty(G)
+        self.lib.orc_softmax_attention(_p(q), G, Dq, _p(K), _p(V), K.shape[0], Dv, float(scale), _p(sk),
+                                       _p(o), _p(lse))
+        return o, lse
+
+    def split_partials(self, q, K, V, scale, bounds):
+        """[(m [G], l [G], acc [G, Dv])] for each key slice [a, b) in bounds."""
+        q, K, V = _mat(q), _f64(K), _f64(V)
+        G, Dq = q.shape
+        Dv = V.shape[1]
+        b = _i64([x for ab in bounds for x in ab])
+        S = len(bounds)
+        m, l, acc = np.empty((S, G)), np.empty((S, G)), np.empty((S, G, Dv))
+        self.lib.orc_split_partials(_p(q), G, Dq, _p(K), _p(V), Dv, float(scale), _p(b), S, _p(m), _p(l), _p(acc))
+        return [(m[s], l[s], acc[s]) for s in range(S)]
+
+    def combine_partials(self, parts, sink=None):
+        """(o [G, D], lse [G]) merged from split partials."""
+        m = _f64(np.stack([p[0] for p in parts]))
+        l = _f64(np.stack([p[1] for p in parts]))
+        acc = _f64(np.stack([p[2] for p in parts]))
+        S, G, D = acc.shape
+        sk = None if sink is None else _f64(sink).reshape(-1)
+        o, lse = np.empty((G, D)), np.empty(G)
+        self.lib.orc_combine_partials(S, G, D, _p(m), _p(l), _p(acc), _p(sk), _p(o), _p(lse))
+        return o, lse
+
+    # --------------------------------------------------------------- Quest
+
+    def num_pages(self, n: int, page_size: int) -> int:
+        return int(self.lib.orc_num_pages(int(n), int(page_size)))
+
+    def page_minmax(self, K, n: int, page_size: int):
+        """(kmin, kmax) [NP, D] over the valid keys of each page."""
+        K = _mat(K)
+        D = K.shape[1]
+        NP = self.num_pages(n, page_size)
+        kmin, kmax = np.empty((NP, D)), np.empty((NP, D))
+        self.lib.orc_page_minmax(_p(K), D, int(n), int(page_size), _p(kmin), _p(kmax))
+        return kmin, kmax
+
+    def quest_bound(self, q, kmin, kmax, chunk: int = 4096):
+        """U [G, NP] = sum_c max(q kmin, q kmax)."""
+        q, kmin, kmax = _mat(q), _mat(kmin), _mat(kmax)
+        G, D = q.shape
+        NP = kmin.shape[0]
+        U = np.empty((G, NP))
+        self.lib.orc_quest_bound(_p(q), G, D, _p(kmin), _p(kmax), NP, _p(U))
+        return U
+
+    def group_score(self, U) -> np.ndarray:
+        U = _mat(U)
+        s = np.empty(U.shape[1])
+        self.lib.orc_group_score(_p(U), U.shape[0], U.shape[1], _p(s))
+        return s
+
+    def forced_pages(self, n: int, page_size: int, n_sink_pages: int, n_local_tokens: int) -> np.ndarray:
+        out = np.empty(self.num_pages(n, page_size) + 1, np.int64)
+        c = self.lib.orc_forced_pages(int(n), int(page_size), int(n_sink_pages), int(n_local_tokens), _p(out))
+        return out[:c].copy()
+
+    def select_topk(self, score, k: int, forced) -> np.ndarray:
+        score, forced = _f64(score).reshape(-1), _i64(forced)
+        NP = score.shape[0]
+        out = np.empty(max(int(k), NP) + 1, np.int64)
+        c = self.lib.orc_select_topk(_p(score), NP, int(k), _p(forced), forced.size, _p(out))
+        if c < 0:
+            raise ValueError("budget smaller than the forced pages")
+        return out[:c].copy()
+
+    def kth_score(self, score, k: int, forced) -> float:
+        score, forced = _f64(score).reshape(-1), _i64(forced)
+        return float(self.lib.orc_kth_score(_p(score), score.shape[0], int(k), _p(forced), forced.size))
+
+    def pages_to_tokens(self, pages, n: int, page_size: int) -> np.ndarray:
+        pages = _i64(pages)
+        out = np.empty(pages.size * int(page_size) + 1, np.int64)
+        c = self.lib.orc_pages_to_tokens(_p(pages), pages.size, int(n), int(page_size), _p(out))
+        return out[:c].copy()
+
+    def quest_select_row(self, q, K, n, page_size, k, n_sink_pages, n_local_tokens):
+        """(pages, group score per page, k-th admitted score) of one row."""
+        q, K = _mat(q), _mat(K)
+        G, D = q.shape
+        NP = self.num_pages(n, page_size)
+        pages = np.empty(max(int(k), NP) + 1, np.int64)
+        score = np.empty(NP)
+        kth = _c_dbl(0.0)
+        c = self.lib.orc_quest_select_row(_p(q), G, D, _p(K), int(n), int(page_size), int(k), int(n_sink_pages),
+                                          int(n_local_tokens), _p(pages), _p(score), ctypes.byref(kth))
+        if c < 0:
+            raise ValueError("budget smaller than the forced pages")
+        return pages[:c].copy(), score, float(kth.value)
+
+    # ----------------------------------------------------------------- FFD
+
+    def thumb_quantize(self, Kb):
+        """(codes [T, D] uint8, s [D]) of one block."""
+        Kb = _mat(Kb)
+        T, D = Kb.shape
+        codes, s = np.empty((T, D), np.uint8), np.empty(D)
+        self.lib.orc_thumb_quantize(_p(Kb), T, D, _p(codes), _p(s))
+        return codes, s
+
+    def thumb_dequant(self, codes, s) -> np.ndarray:
+        codes = _u8(codes)
+        T, D = codes.shape
+        s = _f64(s)
+        rows = 1 if s.size == D else T
+        s = np.ascontiguousarray(s.reshape(rows, D))
+        out = np.empty((T, D))
+        self.lib.orc_thumb_dequant(_p(codes), _p(s), T, D, rows, _p(out))
+        return out
+
+    def pack_codes(self, codes) -> np.ndarray:
+        codes = _u8(codes)
+        T, D = codes.shape
+        out = np.empty((T, D // 4), np.uint8)
+        self.lib.orc_pack_codes(_p(codes), T, D, _p(out))
+        return out
+
+    def unpack_codes(self, packed) -> np.ndarray:
+        packed = _u8(packed)
+        T, W = packed.shape
+        out = np.empty((T, 4 * W), np.uint8)
+        self.lib.orc_unpack_codes(_p(packed), T, W, _p(out))
+        return out
+
+    def thumbnails_row(self, K, n: int, block: int):
+        K = _mat(K)
+        D = K.shape[1]
+        nfull = int(n) // int(block)
+        codes, scales = np.zeros((nfull * block, D), np.uint8), np.zeros((nfull, D))
+        self.lib.orc_thumbnails_row(_p(K), D, int(n), int(block), _p(codes), _p(scales))
+        return codes, scales
+
+    def delta_forced_blocks(self, n: int, block: int) -> np.ndarray:
+        out = np.empty(2, np.int64)
+        c = self.lib.orc_delta_forced_blocks(int(n), int(block), _p(out))
+        return out[:c].copy()
+
+    def pseudo_max(self, q, K, n: int, block: int, scale: float) -> np.ndarray:
+        q, K = _mat(q), _mat(K)
+        G, D = q.shape
+        out = np.empty(G)
+        self.lib.orc_pseudo_max(_p(q), G, D, _p(K), int(n), int(block), float(scale), _p(out))
+        return out
+
+    def delta_block_margin(self, q, K, n, block, scale):
+        """(scanned blocks, margins) of the complete non-forced blocks."""
+        q, K = _mat(q), _mat(K)
+        G, D = q.shape
+        cap = int(n) // int(block) + 1
+        blocks, margins = np.empty(cap, np.int64), np.empty(cap)
+        c = self.lib.orc_delta_block_margin(_p(q), G, D, _p(K), int(n), int(block), float(scale), _p(blocks),
+                                            _p(margins))
+        return blocks[:c].copy(), margins[:c].copy()
+
+    def delta_select_row(self, q, K, n, block, delta, scale):
+        """(kept blocks ascending, (scanned blocks, margins))."""
+        q, K = _mat(q), _mat(K)
+        G, D = q.shape
+        cap = -(-int(n) // int(block)) + 2
+        sel, blocks, margins = np.empty(cap, np.int64), np.empty(cap, np.int64), np.empty(cap)
+        ns = _c_i64(0)
+        c = self.lib.orc_delta_select_row(_p(q), G, D, _p(K), int(n), int(block), float(delta), float(scale),
+                                          _p(sel), _p(blocks), _p(margins), ctypes.byref(ns))
+        k = int(ns.value)
+        return sel[:c].copy(), (blocks[:k].copy(), margins[:k].copy())
+
+    def residual_quantize(self, Kb, codes, s) -> np.ndarray:
+        Kb, codes, s = _mat(Kb), _u8(codes), _f64(s).reshape(-1)
+        T, D = Kb.shape
+        r = np.empty((T, D), np.int8)
+        self.lib.orc_residual_quantize(_p(Kb), _p(codes), _p(s), T, D, _p(r))
+        return r
+
+    def refined_keys(self, codes, s, r) -> np.ndarray:
+        codes = _u8(codes)
+        T, D = codes.shape
+        s = _f64(s)
+        rows = 1 if s.size == D else T
+        s = np.ascontiguousarray(s.reshape(rows, D))
+        r = np.ascontiguousarray(r, dtype=np.int8)
+        out = np.empty((T, D))
+        self.lib.orc_refined_keys(_p(codes), _p(s), _p(r), T, D, rows, _p(out))
+        return out
+
+    def residuals_row(self, K, n: int, block: int):
+        K = _mat(K)
+        D = K.shape[1]
+        nfull = int(n) // int(block)
+        codes, scales = np.zeros((nfull * block, D), np.uint8), np.zeros((nfull, D))
+        res = np.zeros((nfull * block, D), np.int8)
+        self.lib.orc_residuals_row(_p(K), D, int(n), int(block), _p(codes), _p(scales), _p(res))
+        return codes, scales, res
+
+    def refined_attention_row(self, q, K, V, blocks, n, block, scale, sink=None):
+        q, K, V, blocks = _mat(q), _mat(K), _mat(V), _i64(blocks)
+        G, D = q.shape
+        sk = None if sink is None else _f64(sink).reshape(-1)
+        o, lse = np.empty((G, D)), np.empty(G)
+        self.lib.orc_refined_attention_row(_p(q), G, D, _p(K), _p(V), _p(blocks), blocks.size, int(n), int(block),
+                                           float(scale), _p(sk), _p(o), _p(lse))
+        return o, lse
+
+    # --------------------------------------------------- selection quality
+
+    def attention_mass_recall(self, q, K, pages, n: int, page_size: int, scale: float) -> np.ndarray:
+        q, K, pages = _mat(q), _mat(K), _i64(pages)
+        G, D = q.shape
+        out = np.empty(G)
+        self.lib.orc_attention_mass_recall(_p(q), G, D, _p(K), _p(pages), pages.size, int(n), int(page_size),
+                                           float(scale), _p(out))
+        return out
+
+    # ------------------------------------------------------- one decode row
+
+    def sparse_attention_row(self, q, K, V, pages, n, page_size, scale, sink=None):
+        q, K, V, pages = _mat(q), _mat(K), _mat(V), _i64(pages)
+        G, D = q.shape
+        sk = None if sink is None else _f64(sink).reshape(-1)
+        o, lse = np.empty((G, D)), np.empty(G)
+        self.lib.orc_sparse_attention_row(_p(q), G, D, _p(K), _p(V), _p(pages), pages.size, int(n), int(page_size),
+                                          float(scale), _p(sk), _p(o), _p(lse))
+        return o, lse
+
+    # ------------------------------------------------ whole steps (timed)
+
+    @staticmethod
+    def _step_inputs(q, K, V, ctx_len, rows):
+        f32 = np.asarray(K).dtype == np.float32
+        dt = np.float32 if f32 else np.uint16
+        return (np.ascontiguousarray(q, dt), np.ascontiguousarray(K, dt), np.ascontiguousarray(V, dt), int(f32),
+                np.ascontiguousarray(ctx_len, np.int32), np.ascontiguousarray(rows, np.int32))
+
+    def quest_step(self, q, K, V, ctx_len, num_q_heads, page_size, k, n_sink_pages, n_local_tokens,
+                   scale, sink, rows, threads: int = 1, min_busy: float = 0.0):
+        """The Quest step over the listed rows (ids b * Hkv + h) of a
+        workload (bf16 bit patterns or fp32), on `threads` std::threads;
+        returns (pages [nrows, k], o [nrows, G, D], lse [nrows, G], busy
+        seconds, bytes, repetitions)."""
+        q, K, V, f32, ctx, rows = self._step_inputs(q, K, V, ctx_len, rows)
+        B, Hkv, Cap, D = K.shape
+        G = num_q_heads // Hkv
+        sk = None if sink is None else np.ascontiguousarray(sink, np.float32)
+        nr = rows.size
+        pages = np.empty((nr, int(k)), np.int32)
+        o, lse, st = np.empty((nr, G, D)), np.empty((nr, G)), np.empty(3)
+        rc = self.lib.orc_quest_step(_p(q), _p(K), _p(V), f32, _p(ctx), B, int(num_q_heads), Hkv, D, Cap,
+                                     int(page_size), int(k), int(n_sink_pages), int(n_local_tokens),
+                                     float(scale), _p(sk), _p(rows), nr, int(threads), float(min_busy),
+                                     _p(pages), _p(o), _p(lse), _p(st))
+        if rc != 0:
+            raise ValueError("budget smaller than the forced pages")
+        return pages, o, lse, float(st[0]), float(st[1]), int(st[2])
+
+    def delta_step(self, q, K, V, ctx_len, num_q_heads, block, delta, scale, sink, rows, refined=False,
+                   threads: int = 1, min_busy: float = 0.0):
+        """The top-delta step over the listed rows of a bf16 workload; returns
+        (count [nrows], blocks [nrows, Cap/block], o, lse, busy seconds,
+        bytes, repetitions)."""
+        q, K, V, f32, ctx, rows = self._step_inputs(q, K, V, ctx_len, rows)
+        if f32:
+            raise ValueError("the top-delta step takes bf16 inputs")
+        B, Hkv, Cap, D = K.shape
+        G = num_q_heads // Hkv
+        sk = None if sink is None else np.ascontiguousarray(sink, np.float32)
+        nr = rows.size
+        count, blocks = np.empty(nr, np.int32), np.empty((nr, Cap // int(block)), np.int32)
+        o, lse, st = np.empty((nr, G, D)), np.empty((nr, G)), np.empty(3)
+        self.lib.orc_delta_step(_p(q), _p(K), _p(V), f32, _p(ctx), B, int(num_q_heads), Hkv, D, Cap, int(block),
+                                float(delta), float(scale), _p(sk), int(bool(refined)), _p(rows), nr,
+                                int(threads), float(min_busy), _p(count), _p(blocks), _p(o), _p(lse), _p(st))
+        return count, blocks, o, lse, float(st[0]), float(st[1]), int(st[2])
+
+
+_DEFAULT = Oracle()
+
+_FUNCS = ("to_f64", "softmax_attention", "split_partials", "combine_partials", "num_pages", "page_minmax",
+          "quest_bound", "group_score", "forced_pages", "select_topk", "kth_score", "pages_to_tokens",
+          "quest_select_row", "thumb_quantize", "thumb_dequant", "pack_codes", "unpack_codes", "thumbnails_row",
+          "delta_forced_blocks", "pseudo_max", "delta_block_margin", "delta_select_row", "residual_quantize",
+          "refined_keys", "residuals_row", "refined_attention_row", "attention_mass_recall",
+          "sparse_attention_row", "quest_step", "delta_step")
+for _name in _FUNCS:
+    globals()[_name] = getattr(_DEFAULT, _name)
+del _name

@@ -121,3 +121,28 @@ def assert_close(spec: W.Spec, gpu: np.ndarray, ref: np.ndarray, what=""):
     else:
         assert rel <= F32_REL_L2, f"{what}: rel-L2 {rel:.3g}"
     return mx, rel
+
+
+RES_TIE_REL = 1e-6  # float32 rounding of the kernel's residual quotient (a few ulps of 2^-24)
+
+
+def check_residuals(gpu_res: np.ndarray, K: np.ndarray, n: int, block: int) -> int:
+    """Compare a row's GPU 8-bit residuals [>= nfull*block, D] with the
+    oracle's, which decides r = round((k - k^) * 508 / s) exactly.  The
+    kernel decides it in float32, so an element may differ by one only where
+    the exact quotient lies within float32 rounding of a half-integer; such
+    elements are counted and returned.  Codes and scales must agree exactly
+    (checked by the caller)."""
+    codes, scales, ores = O.residuals_row(K, n, block)
+    nfull = n // block
+    got = gpu_res[:nfull * block].astype(np.int32)
+    want = ores.astype(np.int32)
+    bad = np.argwhere(got != want)
+    for t, c in bad:
+        assert abs(int(got[t, c]) - int(want[t, c])) == 1, (t, c, got[t, c], want[t, c])
+        s = scales[t // block, c]
+        kh = (float(codes[t, c]) - 1.5) * (s / 2.0)
+        x = (K[t, c] - kh) * O.RES_DENOM / s
+        frac = x - np.floor(x)
+        assert abs(frac - 0.5) <= RES_TIE_REL * max(1.0, abs(x)), (t, c, x)
+    return len(bad)

@@ -1,7 +1,10 @@
 """FFD 8-bit residuals and the refined attention ("Faster Than Flash",
 Methodology 1 and eq. 4) through the C ABI against the fp64 oracle.
 
-Residual codes are integers decided in float32 on both sides: bit-exact.
+Codes and scales are bit-exact.  The oracle decides each residual integer
+exactly; the kernel decides it in float32, so a residual may differ by one
+only where the exact quotient lies within float32 rounding of a
+half-integer (counted as a tie).
 The refined step (top-delta selection, then attention whose complete blocks
 are scored with k~ = thumbnail level + residual) is compared with the
 oracle's refined attention on the same block sets, within the bf16 output
@@ -45,7 +48,7 @@ def _check_residuals(s, host, codes, scales, res, ctx):
             nfull = n // s.block
             np.testing.assert_array_equal(codes[b, h, :nfull * s.block], O.pack_codes(oc))
             np.testing.assert_array_equal(scales[b, h, :nfull], osc)
-            np.testing.assert_array_equal(res[b, h, :nfull * s.block], ores)
+            PT.check_residuals(res[b, h], O.to_f64(host.K[b, h], s.dtype), n, s.block)
 
 
 @pytest.mark.parametrize("ctx", [[64 * 9 + 5, 64 * 3], [64 * 40]])

@@ -1,57 +1,25 @@
-"""Mutation check of the oracle's pins.
+"""Mutation check of the oracle's pins, on the numpy oracle.
 
-Each case plants one plausible mistake in the fp64 oracle (on the CPU, by
-replacing one of its functions for the duration of the case): a dropped or
-doubled term, a wrong sign, index or comparison, a transposed operand, an
+Each case plants one plausible mistake in the numpy fp64 oracle (on the CPU,
+by replacing one of its functions for the duration of the case): a dropped
+or doubled term, a wrong sign, index or comparison, a transposed operand, an
 off-by-one bound, another reading of a convention.  The pins in
-test_oracle_pins must then fail somewhere; a mistake that every pin lets
-through would mean the pins do not fix that part of the oracle.
-
-The pins run in-process: each test function of test_oracle_pins is called
-with every combination of its parametrize marks, the ones named in the
-case first.  CPU only.
+test_oracle_pins, run against that oracle, must then fail somewhere; a
+mistake that every pin lets through would mean the pins do not fix that part
+of the oracle.  test_oracle_mutations_cpp plants the same mistakes in the
+source of the C++ oracle.  CPU only.
 """
-import itertools
 import math
 
 import numpy as np
 import pytest
 
-from oracle import sls_oracle as O
-from tests import test_oracle_pins as PINS
-
-
-def _pin_cases():
-    cases = []
-    for name, fn in vars(PINS).items():
-        if not (name.startswith("test_") and callable(fn)):
-            continue
-        grids = []
-        for mark in getattr(fn, "pytestmark", []):
-            if mark.name != "parametrize":
-                continue
-            names, values = mark.args[0], mark.args[1]
-            names = [s.strip() for s in names.split(",")] if isinstance(names, str) else list(names)
-            grids.append([dict(zip(names, v if len(names) > 1 else (v,))) for v in values])
-        for combo in itertools.product(*grids):
-            kw = {}
-            for d in combo:
-                kw.update(d)
-            cases.append((name, fn, kw))
-    return cases
-
-
-PIN_CASES = _pin_cases()
+from oracle import numpy_oracle as O
+from tests.pin_runner import PIN_CASES, first_failing_pin
 
 
 def _first_failing_pin(hints):
-    ordered = [c for c in PIN_CASES if c[0] in hints] + [c for c in PIN_CASES if c[0] not in hints]
-    for name, fn, kw in ordered:
-        try:
-            fn(**kw)
-        except Exception:  # an assertion or any error: the planted mistake shows
-            return f"{name}{kw or ''}"
-    return None
+    return first_failing_pin(O, hints)
 
 
 # ---------------------------------------------------------------- mistakes
@@ -198,11 +166,10 @@ def _delta_strict(q, K, n, block, delta, scale):
 
 def _residual(denom=508.0, rounding=np.rint):
     def quantize(Kb, codes, s):
-        k32 = np.asarray(Kb, np.float64).astype(np.float32)
-        e = k32 - O.thumb_dequant(codes, s).astype(np.float32)
-        x = e * np.float32(denom)
-        s32 = np.broadcast_to(np.asarray(s, np.float64).astype(np.float32), x.shape)
-        x = np.where(s32 > 0, x / np.where(s32 > 0, s32, np.float32(1)), np.float32(0)).astype(np.float32)
+        Kb = np.asarray(Kb, np.float64)
+        s = np.broadcast_to(np.asarray(s, np.float64), Kb.shape)
+        e = Kb - O.thumb_dequant(codes, s)
+        x = np.where(s > 0, e * denom / np.where(s > 0, s, 1.0), 0.0)
         return np.clip(rounding(x), -127, 127).astype(np.int8)
     return quantize
 

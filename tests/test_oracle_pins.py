@@ -402,14 +402,14 @@ def test_residual_golden():
 
 def test_residual_error_bound():
     """The refined key is within s/1016 of the key (half a residual step of
-    s/508) up to float32 rounding of the code decision; codes stay in range;
-    an all-zero channel gets 0."""
+    s/508; the nearest level is decided exactly); codes stay in range; an
+    all-zero channel gets 0."""
     K = _bf16_exact(rnd(40, 64, 128) * np.exp(2 * rnd(41, 1, 128)))
     codes, s = O.thumb_quantize(K)
     r = O.residual_quantize(K, codes, s)
     assert r.dtype == np.int8 and np.abs(r.astype(int)).max() <= 127
     err = np.abs(K - O.refined_keys(codes, s, r))
-    assert np.all(err <= s / 1016 * (1 + 1e-5) + 1e-30)
+    assert np.all(err <= s / 1016 * (1 + 1e-12) + 1e-300)
     assert np.max(err / s) > 0.9 / 1016      # the bound is met, not slack
     K[:, 5] = 0
     codes, s = O.thumb_quantize(K)
@@ -418,14 +418,19 @@ def test_residual_error_bound():
 
 def test_residual_is_the_nearest_level_brute_force():
     """Exact rational arithmetic: r is the integer j in [-127, 127] nearest to
-    (k - k^) * 508 / s (ties to the even j), except where float32 rounding of
-    that quotient could move it across a half-integer."""
+    (k - k^) * 508 / s, ties to the even j, for every element (no exclusion:
+    the oracle decides it exactly).  Keys include exact half-integer
+    quotients (s = 127 * 2^e, k = odd * 2^(e-3)), which must round to even."""
     from fractions import Fraction
     K = _bf16_exact(rnd(42, 64, 16) * np.exp(rnd(43, 1, 16)))
     K[3, :] = 0.0
+    # channel 0: s = 127/64 (row 0), k = odd/512 on other rows: 508 k / s = odd/2
+    K[:, 0] = _bf16_exact(K[:, 0] * (1.5 / np.abs(K[:, 0]).max()))
+    K[0, 0] = 127.0 / 64
+    K[1:9, 0] = np.array([1, 3, 5, 7, -1, -3, -9, 11]) / 512.0
     codes, s = O.thumb_quantize(K)
     r = O.residual_quantize(K, codes, s)
-    near = 0
+    halves = 0
     for t in range(K.shape[0]):
         for c in range(K.shape[1]):
             sc = Fraction(float(s[c]))
@@ -433,14 +438,12 @@ def test_residual_is_the_nearest_level_brute_force():
             x = (Fraction(float(K[t, c])) - kh) * 508 / sc
             lo = math.floor(x)
             frac = x - lo
-            if abs(frac - Fraction(1, 2)) < Fraction(1, 10**5) and frac != Fraction(1, 2):
-                near += 1
-                continue
             j = lo + 1 if frac > Fraction(1, 2) else lo
-            if frac == Fraction(1, 2) and lo % 2 != 0:
-                j = lo + 1
+            if frac == Fraction(1, 2):
+                halves += 1
+                j = lo if lo % 2 == 0 else lo + 1
             assert int(r[t, c]) == max(-127, min(127, j)), (t, c, x)
-    assert near < 10
+    assert halves >= 8
 
 
 def test_refined_attention_brute_force():
