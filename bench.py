@@ -215,15 +215,27 @@ def cpu_oracle(s: W.Spec, host, rows, threads: int, min_busy: float = 0.0, refin
     return nbytes / wall / 1e9, threads, wall, nbytes, reps
 
 
-def parity_check(s: W.Spec, host, sel, out):
+def parity_rows(s: W.Spec, count: int = 4):
+    """Rows of the benchmarked step that the CPU-baseline leg checks: the
+    first, the last and seeded others."""
+    rng = np.random.default_rng(s.seed)
+    rows = {0, s.rows - 1} | {int(r) for r in rng.integers(0, s.rows, size=count)}
+    return sorted(rows)[:count + 2]
+
+
+def parity_check(s: W.Spec, host, sel, out, count=None):
     """Sampled rows of the benchmarked step against the oracle (part of the
-    CPU-baseline leg).  Raises if a row disagrees."""
+    CPU-baseline leg).  Raises if a row disagrees; returns the rows, the
+    boundary ties counted and the largest output errors."""
     from tests import parity as PT
-    res = {"rows": [0, s.rows - 1], "ties": 0, "max_abs": 0.0, "rel_l2": 0.0}
+    res = {"rows": parity_rows(s), "ties": 0, "max_abs": 0.0, "rel_l2": 0.0}
     for r in res["rows"]:
         b, h = divmod(r, s.num_kv_heads)
         orc = PT.oracle_row(s, host, b, h)
-        t = PT.check_quest_list(sel[r], orc, int(host.ctx_len[b]), s.page_size, s.k_pages)
+        if s.selector == "quest":
+            t = PT.check_quest_list(sel[r], orc, int(host.ctx_len[b]), s.page_size, s.k_pages)
+        else:
+            t = PT.check_delta_list(int(count[r]), sel[r], orc, s.delta)
         res["ties"] += t
         if t == 0:
             mx, rel = PT.assert_close(s, out[b, h * s.group:(h + 1) * s.group], orc.o, f"row {r}")
@@ -278,13 +290,152 @@ def run_reference(args, s: W.Spec):
 
 
 def _workload_name(s: W.Spec) -> str:
-    return (f"{s.name}: B={s.batch} Hq={s.num_q_heads} Hkv={s.num_kv_heads} D={s.head_dim} "
-            f"ctx={s.ctx_len[0]} P={s.page_size} budget={s.k_pages * s.page_size} tokens {s.dtype}")
+    base = f"{s.name}: B={s.batch} Hq={s.num_q_heads} Hkv={s.num_kv_heads} D={s.head_dim} ctx={s.ctx_len[0]}"
+    if s.selector == "quest":
+        return f"{base} P={s.page_size} budget={s.k_pages * s.page_size} tokens{' sink' if s.has_sink else ''} {s.dtype}"
+    return f"{base} block={s.block} delta={s.delta} {s.dtype}"
 
 
 # ---------------------------------------------------------------------- ours
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth, for context beside the measured peak
+
+
+def make_sets(dw, nsets: int):
+    """`nsets` distinct copies of the cache and the selector metadata (the
+    first is the workload's own).  A one-token page is its own summary, so
+    with page_size 1 each set passes its key cache as kmin and kmax."""
+    s = dw.spec
+    sets = [(dw.K, dw.V, dw.kmin, dw.kmax)]
+    for _ in range(nsets - 1):
+        K, V = dw.K.clone(), dw.V.clone()
+        if s.page_size == 1:
+            kmin = kmax = K
+        else:
+            kmin, kmax = dw.kmin.clone(), dw.kmax.clone()
+        sets.append((K, V, kmin, kmax))
+    return sets
+
+
+def timed_windows(stream, graphs, steps: int, spg: int, world: int, min_total_s: float = 0.2,
+                  max_windows: int = 200):
+    """Time windows of exactly `steps` steps each (graph i replays steps
+    spg*i .. spg*i + spg - 1, buffer sets rotating across graphs), each
+    bracketed by a synchronise (and a barrier on several ranks) and CUDA
+    events on the launching stream, repeated until `min_total_s` seconds of
+    device time have been timed (at least 3 windows).  Returns the windows'
+    seconds, each the max over ranks."""
+    import torch
+    import torch.distributed as dist
+    out, gi = [], 0
+    while len(out) < 3 or (sum(out) < min_total_s and len(out) < max_windows):
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps // spg):
+                graphs[gi % len(graphs)].replay()
+                gi += 1
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t, _ = aggregate(e0.elapsed_time(e1) / 1e3, 0.0, world)
+        out.append(t)
+    return out
+
+
+def window_stats(windows, steps: int) -> dict:
+    us = sorted(1e6 * w / steps for w in windows)
+    n = len(us)
+    return {"windows": n, "steps_per_window": steps, "us_per_step_p10": round(us[n // 10], 3),
+            "us_per_step_p50": round(statistics.median(us), 3), "us_per_step_p90": round(us[(n * 9) // 10], 3),
+            "timed_s": round(sum(windows), 4)}
+
+
+def roofline_block(kernel: str, achieved: float, peak: float, peak_kind: str, traffic, best_seen=None) -> dict:
+    """The line's roofline object for the dominant kernel, with the
+    fraction also against the best bandwidth this run saw and the nominal
+    HBM bandwidth."""
+    best = max(peak, best_seen or 0.0)
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_kind": f"{peak_kind} (burst copy)",
+            "frac_of_best_seen": round(achieved / best, 4), "best_seen_gbs": round(best, 1),
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4), "nominal_gbs": NOMINAL_HBM_GBS}
+
+
+def capture_graphs(stream, sets, steps_obj, run, nsets: int, spg: int):
+    """Single-step graphs (one per buffer set) and the timed loop's graphs
+    of `spg` consecutive steps each (global step i uses set i % nsets,
+    continuing across graphs).  run(step_obj, set) issues one step."""
+    import torch
+    with torch.cuda.stream(stream):
+        for st, bufs in zip(steps_obj, sets):
+            run(st, bufs)  # warm the kernels before capture
+        torch.cuda.synchronize()
+        single = []
+        for st, bufs in zip(steps_obj, sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                run(st, bufs)
+            single.append(g)
+        multi = []
+        for gi in range(nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(spg):
+                    u = (gi * spg + j) % nsets
+                    run(steps_obj[u], sets[u])
+            multi.append(g)
+    torch.cuda.synchronize()
+    return single, multi
+
+
+def replay_spread(stream, graphs, steps: int) -> dict:
+    """p10/p50/p90 of single graph replays, each bracketed by its own
+    events (a separate pass: the timed windows have no events inside)."""
+    import torch
+    nrep = max(200, min(steps, 1000))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+    with torch.cuda.stream(stream):
+        for i, (a, b_) in enumerate(evs):
+            if i % 100 == 0:
+                torch.cuda._sleep(int(2e7))  # keeps the queue ahead of the device
+            a.record(stream)
+            graphs[i % len(graphs)].replay()
+            b_.record(stream)
+    torch.cuda.synchronize()
+    per = sorted(1e3 * a.elapsed_time(b_) for a, b_ in evs)
+    return {"p10": round(per[nrep // 10], 2), "p50": round(per[nrep // 2], 2), "p90": round(per[nrep * 9 // 10], 2),
+            "replays": nrep}
+
+
+def stage_times(stream, stages, reps: int) -> dict:
+    """Mean device time of each named stage issued eagerly between events
+    on the launching stream (queued behind a sleep so the host stays ahead)."""
+    import torch
+    ev = {k: [] for k, _ in stages[0]}
+    with torch.cuda.stream(stream):
+        for i in range(reps):
+            if i % 25 == 0:
+                torch.cuda._sleep(int(4e7))
+            for name, fn in stages[i % len(stages)]:
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b_.record(stream)
+                ev[name].append((a, b_))
+    torch.cuda.synchronize()
+    return {k: 1e3 * statistics.mean(a.elapsed_time(b_) for a, b_ in v) for k, v in ev.items()}
+
+
 def run_ours(args, s: W.Spec):
+    """The Quest step (qwen1p5b, qwen7b, gptoss, tiny) through the public API."""
     import torch
     import torch.distributed as dist
     from sparse_long_context_gb300 import _lib
@@ -305,41 +456,20 @@ def run_ours(args, s: W.Spec):
     nsets = max(2, math.ceil(4 * l2 / nbytes["total"]))
 
     # one untimed step whose sampled rows the CPU-baseline leg checks
-    first_sel, _, first_out, _ = H.run_step(dw)
+    first_sel, _, first_out, _ = H.run_step(dw, args.splits)
 
-    # buffer sets: distinct copies of cache + metadata
-    sets = [(dw.K, dw.V, dw.kmin, dw.kmax)]
-    for _ in range(nsets - 1):
-        sets.append(tuple(t.clone() for t in sets[0]))
-    steps_obj = [ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, args.splits)
-                 for _ in sets]
+    sets = make_sets(dw, nsets)
+    steps_obj = [ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, args.splits) for _ in sets]
+    one = steps_obj[0].one_launch and ops.quest_step_splits(dw.desc, s.k_pages) > 0
     S = steps_obj[0].S
     stream = torch.cuda.Stream()
-    graphs = []
-    with torch.cuda.stream(stream):
-        for st, (K, V, kmin, kmax) in zip(steps_obj, sets):
-            st(dw.q, K, V, kmin, kmax, dw.ctx)  # warm the kernels before capture
-        torch.cuda.synchronize()
-        for st, (K, V, kmin, kmax) in zip(steps_obj, sets):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                st(dw.q, K, V, kmin, kmax, dw.ctx)
-            graphs.append(g)
-        # the timed loop's graphs: `spg` consecutive steps each (global step i
-        # uses buffer set i % nsets, continuing across graphs), as a decode
-        # engine captures a whole iteration; consecutive kernels overlap
-        # their launch with the previous one's tail (programmatic launch)
-        spg = next(r for r in (8, 4, 2, 1) if args.steps % r == 0)
-        mgraphs = []
-        for gi in range(nsets):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for j in range(spg):
-                    u = (gi * spg + j) % nsets
-                    K, V, kmin, kmax = sets[u]
-                    steps_obj[u](dw.q, K, V, kmin, kmax, dw.ctx)
-            mgraphs.append(g)
-    torch.cuda.synchronize()
+    spg = next(r for r in (8, 4, 2, 1) if args.steps % r == 0)
+
+    def run(st, bufs):
+        K, V, kmin, kmax = bufs
+        return st(dw.q, K, V, kmin, kmax, dw.ctx, dw.sink)
+
+    graphs, mgraphs = capture_graphs(stream, sets, steps_obj, run, nsets, spg)
     # kernels the library picked while the graphs were captured (the replays
     # make no host calls); the device-side row counters restart here
     paths_capture = {k: v for k, v in ops.get_stats(reset=True).items() if v}
@@ -351,63 +481,28 @@ def run_ours(args, s: W.Spec):
         for i in range(-(-args.warmup // spg)):
             mgraphs[i % nsets].replay()
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w0 = time.time()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(args.steps // spg):
-            mgraphs[i % nsets].replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    windows = timed_windows(stream, mgraphs, args.steps, spg, world)
     w1 = time.time()
     clocks.window(w0, w1)
-    elapsed = e0.elapsed_time(e1) / 1e3
+    ops.pipeline_check()
     timed_rows = ops.get_stats(reset=True)  # rows the one-launch step handled off its fast path
-    t_max, total_bytes = aggregate(elapsed, float(nbytes["total"] * args.steps), world)
-
-    # per-replay spread: events around single replays (a separate pass, so the
-    # timed loop above has no events inside it)
-    nrep = max(200, min(args.steps, 1000))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
-    with torch.cuda.stream(stream):
-        for i, (a, b_) in enumerate(evs):
-            if i % 100 == 0:
-                torch.cuda._sleep(int(2e7))  # keeps the queue ahead of the device
-            a.record(stream)
-            graphs[i % nsets].replay()
-            b_.record(stream)
-    torch.cuda.synchronize()
-    per_rep = sorted(1e3 * a.elapsed_time(b_) for a, b_ in evs)
-    rep_us = {"p10": round(per_rep[nrep // 10], 2), "p50": round(per_rep[nrep // 2], 2),
-              "p90": round(per_rep[nrep * 9 // 10], 2), "replays": nrep}
+    t_max = statistics.median(windows)
+    total_bytes = nbytes["total"] * args.steps * world
+    rep_us = replay_spread(stream, graphs, args.steps)
 
     # dense decode on the same workload (the sparsity gate forced open: every
-    # row attends its whole context through the same kernel), for the
-    # speedup of the sparse step and dense GB/s against the peak
+    # row attends its whole context through the same kernel)
     dense = None
-    if not args.no_dense and steps_obj[0].one_launch and ops.quest_step_splits(dw.desc, s.k_pages) > 0:
+    if not args.no_dense and one:
         dsteps = [ops.QuestDecode(dw.desc, s.k_pages, s.n_sink_pages, s.n_local_tokens, args.splits,
                                   min_sparsity=1e9) for _ in sets]
-        dgraphs = []
+        dgraphs, _ = capture_graphs(stream, sets, dsteps, run, nsets, 1)
+        nd = max(20, min(args.steps, 200))
         with torch.cuda.stream(stream):
-            for st, (K, V, kmin, kmax) in zip(dsteps, sets):
-                st(dw.q, K, V, kmin, kmax, dw.ctx)
-            torch.cuda.synchronize()
-            for st, (K, V, kmin, kmax) in zip(dsteps, sets):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    st(dw.q, K, V, kmin, kmax, dw.ctx)
-                dgraphs.append(g)
             for i in range(3):
                 dgraphs[i % nsets].replay()
             torch.cuda.synchronize()
-            nd = max(20, min(args.steps, 200))
             d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             d0.record(stream)
             for i in range(nd):
@@ -415,68 +510,55 @@ def run_ours(args, s: W.Spec):
             d1.record(stream)
         torch.cuda.synchronize()
         dense_s = d0.elapsed_time(d1) / 1e3 / nd
-        dense_bytes = sum(s.num_kv_heads * n * 2 * s.head_dim * 2 for n in s.ctx_len)
+        esz = 2 if s.dtype == "bf16" else 4
+        dense_bytes = sum(s.num_kv_heads * n * 2 * s.head_dim * esz for n in s.ctx_len)
         dense = {"us_per_step": round(dense_s * 1e6, 2), "GB/s": round(dense_bytes / dense_s / 1e9, 1),
                  "frac_of_peak": None, "bytes_per_step": int(dense_bytes), "steps": nd}
         del dgraphs, dsteps
 
-    # per-kernel device time: eager launches bracketed by events on the
-    # launching stream, queued behind a sleep so the host stays ahead
-    ksteps = max(50, min(args.steps, 400))
-    one = steps_obj[0].one_launch and ops.quest_step_splits(dw.desc, s.k_pages) > 0
-    ev = {k: ([], []) for k in (("step",) if one else ()) + ("select", "attend")}
-    with torch.cuda.stream(stream):
-        for i in range(ksteps):
-            if i % 25 == 0:
-                torch.cuda._sleep(int(4e7))  # keeps the queue ahead of the device
-            st = steps_obj[i % nsets]
-            K, V, kmin, kmax = sets[i % nsets]
-            stages = [("select", lambda: st.select(dw.q, kmin, kmax, dw.ctx)),
-                      ("attend", lambda: st.attend(dw.q, K, V, dw.ctx))]
-            if one:
-                stages.insert(0, ("step", lambda: st(dw.q, K, V, kmin, kmax, dw.ctx)))
-            for name, fn in stages:
-                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                fn()
-                b_.record(stream)
-                ev[name][0].append(a)
-                ev[name][1].append(b_)
-    torch.cuda.synchronize()
-    kern_us = {k: 1e3 * statistics.mean(a.elapsed_time(b_) for a, b_ in zip(*v)) for k, v in ev.items()}
+    # per-stage device time, eager launches between events
+    def stages_for(i):
+        st = steps_obj[i % nsets]
+        K, V, kmin, kmax = sets[i % nsets]
+        out = [("select", lambda: st.select(dw.q, kmin, kmax, dw.ctx)),
+               ("attend", lambda: st.attend(dw.q, K, V, dw.ctx, dw.sink))]
+        if one:
+            out.insert(0, ("step", lambda: run(st, sets[i % nsets])))
+        return out
+    kern_us = stage_times(stream, [stages_for(i) for i in range(nsets)], max(50, min(args.steps, 400)))
     clk = clocks.stop()
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: per step, the H2D
+    # copy of q from pinned memory, the step and the D2H copy of the output,
+    # issued eagerly, and as a decode loop runs them (one graph per buffer
+    # set), each step followed by a host synchronise
     q_host = dw.q.cpu().pin_memory()
     out_host = torch.empty(steps_obj[0].out.shape, dtype=steps_obj[0].out.dtype).pin_memory()
     q_dev = torch.empty_like(dw.q)
     esteps = max(10, min(args.steps, 300))
+
+    def e2e_step(u):
+        K, V, kmin, kmax = sets[u]
+        q_dev.copy_(q_host, non_blocking=True)
+        o, _ = steps_obj[u](q_dev, K, V, kmin, kmax, dw.ctx, dw.sink)
+        out_host.copy_(o, non_blocking=True)
+
     for i in range(3):
-        K, V, kmin, kmax = sets[i % nsets]
-        steps_obj[i % nsets](q_dev, K, V, kmin, kmax, dw.ctx)
+        e2e_step(i % nsets)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for i in range(esteps):
-        K, V, kmin, kmax = sets[i % nsets]
-        q_dev.copy_(q_host, non_blocking=True)
-        o, _ = steps_obj[i % nsets](q_dev, K, V, kmin, kmax, dw.ctx)
-        out_host.copy_(o, non_blocking=True)
+        e2e_step(i % nsets)
         torch.cuda.current_stream().synchronize()
-    e2e_t = time.perf_counter() - t0
-    e2e_eager_max, _ = aggregate(e2e_t, float(nbytes["total"] * esteps), world)
-    # the same steps as a decode loop runs them: one graph per buffer set
-    # holding the copy of q from pinned host memory, the step and the copy of
-    # the output back, replayed and synchronised every step
+    e2e_eager_max, _ = aggregate(time.perf_counter() - t0, 0.0, world)
     egraphs = []
     with torch.cuda.stream(stream):
-        for u, (K, V, kmin, kmax) in enumerate(sets):
+        for u in range(nsets):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                q_dev.copy_(q_host, non_blocking=True)
-                o, _ = steps_obj[u](q_dev, K, V, kmin, kmax, dw.ctx)
-                out_host.copy_(o, non_blocking=True)
+                e2e_step(u)
             egraphs.append(g)
         for i in range(3):
             egraphs[i % nsets].replay()
@@ -488,14 +570,14 @@ def run_ours(args, s: W.Spec):
             egraphs[i % nsets].replay()
             stream.synchronize()
         e2e_t = time.perf_counter() - t0
-    e2e_max, e2e_bytes = aggregate(e2e_t, float(nbytes["total"] * esteps), world)
+    e2e_max, _ = aggregate(e2e_t, 0.0, world)
+    e2e_bytes = nbytes["total"] * esteps * world
     del egraphs
 
     # multi-step decode from CUDA graphs: each replay appends one token per
     # sequence (cache row + page min/max) and runs the step on the longer
-    # context.  One loop per buffer set, each with its own ctx_len rewound by
-    # `per` tokens, replayed in rotation so consecutive replays do not share
-    # L2.
+    # context; one loop per buffer set, each with its ctx_len rewound by `per`
+    # tokens, replayed in rotation
     loop_rec = None
     if not args.no_loop and one:
         per, warm_tok = 64, 4
@@ -521,12 +603,11 @@ def run_ours(args, s: W.Spec):
         ops.pipeline_check()
         nloop = (per - warm_tok) * len(loops)
         loop_s = l0.elapsed_time(l1) / 1e3 / nloop
-        ctx_end = [int(c) for c in loops[0].dw.ctx.cpu()]
         loop_rec = {"us_per_step": round(loop_s * 1e6, 2), "tokens_per_s": round(s.batch / loop_s, 1),
                     "steps": nloop, "launches_per_step": 2,
                     "what": "graph replay of decode_append (k/v row + page min/max, ctx_len += 1) "
                             "then the one-launch step",
-                    "ctx_after": ctx_end[:4]}
+                    "ctx_after": [int(c) for c in loops[0].dw.ctx.cpu()][:4]}
         del loops
 
     if rank != 0:
@@ -539,44 +620,47 @@ def run_ours(args, s: W.Spec):
         dense["frac_of_peak"] = round(dense["GB/s"] / peak, 4)
     value = total_bytes / t_max / 1e9
     ms_step = 1e3 * t_max / args.steps
+    wst = window_stats(windows, args.steps)
     # dominant kernel: the one-launch step (all bytes of the step), else the
     # larger of the two stages by algorithmic bytes
     if one:
-        dom, dom_bytes, dom_name = "step", nbytes["total"], "quest_step_kernel (score + top-k + attend + combine)"
+        dom_name = "quest_step_kernel (score + top-k + attend + combine)"
+        achieved = nbytes["total"] / (t_max / args.steps) / 1e9   # its average launch over the timed windows
+        single = nbytes["total"] / (rep_us["p50"] * 1e-6) / 1e9
     else:
         dom = "select" if nbytes["select"] >= nbytes["attend"] else "attend"
-        dom_bytes = nbytes[dom]
-        dom_name = ("select: quest_score_kernel + topk_kernel" if dom == "select"
-                    else "attend: attend_tma_kernel with the cluster combine")
-    if one:
-        # the step is this one kernel: its average launch over the timed region
-        achieved = dom_bytes / (t_max / args.steps) / 1e9
-    else:
-        achieved = dom_bytes / (kern_us[dom] * 1e-6) / 1e9
+        dom_name = ("select: quest_score_kernel + top-k kernel (two launches)" if dom == "select"
+                    else "attend: split-K attend with the combine fused")
+        achieved = nbytes[dom] / (kern_us[dom] * 1e-6) / 1e9
+        single = None
+    launches = 1 if one else 3
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "us_per_step": round(1e3 * ms_step, 2), "tokens_per_s": round(s.batch * world / (ms_step / 1e3), 1),
         "frac_of_peak": round(value / peak, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy, see workloads.py)",
+        "vs_baseline": None, "dtype": s.dtype, "data": "synthetic (seeded numpy, see workloads.py)",
         "config": {"workload": _workload_name(s), "batch": s.batch, "ctx_len": s.ctx_len[0],
                    "seq_len": s.ctx_len[0], "page_size": s.page_size, "budget_tokens": s.k_pages * s.page_size,
                    "num_splits": ops.quest_step_splits(dw.desc, s.k_pages) if one else S,
-                   "launches_per_step": 1 if one else 3, "buffer_sets": nsets, "steps_per_graph": spg,
-                   "l2": f"inputs rotate over {nsets} buffer sets ({nsets * nbytes['total'] / 1e6:.0f} MB >= 4x L2 {l2 / 1e6:.0f} MB)",
+                   "launches_per_step": launches, "buffer_sets": nsets, "steps_per_graph": spg,
+                   "l2": f"inputs rotate over {nsets} buffer sets ({nsets * nbytes['total'] / 1e6:.0f} MB >= 4x L2 "
+                         f"{l2 / 1e6:.0f} MB)",
                    "parallelism": f"weak: {world} GPU(s), {s.batch} sequences each"},
         "bytes_per_step": nbytes["total"], "bytes_select": nbytes["select"], "bytes_attend": nbytes["attend"],
+        "timing": dict(wst, how="value and ms_per_step: the median window; each window times exactly `steps` "
+                                "steps, repeated until >= 0.2 s of device time"),
         "kernel_us": {k: round(v, 2) for k, v in kern_us.items()},
         "replay_us": rep_us,
-        "roofline": {"bound": "hbm", "kernel": dom_name,
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": step_traffic(s) if one else None,
-                     "peak_kind": f"{peak_kind} (burst copy)"},
-        "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4)},
+        "roofline": roofline_block(dom_name, achieved, peak, peak_kind, step_traffic(s) if one else None,
+                                   dense["GB/s"] if dense else None),
+        "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4),
+                          "single_step_graph_frac": None if single is None else round(single / peak, 4)},
         "dense": dense,
         "decode_loop": loop_rec,
-        "speedup_vs_dense": round(dense["us_per_step"] / (1e6 * t_max / args.steps), 2) if dense else None,
-        "gpu_launches": (1 if one else 3) * args.steps,  # one step kernel, or score, top-k, attend
+        "speedup_vs_dense": round(dense["us_per_step"] / (1e3 * ms_step), 2) if dense else None,
+        "gpu_launches": launches * args.steps,  # per timed window of `steps` steps
+        "gpu_launches_all_windows": launches * args.steps * wst["windows"],
         "paths": {"at_capture": paths_capture,
                   "timed_rows_dense": timed_rows["step_rows_dense"],
                   "timed_rows_all_keys": timed_rows["step_rows_all_keys"]},
@@ -627,104 +711,160 @@ def delta_bytes(s: W.Spec, ctx, count, block_idx) -> dict:
 
 
 def run_delta(args, s: W.Spec):
-    """The top-delta step on the FFD workload, with the exact-key attend and
-    with the refined (2-bit + 8-bit residual) attend."""
+    """The top-delta step on the FFD workload: select_delta, then attention
+    over the kept blocks with the exact (bf16) keys, which is the workload's
+    step; the refined (2-bit + 8-bit residual) attend is timed beside it."""
     import torch
     from sparse_long_context_gb300 import _lib
     from sparse_long_context_gb300 import harness as H
     from sparse_long_context_gb300 import ops
 
     torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     _lib.load()
     host = W.generate(s)
     dw = H.upload(s, host)
     codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block)
-    exact = ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits)
-    refined = ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits, refined=True)
+    first_sel, first_cnt, first_out, _ = H.run_step(dw, args.splits)
+    probe = ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits)
+    probe.select(dw.q, dw.K, codes, scales, dw.ctx)
+    nb = delta_bytes(s, host.ctx_len, probe.count.cpu().numpy(), probe.block_idx.cpu().numpy())
+    tot_exact, tot_ref = nb["scan"] + nb["attend_exact"], nb["scan"] + nb["attend_refined"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(2, math.ceil(4 * l2 / tot_ref))
+    sets = [(dw.K, dw.V, codes, scales, res)] + [
+        (dw.K.clone(), dw.V.clone(), codes.clone(), scales.clone(), res.clone()) for _ in range(nsets - 1)]
+    exact = [ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits) for _ in sets]
+    refined = [ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits, refined=True) for _ in sets]
     stream = torch.cuda.Stream()
     spg = next(r for r in (8, 4, 2, 1) if args.steps % r == 0)
-    graphs = {}
-    with torch.cuda.stream(stream):
-        exact(dw.q, dw.K, dw.V, codes, scales, dw.ctx, dw.sink)
-        refined(dw.q, dw.K, dw.V, codes, scales, dw.ctx, dw.sink, res=res)
-        torch.cuda.synchronize()
-        for name, st in (("exact", exact), ("refined", refined)):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for _ in range(spg):
-                    st(dw.q, dw.K, dw.V, codes, scales, dw.ctx, dw.sink, res=res)
-            graphs[name] = g
-    ops.pipeline_check()
-    nb = delta_bytes(s, host.ctx_len, refined.count.cpu().numpy(), refined.block_idx.cpu().numpy())
+
+    def run(st, bufs):
+        K, V, c, sc, r = bufs
+        return st(dw.q, K, V, c, sc, dw.ctx, dw.sink, res=r)
+
+    g_exact, m_exact = capture_graphs(stream, sets, exact, run, nsets, spg)
+    g_ref, m_ref = capture_graphs(stream, sets, refined, run, nsets, spg)
+    paths_capture = {k: v for k, v in ops.get_stats(reset=True).items() if v}
     clocks = ClockSampler(0)
     clocks.start()
     time.sleep(0.3)
-    us = {}
-    with torch.cuda.stream(stream):
-        for name, g in graphs.items():
-            for _ in range(-(-args.warmup // spg)):
-                g.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(args.steps // spg):
-                g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            us[name] = 1e3 * e0.elapsed_time(e1) / args.steps
-        # per-stage device time, eager launches between events
-        ev = {k: [] for k in ("select", "attend_exact", "attend_refined")}
-        for i in range(50):
-            if i % 10 == 0:
-                torch.cuda._sleep(int(2e7))
-            for name, fn in (("select", lambda: refined.select(dw.q, dw.K, codes, scales, dw.ctx)),
-                             ("attend_exact", lambda: exact.attend(dw.q, dw.K, dw.V, dw.ctx, dw.sink)),
-                             ("attend_refined", lambda: refined.attend_refined(dw.q, dw.K, dw.V, codes, scales,
-                                                                               res, dw.ctx, dw.sink))):
-                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                fn()
-                b_.record(stream)
-                ev[name].append((a, b_))
-    torch.cuda.synchronize()
+    res_t = {}
+    w0 = time.time()
+    for name, mg in (("exact", m_exact), ("refined", m_ref)):
+        with torch.cuda.stream(stream):
+            for i in range(-(-args.warmup // spg)):
+                mg[i % nsets].replay()
+        torch.cuda.synchronize()
+        res_t[name] = timed_windows(stream, mg, args.steps, spg, 1)
+    w1 = time.time()
+    clocks.window(w0, w1)
+    ops.pipeline_check()
+    rep_us = replay_spread(stream, g_exact, args.steps)
+
+    def stages_for(i):
+        e, r = exact[i % nsets], refined[i % nsets]
+        K, V, c, sc, rr = sets[i % nsets]
+        return [("select", lambda: e.select(dw.q, K, c, sc, dw.ctx)),
+                ("attend_exact", lambda: e.attend(dw.q, K, V, dw.ctx, dw.sink)),
+                ("attend_refined", lambda: r.attend_refined(dw.q, K, V, c, sc, rr, dw.ctx, dw.sink))]
+    for i in range(nsets):  # every set's lists, for the eager stages below
+        exact[i].select(dw.q, sets[i][0], sets[i][2], sets[i][3], dw.ctx)
+        refined[i].select(dw.q, sets[i][0], sets[i][2], sets[i][3], dw.ctx)
+    kus = stage_times(stream, [stages_for(i) for i in range(nsets)], 60)
     ops.pipeline_check()
     clk = clocks.stop()
-    kus = {k: 1e3 * statistics.mean(a.elapsed_time(b_) for a, b_ in v) for k, v in ev.items()}
+
+    # end to end: H2D q (pinned) + the step + D2H out, one graph per set,
+    # each step followed by a host synchronise
+    q_host = dw.q.cpu().pin_memory()
+    out_host = torch.empty(exact[0].out.shape, dtype=exact[0].out.dtype).pin_memory()
+    q_dev = torch.empty_like(dw.q)
+    esteps = max(10, min(args.steps, 200))
+    egraphs = []
+    with torch.cuda.stream(stream):
+        for u in range(nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                q_dev.copy_(q_host, non_blocking=True)
+                K, V, c, sc, r = sets[u]
+                o, _ = exact[u](q_dev, K, V, c, sc, dw.ctx, dw.sink)
+                out_host.copy_(o, non_blocking=True)
+            egraphs.append(g)
+        for i in range(3):
+            egraphs[i % nsets].replay()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for i in range(esteps):
+            egraphs[i % nsets].replay()
+            stream.synchronize()
+        e2e_t = time.perf_counter() - t0
+    del egraphs
+
     peak, peak_kind = load_peaks()
-    tot_ref = nb["scan"] + nb["attend_refined"]
-    value = tot_ref / (us["refined"] * 1e-6) / 1e9
-    achieved = nb["attend_refined"] / (kus["attend_refined"] * 1e-6) / 1e9
-    kept = int(refined.count.sum().item())
+    t_ex = statistics.median(res_t["exact"]) / args.steps
+    t_rf = statistics.median(res_t["refined"]) / args.steps
+    value = tot_exact / t_ex / 1e9
+    kept = int(probe.count.sum().item())
     nblk = sum(-(-n // s.block) for n in s.ctx_len) * s.num_kv_heads
+    dom = "attend_exact" if nb["attend_exact"] >= nb["scan"] else "select"
+    achieved = nb[dom if dom != "select" else "scan"] / (kus[dom] * 1e-6) / 1e9
     line = {
-        "metric": "top-delta decode step us and achieved HBM GB/s, refined attend", "value": round(value, 2),
-        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(us["refined"] / 1e3, 5), "us_per_step": round(us["refined"], 2),
-        "us_per_step_exact_attend": round(us["exact"], 2), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy, see workloads.py)",
-        "config": {"workload": f"{s.name}: B={s.batch} Hq={s.num_q_heads} Hkv={s.num_kv_heads} D={s.head_dim} "
-                               f"ctx={s.ctx_len[0]} block={s.block} delta={s.delta} bf16",
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_ex * 1e3, 5), "us_per_step": round(t_ex * 1e6, 2),
+        "tokens_per_s": round(s.batch / t_ex, 1), "frac_of_peak": round(value / peak, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": s.dtype,
+        "data": "synthetic (seeded numpy, see workloads.py)",
+        "config": {"workload": _workload_name(s), "batch": s.batch, "ctx_len": s.ctx_len[0],
                    "kept_blocks": kept, "kept_fraction": round(kept / nblk, 4), "steps_per_graph": spg,
-                   "l2": f"one buffer set of {(tot_ref) / 1e6:.0f} MB per step (> L2)"},
-        "bytes_per_step": tot_ref, "bytes": nb,
+                   "launches_per_step": 3, "buffer_sets": nsets,
+                   "l2": f"inputs rotate over {nsets} buffer sets ({nsets * tot_ref / 1e6:.0f} MB >= 4x L2 "
+                         f"{l2 / 1e6:.0f} MB)"},
+        "bytes_per_step": tot_exact, "bytes": nb,
+        "timing": dict(window_stats(res_t["exact"], args.steps),
+                       how="value and ms_per_step: the median window of the step with the exact attend"),
+        "refined_step": {"us_per_step": round(t_rf * 1e6, 2), "bytes_per_step": tot_ref,
+                         "GB/s": round(tot_ref / t_rf / 1e9, 1), "frac_of_peak": round(tot_ref / t_rf / 1e9 / peak, 4),
+                         "timing": window_stats(res_t["refined"], args.steps)},
         "kernel_us": {k: round(v, 2) for k, v in kus.items()},
-        "roofline": {"bound": "hbm", "kernel": "attend_refined_kernel (combine fused)",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None, "peak_kind": f"{peak_kind} (burst copy)"},
-        "gpu_launches": 3 * args.steps,  # delta scan, compaction, refined attend
+        "stage_GBs": {"select": round(nb["scan"] / (kus["select"] * 1e-6) / 1e9, 1),
+                      "attend_exact": round(nb["attend_exact"] / (kus["attend_exact"] * 1e-6) / 1e9, 1),
+                      "attend_refined": round(nb["attend_refined"] / (kus["attend_refined"] * 1e-6) / 1e9, 1)},
+        "replay_us": rep_us,
+        "roofline": roofline_block("attend_balanced_kernel (stream-K attend, bf16 keys, combine fused)"
+                                   if dom == "attend_exact" else "delta_scan_mma_kernel + delta_compact_kernel",
+                                   achieved, peak, peak_kind, None),
+        "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4)},
+        "gpu_launches": 3 * args.steps,  # scan, compaction, attend; per timed window of `steps` steps
+        "paths": {"at_capture": paths_capture},
         "clocks": clk,
+        "e2e": {"value": round(tot_exact * esteps / e2e_t / 1e9, 2), "unit": "GB/s",
+                "us_per_step": round(1e6 * e2e_t / esteps, 2),
+                "how": "per step: graph replay of H2D q (pinned) + step + D2H out, then a host synchronise",
+                "h2d_bytes_per_step": int(q_host.numel() * q_host.element_size()),
+                "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
     }
+    if not args.no_cpu_baseline:
+        line["parity"] = parity_check(s, host, first_sel, first_out, first_cnt)
+        rows = [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]
+        ncore = os.cpu_count() or 1
+        gbs, cores, wall, nbo, reps = cpu_oracle(s, host, rows, threads=ncore, min_busy=0.25)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "cpu": cpu_model(),
+                                "sample": f"all {len(rows)} rows of one step (exact attend), fp64 C++ oracle on "
+                                          f"{cores} std::threads, {reps} row evaluations, {nbo / 1e6:.0f} MB in "
+                                          f"{wall:.1f} s ({wall * cores:.0f} core-s)"}
     print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="qwen1p5b", choices=("qwen1p5b", "qwen7b", "ffd"),
-                    help="ffd: the top-delta step with exact and refined attends (a study line)")
+    ap.add_argument("--workload", default="qwen1p5b", choices=W.CONFIG_NAMES,
+                    help="qwen1p5b (default), qwen7b, gptoss, tiny: the Quest step; ffd: the top-delta step")
     ap.add_argument("--ctx", type=int, default=None, help="context length (default: the workload's)")
     ap.add_argument("--batch", type=int, default=None, help="sequences per GPU (default: the workload's)")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-decode comparison")

@@ -257,7 +257,10 @@ size_t sls_select_pages_workspace_size(const sls_attn_desc* desc);
  *   return SLS_EWORKSPACE and enqueue nothing.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before capturing a stream.
+ *   before capturing a stream.  The address is cached with the id of the
+ *   device's CUDA context: after a cudaDeviceReset (a new context, the
+ *   array at a new address) the next call looks it up again, so make that
+ *   call outside stream capture too.
  *   All calls share the array: calls whose kernels may overlap on the GPU
  *   (other streams, other host threads) race on it and must be serialised
  *   by the caller.  No part of it needs to be zero.
