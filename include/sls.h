@@ -64,6 +64,7 @@ typedef int sls_status;
 #define SLS_EWORKSPACE   -4  /* workspace missing or too small */
 #define SLS_ECUDA        -5  /* a CUDA launch or attribute call failed */
 #define SLS_ETIMEOUT     -6  /* a pipelined kernel gave up waiting for its own copies */
+#define SLS_EDEVICE      -7  /* a kernel met page-list entries it could not use (skipped) */
 
 /* ---- element types ----------------------------------------------------- */
 #define SLS_DTYPE_F32  0
@@ -77,6 +78,15 @@ typedef int sls_status;
  * instead of the shared-memory ring filled by tensor-map copies (for
  * comparison; results agree within the same tolerances). */
 #define SLS_FLAG_NO_TMA 2
+/* Test hook of the bounded waits, not for production: in the tensor-map fed
+ * kernels (sls_sparse_decode_attend[_combine] on bf16 pages of >= 16 tokens,
+ * and the one-launch sls_quest_decode_step), the first CTA of the launch
+ * announces 16 bytes on its first attend stage that it never requests, and
+ * that CTA's waits poll a short while only.  The waits on that stage
+ * give up, the first row's outputs become NaN, and the next
+ * sls_pipeline_check() returns SLS_ETIMEOUT.  No copy is issued for the
+ * announced bytes, so nothing faults and nothing waits forever. */
+#define SLS_FLAG_TEST_WAIT_TIMEOUT 4
 
 /*
  * Shapes and element type of one attention layer's decode step.
@@ -492,12 +502,22 @@ sls_status sls_selection_recall(const sls_attn_desc* desc, const void* q, const 
 const char* sls_last_error(void);
 
 /*
- * Health of the pipelined kernels.  Kernels that stage data through shared
- * memory wait for their copies with a bounded number of polls; a wait that
- * gives up makes the affected outputs NaN and is counted on the device.
- * This call synchronises the device, reads and clears that count, and returns
- * SLS_ETIMEOUT if it was non-zero (SLS_ECUDA if the device cannot be read),
- * else SLS_OK.
+ * Device status of the kernels since the previous check ("perf(core): fused
+ * sparse-attention decode via page indirection", Making the selection
+ * inspectable: every call has an observable outcome).  Two kinds of events
+ * are counted on the device:
+ *   - a bounded wait on a copy pipeline that gave up (kernels that stage data
+ *     through shared memory poll their copies a bounded number of times; the
+ *     affected outputs become NaN);
+ *   - a page-list entry that is neither a page of the pool [0, Cap/P) nor the
+ *     -1 padding (the attend and recall kernels skip it: it gives no token).
+ * This call synchronises the device, reads and clears the counts (one atomic
+ * exchange per word, so no count is lost), and returns SLS_ETIMEOUT if any
+ * wait gave up, else SLS_EDEVICE if any bad entry was met, else SLS_OK
+ * (SLS_ECUDA if the device cannot be read); the message gives the counts.
+ * The counts are global to the process: they cover every launch since the
+ * previous check, on every stream and host thread, so only calls ordered
+ * with the check are attributed to it.
  */
 sls_status sls_pipeline_check(void);
 

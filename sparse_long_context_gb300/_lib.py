@@ -10,10 +10,11 @@ from . import build as _build
 LIB_PATH = _build.LIB
 
 SLS_OK, SLS_EINVAL, SLS_EUNSUPPORTED, SLS_EOVERFLOW, SLS_EWORKSPACE, SLS_ECUDA = 0, -1, -2, -3, -4, -5
-SLS_ETIMEOUT = -6
+SLS_ETIMEOUT, SLS_EDEVICE = -6, -7
 SLS_DTYPE_F32, SLS_DTYPE_BF16 = 0, 1
 SLS_FLAG_CUDA_CORES = 1
 SLS_FLAG_NO_TMA = 2
+SLS_FLAG_TEST_WAIT_TIMEOUT = 4  # test hook of the bounded waits (include/sls.h)
 
 
 class AttnDesc(ctypes.Structure):

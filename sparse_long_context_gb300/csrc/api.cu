@@ -63,7 +63,8 @@ sls_status check_desc(const sls_attn_desc* d, sls::Shape* s) {
     return fail(SLS_EINVAL, "capacity %d must be >= 1 and a multiple of page_size %d", d->capacity,
                 d->page_size);
   if (!(d->scale >= 0.f) || std::isinf(d->scale)) return fail(SLS_EINVAL, "scale must be finite and >= 0");
-  if (d->flags & ~(SLS_FLAG_CUDA_CORES | SLS_FLAG_NO_TMA)) return fail(SLS_EINVAL, "unknown flags 0x%x", d->flags);
+  if (d->flags & ~(SLS_FLAG_CUDA_CORES | SLS_FLAG_NO_TMA | SLS_FLAG_TEST_WAIT_TIMEOUT))
+    return fail(SLS_EINVAL, "unknown flags 0x%x", d->flags);
   // element counts of the caches and of the per-row index space
   int64_t rows, elems;
   if (!checked_mul(d->batch, d->num_kv_heads, &rows) || !checked_mul(rows, d->capacity, &elems) ||
@@ -146,8 +147,18 @@ sls_status sls_get_stats(sls_stats* out, int32_t reset) {
 
 sls_status sls_pipeline_check(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(SLS_ECUDA, "device synchronisation failed");
-  const unsigned int n = sls::take_attend_wait_timeouts() + sls::take_step_wait_timeouts();
-  if (n) return fail(SLS_ETIMEOUT, "%u pipelined CTA(s) gave up waiting for their copies", n);
+  unsigned int timeouts = 0, bad = 0;
+  for (auto take : {sls::take_status_attend_cc, sls::take_status_attend_mma, sls::take_status_attend_tma,
+                    sls::take_status_attend_refined, sls::take_status_quest_step, sls::take_status_recall}) {
+    const sls::DeviceStatus st = take();
+    timeouts += st.wait_timeouts;
+    bad += st.bad_page_ids;
+  }
+  if (cudaGetLastError() != cudaSuccess) return fail(SLS_ECUDA, "reading the device status words failed");
+  if (timeouts)
+    return fail(SLS_ETIMEOUT, "%u pipelined CTA(s) gave up waiting for their copies (%u bad page-list entries)",
+                timeouts, bad);
+  if (bad) return fail(SLS_EDEVICE, "%u page-list entries were neither a page of the pool nor -1 (skipped)", bad);
   return SLS_OK;
 }
 

@@ -41,6 +41,7 @@ attend_cc_kernel(const AttendArgs a) {
   const int32_t* plist = a.page_idx ? a.page_idx + (size_t)row * a.idx_stride + sl.e0 : nullptr;
   const T* kb = static_cast<const T*>(a.k) + (size_t)row * a.Cap * D + sub * EPL;
   const T* vb = static_cast<const T*>(a.v) + (size_t)row * a.Cap * D + sub * EPL;
+  stage_page_list(nullptr, 0, plist, sl.e0, sl.nent, a.Cap >> a.pshift, threadIdx.x, NW * 32);  // count bad ids
 
   float qv[GM][EPL];
   {
@@ -257,7 +258,7 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ m_par
   const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
 #pragma unroll
   for (int i = 0; i < CPL; ++i) out[(size_t)idx * D + lane * CPL + i] = from_f32<T>(acc[i] * inv);
-  if (lse && lane == 0) lse[idx] = Ls > 0.f ? M + logf(Ls) : kNegInf;
+  if (lse && lane == 0) lse[idx] = Ls == 0.f ? kNegInf : M + logf(Ls);
 }
 
 template <typename T, int D, int GM>
@@ -327,6 +328,7 @@ cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const vo
   a.o_part = o_part; a.m_part = m_part; a.l_part = l_part;
   a.idx_stride = idx_stride; a.k_fixed = k_fixed; a.S = num_splits;
   a.cluster = 0;
+  a.test_wait = (s.flags & kFlagTestWaitTimeout) ? 1 : 0;
   if (num_splits == 0) {  // the library schedules (fused call only)
     const int entries = page_idx ? (count ? idx_stride : k_fixed) : (s.Cap >> s.pshift);
     a.S = attend_default_splits(s, entries > 0 ? entries : 1);
@@ -335,7 +337,7 @@ cudaError_t launch_attend(const Shape& s, const void* q, const void* k, const vo
   a.Hq = s.Hq; a.Hkv = s.Hkv; a.G = s.G; a.Cap = s.Cap; a.P = s.P; a.pshift = s.pshift;
   a.qscale = s.scale * kLog2e;
   const int rows = s.B * s.Hkv;
-  if (!(s.flags & 1)) {
+  if (!(s.flags & kFlagCudaCores)) {
     bool handled = false;
     cudaError_t e = launch_attend_tma(s, a, st, &handled);
     if (handled) {
@@ -380,5 +382,7 @@ cudaError_t launch_combine(const Shape& s, const float* o_part, const float* m_p
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+DeviceStatus take_status_attend_cc() { return take_status_here(); }
 
 }  // namespace sls

@@ -2,6 +2,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "status.cuh"
 
 namespace sls {
 
@@ -25,6 +26,7 @@ struct AttendArgs {
   float* lse;         // [B, Hq] or null
   int cluster;        // 1: the S splits of a row form one thread-block cluster and
                       // combine through distributed shared memory (no partials in global memory)
+  int test_wait = 0;  // wait-timeout test hook: CTA 0 plants a copy phase that never completes
 };
 
 // Slice [e0, e1) of row `row`'s page list handled by split `split`.
@@ -47,6 +49,21 @@ __device__ __forceinline__ Slice attend_slice(const AttendArgs& a, int row, int 
   const int e1 = min(sl.e0 + per, cnt);
   sl.nent = e1 > sl.e0 ? e1 - sl.e0 : 0;
   return sl;
+}
+
+// Copies list entries [0, min(nent, cap)) into s_pg (shared memory) and counts
+// the entries of [0, nent) that are neither a page of the pool nor -1, once
+// per CTA (bad entries are skipped by the kernels: they give no token).
+// plist null: the dense list e0, e0 + 1, ...
+__device__ __forceinline__ void stage_page_list(int* s_pg, int cap, const int32_t* plist, int e0, int nent,
+                                                int npages, int tid, int nthreads) {
+  unsigned int bad = 0;
+  for (int e = tid; e < nent; e += nthreads) {
+    const int pg = plist ? __ldg(plist + e) : e0 + e;
+    if (e < cap) s_pg[e] = pg;
+    bad += bad_page_id(pg, npages) ? 1u : 0u;
+  }
+  note_bad_pages(bad);
 }
 
 // Position of a token given its page (or -1 when the slot is empty, the
@@ -101,7 +118,7 @@ __device__ __forceinline__ void combine_row_if_last(const AttendArgs& a, int row
     if (lane == 0) {
       s_m[g] = M;
       s_inv[g] = Ls > 0.f ? 1.f / Ls : 0.f;
-      if (a.lse) a.lse[hq0 + g] = Ls > 0.f ? M + logf(Ls) : kNegInf;
+      if (a.lse) a.lse[hq0 + g] = Ls == 0.f ? kNegInf : M + logf(Ls);
     }
   }
   __syncthreads();

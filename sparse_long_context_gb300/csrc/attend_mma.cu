@@ -206,8 +206,7 @@ __device__ __forceinline__ void attend_run(const AttendArgs& a, int row, const S
   const bf16* kl = static_cast<const bf16*>(a.k) + (size_t)row * a.Cap * D + m * 8;    // chunk 4s+m: +32s
   const bf16* vl = static_cast<const bf16*>(a.v) + (size_t)row * a.Cap * D + r * CPR;  // lane's V channels
 
-  for (int i = threadIdx.x; i < min(sl.nent, kStagedEntries); i += NW * 32)
-    sh.s_pg[i] = plist ? __ldg(plist + i) : sl.e0 + i;
+  stage_page_list(sh.s_pg, kStagedEntries, plist, sl.e0, sl.nent, a.Cap >> a.pshift, threadIdx.x, NW * 32);
 
   // Q as the A operand: row r = head r (rows 8..15 are zero)
   uint32_t qa[NS][4];
@@ -324,5 +323,7 @@ cudaError_t launch_attend_mma(const Shape& s, const AttendArgs& a, cudaStream_t 
   if (s.D == 128) return paged ? attend_mma_launch<128, true>(a, grid, st) : attend_mma_launch<128, false>(a, grid, st);
   return paged ? attend_mma_launch<64, true>(a, grid, st) : attend_mma_launch<64, false>(a, grid, st);
 }
+
+DeviceStatus take_status_attend_mma() { return take_status_here(); }
 
 }  // namespace sls

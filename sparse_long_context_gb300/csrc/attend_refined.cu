@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kRefWarps * 32, 1) attend_balanced_kernel(cons
     sl.nent = (int)(seg_end - e);
     sl.ntok = sl.nent << a.pshift;
     const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + e0;
-    for (int i = threadIdx.x; i < min(sl.nent, kRefStaged); i += NT) sh.s_pg[i] = __ldg(plist + i);
+    stage_page_list(sh.s_pg, kRefStaged, plist, 0, sl.nent, a.Cap >> a.pshift, threadIdx.x, NT);
 
     uint32_t qa[NS][4];
     {
@@ -640,5 +640,7 @@ cudaError_t launch_attend_refined(const Shape& s, const void* q, const void* k, 
   ra.res = res;
   return s.D == 128 ? balanced_launch<128>(ra, st) : balanced_launch<64>(ra, st);
 }
+
+DeviceStatus take_status_attend_refined() { return take_status_here(); }
 
 }  // namespace sls

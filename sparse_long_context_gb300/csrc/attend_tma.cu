@@ -29,7 +29,6 @@ namespace sls {
 constexpr int kTmaMinBlocks = 3;      // resident CTAs per SM the budgets are sized for
 constexpr int kTmaStaged = 256;       // page-list entries staged in shared memory
 
-__device__ unsigned int g_attend_wait_timeouts = 0;
 
 // First cache position of group gi of the slice and the number of its tokens
 // inside the context (<= 0 when the group is empty: padded entry, page out
@@ -80,7 +79,7 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   const int row = blockIdx.x / a.S, split = blockIdx.x % a.S;
   const Slice sl = attend_slice(a, row, split);
   const int32_t* plist = a.page_idx ? a.page_idx + (size_t)row * a.idx_stride + sl.e0 : nullptr;
-  for (int e = threadIdx.x; e < min(sl.nent, kTmaStaged); e += NT) s_pg[e] = plist ? __ldg(plist + e) : sl.e0 + e;
+  stage_page_list(s_pg, kTmaStaged, plist, sl.e0, sl.nent, a.Cap >> a.pshift, threadIdx.x, NT);
   __syncthreads();
   const int ngroups = (sl.nent << a.pshift) >> 4;
   const int b = row / a.Hkv, h = row % a.Hkv;
@@ -91,6 +90,11 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
 #pragma unroll
   for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
 
+  // the wait-timeout test hook: CTA 0 announces bytes for its first stage
+  // that it never requests, and its waits poll briefly
+  const bool plant = a.test_wait && blockIdx.x == 0;
+  const uint32_t tries = plant ? kTestWaitTries : kWaitTries;
+
   if (warp == W) {
     // producer: lane 0 issues the copies of every group in order
     if (lane == 0) {
@@ -99,13 +103,15 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       for (int gi = 0; gi < ngroups; ++gi) {
         const int st = gi % NST;
         const uint32_t use = gi / NST;
-        if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1)) {
+        if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1, tries)) {
           ok = false;
           break;
         }
         int lim;
         const int base = group_base(a, sl, s_pg, plist, gi, lim);
-        if (lim > 0) {
+        if (plant && gi == 0) {
+          mbar_arrive_expect_tx(&full[st], 16);  // no copy is issued: this phase never completes
+        } else if (lim > 0) {
           mbar_arrive_expect_tx(&full[st], L::STAGE);
           const int y = row * a.Cap + base;
           unsigned char* dst = ring + st * L::STAGE;
@@ -118,8 +124,8 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       }
       // every copy issued has landed before the CTA reuses or leaves the ring
       for (int gi = max(0, issued - NST); gi < issued; ++gi)
-        if (!mbar_wait(&full[gi % NST], (gi / NST) & 1)) ok = false;
-      if (!ok) atomicAdd(&g_attend_wait_timeouts, 1u);
+        if (!mbar_wait(&full[gi % NST], (gi / NST) & 1, tries)) ok = false;
+      if (!ok) note_wait_timeout();
     }
   } else {
     const int r = lane >> 2, m = lane & 3;
@@ -136,7 +142,7 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     bool ok = true;
     for (int gi = warp; gi < ngroups; gi += W) {
       const int st = gi % NST;
-      if (!mbar_wait(&full[st], (gi / NST) & 1)) {
+      if (!mbar_wait(&full[st], (gi / NST) & 1, tries)) {
         ok = false;
         break;
       }
@@ -147,8 +153,11 @@ attend_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       if (lane == 0) mbar_arrive(&empty[st]);
     }
     if (!ok) {
-      if (lane == 0) atomicAdd(&g_attend_wait_timeouts, 1u);
-      m_run = __int_as_float(0x7fffffff);  // the row's output becomes NaN
+      if (lane == 0) note_wait_timeout();
+      // an infinite running max makes this warp's merge weight inf - inf = NaN
+      // at every later merge, so the row's output and lse become NaN (a NaN
+      // max would be dropped by fmaxf and the partial silently ignored)
+      m_run = __int_as_float(0x7f800000);
     }
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
@@ -309,14 +318,6 @@ cudaError_t launch_attend_tma(const Shape& s, const AttendArgs& a, cudaStream_t 
   return s.D == 64 ? tma_launch<64>(s, a, st, handled) : tma_launch<128>(s, a, st, handled);
 }
 
-unsigned int take_attend_wait_timeouts() {
-  unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_attend_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
-  if (v) {
-    const unsigned int zero = 0;
-    cudaMemcpyToSymbol(g_attend_wait_timeouts, &zero, sizeof(zero));
-  }
-  return v;
-}
+DeviceStatus take_status_attend_tma() { return take_status_here(); }
 
 }  // namespace sls

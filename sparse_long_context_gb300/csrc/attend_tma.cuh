@@ -247,7 +247,7 @@ __device__ __forceinline__ void cluster_push_combine(const AttendArgs& a, int ro
     __nv_bfloat162* op = reinterpret_cast<__nv_bfloat162*>(static_cast<bf16*>(a.out) + (hq0 + g) * D + d);
     op[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
     op[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    if (d == 0 && a.lse) a.lse[hq0 + g] = Ls > 0.f ? M + logf(Ls) : kNegInf;
+    if (d == 0 && a.lse) a.lse[hq0 + g] = Ls == 0.f ? kNegInf : M + logf(Ls);
   }
 }
 

@@ -45,6 +45,11 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return launch_pdl_cluster(kern, grid, block, smem, 1, st, std::forward<Args>(args)...);
 }
 
+// Descriptor flags (the public SLS_FLAG_* values).
+constexpr int kFlagCudaCores = 1;
+constexpr int kFlagNoTma = 2;
+constexpr int kFlagTestWaitTimeout = 4;
+
 struct Shape {
   int B, Hq, Hkv, G, D, P, pshift, Cap, dtype, flags;
   float scale;
@@ -92,8 +97,18 @@ int attend_default_splits(const Shape& s, int max_entries);
 bool attend_tma_eligible(const Shape& s);
 int attend_tma_per_sm(const Shape& s);
 int attend_tma_splits(const Shape& s, int groups_per_row);
-// Reads and clears the count of attend CTAs whose bounded waits gave up.
-unsigned int take_attend_wait_timeouts();
+// Device status words of each translation unit whose kernels count them,
+// read and cleared by take_status_<unit>() (see status.cuh).
+struct DeviceStatus {
+  unsigned int bad_page_ids;   // page-list entries that are neither a page of the pool nor the -1 padding
+  unsigned int wait_timeouts;  // bounded waits on a copy pipeline that gave up
+};
+DeviceStatus take_status_attend_cc();
+DeviceStatus take_status_attend_mma();
+DeviceStatus take_status_attend_tma();
+DeviceStatus take_status_attend_refined();
+DeviceStatus take_status_quest_step();
+DeviceStatus take_status_recall();
 
 // Fused Quest step (bf16, pages of >= 16 tokens): select + attend + combine
 // in one launch.  *handled is false (and nothing is enqueued) when the shape
@@ -104,7 +119,6 @@ cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache
                               const void* kmin, const void* kmax, const int32_t* ctx_len, int k, int n_sink,
                               int n_local, const float* sink, int32_t* page_idx, void* out, float* lse,
                               int num_splits, float min_sparsity, cudaStream_t st, bool* handled);
-unsigned int take_step_wait_timeouts();
 
 // Selection quality: attention-mass recall of page lists (a diagnostic).
 size_t recall_workspace(const Shape& s);

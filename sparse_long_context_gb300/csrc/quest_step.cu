@@ -37,7 +37,6 @@ constexpr int kStepMaxChunk = 8192;  // pages scored by one CTA (keys kept in sh
 constexpr int kStepMaxK = 4096;      // page budget (the row's list sits in shared memory)
 constexpr uint32_t kForcedKey32 = 0xffffffffu;
 
-__device__ unsigned int g_step_wait_timeouts = 0;
 __device__ unsigned long long g_step_rows_dense = 0;     // rows attended densely (sparsity gate)
 __device__ unsigned long long g_step_rows_all_keys = 0;  // rows selected from all keys
 
@@ -665,10 +664,10 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   bool ok = true;    // this thread's waits all succeeded
 
   // producer's and consumers' walk of `n` stages starting at ring position seq0
-  auto producer_wait = [&](uint32_t q) -> bool {
+  auto producer_wait = [&](uint32_t q, uint32_t tries = kWaitTries) -> bool {
     const int st = q % NST;
     const uint32_t use = q / NST;
-    return use == 0 || mbar_wait(&empty[st], (use - 1) & 1);
+    return use == 0 || mbar_wait(&empty[st], (use - 1) & 1, tries);
   };
 
   if (dense) {
@@ -898,19 +897,25 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   float m_run = kNegInf, l_run = 0.f;
 #pragma unroll
   for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  // the wait-timeout test hook: CTA 0 announces bytes for its first attend
+  // stage that it never requests, and its attend waits poll briefly
+  const bool plant = a.test_wait && blockIdx.x == 0;
+  const uint32_t tries = plant ? kTestWaitTries : kWaitTries;
   if (warp == W) {
     if (lane == 0) {
       int issued = 0;
       for (int gi = 0; gi < ngroups; ++gi) {
         const uint32_t q = seq + gi;
         const int st = q % NST;
-        if (!producer_wait(q)) {
+        if (!producer_wait(q, tries)) {
           ok = false;
           break;
         }
         int lim;
         const int base = group_at(gi, lim);
-        if (lim > 0) {
+        if (plant && gi == 0) {
+          mbar_arrive_expect_tx(&full[st], 16);  // no copy is issued: this phase never completes
+        } else if (lim > 0) {
           mbar_arrive_expect_tx(&full[st], L::STAGE);
           const int y = row * a.Cap + base;
           unsigned char* dst = ring + st * L::STAGE;
@@ -924,9 +929,9 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       // every copy issued has landed before the ring is reused or left
       for (int gi = max(0, issued - NST); gi < issued; ++gi) {
         const uint32_t q = seq + gi;
-        if (!mbar_wait(&full[q % NST], (q / NST) & 1)) ok = false;
+        if (!mbar_wait(&full[q % NST], (q / NST) & 1, tries)) ok = false;
       }
-      if (!ok) atomicAdd(&g_step_wait_timeouts, 1u);
+      if (!ok) note_wait_timeout();
     }
   } else {
     const int r = lane >> 2, m = lane & 3;
@@ -941,7 +946,7 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     for (int gi = (W + warp - (int)(seq % W)) % W; gi < ngroups; gi += W) {
       const uint32_t q = seq + gi;
       const int st = q % NST;
-      if (!mbar_wait(&full[st], (q / NST) & 1)) {
+      if (!mbar_wait(&full[st], (q / NST) & 1, tries)) {
         ok = false;
         break;
       }
@@ -952,8 +957,11 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       if (lane == 0) mbar_arrive(&empty[st]);
     }
     if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0) atomicAdd(&g_step_wait_timeouts, 1u);
-      m_run = __int_as_float(0x7fffffff);  // the row's output becomes NaN
+      if (lane == 0) note_wait_timeout();
+      // an infinite running max makes this warp's merge weight inf - inf = NaN
+      // at every later merge, so the row's output and lse become NaN (a NaN
+      // max would be dropped by fmaxf and the partial silently ignored)
+      m_run = __int_as_float(0x7f800000);
     }
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
@@ -1090,6 +1098,7 @@ cudaError_t launch_quest_step(const Shape& s, const void* q, const void* k_cache
   a.out = out;
   a.lse = lse;
   a.cluster = 1;
+  a.test_wait = (s.flags & kFlagTestWaitTimeout) ? 1 : 0;
   a.S = num_splits > 0 ? std::min(num_splits, kMaxClusterSplits) : quest_step_splits(s, k);
   sa.page_idx = page_idx;
   sa.k = k;
@@ -1114,14 +1123,6 @@ void take_step_row_stats(unsigned long long* dense, unsigned long long* all_keys
   }
 }
 
-unsigned int take_step_wait_timeouts() {
-  unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_step_wait_timeouts, sizeof(v)) != cudaSuccess) return 0;
-  if (v) {
-    const unsigned int zero = 0;
-    cudaMemcpyToSymbol(g_step_wait_timeouts, &zero, sizeof(zero));
-  }
-  return v;
-}
+DeviceStatus take_status_quest_step() { return take_status_here(); }
 
 }  // namespace sls

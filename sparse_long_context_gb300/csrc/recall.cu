@@ -11,6 +11,7 @@
 //                        merges its threads' triples and writes one per head.
 // recall_combine_kernel  merges the splits of each (row, head): s / z.
 #include "common.cuh"
+#include "status.cuh"
 #include "launch.h"
 
 namespace sls {
@@ -56,10 +57,13 @@ recall_partial_kernel(const void* q_, const void* k_, const int32_t* page_idx, i
     int cnt = count ? count[row] : k_fixed;
     cnt = cnt < 0 ? 0 : (cnt > idx_stride ? idx_stride : cnt);
     const int32_t* pl = page_idx + (size_t)row * idx_stride;
+    unsigned int bad = 0;
     for (int e = threadIdx.x; e < cnt; e += kRecallThreads) {
       const int pg = pl[e];
       if (pg >= 0 && pg < NP) atomicOr(&bitmap[pg >> 5], 1u << (pg & 31));
+      bad += (split == 0 && bad_page_id(pg, Cap >> pshift)) ? 1u : 0u;  // counted by one CTA of the row
     }
+    note_bad_pages(bad);
   }
   __syncthreads();
   const int per = (N + S - 1) / S;
@@ -167,5 +171,7 @@ cudaError_t launch_recall(const Shape& s, const void* q, const void* k, const in
   return s.D == 64 ? recall_launch_g<bf16, 64>(s, q, k, page_idx, idx_stride, count, k_fixed, ctx_len, recall, part, st)
                    : recall_launch_g<bf16, 128>(s, q, k, page_idx, idx_stride, count, k_fixed, ctx_len, recall, part, st);
 }
+
+DeviceStatus take_status_recall() { return take_status_here(); }
 
 }  // namespace sls

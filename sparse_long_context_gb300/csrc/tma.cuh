@@ -12,6 +12,10 @@
 namespace sls {
 
 constexpr uint32_t kWaitTries = 1u << 22;
+// Poll limit of the waits of the CTA that plants a never-completing phase
+// under the wait-timeout test hook (SLS_FLAG_TEST_WAIT_TIMEOUT), so that its
+// waits give up quickly; every other CTA keeps kWaitTries.
+constexpr uint32_t kTestWaitTries = 1u << 12;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -36,11 +40,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// Waits until the phase of parity `parity` has completed.  The caller must
-// know that this phase is the barrier's current or previous one.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Waits until the phase of parity `parity` has completed, polling at most
+// `tries` times.  The caller must know that this phase is the barrier's
+// current or previous one.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t tries = kWaitTries) {
   const uint32_t addr = smem_u32(bar);
-  for (uint32_t it = 0; it < kWaitTries; ++it) {
+  for (uint32_t it = 0; it < tries; ++it) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"

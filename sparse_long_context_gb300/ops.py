@@ -36,11 +36,14 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
 
 
 def make_desc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, dtype,
-              scale: float = 0.0, cuda_cores: bool = False, no_tma: bool = False) -> L.AttnDesc:
+              scale: float = 0.0, cuda_cores: bool = False, no_tma: bool = False,
+              test_wait_timeout: bool = False) -> L.AttnDesc:
     """Descriptor of one layer's decode shapes (the C ABI's sls_attn_desc); dtype is a torch dtype
-    or an SLS_DTYPE_* code, scale 0 means 1/sqrt(head_dim)."""
+    or an SLS_DTYPE_* code, scale 0 means 1/sqrt(head_dim).  test_wait_timeout sets the
+    bounded-wait test hook (SLS_FLAG_TEST_WAIT_TIMEOUT; tests only)."""
     code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
-    flags = (L.SLS_FLAG_CUDA_CORES if cuda_cores else 0) | (L.SLS_FLAG_NO_TMA if no_tma else 0)
+    flags = ((L.SLS_FLAG_CUDA_CORES if cuda_cores else 0) | (L.SLS_FLAG_NO_TMA if no_tma else 0)
+             | (L.SLS_FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0))
     return L.AttnDesc(batch, num_q_heads, num_kv_heads, head_dim, page_size, capacity, code,
                       flags, float(scale))
 
@@ -53,8 +56,10 @@ def get_stats(reset: bool = False) -> dict:
 
 
 def pipeline_check() -> None:
-    """Synchronises the device; raises SlsError if a pipelined kernel gave up
-    waiting for its copies since the last check."""
+    """Synchronises the device and reads the device status words; raises
+    SlsError with code SLS_ETIMEOUT if a pipelined kernel gave up waiting for
+    its copies, or SLS_EDEVICE if a kernel met (and skipped) page-list entries
+    that are neither a page of the pool nor -1, since the last check."""
     L.call("sls_pipeline_check")
 
 
