@@ -236,11 +236,13 @@ sls_status sls_thumb_residual_update(const sls_attn_desc* desc, const void* k_ca
  *            pages: k >= n_sink_pages + ceil(n_local_tokens/P) + 1
  *   page_idx [B*Hkv, k] int32 (written)
  *   workspace >= sls_select_pages_workspace_size() bytes of device memory
- *            (one 32-bit key per page of every row; contents on entry are
- *            ignored and on exit unspecified)
+ *            (one 32-bit key per page of every row, and for rows of more
+ *            than 8192 pages the candidates of the scoring CTAs: 12.5 more
+ *            bytes per page; contents on entry are ignored and on exit
+ *            unspecified)
  * The score is computed in fp32; two pages whose scores differ by less
  * than the fp32 rounding of the sum may rank either way.  Rows may hold at
- * most 8 * 32768 pages (Cap/P); larger capacities return SLS_EUNSUPPORTED.
+ * most 262144 pages (Cap/P); larger capacities return SLS_EUNSUPPORTED.
  */
 sls_status sls_select_pages(const sls_attn_desc* desc, const void* q,
                             const void* kmin, const void* kmax,
@@ -545,6 +547,8 @@ typedef struct sls_stats {
   uint64_t combine;                   /* separate combine launches */
   uint64_t metadata;                  /* page min/max, thumbnail, residual and append launches */
   uint64_t recall;                    /* selection-recall launches */
+  uint64_t select_rows_all_keys;      /* rows wider than 8192 pages whose sls_select_pages top-k
+                                         ranked all of the row's keys (the candidate check failed) */
 } sls_stats;
 
 /* Fills *out with the counters (synchronising the device to read the row

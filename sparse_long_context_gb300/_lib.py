@@ -31,7 +31,8 @@ class Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "quest_step_one_launch", "quest_step_two_launch", "step_rows_dense", "step_rows_all_keys",
         "select_pages", "select_delta_tensor_cores", "select_delta_cuda_cores", "attend_tma", "attend_mma",
-        "attend_cuda_cores", "attend_stream_k", "attend_refined", "combine", "metadata", "recall")]
+        "attend_cuda_cores", "attend_stream_k", "attend_refined", "combine", "metadata", "recall",
+        "select_rows_all_keys")]
 
 
 _P = ctypes.c_void_p

@@ -142,6 +142,7 @@ sls_status sls_get_stats(sls_stats* out, int32_t reset) {
   sls::take_step_row_stats(&dense, &all_keys, reset != 0);
   out->step_rows_dense = dense;
   out->step_rows_all_keys = all_keys;
+  out->select_rows_all_keys = sls::take_select_rows_all_keys(reset != 0);
   return ok();
 }
 
@@ -281,10 +282,9 @@ sls_status sls_select_pages(const sls_attn_desc* desc, const void* q, const void
                 (long long)forced_max);
   if (s.P == 1 && kmin != kmax)
     return fail(SLS_EINVAL, "page_size 1: pass the key cache as both kmin and kmax");
-  const size_t chunk = (size_t)(npcap + sls::select_pages_cluster() - 1) / sls::select_pages_cluster();
-  if (chunk * 4 > sls::select_pages_smem_limit())
-    return fail(SLS_EUNSUPPORTED, "Cap/P=%d pages per row exceeds the supported %zu", npcap,
-                sls::select_pages_smem_limit() / 4 * sls::select_pages_cluster());
+  if (npcap > sls::select_pages_max_pages())
+    return fail(SLS_EUNSUPPORTED, "Cap/P=%d pages per row exceeds the supported %d", npcap,
+                sls::select_pages_max_pages());
   const size_t need = sls::select_pages_workspace(s);
   if (!workspace || workspace_bytes < need)
     return fail(SLS_EWORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
@@ -485,10 +485,9 @@ sls_status sls_quest_decode_step(const sls_attn_desc* desc, const void* q, const
     return fail(SLS_EUNSUPPORTED, "min_sparsity needs the one-launch step (bf16, pages of >= 16 tokens)");
   // two launches: select into page_idx (or the workspace), then attend with the fused combine
   sls::stat_add(sls::kStatStepTwoLaunch);
-  const size_t chunk = (size_t)(npcap + sls::select_pages_cluster() - 1) / sls::select_pages_cluster();
-  if (chunk * 4 > sls::select_pages_smem_limit())
-    return fail(SLS_EUNSUPPORTED, "Cap/P=%d pages per row exceeds the supported %zu", npcap,
-                sls::select_pages_smem_limit() / 4 * sls::select_pages_cluster());
+  if (npcap > sls::select_pages_max_pages())
+    return fail(SLS_EUNSUPPORTED, "Cap/P=%d pages per row exceeds the supported %d", npcap,
+                sls::select_pages_max_pages());
   char* w = static_cast<char*>(workspace);
   void* sel_ws = w;
   w += align256(sls::select_pages_workspace(s));

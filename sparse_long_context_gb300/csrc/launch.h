@@ -149,6 +149,8 @@ void stat_add(StatId id);
 // Rows the one-launch step attended densely (sparsity gate) and rows whose
 // cluster selected from all of the row's keys, counted on the device.
 void take_step_row_stats(unsigned long long* dense, unsigned long long* all_keys, bool reset);
+// Wide rows of sls_select_pages whose top-k CTA selected from all keys.
+unsigned long long take_select_rows_all_keys(bool reset);
 
 inline int sm_count() {
   static int cache[64] = {0};
@@ -159,9 +161,7 @@ inline int sm_count() {
   return cache[dev] > 0 ? cache[dev] : 1;
 }
 
-// Largest dynamic shared memory one top-k CTA may use, and the largest
-// cluster it may spread a row over.
-size_t select_pages_smem_limit();
-int select_pages_cluster();
+// Most pages (Cap/P) a row of sls_select_pages may hold.
+int select_pages_max_pages();
 
 }  // namespace sls

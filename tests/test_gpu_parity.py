@@ -342,6 +342,61 @@ def test_topk_with_the_best_pages_in_one_split(splits, npg):
         assert st["step_rows_all_keys"] == 0, st
 
 
+def _wide_step(s, host, **kw):
+    dw = PT.upload(s, host, **kw)
+    ops.get_stats(reset=True)
+    sel, cnt, out, lse = PT.run_step(dw, one_launch=False)
+    return dw, sel, cnt, out, lse, ops.get_stats(reset=True)
+
+
+@pytest.mark.parametrize("ctx", [[20000, 9000], [65536, 131072 - 5]])
+def test_wide_rows_rank_the_scoring_ctas_candidates(ctx):
+    """Rows of more than 8192 one-token pages: the scoring CTAs send their
+    candidates and the top-k CTA ranks only those; the check T >= every
+    CTA's threshold holds, so no row falls back to all keys."""
+    s = W.spec("gptoss", batch=len(ctx), ctx_len=ctx, capacity=max(ctx))
+    host = W.generate(s)
+    dw, sel, cnt, out, lse, st = _wide_step(s, host)
+    check_all_rows(s, host, sel, cnt, out, lse)
+    assert st["select_rows_all_keys"] == 0, st
+
+
+@pytest.mark.parametrize("run", [600, 3000])
+def test_wide_rows_with_the_best_tokens_in_one_place(run):
+    """A run of tokens whose keys align with the query holds most of the
+    row's top 4096: a scoring CTA holds far more than twice its share, the
+    check fails and the row is selected from all its keys."""
+    s = W.spec("gptoss", batch=1, ctx_len=[40000], capacity=40000)
+    host = W.generate(s)
+    K = W.bf16_bits_to_f32(host.K[0]).copy()
+    q = W.bf16_bits_to_f32(host.q[0])
+    t0 = 12000
+    for h in range(s.num_kv_heads):
+        sgn = np.sign(q[h * s.group])
+        K[h, t0:t0 + run] = np.abs(K[h, t0:t0 + run]) * sgn[None, :] * 1.5
+    host.K[0] = _bits(K)
+    dw, sel, cnt, out, lse, st = _wide_step(s, host)
+    check_all_rows(s, host, sel, cnt, out, lse)
+    if run == 3000:
+        assert st["select_rows_all_keys"] >= 1, st
+
+
+def test_wide_rows_exact_ties_go_to_lower_pages():
+    """Sixteen-token pages repeating four key patterns over 10000 pages: the
+    bounds take four values, so T's bin narrows to one value and the ties at
+    the budget boundary go to the lower pages."""
+    s = W.spec("qwen7b", batch=1, ctx_len=[160000], capacity=160000)
+    s.k_pages = 3000
+    host = W.generate(s)
+    pat = host.K[0, :, :4 * 16].copy()
+    for p in range(1, 10000):
+        host.K[0, :, p * 16:(p + 1) * 16] = pat[:, (p % 4) * 16:(p % 4 + 1) * 16]
+    dw, sel, cnt, out, lse, st = _wide_step(s, host)
+    for h in range(s.num_kv_heads):
+        orc = PT.oracle_row(s, host, 0, h)
+        assert np.array_equal(sel[h], orc.pages), h   # equal scores: no tolerance needed
+
+
 # 2..16 splits combine inside a thread-block cluster, more through global memory
 @pytest.mark.parametrize("splits", [1, 2, 3, 8, 13, 16, 17, 64, 1024])
 def test_split_counts_do_not_change_the_result(splits):
