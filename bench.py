@@ -844,6 +844,10 @@ def run_delta(args, s: W.Spec):
                 "h2d_bytes_per_step": int(q_host.numel() * q_host.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())},
     }
+    # top-delta against Quest top-k at the same mean budget: recall and each
+    # selector's own device time ("Faster Than Flash", selection-rule overhead)
+    from sparse_long_context_gb300 import diagnostics as DG
+    line["selection_comparison"] = DG.delta_vs_topk(dw)
     if not args.no_cpu_baseline:
         line["parity"] = parity_check(s, host, first_sel, first_out, first_cnt)
         rows = [(b, h) for b in range(s.batch) for h in range(s.num_kv_heads)]

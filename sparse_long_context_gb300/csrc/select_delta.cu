@@ -251,6 +251,10 @@ template <int I>
 __device__ __forceinline__ uint32_t code_pair_sub(uint32_t w, uint32_t w8) {
   return (I < 4 ? w : w8) & (0x00030003u << (2 * (I & 3)));
 }
+// The same with the pair index I given at run time (unrolled loops fold it).
+__device__ __forceinline__ uint32_t code_pair_sub_rt(uint32_t w, uint32_t w8, int I) {
+  return (I < 4 ? w : w8) & (0x00030003u << (2 * (I & 3)));
+}
 
 __device__ __forceinline__ void mma_f16_d(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
@@ -290,6 +294,39 @@ __device__ __forceinline__ void load_scan_codes(ScanCodes<D>& sc, const uint8_t*
       }
     }
   }
+}
+
+// Best margin over the block's tokens for this lane's heads 2m, 2m + 1:
+// scale * q.k^ - m~ = (level sums) + off, with the codes entering the MMA as
+// fp16 subnormals and the weights as fp16 hi parts (and lo parts with LO).
+template <int D, bool LO>
+__device__ __forceinline__ float scan_block_tiles(const ScanCodes<D>& cur, const uint32_t (&whi)[D / 16][2],
+                                                  const uint32_t (&wlo)[D / 16][2], int ntile, bool hv0, bool hv1,
+                                                  float off0, float off1) {
+  constexpr int CPL = D / 4;
+  float best = kNegInf;
+#pragma unroll
+  for (int mt = 0; mt < kMaxScanTiles; ++mt) {
+    if (mt >= ntile) break;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int wd = 0; wd < CPL / 16; ++wd) {
+      const uint32_t x = cur.c[mt][0][wd], y = cur.c[mt][1][wd];  // tokens r and r + 8
+      const uint32_t x8 = x >> 8, y8 = y >> 8;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // channel pairs (2k, 2k + 1) of the word's two 8-channel halves
+        const uint32_t a0 = code_pair_sub_rt(x, x8, 2 * k), a1 = code_pair_sub_rt(y, y8, 2 * k);
+        const uint32_t a2 = code_pair_sub_rt(x, x8, 2 * k + 1), a3 = code_pair_sub_rt(y, y8, 2 * k + 1);
+        mma_f16_d(acc, a0, a1, a2, a3, whi[4 * wd + k][0], whi[4 * wd + k][1]);
+        if constexpr (LO) mma_f16_d(acc, a0, a1, a2, a3, wlo[4 * wd + k][0], wlo[4 * wd + k][1]);
+      }
+    }
+    // acc (64 2^-24 times the level sums): tokens r (0, 1) and r + 8 (2, 3), heads 2m (0, 2) and 2m + 1 (1, 3)
+    constexpr float kUnscale = 262144.f;  // 2^24 / 64
+    if (hv0) best = fmaxf(best, fmaxf(acc[0], acc[2]) * kUnscale + off0);
+    if (hv1) best = fmaxf(best, fmaxf(acc[1], acc[3]) * kUnscale + off1);
+  }
+  return best;
 }
 
 template <int D>
@@ -339,10 +376,10 @@ delta_scan_mma_kernel(const DeltaArgs a) {
   while (j < j1) {
     const int jn = j + kDeltaWarps;
     if (jn < j1) load_scan_codes<D>(nxt, crow + (size_t)jn * a.block * (D / 4), srow + (size_t)jn * D, ntile, lane);
-    // weights of the block: hi/lo fp16 pairs per k-step, and their fp32 sum
-    uint32_t whi[KS][2], wlo[KS][2];
-    float wsum = 0.f;
+    // weights of the block in fp16 hi parts (per k-step), their fp32 sum, and
+    // the sum of their magnitudes, which bounds what the lo parts w - hi add
     float wc[CPL];
+    float wsum = 0.f, wabs = 0.f;
 #pragma unroll
     for (int v = 0; v < CPL / 8; ++v) {
       float sv[8];
@@ -351,56 +388,56 @@ delta_scan_mma_kernel(const DeltaArgs a) {
       for (int e = 0; e < 8; ++e) {
         wc[8 * v + e] = qh[8 * v + e] * sv[e];
         // the level sum takes the unscaled weights (exact: powers of two)
-        wsum += wc[8 * v + e] * (1.f / (64 >> (2 * (e & 3))));
+        const float u = 1.f / (64 >> (2 * (e & 3)));
+        wsum += wc[8 * v + e] * u;
+        wabs += fabsf(wc[8 * v + e]) * u;
       }
     }
+    uint32_t whi[KS][2];
 #pragma unroll
     for (int wd = 0; wd < CPL / 16; ++wd) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {  // register i of word wd: channels (i, i + 8)
-        const float w0 = wc[16 * wd + i], w1 = wc[16 * wd + i + 8];
-        const __half2 hi = __floats2half2_rn(w0, w1);
-        const __half2 lo = __floats2half2_rn(w0 - __low2float(hi), w1 - __high2float(hi));
+        const __half2 hi = __floats2half2_rn(wc[16 * wd + i], wc[16 * wd + i + 8]);
         whi[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&hi);
-        wlo[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&lo);
       }
     }
     wsum += __shfl_xor_sync(0xffffffffu, wsum, 1);
     wsum += __shfl_xor_sync(0xffffffffu, wsum, 2);  // head r's sum over all channels
     const float ws0 = __shfl_sync(0xffffffffu, wsum, 8 * m), ws1 = __shfl_sync(0xffffffffu, wsum, 8 * m + 4);
     const float off0 = -1.5f * ws0 - mt0, off1 = -1.5f * ws1 - mt1;
-    float best = kNegInf;
-#pragma unroll
-    for (int mt = 0; mt < kMaxScanTiles; ++mt) {
-      if (mt >= ntile) break;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // 1. every token scored with the hi parts only
+    float best = scan_block_tiles<D, false>(cur, whi, whi, ntile, hv0, hv1, off0, off1);
+    best = warp_max(best);
+    // A token's score differs from the hi-only one by sum_c code_c (w_c - hi_c)
+    // <= 3 sum_c |w_c - hi_c|, with |w - hi| <= 2^-11 |w| for a normal fp16 hi
+    // and at most the subnormal step 2^-25 below that (in the scaled units of
+    // the weights, so 2^-25 u in the level sums); fp32 accumulation adds far
+    // less than the 2x slack taken here.  Only a block whose hi-only margin
+    // lies that close to -delta can decide the other way: it is scored again
+    // with hi + lo (exact to fp32 rounding).
+    wabs += __shfl_xor_sync(0xffffffffu, wabs, 1);
+    wabs += __shfl_xor_sync(0xffffffffu, wabs, 2);
+    const float err = warp_max(6.f * (wabs * 0x1p-11f + (float)D * 0x1p-25f));
+    if (fabsf(best + a.delta) <= err) {  // warp-uniform
+      // the weights again (not kept live across the hi-only pass), then w - hi;
+      // word wd holds channels 16 wd + i and 16 wd + i + 8 in register i
+      uint32_t wlo[KS][2];
 #pragma unroll
       for (int wd = 0; wd < CPL / 16; ++wd) {
-        const uint32_t x = cur.c[mt][0][wd], y = cur.c[mt][1][wd];  // tokens r and r + 8
-        const uint32_t x8 = x >> 8, y8 = y >> 8;
-        mma_f16_d(acc, code_pair_sub<0>(x, x8), code_pair_sub<0>(y, y8), code_pair_sub<1>(x, x8),
-                  code_pair_sub<1>(y, y8), whi[4 * wd][0], whi[4 * wd][1]);
-        mma_f16_d(acc, code_pair_sub<0>(x, x8), code_pair_sub<0>(y, y8), code_pair_sub<1>(x, x8),
-                  code_pair_sub<1>(y, y8), wlo[4 * wd][0], wlo[4 * wd][1]);
-        mma_f16_d(acc, code_pair_sub<2>(x, x8), code_pair_sub<2>(y, y8), code_pair_sub<3>(x, x8),
-                  code_pair_sub<3>(y, y8), whi[4 * wd + 1][0], whi[4 * wd + 1][1]);
-        mma_f16_d(acc, code_pair_sub<2>(x, x8), code_pair_sub<2>(y, y8), code_pair_sub<3>(x, x8),
-                  code_pair_sub<3>(y, y8), wlo[4 * wd + 1][0], wlo[4 * wd + 1][1]);
-        mma_f16_d(acc, code_pair_sub<4>(x, x8), code_pair_sub<4>(y, y8), code_pair_sub<5>(x, x8),
-                  code_pair_sub<5>(y, y8), whi[4 * wd + 2][0], whi[4 * wd + 2][1]);
-        mma_f16_d(acc, code_pair_sub<4>(x, x8), code_pair_sub<4>(y, y8), code_pair_sub<5>(x, x8),
-                  code_pair_sub<5>(y, y8), wlo[4 * wd + 2][0], wlo[4 * wd + 2][1]);
-        mma_f16_d(acc, code_pair_sub<6>(x, x8), code_pair_sub<6>(y, y8), code_pair_sub<7>(x, x8),
-                  code_pair_sub<7>(y, y8), whi[4 * wd + 3][0], whi[4 * wd + 3][1]);
-        mma_f16_d(acc, code_pair_sub<6>(x, x8), code_pair_sub<6>(y, y8), code_pair_sub<7>(x, x8),
-                  code_pair_sub<7>(y, y8), wlo[4 * wd + 3][0], wlo[4 * wd + 3][1]);
+        float sa[8], sb[8];
+        unpack_vec(cur.sv[2 * wd], sa);
+        unpack_vec(cur.sv[2 * wd + 1], sb);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float w0 = qh[16 * wd + i] * sa[i], w1 = qh[16 * wd + i + 8] * sb[i];
+          const __half2 hi = __floats2half2_rn(w0, w1);
+          const __half2 lo = __floats2half2_rn(w0 - __low2float(hi), w1 - __high2float(hi));
+          wlo[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&lo);
+        }
       }
-      // acc (64 2^-24 times the level sums): tokens r (0, 1) and r + 8 (2, 3), heads 2m (0, 2) and 2m + 1 (1, 3)
-      constexpr float kUnscale = 262144.f;  // 2^24 / 64
-      if (hv0) best = fmaxf(best, fmaxf(acc[0], acc[2]) * kUnscale + off0);
-      if (hv1) best = fmaxf(best, fmaxf(acc[1], acc[3]) * kUnscale + off1);
+      best = warp_max(scan_block_tiles<D, true>(cur, whi, wlo, ntile, hv0, hv1, off0, off1));
     }
-    best = warp_max(best);
     if (lane == 0) a.flags[(size_t)row * a.nblk_cap + j] = best >= -a.delta ? 1 : 0;
     cur = nxt;
     j = jn;

@@ -8,7 +8,10 @@ For one decode step of a workload this reports, per query head:
 * the relative L2 error of the sparse output against dense attention over
   the whole context (the split-K attend kernel with no page list);
 * for the top-delta workload, top-delta against Quest top-k at the same
-  budget (the mean number of blocks top-delta keeps per row): recall of both;
+  budget (the mean number of blocks top-delta keeps per row): recall of both,
+  and the device time of each selector run as its own kernels ("Faster Than
+  Flash", the selection-rule overhead at identical keep ratios), L2 flushed
+  before every timed launch;
 * needle recall: the share of each row's planted needle pages (blocks) that
   its list holds (the synthetic queries are built to look for the needles,
   so this checks the generator as much as the selection).
@@ -70,7 +73,24 @@ def quest_quality(dw: H.DeviceWorkload) -> dict:
             "rel_l2_vs_dense": _stats(rel.cpu().numpy()), "needle_recall": _stats(nr) if nr.size else None}
 
 
-def delta_vs_topk(dw: H.DeviceWorkload) -> dict:
+def _timed(fn, reps: int = 30) -> float:
+    """Mean device time (us) of fn() over reps launches, each preceded by a
+    write of a buffer larger than L2 (outside the timed events)."""
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    return float(np.mean([1e3 * a.elapsed_time(b) for a, b in times[3:]]))
+
+
+def delta_vs_topk(dw: H.DeviceWorkload, time_selectors: bool = True) -> dict:
     """Top-delta's kept blocks against Quest top-k at the same mean budget."""
     s = dw.spec
     step = H.make_step(dw)
@@ -82,12 +102,22 @@ def delta_vs_topk(dw: H.DeviceWorkload) -> dict:
     page_idx = ops.select_pages(dw.desc, dw.q, kmin, kmax, dw.ctx, k, 1, s.block)
     rec_q = ops.selection_recall(dw.desc, dw.q, dw.K, page_idx, dw.ctx)
     ops.pipeline_check()
+    times = None
+    if time_selectors:
+        ws = ops.select_pages_workspace(dw.desc)
+        times = {"select_delta_us": _timed(lambda: step.select(dw.q, dw.K, dw.codes, dw.scales, dw.ctx)),
+                 "select_pages_us": _timed(lambda: ops.select_pages(dw.desc, dw.q, kmin, kmax, dw.ctx, k, 1, s.block,
+                                                                    out=page_idx, workspace=ws)),
+                 "how": "each selector alone (top-delta: scan + compaction; Quest: bound + top-k over "
+                        f"{s.block}-token page min/max at the matched budget), L2 flushed before each launch"}
+        ops.pipeline_check()
     nr = needle_recall(step.block_idx.cpu().numpy(), cnt.cpu().numpy(), dw.host.needles, s.block, s.num_kv_heads)
     nblk = np.array([-(-int(n) // s.block) for n in s.ctx_len for _ in range(s.num_kv_heads)])
     return {"selector": "top-delta", "delta": s.delta,
             "kept_fraction": float(cnt.cpu().numpy().sum() / nblk.sum()),
             "recall_top_delta": _stats(rec_d.cpu().numpy()),
             "matched_budget_blocks": k, "recall_quest_topk": _stats(rec_q.cpu().numpy()),
+            "selector_time": times,
             "needle_recall_top_delta": _stats(nr) if nr.size else None}
 
 
