@@ -44,9 +44,10 @@ METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak) for select+att
 # written; traffic grows with the rows, so x4 for batch 32).  Reported only
 # for that workload and only while the kernel's sources hash to the ones
 # captured; otherwise null.
-STEP_TRAFFIC_B32 = 4 * (50.475264e6 + 0.102912e6)
-STEP_SOURCES = ("quest_step.cu", "attend_tma.cuh", "tma.cuh", "mma.cuh", "attend_common.cuh", "common.cuh")
-STEP_SOURCES_SHA256 = "47e78991e4c5f32f831eb2f0adca24a306946651ca07f62fdb6ea567eb81491a"
+STEP_TRAFFIC_B32 = 4 * (50.471168e6 + 0.108288e6)
+STEP_SOURCES = ("quest_step.cu", "attend_tma.cuh", "tma.cuh", "mma.cuh", "attend_common.cuh", "common.cuh",
+                "status.cuh")
+STEP_SOURCES_SHA256 = "7afc1aef82b38b6abc2c952f887a386ec1c4e8f3c180e3eca0e2a067f29f14bf"
 
 
 def step_traffic(s: W.Spec):
