@@ -279,8 +279,8 @@ static cudaError_t attend_cc_g(const AttendArgs& a, int rows, cudaStream_t st) {
 
 cudaError_t launch_attend_mma(const Shape& s, const AttendArgs& a, cudaStream_t st, bool* handled);
 cudaError_t launch_attend_tma(const Shape& s, const AttendArgs& a, cudaStream_t st, bool* handled);
-const void* attend_mma_kernel_ptr();
-size_t attend_mma_kernel_smem();
+const void* attend_mma_kernel_ptr(int D);
+size_t attend_mma_kernel_smem(int D);
 int attend_mma_kernel_threads();
 
 int max_auto_splits(const Shape& s) {
@@ -292,17 +292,18 @@ int max_auto_splits(const Shape& s) {
 int attend_default_splits(const Shape& s, int max_entries) {
   // one wave of attend CTAs over all rows (at most one CTA per slot), each
   // slice at least 64 tokens
-  static int mma_per_sm = 0;
-  if (mma_per_sm == 0) {
-    cudaFuncSetAttribute(attend_mma_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)attend_mma_kernel_smem());
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&mma_per_sm, attend_mma_kernel_ptr(),
+  static int mma_per_sm[2] = {0, 0};  // D = 64, D = 128
+  const int di = s.D == 64 ? 0 : 1;
+  if (mma_per_sm[di] == 0) {
+    cudaFuncSetAttribute(attend_mma_kernel_ptr(s.D), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)attend_mma_kernel_smem(s.D));
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&mma_per_sm[di], attend_mma_kernel_ptr(s.D),
                                                       attend_mma_kernel_threads(),
-                                                      attend_mma_kernel_smem()) != cudaSuccess)
-      mma_per_sm = 1;
+                                                      attend_mma_kernel_smem(s.D)) != cudaSuccess)
+      mma_per_sm[di] = 1;
   }
   if (attend_tma_eligible(s)) return attend_tma_splits(s, (int)(((long long)max_entries << s.pshift) / 16));
-  const int per_sm = mma_per_sm;
+  const int per_sm = mma_per_sm[di];
   const int rows = s.B * s.Hkv;
   const int slots = sm_count() * (per_sm > 0 ? per_sm : 1);
   int S = slots / rows;

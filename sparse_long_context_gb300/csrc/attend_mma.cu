@@ -27,7 +27,11 @@ namespace sls {
 //   V of tokens 2m, 2m+1, 2m+8, 2m+9, VL chunks each (A operand of O^T),
 // and the positions that decide which tokens are valid.
 constexpr int kAttnWarps = 8;
-constexpr int kAttnMinBlocks = 1;  // resident CTAs per SM the register budget is sized for
+// Resident CTAs per SM the register budget is sized for: one at D = 128;
+// two at D = 64, whose groups need half the registers, so that twice the
+// warps keep gathers in flight (one-token pages gather single 128-byte rows).
+template <int D>
+constexpr int attn_min_blocks() { return D == 64 ? 2 : 1; }
 constexpr int kStagedEntries = 1024;  // page-list entries staged in shared memory
 
 __device__ __forceinline__ float ex2(float x) {
@@ -283,7 +287,7 @@ __device__ __forceinline__ void attend_run(const AttendArgs& a, int row, const S
 }
 
 template <int D, bool PAGED>
-__global__ void __launch_bounds__(kAttnWarps * 32, kAttnMinBlocks)
+__global__ void __launch_bounds__(kAttnWarps * 32, attn_min_blocks<D>())
 attend_mma_kernel(const AttendArgs a) {
   pdl_wait_then_release();
   extern __shared__ float sO[];  // [NW][8][D]
@@ -310,8 +314,11 @@ static cudaError_t attend_mma_launch(const AttendArgs& a, int grid, cudaStream_t
   return cudaGetLastError();
 }
 
-const void* attend_mma_kernel_ptr() { return reinterpret_cast<const void*>(attend_mma_kernel<128, true>); }
-size_t attend_mma_kernel_smem() { return attend_mma_smem<128>(); }
+const void* attend_mma_kernel_ptr(int D) {
+  return D == 64 ? reinterpret_cast<const void*>(attend_mma_kernel<64, false>)
+                 : reinterpret_cast<const void*>(attend_mma_kernel<128, true>);
+}
+size_t attend_mma_kernel_smem(int D) { return D == 64 ? attend_mma_smem<64>() : attend_mma_smem<128>(); }
 int attend_mma_kernel_threads() { return kAttnWarps * 32; }
 
 cudaError_t launch_attend_mma(const Shape& s, const AttendArgs& a, cudaStream_t st, bool* handled) {
