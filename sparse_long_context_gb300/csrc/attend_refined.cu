@@ -11,7 +11,10 @@
 // row leaves the kernel as slow as its longest row.  Here the rows' lists,
 // concatenated, are cut into one equal range of entries per CTA (one 8-warp
 // CTA per SM, stream-K style; attend_balanced_kernel).  Without codes the
-// same kernel attends with the bf16 keys everywhere.
+// bf16 keys are attended everywhere: by attend_stream_tma_kernel (the same
+// partition, every warp streaming its groups through its own ring of
+// tensor-map copies) where the shape allows tensor maps, else by the same
+// register-fed kernel.
 //
 // Within an item a warp walks 16-token groups with two groups in flight in
 // registers (the shape of the register-fed attend).  Lane (r, m) owns the
@@ -32,6 +35,7 @@
 #include <algorithm>
 
 #include "attend_common.cuh"
+#include "attend_tma.cuh"
 #include "launch.h"
 #include "mma.cuh"
 
@@ -272,17 +276,21 @@ constexpr int kRefMaxRows = 4096;  // rows whose list prefix one CTA keeps in sh
 
 constexpr int kRefMaxContrib = 1024;  // CTAs sharing one row (one CTA per SM)
 
+constexpr int kRefMaxWarps = 16;  // warps of any kernel that uses RefSmem
+
 struct RefSmem {
   float sM[kRefWarps][8], sL[kRefWarps][8];
   int s_pg[kRefStaged];
-  int s_tmp[kRefWarps];
+  int s_tmp[kRefMaxWarps];
+  int s_fail;
   int s_slot[kRefMaxContrib];
   int s_ncontrib;
   int s_last;
   float s_w[8][64], s_m[8], s_inv[8];
 };
 
-// Exclusive scan of one int per thread (256 threads); `total` gets the sum.
+// Exclusive scan of one int per thread (NW warps); `total` gets the sum.
+template <int NW>
 __device__ __forceinline__ int ref_scan(int v, int* tmp, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -296,7 +304,7 @@ __device__ __forceinline__ int ref_scan(int v, int* tmp, int& total) {
   int before = 0;
   total = 0;
 #pragma unroll
-  for (int w = 0; w < kRefWarps; ++w) {
+  for (int w = 0; w < NW; ++w) {
     const int t = tmp[w];
     before += w < warp ? t : 0;
     total += t;
@@ -327,8 +335,178 @@ __device__ __forceinline__ void finish_head(const AttendArgs& a, size_t hq, int 
     f = M == kNegInf ? 0.f : expf(M - Mx);
     L = lv * f + (a.sink ? expf(sk - Mx) : 0.f);
   }
-  static_cast<bf16*>(a.out)[hq * D + d] = __float2bfloat16(L > 0.f ? av * f / L : 0.f);
-  if (d == 0 && a.lse) a.lse[hq] = L > 0.f ? Mx + logf(L) : kNegInf;
+  // a NaN normaliser (a wait that gave up) stays NaN in the output and lse
+  static_cast<bf16*>(a.out)[hq * D + d] = __float2bfloat16(L == 0.f ? 0.f : av * f / L);
+  if (d == 0 && a.lse) a.lse[hq] = L == 0.f ? kNegInf : Mx + logf(L);
+}
+
+// Stream-K setup: s_pref[row] = the first entry of each row's list in the
+// concatenation (s_pref[rows] = T, the total), rows with an empty list
+// written (output 0, lse -inf or the sink alone), and this CTA's entry range
+// [lo, hi) with the row holding lo.  False when the CTA has no entries.
+template <int D, int NT>
+__device__ __forceinline__ bool stream_k_begin(const AttendArgs& a, int rows, RefSmem& sh, int* s_pref, int& T,
+                                               long long& lo, long long& hi, int& row) {
+  const int G = a.G, grid = gridDim.x, c = blockIdx.x;
+  const int RPT = (rows + NT - 1) / NT;
+  const int r0 = threadIdx.x * RPT;
+  int csum = 0;
+  for (int i = 0; i < RPT; ++i) {
+    const int row = r0 + i;
+    if (row < rows) csum += min(max(a.count[row], 0), a.idx_stride);
+  }
+  int acc = ref_scan<NT / 32>(csum, sh.s_tmp, T);
+  for (int i = 0; i < RPT; ++i) {
+    const int row = r0 + i;
+    if (row < rows) {
+      s_pref[row] = acc;
+      acc += min(max(a.count[row], 0), a.idx_stride);
+    }
+  }
+  if (threadIdx.x == 0) s_pref[rows] = T;
+  __syncthreads();
+
+  // rows with an empty list: output 0, lse -inf (or the sink alone)
+  for (int row = c; row < rows; row += grid) {
+    if (s_pref[row + 1] != s_pref[row]) continue;
+    const int b = row / a.Hkv, h = row % a.Hkv;
+    for (int i = threadIdx.x; i < G * D; i += NT)
+      finish_head(a, (size_t)b * a.Hq + (size_t)h * G + i / D, h, i / D, kNegInf, 0.f, 0.f, i % D, D);
+  }
+  if (T == 0) return false;
+  lo = range_lo(T, c, grid);
+  hi = range_lo(T, c + 1, grid);
+  if (lo >= hi) return false;
+  // the row holding entry lo: the last row whose first entry is <= lo
+  {
+    int l = 0, u = rows - 1;
+    while (l < u) {
+      const int mid = (l + u + 1) >> 1;
+      if (s_pref[mid] <= lo) l = mid;
+      else u = mid - 1;
+    }
+    row = l;
+  }
+  return true;
+}
+
+// End of one row segment of a stream-K CTA: `partial(g, d, M, av, lv)`
+// gives the CTA's merged state of head g, channel d (running max M in
+// natural-log units, accumulator av and normaliser lv relative to exp(M)).
+// A row the CTA holds entirely is finished in place; otherwise the CTA
+// writes its partial to its slot (2c for the segment its range starts in,
+// 2c + 1 for the one it ends in) and the row's last contributor to arrive
+// merges the slots in CTA order.
+template <int D, int NT, typename Partial>
+__device__ __forceinline__ void finish_segment(const RefinedArgs& ra, RefSmem& sh, const int* s_pref, int row,
+                                               long long e, long long seg_end, long long lo, int c, int T, int grid,
+                                               Partial partial) {
+  const AttendArgs& a = ra.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NW = NT / 32;
+  const int G = a.G;
+  const int b = row / a.Hkv, h = row % a.Hkv;
+  const bool whole = e == s_pref[row] && seg_end == s_pref[row + 1];
+  const int slot = e == lo ? 2 * c : 2 * c + 1;
+  const size_t hq0 = (size_t)b * a.Hq + (size_t)h * G;
+  for (int i = threadIdx.x; i < G * D; i += NT) {
+    const int g = i / D, d = i % D;
+    float Mn, av, lv;
+    partial(g, d, Mn, av, lv);
+    if (whole) {
+      finish_head(a, hq0 + g, h, g, Mn, lv, av, d, D);
+    } else {
+      const size_t sg = (size_t)slot * G + g;
+      ra.po[sg * D + d] = av;
+      if (d == 0) {
+        ra.pm[sg] = Mn;
+        ra.pl[sg] = lv;
+      }
+    }
+  }
+  if (!whole) {
+    // the row's contributors are the CTAs from the one holding its first
+    // entry to the one holding its last; the last to arrive merges
+    // (skipping CTAs with empty ranges, which exist when T < grid); CTA k
+    // wrote slot 2k when its range starts inside the row, else 2k + 1
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int cf = cta_of(s_pref[row], T, grid), cl = cta_of((long long)s_pref[row + 1] - 1, T, grid);
+      int n = 0;
+      for (int k = cf; k <= cl && n < kRefMaxContrib; ++k) {
+        const long long klo = range_lo(T, k, grid);
+        if (klo < range_lo(T, k + 1, grid)) sh.s_slot[n++] = klo >= s_pref[row] ? 2 * k : 2 * k + 1;
+      }
+      sh.s_ncontrib = n;
+      sh.s_last = atomicAdd(a.tickets + row, 1) == n - 1;
+    }
+    __syncthreads();
+    const int ncontrib = sh.s_ncontrib;
+    if (sh.s_last) {
+      __threadfence();
+      auto slot_of = [&](int j) -> size_t { return (size_t)sh.s_slot[j]; };
+      for (int g = warp; g < G; g += NW) {
+        float M = kNegInf;
+        for (int j = lane; j < ncontrib; j += 32) M = fmaxf(M, __ldcg(ra.pm + slot_of(j) * G + g));
+        M = warp_max(M);
+        const float sk = a.sink ? a.sink[h * G + g] : kNegInf;
+        M = fmaxf(M, sk);
+        float Ls = 0.f;
+        for (int j = lane; j < ncontrib; j += 32) {
+          const float ms = __ldcg(ra.pm + slot_of(j) * G + g);
+          const float w = (ms == kNegInf || M == kNegInf) ? 0.f : expf(ms - M);
+          Ls += __ldcg(ra.pl + slot_of(j) * G + g) * w;
+          if (j < 64) sh.s_w[g][j] = w;
+        }
+        Ls = warp_sum(Ls);
+        if (a.sink && M != kNegInf) Ls += expf(sk - M);
+        if (lane == 0) {
+          sh.s_m[g] = M;
+          sh.s_inv[g] = Ls == 0.f ? 0.f : 1.f / Ls;  // NaN stays NaN
+          if (a.lse) a.lse[hq0 + g] = Ls == 0.f ? kNegInf : M + logf(Ls);
+        }
+      }
+      __syncthreads();
+      constexpr int C4 = D / 4;
+      for (int i = threadIdx.x; i < G * C4; i += NT) {
+        const int g = i / C4, cc = i % C4;
+        const float M = sh.s_m[g];
+        float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = 0; j0 < ncontrib; j0 += 8) {
+          float4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            v[u] = j0 + u < ncontrib
+                       ? __ldcg(reinterpret_cast<const float4*>(ra.po + (slot_of(j0 + u) * G + g) * D) + cc)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u;
+            if (j >= ncontrib) break;
+            float w;
+            if (j < 64) {
+              w = sh.s_w[g][j];
+            } else {
+              const float ms = __ldcg(ra.pm + slot_of(j) * G + g);
+              w = (ms == kNegInf || M == kNegInf) ? 0.f : expf(ms - M);
+            }
+            accv.x = fmaf(v[u].x, w, accv.x);
+            accv.y = fmaf(v[u].y, w, accv.y);
+            accv.z = fmaf(v[u].z, w, accv.z);
+            accv.w = fmaf(v[u].w, w, accv.w);
+          }
+        }
+        const float inv = sh.s_inv[g];
+        bf16* op = static_cast<bf16*>(a.out) + (hq0 + g) * D + 4 * cc;
+        op[0] = __float2bfloat16(accv.x * inv);
+        op[1] = __float2bfloat16(accv.y * inv);
+        op[2] = __float2bfloat16(accv.z * inv);
+        op[3] = __float2bfloat16(accv.w * inv);
+      }
+      if (threadIdx.x == 0) a.tickets[row] = 0;  // ready for the next call
+    }
+  }
 }
 
 // Stream-K over the rows' lists (top-delta keeps a different number of
@@ -353,47 +531,9 @@ __global__ void __launch_bounds__(kRefWarps * 32, 1) attend_balanced_kernel(cons
   const int r = lane >> 2, m = lane & 3;
   const int G = a.G, rows = ra.rows, grid = gridDim.x, c = blockIdx.x;
 
-  // 1. prefix of the rows' list lengths
-  const int RPT = (rows + NT - 1) / NT;
-  const int r0 = threadIdx.x * RPT;
-  int csum = 0;
-  for (int i = 0; i < RPT; ++i) {
-    const int row = r0 + i;
-    if (row < rows) csum += min(max(a.count[row], 0), a.idx_stride);
-  }
-  int T;
-  int acc = ref_scan(csum, sh.s_tmp, T);
-  for (int i = 0; i < RPT; ++i) {
-    const int row = r0 + i;
-    if (row < rows) {
-      s_pref[row] = acc;
-      acc += min(max(a.count[row], 0), a.idx_stride);
-    }
-  }
-  if (threadIdx.x == 0) s_pref[rows] = T;
-  __syncthreads();
-
-  // rows with an empty list: output 0, lse -inf (or the sink alone)
-  for (int row = c; row < rows; row += grid) {
-    if (s_pref[row + 1] != s_pref[row]) continue;
-    const int b = row / a.Hkv, h = row % a.Hkv;
-    for (int i = threadIdx.x; i < G * D; i += NT)
-      finish_head(a, (size_t)b * a.Hq + (size_t)h * G + i / D, h, i / D, kNegInf, 0.f, 0.f, i % D, D);
-  }
-  if (T == 0) return;
-  const long long lo = range_lo(T, c, grid), hi = range_lo(T, c + 1, grid);
-  if (lo >= hi) return;
-  // the row holding entry lo: the last row whose first entry is <= lo
-  int row;
-  {
-    int l = 0, u = rows - 1;
-    while (l < u) {
-      const int mid = (l + u + 1) >> 1;
-      if (s_pref[mid] <= lo) l = mid;
-      else u = mid - 1;
-    }
-    row = l;
-  }
+  int T, row;
+  long long lo, hi;
+  if (!stream_k_begin<D, NT>(a, rows, sh, s_pref, T, lo, hi, row)) return;
   long long e = lo;
   while (e < hi) {
     const long long seg_end = min(hi, (long long)s_pref[row + 1]);
@@ -464,119 +604,203 @@ __global__ void __launch_bounds__(kRefWarps * 32, 1) attend_balanced_kernel(cons
       sO[(warp * 8 + 2 * m + 1) * D + ch + 1] = o[t][3];
     }
     __syncthreads();
-    const bool whole = e == s_pref[row] && seg_end == s_pref[row + 1];
-    const int slot = e == lo ? 2 * c : 2 * c + 1;
-    const size_t hq0 = (size_t)b * a.Hq + (size_t)h * G;
-    for (int i = threadIdx.x; i < G * D; i += NT) {
-      const int g = i / D, d = i % D;
-      float M = kNegInf;
+    finish_segment<D, NT>(ra, sh, s_pref, row, e, seg_end, lo, c, T, grid, [&](int g, int d, float& M, float& av,
+                                                                                float& lv) {
+      float Mb = kNegInf;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, sh.sM[w][g]);
-      float av = 0.f, lv = 0.f;
-      if (M != kNegInf) {
+      for (int w = 0; w < NW; ++w) Mb = fmaxf(Mb, sh.sM[w][g]);
+      av = 0.f;
+      lv = 0.f;
+      if (Mb != kNegInf) {
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
           if (sh.sM[w][g] == kNegInf) continue;
-          const float f = exp2f(sh.sM[w][g] - M);
+          const float f = exp2f(sh.sM[w][g] - Mb);
           av += sO[(w * 8 + g) * D + d] * f;
           lv += sh.sL[w][g] * f;
         }
       }
-      const float Mn = M == kNegInf ? kNegInf : M * kLn2;
-      if (whole) {
-        finish_head(a, hq0 + g, h, g, Mn, lv, av, d, D);
+      M = Mb == kNegInf ? kNegInf : Mb * kLn2;
+    });
+    __syncthreads();  // shared memory is reused by the next segment
+    e = seg_end;
+    ++row;
+    while (row < rows && s_pref[row + 1] == s_pref[row]) ++row;  // empty rows hold no entries
+  }
+}
+
+// The same stream-K partition with bf16 keys, fed by the tensor memory
+// accelerator (the top-delta step's default attend).  The segment's 16-token
+// groups go to the W warps in turn (group gi to warp gi % W), and every warp
+// streams its own groups through its own ring of S shared-memory stages: its
+// lane 0 copies a group's K and V with the split-K tensor-map attend's boxes
+// (stage layout, tensor maps and group arithmetic shared with it) and refills
+// a stage with the warp's group S further on once the warp has scored it.
+// A late copy then holds up one warp, not the CTA.  The ring positions run
+// on across the CTA's row segments; a segment ends with the warps' merge and
+// the stream-K epilogue.  A wait that gives up poisons the segment's output
+// (NaN) and every later segment of the CTA, and is counted.
+template <int D, int W, int S>
+struct StreamLayout {
+  static constexpr size_t RING = (size_t)W * S * TmaLayout<D>::STAGE;
+  static constexpr size_t MERGE = (size_t)W * 8 * D * sizeof(float);  // the warps' accumulators
+  static constexpr size_t REGION = RING > MERGE ? RING : MERGE;
+};
+
+// First cache position of group gi of the segment and its token count
+// inside the context (<= 0: padded entry, bad page or past the context).
+__device__ __forceinline__ int stream_group_base(const AttendArgs& a, int N, const int* s_pg, const int32_t* plist,
+                                                 int gi, int& lim) {
+  const int j0 = gi << 4;
+  const int e = j0 >> a.pshift;
+  const int pg = e < kRefStaged ? s_pg[e] : __ldg(plist + e);
+  lim = 0;
+  if ((unsigned)pg >= (unsigned)(a.Cap >> a.pshift)) return 0;
+  const int base = (pg << a.pshift) + (j0 & (a.P - 1));
+  lim = min(N - base, 16);
+  return base;
+}
+
+template <int D, int W, int S>
+__global__ void __launch_bounds__(W * 32, 1)
+attend_stream_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                         const RefinedArgs ra) {
+  using L = TmaLayout<D>;
+  constexpr int KS = D / 16;
+  constexpr int NT = W * 32;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* ring = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  int* s_pref = reinterpret_cast<int*>(ring + StreamLayout<D, W, S>::REGION);  // [rows + 1]
+  __shared__ RefSmem sh;
+  __shared__ uint64_t full[W][S];
+  __shared__ float sM[W][8], sL[W][8], sF[W][8];  // warps' max, sum and merge weight per head
+  __shared__ float sHm[8], sHl[8];                 // the CTA's merged max (natural log) and sum
+  const AttendArgs& a = ra.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, m = lane & 3;
+  const int G = a.G, rows = ra.rows, grid = gridDim.x, c = blockIdx.x;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < W; ++w)
+      for (int s = 0; s < S; ++s) mbar_init(&full[w][s], 1);
+    mbar_fence_init();
+    tma_prefetch_map(&tk);
+    tma_prefetch_map(&tv);
+    sh.s_fail = 0;
+  }
+  pdl_wait_then_release();
+  int T, row;
+  long long lo, hi;
+  if (!stream_k_begin<D, NT>(a, rows, sh, s_pref, T, lo, hi, row)) return;  // after its barrier: inits visible
+
+  // the wait-timeout test hook: warp 0 of CTA 0 announces bytes for its first
+  // stage that it never requests, and its waits poll briefly
+  const bool plant = a.test_wait && c == 0 && warp == 0;
+  const uint32_t tries = plant ? kTestWaitTries : kWaitTries;
+  unsigned char* wring = ring + (size_t)warp * S * L::STAGE;
+  const uint32_t wring_u32 = smem_u32(wring);
+  uint32_t wseq = 0;  // this warp's ring position (groups it has taken so far)
+  long long e = lo;
+  while (e < hi) {
+    const long long seg_end = min(hi, (long long)s_pref[row + 1]);
+    const int b = row / a.Hkv, h = row % a.Hkv;
+    const int N = clamp_len(a.ctx_len[b], a.Cap);
+    const int nent = (int)(seg_end - e);
+    const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + (int)(e - s_pref[row]);
+    stage_page_list(sh.s_pg, kRefStaged, plist, 0, nent, a.Cap >> a.pshift, threadIdx.x, NT);
+    __syncthreads();
+    const bool failed = sh.s_fail != 0;  // an earlier segment gave up: no more copies
+    const int ngroups = (nent << a.pshift) >> 4;
+    const int nk = ngroups > warp ? (ngroups - warp + W - 1) / W : 0;  // this warp's groups: warp + W k
+
+    // lane 0: the copy of the warp's k-th group of the segment into its stage
+    auto issue = [&](int k) {
+      const uint32_t q = wseq + k;
+      const int st = q % S;
+      int lim;
+      const int base = stream_group_base(a, N, sh.s_pg, plist, warp + W * k, lim);
+      if (plant && q == 0) {
+        mbar_arrive_expect_tx(&full[warp][st], 16);  // no copy is issued: this phase never completes
+      } else if (lim > 0) {
+        mbar_arrive_expect_tx(&full[warp][st], L::STAGE);
+        const int y = row * a.Cap + base;
+        unsigned char* dst = wring + st * L::STAGE;
+        tma_load_3d(dst, &tk, 0, y, 0, &full[warp][st]);
+        tma_load_3d(dst + L::GROUP, &tv, 0, y, 0, &full[warp][st]);
       } else {
-        const size_t sg = (size_t)slot * G + g;
-        ra.po[sg * D + d] = av;
-        if (d == 0) {
-          ra.pm[sg] = Mn;
-          ra.pl[sg] = lv;
+        mbar_arrive(&full[warp][st]);  // nothing to copy: the phase completes at once
+      }
+    };
+    // S - 1 groups in flight ahead of the one being scored: the stage of
+    // group k + S - 1 is the one group k - 1 left, refilled before group k is
+    // scored
+    if (lane == 0 && !failed)
+      for (int k = 0; k < min(S - 1, nk); ++k) issue(k);
+    __syncwarp();
+
+    float o[KS][4];
+    float m_run = kNegInf, l_run = 0.f;
+#pragma unroll
+    for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    // Q as the A operand: a0 = Q[head r][16ks + 2m, +1], a2 = Q[r][16ks + 8 + 2m, +1]
+    uint32_t qa[KS][2];
+    const bf16* qp = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G + r) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * m)) : 0u;
+      qa[ks][1] = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * m)) : 0u;
+    }
+    bool ok = !failed;
+    int k = 0;
+    if (ok) {
+      for (; k < nk; ++k) {
+        if (lane == 0 && k + S - 1 < nk) issue(k + S - 1);  // into the stage group k - 1 has left
+        const uint32_t q = wseq + k;
+        const int st = q % S;
+        if (!mbar_wait(&full[warp][st], (q / S) & 1, tries)) {
+          ok = false;
+          break;
         }
+        int lim;
+        stream_group_base(a, N, sh.s_pg, plist, warp + W * k, lim);
+        if (lim > 0) tma_group<D>(wring_u32 + st * L::STAGE, lim, qa, o, m_run, l_run, a.qscale, lane);
+        // the stage is read before the copy engine may write it again
+        __syncwarp();
+        if (lane == 0) fence_proxy_async_smem();
       }
     }
-    if (!whole) {
-      // the row's contributors are the CTAs from the one holding its first
-      // entry to the one holding its last; the last to arrive merges
-      // (skipping CTAs with empty ranges, which exist when T < grid); CTA k
-      // wrote slot 2k when its range starts inside the row, else 2k + 1
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const int cf = cta_of(s_pref[row], T, grid), cl = cta_of((long long)s_pref[row + 1] - 1, T, grid);
-        int n = 0;
-        for (int k = cf; k <= cl && n < kRefMaxContrib; ++k) {
-          const long long klo = range_lo(T, k, grid);
-          if (klo < range_lo(T, k + 1, grid)) sh.s_slot[n++] = klo >= s_pref[row] ? 2 * k : 2 * k + 1;
-        }
-        sh.s_ncontrib = n;
-        sh.s_last = atomicAdd(a.tickets + row, 1) == n - 1;
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) {
+        note_wait_timeout();
+        sh.s_fail = 1;
+        // the copies still in flight land before the ring is reused or left
+        if (!failed)
+          for (int k2 = k; k2 < min(nk, k + S - 1); ++k2)
+            mbar_wait(&full[warp][(wseq + k2) % S], ((wseq + k2) / S) & 1, tries);
       }
-      __syncthreads();
-      const int ncontrib = sh.s_ncontrib;
-      if (sh.s_last) {
-        __threadfence();
-        auto slot_of = [&](int j) -> size_t { return (size_t)sh.s_slot[j]; };
-        for (int g = warp; g < G; g += NW) {
-          float M = kNegInf;
-          for (int j = lane; j < ncontrib; j += 32) M = fmaxf(M, __ldcg(ra.pm + slot_of(j) * G + g));
-          M = warp_max(M);
-          const float sk = a.sink ? a.sink[h * G + g] : kNegInf;
-          M = fmaxf(M, sk);
-          float Ls = 0.f;
-          for (int j = lane; j < ncontrib; j += 32) {
-            const float ms = __ldcg(ra.pm + slot_of(j) * G + g);
-            const float w = (ms == kNegInf || M == kNegInf) ? 0.f : expf(ms - M);
-            Ls += __ldcg(ra.pl + slot_of(j) * G + g) * w;
-            if (j < 64) sh.s_w[g][j] = w;
-          }
-          Ls = warp_sum(Ls);
-          if (a.sink && M != kNegInf) Ls += expf(sk - M);
-          if (lane == 0) {
-            sh.s_m[g] = M;
-            sh.s_inv[g] = Ls > 0.f ? 1.f / Ls : 0.f;
-            if (a.lse) a.lse[hq0 + g] = Ls > 0.f ? M + logf(Ls) : kNegInf;
-          }
-        }
-        __syncthreads();
-        constexpr int C4 = D / 4;
-        for (int i = threadIdx.x; i < G * C4; i += NT) {
-          const int g = i / C4, cc = i % C4;
-          const float M = sh.s_m[g];
-          float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int j0 = 0; j0 < ncontrib; j0 += 8) {
-            float4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              v[u] = j0 + u < ncontrib
-                         ? __ldcg(reinterpret_cast<const float4*>(ra.po + (slot_of(j0 + u) * G + g) * D) + cc)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int j = j0 + u;
-              if (j >= ncontrib) break;
-              float w;
-              if (j < 64) {
-                w = sh.s_w[g][j];
-              } else {
-                const float ms = __ldcg(ra.pm + slot_of(j) * G + g);
-                w = (ms == kNegInf || M == kNegInf) ? 0.f : expf(ms - M);
-              }
-              accv.x = fmaf(v[u].x, w, accv.x);
-              accv.y = fmaf(v[u].y, w, accv.y);
-              accv.z = fmaf(v[u].z, w, accv.z);
-              accv.w = fmaf(v[u].w, w, accv.w);
-            }
-          }
-          const float inv = sh.s_inv[g];
-          bf16* op = static_cast<bf16*>(a.out) + (hq0 + g) * D + 4 * cc;
-          op[0] = __float2bfloat16(accv.x * inv);
-          op[1] = __float2bfloat16(accv.y * inv);
-          op[2] = __float2bfloat16(accv.z * inv);
-          op[3] = __float2bfloat16(accv.w * inv);
-        }
-        if (threadIdx.x == 0) a.tickets[row] = 0;  // ready for the next call
-      }
+      // an infinite running max makes this warp's merge weight inf - inf =
+      // NaN at every later merge: the row's output and lse become NaN
+      m_run = __int_as_float(0x7f800000);
     }
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (m == 0) {
+      sM[warp][r] = m_run;
+      sL[warp][r] = l_run;
+    }
+    wseq += failed ? 0u : (uint32_t)nk;
+    __syncthreads();  // every warp's stages have been consumed (or drained): the rings become the merge area
+
+    float* sO = reinterpret_cast<float*>(ring);  // [W][8 heads][D]
+    merge_warps<D, W>(o, G, sO, sM, sL, sF, sHm, sHl);
+    finish_segment<D, NT>(ra, sh, s_pref, row, e, seg_end, lo, c, T, grid,
+                          [&](int g, int d, float& M, float& av, float& lv) {
+                            av = 0.f;
+#pragma unroll
+                            for (int w = 0; w < W; ++w) av = fmaf(sO[(w * 8 + g) * D + d], sF[w][g], av);
+                            M = sHm[g];
+                            lv = sHl[g];
+                          });
     __syncthreads();  // shared memory is reused by the next segment
     e = seg_end;
     ++row;
@@ -596,6 +820,29 @@ size_t refined_workspace(const Shape& s) {
   const size_t slots = 2 * (size_t)balanced_grid();
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   return al(rows * 4) + al(slots * s.G * s.D * 4) + 2 * al(slots * s.G * 4);
+}
+
+// One CTA of kStreamWarps warps per SM, each warp with a ring of two
+// 16-token groups at D = 128 (four at D = 64): the ring depth beyond that
+// bought nothing measurable, and more warps or CTAs per SM were slower.
+constexpr int kStreamWarps = 8;
+
+template <int D>
+static cudaError_t stream_tma_launch(const Shape& s, const RefinedArgs& ra, cudaStream_t st, bool* handled) {
+  constexpr int W = kStreamWarps, S = 256 / D;
+  CUtensorMap tk, tv;
+  const uint64_t tokens = (uint64_t)s.B * s.Hkv * s.Cap;
+  if (!encode_rows_map(&tk, ra.a.k, tokens, D) || !encode_rows_map(&tv, ra.a.v, tokens, D)) return cudaSuccess;
+  const size_t smem = StreamLayout<D, W, S>::REGION + (size_t)(ra.rows + 1) * sizeof(int) + 1024;
+  if (smem > 227 * 1024) return cudaSuccess;
+  *handled = true;
+  cudaError_t e = cudaFuncSetAttribute(attend_stream_tma_kernel<D, W, S>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  stat_add(kStatAttendStreamKTma);
+  e = launch_pdl(attend_stream_tma_kernel<D, W, S>, dim3(balanced_grid()), dim3(W * 32), smem, st, tk, tv, ra);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 template <int D>
@@ -638,6 +885,15 @@ cudaError_t launch_attend_refined(const Shape& s, const void* q, const void* k, 
   ra.codes = codes;
   ra.scales = static_cast<const bf16*>(scales);
   ra.res = res;
+  a.test_wait = (s.flags & kFlagTestWaitTimeout) ? 1 : 0;
+  // bf16 keys: the tensor-map fed kernel where the shape allows it
+  if (!codes && attend_tma_eligible(s) &&
+      !((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)) {
+    bool handled = false;
+    const cudaError_t e = s.D == 128 ? stream_tma_launch<128>(s, ra, st, &handled)
+                                     : stream_tma_launch<64>(s, ra, st, &handled);
+    if (handled || e != cudaSuccess) return e;
+  }
   return s.D == 128 ? balanced_launch<128>(ra, st) : balanced_launch<64>(ra, st);
 }
 

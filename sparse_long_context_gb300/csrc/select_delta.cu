@@ -232,8 +232,7 @@ delta_scan_kernel(const DeltaArgs a) {
 // and B = w split into fp16 hi + lo parts (w - hi is exact in fp32),
 // accumulated in fp32: the same scores as the CUDA-core scan to about 2^-22
 // relative.  Lane (r, m) owns channels [m D/4, (m+1) D/4), tokens r and
-// r + 8 of each 16-token tile and head r of B.  A warp takes one block at a
-// time and loads the codes of its next block before scoring the current one.
+// r + 8 of each 16-token tile and column r of B.
 //
 // Codes go to the tensor cores as fp16 subnormals, decoded by one AND each:
 // a 32-bit code word holds the 16 codes of 16 consecutive channels (channel
@@ -264,79 +263,154 @@ __device__ __forceinline__ void mma_f16_d(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int D>
-struct ScanCodes {
+// The codes of NTILE 16-token tiles of one block: lane (r, m) holds words
+// [m W, (m + 1) W) of tokens r and r + 8 of each tile.
+template <int D, int NTILE>
+struct ScanTiles {
   static constexpr int W = D / 64;  // 32-bit code words per token and lane (D/4 channels)
-  uint32_t c[kMaxScanTiles][2][W];  // [m-tile][token r, r + 8][word]
-  uint4 sv[D / 32];                 // the block's scales of the lane's D/4 channels (bf16)
+  uint32_t c[NTILE][2][W];          // [m-tile][token r, r + 8][word]
 };
 
-template <int D>
-__device__ __forceinline__ void load_scan_codes(ScanCodes<D>& sc, const uint8_t* cblk, const bf16* sblk, int ntile,
-                                                int lane) {
-  constexpr int W = ScanCodes<D>::W;
+template <int D, int NTILE>
+__device__ __forceinline__ void load_scan_tiles(ScanTiles<D, NTILE>& sc, const uint8_t* cblk, int lane) {
+  constexpr int W = ScanTiles<D, NTILE>::W;
   const int r = lane >> 2, m = lane & 3;
 #pragma unroll
-  for (int v = 0; v < D / 32; ++v) sc.sv[v] = __ldg(reinterpret_cast<const uint4*>(sblk + m * (D / 4) + 8 * v));
-#pragma unroll
-  for (int mt = 0; mt < kMaxScanTiles; ++mt) {
+  for (int mt = 0; mt < NTILE; ++mt) {
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const uint8_t* p = cblk + (size_t)(16 * mt + 8 * t + r) * (D / 4) + m * (D / 16);
-      if (mt < ntile) {
-        if constexpr (W == 2) {
-          const uint2 v = *reinterpret_cast<const uint2*>(p);
-          sc.c[mt][t][0] = v.x;
-          sc.c[mt][t][1] = v.y;
-        } else {
-          sc.c[mt][t][0] = *reinterpret_cast<const uint32_t*>(p);
-        }
+      if constexpr (W == 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        sc.c[mt][t][0] = v.x;
+        sc.c[mt][t][1] = v.y;
+      } else {
+        sc.c[mt][t][0] = *reinterpret_cast<const uint32_t*>(p);
       }
     }
   }
 }
 
-// Best margin over the block's tokens for this lane's heads 2m, 2m + 1:
-// scale * q.k^ - m~ = (level sums) + off, with the codes entering the MMA as
-// fp16 subnormals and the weights as fp16 hi parts (and lo parts with LO).
-template <int D, bool LO>
-__device__ __forceinline__ float scan_block_tiles(const ScanCodes<D>& cur, const uint32_t (&whi)[D / 16][2],
-                                                  const uint32_t (&wlo)[D / 16][2], int ntile, bool hv0, bool hv1,
-                                                  float off0, float off1) {
+// The block's scales (bf16) of the lane's D/4 channels; zero for a block
+// past the part's end.
+template <int D>
+__device__ __forceinline__ void load_scan_scales(uint4 (&sv)[D / 32], const bf16* sblk, bool valid, int lane) {
+  const int m = lane & 3;
+#pragma unroll
+  for (int v = 0; v < D / 32; ++v)
+    sv[v] = valid ? __ldg(reinterpret_cast<const uint4*>(sblk + m * (D / 4) + 8 * v)) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Best margin over the block's tokens for this lane's output columns 2m,
+// 2m + 1 (scale * q.k^ - m~ = level sums + off), with the codes entering the
+// MMA as fp16 subnormals and the weights as fp16 hi parts (and lo parts with
+// LO).  The k-steps run outermost, so the NTILE accumulator chains are
+// independent and their MMAs overlap.
+template <int D, int NTILE, bool LO>
+__device__ __forceinline__ float scan_tiles(const ScanTiles<D, NTILE>& cur, const uint32_t (&whi)[D / 16][2],
+                                            const uint32_t (&wlo)[D / 16][2], bool hv0, bool hv1, float off0,
+                                            float off1) {
   constexpr int CPL = D / 4;
-  float best = kNegInf;
+  float acc[NTILE][4];
 #pragma unroll
-  for (int mt = 0; mt < kMaxScanTiles; ++mt) {
-    if (mt >= ntile) break;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int mt = 0; mt < NTILE; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
 #pragma unroll
-    for (int wd = 0; wd < CPL / 16; ++wd) {
-      const uint32_t x = cur.c[mt][0][wd], y = cur.c[mt][1][wd];  // tokens r and r + 8
-      const uint32_t x8 = x >> 8, y8 = y >> 8;
+  for (int wd = 0; wd < CPL / 16; ++wd) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // channel pairs (2k, 2k + 1) of the word's two 8-channel halves
+    for (int k = 0; k < 4; ++k) {  // channel pairs (2k, 2k + 1) of the word's two 8-channel halves
+#pragma unroll
+      for (int mt = 0; mt < NTILE; ++mt) {
+        const uint32_t x = cur.c[mt][0][wd], y = cur.c[mt][1][wd];  // tokens r and r + 8
+        const uint32_t x8 = x >> 8, y8 = y >> 8;
         const uint32_t a0 = code_pair_sub_rt(x, x8, 2 * k), a1 = code_pair_sub_rt(y, y8, 2 * k);
         const uint32_t a2 = code_pair_sub_rt(x, x8, 2 * k + 1), a3 = code_pair_sub_rt(y, y8, 2 * k + 1);
-        mma_f16_d(acc, a0, a1, a2, a3, whi[4 * wd + k][0], whi[4 * wd + k][1]);
-        if constexpr (LO) mma_f16_d(acc, a0, a1, a2, a3, wlo[4 * wd + k][0], wlo[4 * wd + k][1]);
+        mma_f16_d(acc[mt], a0, a1, a2, a3, whi[4 * wd + k][0], whi[4 * wd + k][1]);
+        if constexpr (LO) mma_f16_d(acc[mt], a0, a1, a2, a3, wlo[4 * wd + k][0], wlo[4 * wd + k][1]);
       }
     }
-    // acc (64 2^-24 times the level sums): tokens r (0, 1) and r + 8 (2, 3), heads 2m (0, 2) and 2m + 1 (1, 3)
-    constexpr float kUnscale = 262144.f;  // 2^24 / 64
-    if (hv0) best = fmaxf(best, fmaxf(acc[0], acc[2]) * kUnscale + off0);
-    if (hv1) best = fmaxf(best, fmaxf(acc[1], acc[3]) * kUnscale + off1);
+  }
+  // acc (64 2^-24 times the level sums): tokens r (0, 1) and r + 8 (2, 3), columns 2m (0, 2) and 2m + 1 (1, 3)
+  constexpr float kUnscale = 262144.f;  // 2^24 / 64
+  float best = kNegInf;
+#pragma unroll
+  for (int mt = 0; mt < NTILE; ++mt) {
+    if (hv0) best = fmaxf(best, fmaxf(acc[mt][0], acc[mt][2]) * kUnscale + off0);
+    if (hv1) best = fmaxf(best, fmaxf(acc[mt][1], acc[mt][3]) * kUnscale + off1);
   }
   return best;
 }
 
-template <int D>
+// The lane's weights for B column r: hi parts per k-step (word wd holds
+// channels 16 wd + i and 16 wd + i + 8 in register i), the column's fp32
+// level-sum weight total and the total of their magnitudes (over the lane's
+// channels), or the lo parts w - hi.
+template <int D, bool LO>
+__device__ __forceinline__ void scan_weights(const float* qh, const uint4 (&sv)[D / 32], uint32_t (&wout)[D / 16][2],
+                                             float& wsum, float& wabs) {
+  constexpr int CPL = D / 4;
+  wsum = 0.f;
+  wabs = 0.f;
+#pragma unroll
+  for (int wd = 0; wd < CPL / 16; ++wd) {
+    float sa[8], sb[8];
+    unpack_vec(sv[2 * wd], sa);
+    unpack_vec(sv[2 * wd + 1], sb);
+    const float4 qa0 = *reinterpret_cast<const float4*>(qh + 16 * wd);
+    const float4 qa1 = *reinterpret_cast<const float4*>(qh + 16 * wd + 4);
+    const float4 qb0 = *reinterpret_cast<const float4*>(qh + 16 * wd + 8);
+    const float4 qb1 = *reinterpret_cast<const float4*>(qh + 16 * wd + 12);
+    const float qa[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qa1.x, qa1.y, qa1.z, qa1.w};
+    const float qb[8] = {qb0.x, qb0.y, qb0.z, qb0.w, qb1.x, qb1.y, qb1.z, qb1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float w0 = qa[i] * sa[i], w1 = qb[i] * sb[i];
+      const __half2 hi = __floats2half2_rn(w0, w1);
+      if constexpr (LO) {
+        const __half2 lo = __floats2half2_rn(w0 - __low2float(hi), w1 - __high2float(hi));
+        wout[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&lo);
+      } else {
+        wout[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&hi);
+        // the level sum takes the unscaled weights (exact: powers of two)
+        const float u = 1.f / (64 >> (2 * (i & 3)));
+        wsum = fmaf(w0 + w1, u, wsum);
+        wabs = fmaf(fabsf(w0) + fabsf(w1), u, wabs);
+      }
+    }
+  }
+}
+
+// A block scored again with hi + lo weights (exact to fp32 rounding): its
+// codes and the pair's scales read again, outside the main loop's registers
+// (rare: only blocks whose hi-only margin lies near -delta come here).
+template <int D, int NTILE>
+__device__ __noinline__ float rescan_block(const uint8_t* cblk, const bf16* sblk, bool svalid, const float* qh,
+                                          bool hv0, bool hv1, float off0, float off1) {
+  const int lane = threadIdx.x & 31;
+  ScanTiles<D, NTILE> c;
+  load_scan_tiles<D, NTILE>(c, cblk, lane);
+  uint4 sv[D / 32];
+  load_scan_scales<D>(sv, sblk, svalid, lane);
+  uint32_t whi[D / 16][2], wlo[D / 16][2];
+  float ds, da;
+  scan_weights<D, false>(qh, sv, whi, ds, da);
+  scan_weights<D, true>(qh, sv, wlo, ds, da);
+  return warp_max(scan_tiles<D, NTILE, true>(c, whi, wlo, hv0, hv1, off0, off1));
+}
+
+// One CTA per (row, part of the row's blocks); a warp scores NB blocks at a
+// time (NB = 2 when G <= 4: B columns 0..3 carry the heads' weights for the
+// first block and columns 4..7 those for the second, so every lane computes
+// weights that are used, once per two blocks).  The codes of the warp's next
+// block, and the scales of its next pair, are in flight while it scores.
+template <int D, int NTILE, int NB>
 __global__ void __launch_bounds__(kDeltaThreads, 2)
 delta_scan_mma_kernel(const DeltaArgs a) {
   pdl_wait_then_release();
-  constexpr int KS = D / 16;      // k-steps
-  constexpr int CPL = D / 4;      // channels per lane
+  constexpr int KS = D / 16;  // k-steps
+  constexpr int CPL = D / 4;  // channels per lane
   __shared__ float s_mt[kDeltaWarps][8];
   __shared__ float s_m[8];
+  __shared__ __align__(16) float s_qh[32][CPL + 4];  // per lane: its column's q, padded against bank conflicts
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, m = lane & 3;
   const int row = blockIdx.x / a.SPL, part = blockIdx.x % a.SPL;
@@ -351,96 +425,76 @@ delta_scan_mma_kernel(const DeltaArgs a) {
   if (j0 >= j1) return;
   const bf16* qrow = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G) * D;
   const bf16* krow = static_cast<const bf16*>(a.k) + (size_t)row * a.Cap * D;
-  pseudo_max_cta<bf16, D, 8>(a, qrow, krow, N, last, s_mt, s_m);
 
-  // q * scale / 2 of head r on the lane's channels, times 64 / f for the
-  // code scaling f = 1, 4, 16, 64 of the channel's place in its code byte
-  float qh[CPL];
-#pragma unroll
-  for (int v = 0; v < CPL / 8; ++v) {
-    float t[8];
-    if (r < G) load_vec(qrow + (size_t)r * D + m * CPL + 8 * v, t);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qh[8 * v + e] = r < G ? t[e] * a.scale * (0.5f * (64 >> (2 * (e & 3)))) : 0.f;
+  // column r of B is head r (NB = 1) or head r & 3 of block r >> 2 (NB = 2);
+  // lane l = 4 r + m holds q * scale / 2 of that head on channels
+  // [m D/4, (m+1) D/4), times 64 / f for the code scaling f = 1, 4, 16, 64
+  // of the channel's place in its code byte
+  for (int i = threadIdx.x; i < 32 * CPL; i += kDeltaThreads) {
+    const int l = i / CPL, e = i % CPL;
+    const int g = NB == 2 ? ((l >> 2) & 3) : (l >> 2);
+    s_qh[l][e] = g < G ? __bfloat162float(qrow[(size_t)g * D + (l & 3) * CPL + e]) * a.scale *
+                             (0.5f * (64 >> (2 * (e & 3))))
+                       : 0.f;
   }
-  // the pseudo-max of the lane's two output heads 2m, 2m + 1
-  const bool hv0 = 2 * m < G, hv1 = 2 * m + 1 < G;
-  const float mt0 = hv0 ? s_m[2 * m] : 0.f, mt1 = hv1 ? s_m[2 * m + 1] : 0.f;
-  const int ntile = a.block >> 4;
+  pseudo_max_cta<bf16, D, 8>(a, qrow, krow, N, last, s_mt, s_m);  // ends with a CTA barrier
+  const float* qh = s_qh[lane];
+  // output columns 2m, 2m + 1: their heads, and the block of the pair they score
+  const int h0 = NB == 2 ? (2 * m) & 3 : 2 * m, h1 = h0 + 1;
+  const int out_half = NB == 2 ? m >> 1 : 0;
+  const int w_half = NB == 2 ? r >> 2 : 0;  // the block of the pair whose weights this lane computes
+  const bool hv0 = h0 < G, hv1 = h1 < G;
+  const float mt0 = hv0 ? s_m[h0] : 0.f, mt1 = hv1 ? s_m[h1] : 0.f;
   const bf16* srow = static_cast<const bf16*>(a.scales) + (size_t)row * a.nblk_cap * D;
   const uint8_t* crow = a.codes + (size_t)row * a.Cap * (D / 4);
+  constexpr int kStride = kDeltaWarps * NB;
 
-  ScanCodes<D> cur, nxt;
-  int j = j0 + warp;
-  if (j < j1) load_scan_codes<D>(cur, crow + (size_t)j * a.block * (D / 4), srow + (size_t)j * D, ntile, lane);
-  while (j < j1) {
-    const int jn = j + kDeltaWarps;
-    if (jn < j1) load_scan_codes<D>(nxt, crow + (size_t)jn * a.block * (D / 4), srow + (size_t)jn * D, ntile, lane);
-    // weights of the block in fp16 hi parts (per k-step), their fp32 sum, and
-    // the sum of their magnitudes, which bounds what the lo parts w - hi add
-    float wc[CPL];
-    float wsum = 0.f, wabs = 0.f;
-#pragma unroll
-    for (int v = 0; v < CPL / 8; ++v) {
-      float sv[8];
-      unpack_vec(cur.sv[v], sv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        wc[8 * v + e] = qh[8 * v + e] * sv[e];
-        // the level sum takes the unscaled weights (exact: powers of two)
-        const float u = 1.f / (64 >> (2 * (e & 3)));
-        wsum += wc[8 * v + e] * u;
-        wabs += fabsf(wc[8 * v + e]) * u;
-      }
-    }
+  ScanTiles<D, NTILE> cur, nxt;
+  uint4 sv[D / 32];
+  int jg = j0 + warp * NB;
+  if (jg < j1) {
+    load_scan_tiles<D, NTILE>(cur, crow + (size_t)jg * a.block * (D / 4), lane);
+    load_scan_scales<D>(sv, srow + (size_t)(jg + w_half) * D, jg + w_half < j1, lane);
+  }
+  while (jg < j1) {
+    const int jn = jg + kStride;
+    // the pair's weights: fp16 hi parts, and the fp32 sums that give each
+    // column's offset and bound what the lo parts w - hi add
     uint32_t whi[KS][2];
-#pragma unroll
-    for (int wd = 0; wd < CPL / 16; ++wd) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {  // register i of word wd: channels (i, i + 8)
-        const __half2 hi = __floats2half2_rn(wc[16 * wd + i], wc[16 * wd + i + 8]);
-        whi[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&hi);
-      }
-    }
+    float wsum, wabs;
+    scan_weights<D, false>(qh, sv, whi, wsum, wabs);
     wsum += __shfl_xor_sync(0xffffffffu, wsum, 1);
-    wsum += __shfl_xor_sync(0xffffffffu, wsum, 2);  // head r's sum over all channels
+    wsum += __shfl_xor_sync(0xffffffffu, wsum, 2);  // column r's sum over all channels
     const float ws0 = __shfl_sync(0xffffffffu, wsum, 8 * m), ws1 = __shfl_sync(0xffffffffu, wsum, 8 * m + 4);
     const float off0 = -1.5f * ws0 - mt0, off1 = -1.5f * ws1 - mt1;
-    // 1. every token scored with the hi parts only
-    float best = scan_block_tiles<D, false>(cur, whi, whi, ntile, hv0, hv1, off0, off1);
-    best = warp_max(best);
     // A token's score differs from the hi-only one by sum_c code_c (w_c - hi_c)
     // <= 3 sum_c |w_c - hi_c|, with |w - hi| <= 2^-11 |w| for a normal fp16 hi
     // and at most the subnormal step 2^-25 below that (in the scaled units of
     // the weights, so 2^-25 u in the level sums); fp32 accumulation adds far
     // less than the 2x slack taken here.  Only a block whose hi-only margin
     // lies that close to -delta can decide the other way: it is scored again
-    // with hi + lo (exact to fp32 rounding).
+    // with hi + lo (exact to fp32 rounding).  The bound is the largest over
+    // every column of the pair.
     wabs += __shfl_xor_sync(0xffffffffu, wabs, 1);
     wabs += __shfl_xor_sync(0xffffffffu, wabs, 2);
     const float err = warp_max(6.f * (wabs * 0x1p-11f + (float)D * 0x1p-25f));
-    if (fabsf(best + a.delta) <= err) {  // warp-uniform
-      // the weights again (not kept live across the hi-only pass), then w - hi;
-      // word wd holds channels 16 wd + i and 16 wd + i + 8 in register i
-      uint32_t wlo[KS][2];
 #pragma unroll
-      for (int wd = 0; wd < CPL / 16; ++wd) {
-        float sa[8], sb[8];
-        unpack_vec(cur.sv[2 * wd], sa);
-        unpack_vec(cur.sv[2 * wd + 1], sb);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float w0 = qh[16 * wd + i] * sa[i], w1 = qh[16 * wd + i + 8] * sb[i];
-          const __half2 hi = __floats2half2_rn(w0, w1);
-          const __half2 lo = __floats2half2_rn(w0 - __low2float(hi), w1 - __high2float(hi));
-          wlo[4 * wd + (i >> 1)][i & 1] = *reinterpret_cast<const uint32_t*>(&lo);
-        }
-      }
-      best = warp_max(scan_block_tiles<D, true>(cur, whi, wlo, ntile, hv0, hv1, off0, off1));
+    for (int hb = 0; hb < NB; ++hb) {
+      const int j = jg + hb;
+      if (j >= j1) break;  // warp-uniform
+      const int jnext = hb + 1 < NB ? j + 1 : jn;
+      if (jnext < j1) load_scan_tiles<D, NTILE>(nxt, crow + (size_t)jnext * a.block * (D / 4), lane);
+      if (hb == 0 && jn < j1)  // this pair's scales are spent: the next pair's
+        load_scan_scales<D>(sv, srow + (size_t)(jn + w_half) * D, jn + w_half < j1, lane);
+      const bool mine = out_half == hb;
+      float best = warp_max(scan_tiles<D, NTILE, false>(cur, whi, whi, hv0 && mine, hv1 && mine, off0, off1));
+      if (fabsf(best + a.delta) <= err)  // warp-uniform
+        best = rescan_block<D, NTILE>(crow + (size_t)j * a.block * (D / 4), srow + (size_t)(jg + w_half) * D,
+                                      jg + w_half < j1, qh, hv0 && mine, hv1 && mine, off0, off1);
+      if (lane == 0) a.flags[(size_t)row * a.nblk_cap + j] = best >= -a.delta ? 1 : 0;
+      cur = nxt;
     }
-    if (lane == 0) a.flags[(size_t)row * a.nblk_cap + j] = best >= -a.delta ? 1 : 0;
-    cur = nxt;
-    j = jn;
+    jg = jn;
   }
 }
 
@@ -502,9 +556,14 @@ static cudaError_t delta_launch(const DeltaArgs& a, int rows, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D>
-static cudaError_t delta_mma_launch(const DeltaArgs& a, int rows, cudaStream_t st) {
-  cudaError_t e = launch_pdl(delta_scan_mma_kernel<D>, dim3(rows * a.SPL), dim3(kDeltaThreads), 0, st, a);
+template <int D, int NTILE, int NB>
+static cudaError_t delta_scan_launch(const DeltaArgs& a, int rows, cudaStream_t st) {
+  return launch_pdl(delta_scan_mma_kernel<D, NTILE, NB>, dim3(rows * a.SPL), dim3(kDeltaThreads), 0, st, a);
+}
+
+template <int D, int NTILE>
+static cudaError_t delta_mma_launch_t(const DeltaArgs& a, int rows, cudaStream_t st) {
+  cudaError_t e = a.G <= 4 ? delta_scan_launch<D, NTILE, 2>(a, rows, st) : delta_scan_launch<D, NTILE, 1>(a, rows, st);
   if (e != cudaSuccess) return e;
   e = launch_pdl(delta_compact_kernel, dim3(rows), dim3(1024), 0, st, a);
   if (e != cudaSuccess) return e;
@@ -543,11 +602,13 @@ cudaError_t launch_select_delta(const Shape& s, const void* q, const void* k,
     stat_add(kStatDeltaCudaCores);
     return s.D == 64 ? delta_g<float, 64>(a, rows, st) : delta_g<float, 128>(a, rows, st);
   }
-  if (!(s.flags & 1) && s.G <= 8 && block <= 16 * kMaxScanTiles) {  // tensor cores unless asked for CUDA cores
+  if (!(s.flags & 1) && s.G <= 8 && block >= 16 && block <= 16 * kMaxScanTiles) {  // tensor cores unless asked for CUDA cores
     // one wave of two CTAs per SM (each recomputes the row's pseudo-max once)
     a.SPL = std::max(1, std::min(maxblk, (2 * sm_count()) / rows));
     stat_add(kStatDeltaTensorCores);
-    return s.D == 64 ? delta_mma_launch<64>(a, rows, st) : delta_mma_launch<128>(a, rows, st);
+    const int nt = block >> 4;
+    if (s.D == 64) return nt == 1 ? delta_mma_launch_t<64, 1>(a, rows, st) : nt == 2 ? delta_mma_launch_t<64, 2>(a, rows, st) : delta_mma_launch_t<64, 4>(a, rows, st);
+    return nt == 1 ? delta_mma_launch_t<128, 1>(a, rows, st) : nt == 2 ? delta_mma_launch_t<128, 2>(a, rows, st) : delta_mma_launch_t<128, 4>(a, rows, st);
   }
   stat_add(kStatDeltaCudaCores);
   return s.D == 64 ? delta_g<bf16, 64>(a, rows, st) : delta_g<bf16, 128>(a, rows, st);

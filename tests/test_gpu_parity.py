@@ -39,13 +39,21 @@ SMALL_QUEST = {
 SMALL_DELTA = {
     "ffd_ragged": dict(name="ffd", ctx_len=[65536 + 100, 20000], capacity=65536 + 128),
     "ffd_aligned": dict(name="ffd", batch=1, ctx_len=8192),
+    # the tensor-core scan's other forms: G = 8 (one block per weight set),
+    # D = 64, 16- and 32-token blocks, odd block counts per part
+    "ffd_g8_d64_b16": dict(name="ffd", ctx_len=[5000, 777], num_q_heads=32, num_kv_heads=4, head_dim=64,
+                           block=16, page_size=16),
+    "ffd_g2_b32": dict(name="ffd", ctx_len=[12345, 64 * 37 + 1], num_q_heads=16, num_kv_heads=8, block=32,
+                       page_size=32),
+    "ffd_d64_b64": dict(name="ffd", ctx_len=[30000 + 64, 64 * 3 + 17], head_dim=64),
 }
 
 
 def make(case):
     kw = dict(case)
     name = kw.pop("name", None)
-    fields = {f: kw.pop(f) for f in ("page_size", "k_pages", "n_sink_pages") if f in kw}
+    fields = {f: kw.pop(f) for f in ("page_size", "k_pages", "n_sink_pages", "block", "num_q_heads", "num_kv_heads",
+                                     "head_dim") if f in kw}
     s = W.spec(name, **kw)
     for f, v in fields.items():
         setattr(s, f, v)
@@ -188,7 +196,7 @@ def test_delta_step_small(key, path):
     dw = PT.upload(s, host, **PATHS[path])
     sel, cnt, out, lse = PT.run_step(dw)
     ties = check_all_rows(s, host, sel, cnt, out, lse, dw)
-    kept = cnt.sum() / sum((n + 63) // 64 for n in host.ctx_len for _ in range(s.num_kv_heads))
+    kept = cnt.sum() / sum((n + s.block - 1) // s.block for n in host.ctx_len for _ in range(s.num_kv_heads))
     print(f"{key}: kept fraction {kept:.3f}, boundary ties {ties}")
 
 
