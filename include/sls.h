@@ -550,6 +550,7 @@ typedef struct sls_stats {
   uint64_t select_rows_all_keys;      /* rows wider than 8192 pages whose sls_select_pages top-k
                                          ranked all of the row's keys (the candidate check failed) */
   uint64_t attend_stream_k_tma;       /* of attend_stream_k: the tensor-map fed kernel */
+  uint64_t attend_refined_tma;        /* of attend_refined: the tensor-map fed kernel */
 } sls_stats;
 
 /* Fills *out with the counters (synchronising the device to read the row

@@ -32,7 +32,7 @@ class Stats(ctypes.Structure):
         "quest_step_one_launch", "quest_step_two_launch", "step_rows_dense", "step_rows_all_keys",
         "select_pages", "select_delta_tensor_cores", "select_delta_cuda_cores", "attend_tma", "attend_mma",
         "attend_cuda_cores", "attend_stream_k", "attend_refined", "combine", "metadata", "recall",
-        "select_rows_all_keys", "attend_stream_k_tma")]
+        "select_rows_all_keys", "attend_stream_k_tma", "attend_refined_tma")]
 
 
 _P = ctypes.c_void_p

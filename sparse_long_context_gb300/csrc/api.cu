@@ -138,6 +138,7 @@ sls_status sls_get_stats(sls_stats* out, int32_t reset) {
   out->metadata = take(sls::kStatMetadata);
   out->recall = take(sls::kStatRecall);
   out->attend_stream_k_tma = take(sls::kStatAttendStreamKTma);
+  out->attend_refined_tma = take(sls::kStatAttendRefinedTma);
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(SLS_ECUDA, "device synchronisation failed");
   unsigned long long dense = 0, all_keys = 0;
   sls::take_step_row_stats(&dense, &all_keys, reset != 0);

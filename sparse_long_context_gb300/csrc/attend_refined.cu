@@ -808,6 +808,250 @@ attend_stream_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
   }
 }
 
+// The refined attend of attend_balanced_kernel fed by the tensor memory
+// accelerator (D = 128): the same stream-K partition, and every warp streams
+// its own groups through its own ring of S stages, as in
+// attend_stream_tma_kernel.  A warp takes whole blocks (list entries warp,
+// warp + W, ...) and their groups one after the other, so the fp16 hi/lo
+// parts of q s are formed once per block, from scales loaded while the
+// warp's previous block was attended.  A stage holds, for a group of a
+// complete block, its 8-bit residuals (16 rows of D bytes, 128-byte swizzle:
+// chunk c of token t at chunk c ^ (t % 8)) at offset 0, its codes (16 rows
+// of D/4 bytes) at kRefCodesOff and its V at TmaLayout::GROUP; for a group
+// of the newest, partial block its bf16 K and V as in the bf16 kernel.
+constexpr int kRefCodesOff = 2048;  // after the 16 residual rows of 128 bytes
+
+// Scores of a refined group from its stage: lane (r, m) reads the codes
+// (8 bytes) and residuals (32 bytes) of its channel quarter for tokens r and
+// r + 8 and forms sc with the B operands decoded by refined_step, as the
+// register-fed kernel does from its loads.
+__device__ __forceinline__ void refined_scores_smem(uint32_t stage, const uint32_t (&hi)[4][4],
+                                                    const uint32_t (&lo)[4][4], float (&sc)[2][2][4], int lane) {
+  const int r = lane >> 2, m = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) sc[nt][c][0] = sc[nt][c][1] = sc[nt][c][2] = sc[nt][c][3] = 0.f;
+  uint32_t cw[2][2], rw[2][8];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int tok = r + 8 * nt;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(cw[nt][0]), "=r"(cw[nt][1])
+                 : "r"(stage + kRefCodesOff + tok * 32 + m * 8));
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(rw[nt][4 * u]), "=r"(rw[nt][4 * u + 1]), "=r"(rw[nt][4 * u + 2]), "=r"(rw[nt][4 * u + 3])
+                   : "r"(stage + tok * 128 + (((2 * m + u) ^ r) << 4)));
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t n[4];
+      refined_step(cw[nt][s >> 1] >> (16 * (s & 1)), rw[nt][2 * s], rw[nt][2 * s + 1], n);
+      mma_f16(sc[nt][0], hi[s][0], 0u, hi[s][1], 0u, n[0], n[1]);
+      mma_f16(sc[nt][1], hi[s][2], 0u, hi[s][3], 0u, n[2], n[3]);
+      mma_f16(sc[nt][0], lo[s][0], 0u, lo[s][1], 0u, n[0], n[1]);
+      mma_f16(sc[nt][1], lo[s][2], 0u, lo[s][3], 0u, n[2], n[3]);
+    }
+  }
+}
+
+template <int W, int S>
+__global__ void __launch_bounds__(W * 32, 1)
+attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                          const __grid_constant__ CUtensorMap tcodes, const __grid_constant__ CUtensorMap tres,
+                          const RefinedArgs ra) {
+  constexpr int D = 128;
+  using L = TmaLayout<D>;
+  constexpr int KS = D / 16, NS = D / 32;
+  constexpr int NT = W * 32;
+  constexpr uint32_t kRefinedBytes = 16 * D + 16 * (D / 4) + L::GROUP;  // residuals, codes, V
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* ring = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  int* s_pref = reinterpret_cast<int*>(ring + StreamLayout<D, W, S>::REGION);  // [rows + 1]
+  __shared__ RefSmem sh;
+  __shared__ uint64_t full[W][S];
+  __shared__ float sM[W][8], sL[W][8], sF[W][8];
+  __shared__ float sHm[8], sHl[8];
+  const AttendArgs& a = ra.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, m = lane & 3;
+  const int G = a.G, rows = ra.rows, grid = gridDim.x, c = blockIdx.x;
+  const int gpb = a.P >> 4;  // groups per block
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < W; ++w)
+      for (int s = 0; s < S; ++s) mbar_init(&full[w][s], 1);
+    mbar_fence_init();
+    tma_prefetch_map(&tk);
+    tma_prefetch_map(&tv);
+    tma_prefetch_map(&tcodes);
+    tma_prefetch_map(&tres);
+    sh.s_fail = 0;
+  }
+  pdl_wait_then_release();
+  int T, row;
+  long long lo, hi;
+  if (!stream_k_begin<D, NT>(a, rows, sh, s_pref, T, lo, hi, row)) return;  // after its barrier: inits visible
+
+  const bool plant = a.test_wait && c == 0 && warp == 0;
+  const uint32_t tries = plant ? kTestWaitTries : kWaitTries;
+  unsigned char* wring = ring + (size_t)warp * S * L::STAGE;
+  const uint32_t wring_u32 = smem_u32(wring);
+  uint32_t wseq = 0;
+  long long e = lo;
+  while (e < hi) {
+    const long long seg_end = min(hi, (long long)s_pref[row + 1]);
+    const int b = row / a.Hkv, h = row % a.Hkv;
+    const int N = clamp_len(a.ctx_len[b], a.Cap);
+    const int nent = (int)(seg_end - e);
+    const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + (int)(e - s_pref[row]);
+    stage_page_list(sh.s_pg, kRefStaged, plist, 0, nent, a.Cap >> a.pshift, threadIdx.x, NT);
+    __syncthreads();
+    const bool failed = sh.s_fail != 0;
+    const int nblk = nent > warp ? (nent - warp + W - 1) / W : 0;  // this warp's blocks: warp + W j
+    const int nk = nblk * gpb;
+    auto page_of = [&](int eb) { return eb < kRefStaged ? sh.s_pg[eb] : __ldg(plist + eb); };
+    // group k of this warp: group k % gpb of its block k / gpb
+    auto group_of = [&](int k) { return (warp + W * (k / gpb)) * gpb + (k % gpb); };
+    auto refined_at = [&](int base, int lim) { return lim > 0 && (((base >> a.pshift) + 1) << a.pshift) <= N; };
+
+    auto issue = [&](int k) {
+      const uint32_t q = wseq + k;
+      const int st = q % S;
+      int lim;
+      const int base = stream_group_base(a, N, sh.s_pg, plist, group_of(k), lim);
+      unsigned char* dst = wring + st * L::STAGE;
+      const int y = row * a.Cap + base;
+      if (plant && q == 0) {
+        mbar_arrive_expect_tx(&full[warp][st], 16);  // no copy is issued: this phase never completes
+      } else if (refined_at(base, lim)) {
+        mbar_arrive_expect_tx(&full[warp][st], kRefinedBytes);
+        tma_load_2d(dst, &tres, 0, y, &full[warp][st]);
+        tma_load_2d(dst + kRefCodesOff, &tcodes, 0, y, &full[warp][st]);
+        tma_load_3d(dst + L::GROUP, &tv, 0, y, 0, &full[warp][st]);
+      } else if (lim > 0) {
+        mbar_arrive_expect_tx(&full[warp][st], L::STAGE);
+        tma_load_3d(dst, &tk, 0, y, 0, &full[warp][st]);
+        tma_load_3d(dst + L::GROUP, &tv, 0, y, 0, &full[warp][st]);
+      } else {
+        mbar_arrive(&full[warp][st]);
+      }
+    };
+    if (lane == 0 && !failed)
+      for (int k = 0; k < min(S - 1, nk); ++k) issue(k);
+    __syncwarp();
+
+    float o[KS][4];
+    float m_run = kNegInf, l_run = 0.f;
+#pragma unroll
+    for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    // Q is read where it is used (L1-resident): per block for the refined
+    // weights, per group for the bf16 groups of the newest block
+    const bf16* qp = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G + r) * D;
+    // the scales of the warp's next block (lane's channel quarter), in flight
+    const bf16* srow = ra.scales + (size_t)row * (a.Cap >> a.pshift) * D + m * (D / 4);
+    uint4 sv[NS];
+    auto load_scales = [&](int eb) {
+      const int pg = eb < nent ? page_of(eb) : -1;
+      const bool okp = (unsigned)pg < (unsigned)(a.Cap >> a.pshift);
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+        sv[s] = okp ? __ldg(reinterpret_cast<const uint4*>(srow + (size_t)pg * D + 8 * s)) : make_uint4(0, 0, 0, 0);
+    };
+    if (nk > 0) load_scales(warp);
+    uint32_t whi[NS][4], wlo[NS][4];
+    bool ok = !failed;
+    int k = 0;
+    if (ok) {
+      for (; k < nk; ++k) {
+        if (lane == 0 && k + S - 1 < nk) issue(k + S - 1);
+        if (k % gpb == 0) {
+          // a new block: the fp16 hi/lo parts of q s (lane (r, m): head r,
+          // channels [m D/4, (m+1) D/4) as pairs), then the next block's scales
+#pragma unroll
+          for (int s = 0; s < NS; ++s) {
+            const uint4 cq =
+                r < G ? __ldg(reinterpret_cast<const uint4*>(qp + m * (D / 4) + 8 * s)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const uint32_t sw = (&sv[s].x)[p], qw = (&cq.x)[p];
+              const float xa = bf16_lo_f(qw) * bf16_lo_f(sw);  // exact
+              const float xb = bf16_hi_f(qw) * bf16_hi_f(sw);
+              const __half2 hh = __floats2half2_rn(xa, xb);
+              whi[s][p] = h2_bits(hh);
+              wlo[s][p] = h2_bits(__floats2half2_rn(xa - __low2float(hh), xb - __high2float(hh)));
+            }
+          }
+          load_scales(warp + W * (k / gpb + 1));
+        }
+        const uint32_t q = wseq + k;
+        const int st = q % S;
+        if (!mbar_wait(&full[warp][st], (q / S) & 1, tries)) {
+          ok = false;
+          break;
+        }
+        int lim;
+        const int base = stream_group_base(a, N, sh.s_pg, plist, group_of(k), lim);
+        const uint32_t stage = wring_u32 + st * L::STAGE;
+        if (refined_at(base, lim)) {
+          float sc[2][2][4];
+          refined_scores_smem(stage, whi, wlo, sc, lane);
+          tma_softmax_pv<D>(sc, stage + L::GROUP, lim, o, m_run, l_run, a.qscale * (1.f / 508.f), lane);
+        } else if (lim > 0) {
+          uint32_t qa[KS][2];  // tma_group's fragments: a0 = Q[head r][16ks + 2m, +1], a2 = Q[r][16ks + 8 + 2m, +1]
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            qa[ks][0] = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * m)) : 0u;
+            qa[ks][1] = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * m)) : 0u;
+          }
+          tma_group<D>(stage, lim, qa, o, m_run, l_run, a.qscale, lane);
+        }
+        __syncwarp();
+        if (lane == 0) fence_proxy_async_smem();
+      }
+    }
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) {
+        note_wait_timeout();
+        sh.s_fail = 1;
+        if (!failed)
+          for (int k2 = k; k2 < min(nk, k + S - 1); ++k2)
+            mbar_wait(&full[warp][(wseq + k2) % S], ((wseq + k2) / S) & 1, tries);
+      }
+      // an infinite running max makes this warp's merge weight inf - inf =
+      // NaN at every later merge: the row's output and lse become NaN
+      m_run = __int_as_float(0x7f800000);
+    }
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (m == 0) {
+      sM[warp][r] = m_run;
+      sL[warp][r] = l_run;
+    }
+    wseq += failed ? 0u : (uint32_t)nk;
+    __syncthreads();  // every warp's stages have been consumed (or drained): the rings become the merge area
+
+    float* sO = reinterpret_cast<float*>(ring);  // [W][8 heads][D]
+    merge_warps<D, W>(o, G, sO, sM, sL, sF, sHm, sHl);
+    finish_segment<D, NT>(ra, sh, s_pref, row, e, seg_end, lo, c, T, grid,
+                          [&](int g, int d, float& M, float& av, float& lv) {
+                            av = 0.f;
+#pragma unroll
+                            for (int w = 0; w < W; ++w) av = fmaf(sO[(w * 8 + g) * D + d], sF[w][g], av);
+                            M = sHm[g];
+                            lv = sHl[g];
+                          });
+    __syncthreads();
+    e = seg_end;
+    ++row;
+    while (row < rows && s_pref[row + 1] == s_pref[row]) ++row;
+  }
+}
+
 bool refined_supported(const Shape& s) {
   return s.dtype == 1 && s.G <= 8 && s.P >= 16 && (s.D == 64 || s.D == 128) && s.B * s.Hkv <= kRefMaxRows;
 }
@@ -826,6 +1070,9 @@ size_t refined_workspace(const Shape& s) {
 // 16-token groups at D = 128 (four at D = 64): the ring depth beyond that
 // bought nothing measurable, and more warps or CTAs per SM were slower.
 constexpr int kStreamWarps = 8;
+// Stages per warp of the refined kernel: its groups take longer to score
+// than to copy, and three stages measured the same as two.
+constexpr int kRefinedStages = 2;
 
 template <int D>
 static cudaError_t stream_tma_launch(const Shape& s, const RefinedArgs& ra, cudaStream_t st, bool* handled) {
@@ -841,6 +1088,27 @@ static cudaError_t stream_tma_launch(const Shape& s, const RefinedArgs& ra, cuda
   if (e != cudaSuccess) return e;
   stat_add(kStatAttendStreamKTma);
   e = launch_pdl(attend_stream_tma_kernel<D, W, S>, dim3(balanced_grid()), dim3(W * 32), smem, st, tk, tv, ra);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// The refined attend on tensor-map fed rings (D = 128; the bf16 kernel's
+// grid).
+static cudaError_t refined_tma_launch(const Shape& s, const RefinedArgs& ra, cudaStream_t st, bool* handled) {
+  constexpr int D = 128, W = kStreamWarps, S = kRefinedStages;
+  CUtensorMap tk, tv, tc, tr;
+  const uint64_t tokens = (uint64_t)s.B * s.Hkv * s.Cap;
+  if (!encode_rows_map(&tk, ra.a.k, tokens, D) || !encode_rows_map(&tv, ra.a.v, tokens, D) ||
+      !encode_bytes_map(&tc, ra.codes, tokens, D / 4) || !encode_bytes_map(&tr, ra.res, tokens, D))
+    return cudaSuccess;
+  const size_t smem = StreamLayout<D, W, S>::REGION + (size_t)(ra.rows + 1) * sizeof(int) + 1024;
+  if (smem > 227 * 1024) return cudaSuccess;
+  *handled = true;
+  cudaError_t e = cudaFuncSetAttribute(attend_refined_tma_kernel<W, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  stat_add(kStatAttendRefinedTma);
+  e = launch_pdl(attend_refined_tma_kernel<W, S>, dim3(balanced_grid()), dim3(W * 32), smem, st, tk, tv, tc, tr, ra);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -886,12 +1154,18 @@ cudaError_t launch_attend_refined(const Shape& s, const void* q, const void* k, 
   ra.scales = static_cast<const bf16*>(scales);
   ra.res = res;
   a.test_wait = (s.flags & kFlagTestWaitTimeout) ? 1 : 0;
-  // bf16 keys: the tensor-map fed kernel where the shape allows it
-  if (!codes && attend_tma_eligible(s) &&
-      !((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)) {
+  // the tensor-map fed kernels where the shape allows them
+  const bool aligned = !((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+                          reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(res)) & 15);
+  if (!codes && attend_tma_eligible(s) && aligned) {
     bool handled = false;
     const cudaError_t e = s.D == 128 ? stream_tma_launch<128>(s, ra, st, &handled)
                                      : stream_tma_launch<64>(s, ra, st, &handled);
+    if (handled || e != cudaSuccess) return e;
+  }
+  if (codes && s.D == 128 && attend_tma_eligible(s) && aligned) {
+    bool handled = false;
+    const cudaError_t e = refined_tma_launch(s, ra, st, &handled);
     if (handled || e != cudaSuccess) return e;
   }
   return s.D == 128 ? balanced_launch<128>(ra, st) : balanced_launch<64>(ra, st);

@@ -222,6 +222,20 @@ bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, int D) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_bytes_map(CUtensorMap* map, const void* base, uint64_t rows, int row_bytes) {
+  auto fn = encode_fn();
+  if (!fn || (row_bytes != 128 && row_bytes % 16 != 0) || row_bytes > 256) return false;
+  // rows of row_bytes bytes, box 16 rows; rows of exactly 128 bytes land
+  // with the 128-byte swizzle (chunk c of row t at chunk c ^ (t % 8))
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)row_bytes, 16};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool attend_tma_eligible(const Shape& s) {
   return s.dtype == 1 && !(s.flags & 3) && s.G <= 8 && s.P >= 16 && (s.D == 64 || s.D == 128) &&
          (long long)s.B * s.Hkv * s.Cap < (1ll << 31) && encode_fn() != nullptr;

@@ -254,5 +254,9 @@ __device__ __forceinline__ void cluster_push_combine(const AttendArgs& a, int ro
 // Host: 3-D tensor map over `rows` rows of D bf16 channels (a K or V cache
 // viewed as [tokens, D], or page metadata as [pages, D]), box 64 x 16 x D/64.
 bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, int D);
+// Host: 2-D tensor map over `rows` rows of row_bytes bytes (thumbnail codes
+// or 8-bit residuals), box row_bytes x 16 rows; rows of 128 bytes use the
+// 128-byte swizzle.  False if the driver refuses it.
+bool encode_bytes_map(CUtensorMap* map, const void* base, uint64_t rows, int row_bytes);
 
 }  // namespace sls

@@ -143,7 +143,7 @@ cudaError_t launch_combine(const Shape& s, const float* o_part, const float* m_p
 enum StatId {
   kStatStepOneLaunch, kStatStepTwoLaunch, kStatSelectPages, kStatDeltaTensorCores, kStatDeltaCudaCores,
   kStatAttendTma, kStatAttendMma, kStatAttendCudaCores, kStatAttendStreamK, kStatAttendRefined, kStatCombine,
-  kStatMetadata, kStatRecall, kStatAttendStreamKTma, kStatCount
+  kStatMetadata, kStatRecall, kStatAttendStreamKTma, kStatAttendRefinedTma, kStatCount
 };
 void stat_add(StatId id);
 // Rows the one-launch step attended densely (sparsity gate) and rows whose

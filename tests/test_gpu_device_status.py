@@ -163,15 +163,20 @@ def test_a_wait_that_gives_up_is_reported(entry):
     np.testing.assert_array_equal(again, ok_out)
 
 
-def test_a_stream_k_wait_that_gives_up_is_reported():
-    """The tensor-map fed stream-K attend (bf16 keys over block lists): under
-    the hook the first CTA's first stage never fills.  Every row keeps all
-    41 blocks (328 entries, more than one per CTA), so the first CTA's range
-    holds entries of row 0 only: row 0 becomes NaN, every other row is
-    unchanged, and the next clean call is correct again."""
+@pytest.mark.parametrize("refined", [False, True])
+def test_a_stream_k_wait_that_gives_up_is_reported(refined):
+    """The tensor-map fed stream-K attends (bf16 keys, or the refined keys,
+    over block lists): under the hook the first CTA's first stage never
+    fills.  Every row keeps all 41 blocks (328 entries, more than one per
+    CTA), so the first CTA's range holds entries of row 0 only: row 0 becomes
+    NaN, every other row is unchanged, and the next clean call is correct
+    again."""
     s = W.spec("ffd", batch=1, ctx_len=64 * 40 + 9, capacity=64 * 48)
     host = W.generate(s)
     dw = PT.upload(s, host)
+    codes = scales = res = None
+    if refined:
+        codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block)
     npool = s.capacity // s.block
     lists = np.full((s.rows, npool), -1, dtype=np.int32)
     count = np.zeros(s.rows, dtype=np.int32)
@@ -184,7 +189,7 @@ def test_a_stream_k_wait_that_gives_up_is_reported():
                            dw.K.dtype, test_wait_timeout=True)
 
     def run(desc):
-        out, lse = ops.refined_decode_attend_combine(desc, dw.q, dw.K, dw.V, None, None, None, idx, cnt, dw.ctx)
+        out, lse = ops.refined_decode_attend_combine(desc, dw.q, dw.K, dw.V, codes, scales, res, idx, cnt, dw.ctx)
         return out.float().cpu().numpy(), lse.cpu().numpy()
 
     G = s.group
@@ -195,7 +200,7 @@ def test_a_stream_k_wait_that_gives_up_is_reported():
     t_out, t_lse = run(hooked)
     code = _check_status()
     assert code == L.SLS_ETIMEOUT, (code, L.load().sls_last_error())
-    assert ops.get_stats(reset=True)["attend_stream_k_tma"] >= 2
+    assert ops.get_stats(reset=True)["attend_refined_tma" if refined else "attend_stream_k_tma"] >= 2
     assert np.isnan(t_out[0, :G]).all() and np.isnan(t_lse[0, :G]).all()
     np.testing.assert_array_equal(t_out[0, G:], ok_out[0, G:])
     np.testing.assert_array_equal(t_lse[0, G:], ok_lse[0, G:])

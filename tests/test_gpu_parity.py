@@ -31,6 +31,9 @@ SMALL_QUEST = {
     "tiny_ragged": dict(name="tiny", ctx_len=[1000]),
     "qwen7b_ragged": dict(name="qwen7b", ctx_len=[8197, 3000, 700], capacity=8208),
     "qwen1p5b_4k": dict(name="qwen1p5b", batch=3, ctx_len=4096),
+    # an odd number of rows, and rows of different contexts, one within the budget
+    "odd_rows": dict(name="qwen7b", batch=3, ctx_len=[6000, 300, 4100], capacity=6016, num_q_heads=12,
+                     num_kv_heads=3),
     "gptoss_ragged": dict(name="gptoss", ctx_len=[20000, 5003], capacity=20000),
     # D = 64 and G = 8 with 16-token pages (the tensor-map path at its other head size)
     "gptoss_p16": dict(name="gptoss", ctx_len=[5003, 1000], capacity=5008, page_size=16, k_pages=64,

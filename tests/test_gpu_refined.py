@@ -87,8 +87,8 @@ SMALL = {
 }
 
 
-def _refined_step(s, host):
-    dw = PT.upload(s, host)
+def _refined_step(s, host, no_tma=False):
+    dw = PT.upload(s, host, no_tma=no_tma)
     codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block)
     step = ops.DeltaDecode(dw.desc, s.block, s.delta, refined=True)
     out, lse = step(dw.q, dw.K, dw.V, codes, scales, dw.ctx, dw.sink, res=res)
@@ -101,11 +101,16 @@ def _refined_oracle(s, host, b, h, blocks):
     return O.refined_attention_row(q, K, V, blocks, int(host.ctx_len[b]), s.block, s.scale, sink)
 
 
+# the tensor-map fed refined attend (the default at D = 128) and the register-fed one
+@pytest.mark.parametrize("no_tma", [False, True])
 @pytest.mark.parametrize("key", list(SMALL))
-def test_refined_step_matches_oracle(key):
+def test_refined_step_matches_oracle(key, no_tma):
     s = W.spec("ffd", **SMALL[key])
     host = W.generate(s)
-    dw, (codes, scales, res), step, out, lse = _refined_step(s, host)
+    ops.get_stats(reset=True)
+    dw, (codes, scales, res), step, out, lse = _refined_step(s, host, no_tma)
+    st = ops.get_stats(reset=True)
+    assert st["attend_refined"] == 1 and st["attend_refined_tma"] == (0 if no_tma else 1), st
     sel, cnt = step.block_idx.cpu().numpy(), step.count.cpu().numpy()
     G = s.group
     ties = 0
@@ -152,6 +157,7 @@ def test_refined_scores_differ_from_exact_ones():
     out_ex, _ = exact(dw.q, dw.K, dw.V, dw.codes, dw.scales, dw.ctx, dw.sink)
     st = ops.get_stats(reset=True)
     assert st["attend_refined"] == 1 and st["attend_stream_k"] == 1, st
+    assert st["attend_refined_tma"] == 1 and st["attend_stream_k_tma"] == 1, st
     assert st["select_delta_tensor_cores"] == 2 and st["select_delta_cuda_cores"] == 0, st
     out_ex = out_ex.float().cpu().numpy().astype(np.float64)
     assert np.abs(out_ref - out_ex).max() > 0
