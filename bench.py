@@ -44,23 +44,43 @@ METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak) for select+att
 # written; traffic grows with the rows, so x4 for batch 32).  Reported only
 # for that workload and only while the kernel's sources hash to the ones
 # captured; otherwise null.
-STEP_TRAFFIC_B32 = 4 * (50.471168e6 + 0.108288e6)
+STEP_TRAFFIC_B32 = 4 * (50.470656e6 + 0.150784e6)
 STEP_SOURCES = ("quest_step.cu", "attend_tma.cuh", "tma.cuh", "mma.cuh", "attend_common.cuh", "common.cuh",
                 "status.cuh")
-STEP_SOURCES_SHA256 = "7afc1aef82b38b6abc2c952f887a386ec1c4e8f3c180e3eca0e2a067f29f14bf"
+STEP_SOURCES_SHA256 = "4fbb8ce9d266b32bd44b705feb35c795fa78438094d50997d94ce6d1de5cf5f0"
+
+
+# DRAM bytes per launch of the top-delta step's bf16-key attend
+# (attend_stream_tma_kernel) on the ffd workload, from the committed capture
+# (profiles/topdelta_ffd_256k.md, read + written; the kept set is the seeded
+# workload's), under the same source-hash rule.
+FFD_ATTEND_TRAFFIC = 490.945280e6 + 3.271424e6
+FFD_ATTEND_SOURCES = ('attend_refined.cu', 'attend_tma.cuh', 'tma.cuh', 'mma.cuh', 'attend_common.cuh', 'common.cuh', 'status.cuh')
+FFD_ATTEND_SOURCES_SHA256 = "94b5f29e04f9daf321c053b1a19e97eb1f4f8ee05885e72b0e034c235c4d520c"
+
+
+def sources_sha256(files) -> str:
+    import hashlib
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "sparse_long_context_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ffd_attend_traffic(s: W.Spec):
+    """Per-launch DRAM bytes of the ffd attend for the captured workload, else None."""
+    if (s.name, s.batch, s.ctx_len[0]) != ("ffd", 2, 262144):
+        return None
+    return round(FFD_ATTEND_TRAFFIC) if sources_sha256(FFD_ATTEND_SOURCES) == FFD_ATTEND_SOURCES_SHA256 else None
 
 
 def step_traffic(s: W.Spec):
     """Per-launch DRAM bytes of the step kernel for the captured workload, else None."""
-    import hashlib
     if (s.name, s.batch, s.ctx_len[0]) != ("qwen1p5b", 32, 65536):
         return None
-    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "sparse_long_context_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in STEP_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
-    return round(STEP_TRAFFIC_B32) if h.hexdigest() == STEP_SOURCES_SHA256 else None
+    return round(STEP_TRAFFIC_B32) if sources_sha256(STEP_SOURCES) == STEP_SOURCES_SHA256 else None
 
 
 # ------------------------------------------------------------------ helpers
@@ -832,9 +852,10 @@ def run_delta(args, s: W.Spec):
                       "attend_exact": round(nb["attend_exact"] / (kus["attend_exact"] * 1e-6) / 1e9, 1),
                       "attend_refined": round(nb["attend_refined"] / (kus["attend_refined"] * 1e-6) / 1e9, 1)},
         "replay_us": rep_us,
-        "roofline": roofline_block("attend_balanced_kernel (stream-K attend, bf16 keys, combine fused)"
-                                   if dom == "attend_exact" else "delta_scan_mma_kernel + delta_compact_kernel",
-                                   achieved, peak, peak_kind, None),
+        "roofline": roofline_block("attend_stream_tma_kernel (stream-K attend, bf16 keys, tensor-map fed, "
+                                   "combine fused)" if dom == "attend_exact"
+                                   else "delta_scan_mma_kernel + delta_compact_kernel",
+                                   achieved, peak, peak_kind, ffd_attend_traffic(s) if dom == "attend_exact" else None),
         "step_roofline": {"achieved": round(value, 1), "peak": peak, "frac": round(value / peak, 4)},
         "gpu_launches": 3 * args.steps,  # scan, compaction, attend; per timed window of `steps` steps
         "paths": {"at_capture": paths_capture},
