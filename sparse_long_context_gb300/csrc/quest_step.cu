@@ -682,10 +682,13 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     const int nloc = max(0, min(sa.chunk, NP - p0));
     const int n1 = (nloc + 15) >> 4;
     const int first_local = a.P > 0 && sa.n_local > 0 ? (max(N - sa.n_local, 0) >> a.pshift) : NP;
+    // Every thread completes the cluster arrive made at entry while the first
+    // copies are in flight (a wait on a phase long complete still takes a
+    // while), before its first access to another CTA's shared memory.
     if (warp == W) {
-      if (lane == 0) {
-        int issued = 0;
-        for (int i = 0; i < n1; ++i) {
+      int issued = 0;
+      auto issue = [&](int i0, int i1) {
+        for (int i = i0; i < i1; ++i) {
           const uint32_t q = seq + i;
           const int st = q % NST;
           if (!producer_wait(q)) {
@@ -699,6 +702,12 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
           tma_load_3d(dst + L::GROUP, &tmin, 0, y, 0, &full[st]);
           issued = i + 1;
         }
+      };
+      if (lane == 0) issue(0, min(NST, n1));  // the ring's first round needs no free stage
+      __syncwarp();
+      asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+      if (lane == 0) {
+        if (ok) issue(NST, n1);
         // the copies have landed before the ring turns into scratch space
         for (int i = max(0, issued - NST); i < issued; ++i) {
           const uint32_t q = seq + i;
@@ -706,6 +715,7 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
         }
       }
     } else {
+      asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
       const int r = lane >> 2, m = lane & 3;
       // q split by sign as the B operand: b0 = q[head r][16ks + 2m, +1], b1 = q[r][16ks + 8 + 2m, +1]
       uint32_t bp[KS][2], bn[KS][2];
@@ -745,7 +755,6 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     __syncthreads();  // keys complete; the ring is free
 
     // ------------------------------------------------------------ 2. top-k
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // completes the arrive made at entry
     bool use_all = sa.topk_mode != 0;
     if (!use_all) {
       // Candidates: each CTA sends its forced keys and about its cand_m
