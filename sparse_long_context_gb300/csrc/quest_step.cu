@@ -767,6 +767,13 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       const int cap = sa.cand_cap;
       uint32_t* scratch = reinterpret_cast<uint32_t*>(ring);
       uint2* cand = reinterpret_cast<uint2*>(ring + kTopkScratchBytes);  // [C][cap] (key, page) pairs
+      // empty candidate slots read as key 0; once they are zeroed (and the
+      // ring is free) the CTA arrives on the cluster barrier, and the other
+      // CTAs write into them only after its wait, which comes after this
+      // CTA's own threshold and compaction
+      for (int i = threadIdx.x; i < C * cap / 2; i += NT) reinterpret_cast<uint4*>(cand)[i] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+      asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
       uint32_t kk[kLocalKeys];
       load_keys_reg<NT, kLocalKeys>(keys, nloc, kk);
       const uint32_t tau = top_bin_threshold<NT, kLocalKeys>(kk, sa.cand_m, scratch, scan_tmp);
@@ -774,8 +781,6 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       int cnt = 0;
 #pragma unroll
       for (int j = 0; j < kLocalKeys; ++j) cnt += kk[j] >= tau;  // slots past nloc hold 0 < tau
-      // empty candidate slots read as key 0 (the scan's barrier orders this before the compaction)
-      for (int i = threadIdx.x; i < C * cap / 2; i += NT) reinterpret_cast<uint4*>(cand)[i] = make_uint4(0u, 0u, 0u, 0u);
       int total;
       const int off = block_scan_excl<NT>(cnt, scan_tmp, total);
       const bool ovf = total > cap;
@@ -791,7 +796,8 @@ quest_step_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
           o += in;
         }
       }
-      cl.sync();  // every ring is free; the compacted block is complete
+      __syncthreads();  // the compacted block is complete
+      asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // every ring is free and zeroed
       if (threadIdx.x < C) {
         cl.map_shared_rank(s_cand_n, (int)threadIdx.x)[split] = ovf ? -1 : total;
         cl.map_shared_rank(s_cand_tau, (int)threadIdx.x)[split] = tau;
