@@ -44,10 +44,10 @@ METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak) for select+att
 # written; traffic grows with the rows, so x4 for batch 32).  Reported only
 # for that workload and only while the kernel's sources hash to the ones
 # captured; otherwise null.
-STEP_TRAFFIC_B32 = 4 * (50.470656e6 + 0.150784e6)
+STEP_TRAFFIC_B32 = 4 * (50.470656e6 + 0.113664e6)
 STEP_SOURCES = ("quest_step.cu", "attend_tma.cuh", "tma.cuh", "mma.cuh", "attend_common.cuh", "common.cuh",
                 "status.cuh")
-STEP_SOURCES_SHA256 = "4fbb8ce9d266b32bd44b705feb35c795fa78438094d50997d94ce6d1de5cf5f0"
+STEP_SOURCES_SHA256 = "b5c18b5bb3639e18f0c775ab1a5ebab5a4e7b7f423ec1d1392393fb866f629e3"
 
 
 # DRAM bytes per launch of the top-delta step's bf16-key attend
