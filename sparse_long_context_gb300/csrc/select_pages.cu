@@ -528,7 +528,7 @@ __device__ __forceinline__ void emit_candidates(const SelectArgs& a, int row, in
   int b = kCandBins;
   if (cut) {
     // 2. histogram of the scores; bin b is where the count from the top reaches want
-#pragma unroll 1
+#pragma unroll 4
     for (int i = tid; i < nloc; i += NT) {
       const uint32_t kk = keys[i];
       if (kk != kForcedKey) atomicAdd(&sh.hist[bin_of(kk)], 1u);
@@ -558,7 +558,7 @@ __device__ __forceinline__ void emit_candidates(const SelectArgs& a, int row, in
   const int i0 = min(tid * per, nloc), i1 = min(i0 + per, nloc);
   int mine = 0;
   uint32_t mn = 0xffffffffu;
-#pragma unroll 1
+#pragma unroll 4
   for (int i = i0; i < i1; ++i) {
     const uint32_t kk = keys[i];
     if (!cut || kk == kForcedKey || bin_of(kk) <= b) {
@@ -577,7 +577,7 @@ __device__ __forceinline__ void emit_candidates(const SelectArgs& a, int row, in
   if (!cut) tau = 0;
   uint32_t* ck = a.cand_key + (size_t)row * a.npcap + p0;
   int32_t* cp = a.cand_page + (size_t)row * a.npcap + p0;
-#pragma unroll 1
+#pragma unroll 4
   for (int i = i0; i < i1; ++i) {
     const uint32_t kk = keys[i];
     if (kk >= tau) {
