@@ -9,9 +9,10 @@ inputs (no real KV cache exists here).
 value = algorithmic bytes of the step (page min/max metadata of every page
 + K and V of the selected tokens) / device time per step, in GB/s.
 
-The timed region replays CUDA graphs of up to 8 consecutive steps each (a
-decode engine captures a whole iteration in one graph; consecutive step
-kernels overlap launch and tail through programmatic dependent launch).
+The timed region replays CUDA graphs of up to 32 consecutive steps each (a
+decode engine captures a whole iteration over the model's layers in one
+graph; consecutive step kernels overlap launch and tail through
+programmatic dependent launch).
 NSETS copies of the KV cache and metadata rotate, step i using set
 i % NSETS, so that consecutive steps never find their bytes in L2
 (NSETS * step bytes >= 4 * L2).  `replay_us` times graphs of one step.  `python bench.py --impl
@@ -338,6 +339,13 @@ def make_sets(dw, nsets: int):
     return sets
 
 
+def steps_per_graph(steps: int) -> int:
+    """Consecutive steps captured in one timed graph: the largest divisor of
+    `steps` up to 32 (a decode engine replays one graph per iteration over a
+    model's layers, each layer one step)."""
+    return next(r for r in range(min(32, steps), 0, -1) if steps % r == 0)
+
+
 def timed_windows(stream, graphs, steps: int, spg: int, world: int, min_total_s: float = 0.2,
                   max_windows: int = 200):
     """Time windows of exactly `steps` steps each (graph i replays steps
@@ -484,7 +492,7 @@ def run_ours(args, s: W.Spec):
     one = steps_obj[0].one_launch and ops.quest_step_splits(dw.desc, s.k_pages) > 0
     S = steps_obj[0].S
     stream = torch.cuda.Stream()
-    spg = next(r for r in (8, 4, 2, 1) if args.steps % r == 0)
+    spg = steps_per_graph(args.steps)
 
     def run(st, bufs):
         K, V, kmin, kmax = bufs
@@ -758,7 +766,7 @@ def run_delta(args, s: W.Spec):
     exact = [ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits) for _ in sets]
     refined = [ops.DeltaDecode(dw.desc, s.block, s.delta, args.splits, refined=True) for _ in sets]
     stream = torch.cuda.Stream()
-    spg = next(r for r in (8, 4, 2, 1) if args.steps % r == 0)
+    spg = steps_per_graph(args.steps)
 
     def run(st, bufs):
         K, V, c, sc, r = bufs
