@@ -719,9 +719,10 @@ topk_wide_kernel(const SelectArgs a) {
       const int o = soff[c], cnt = soff[c + 1] - o;
       const uint32_t* ck = a.cand_key + (size_t)row * a.npcap + (size_t)c * a.chunk;
       const int32_t* cp = a.cand_page + (size_t)row * a.npcap + (size_t)c * a.chunk;
-      for (int j = lane; j < cnt; j += 32) {
-        skey[o + j] = ck[j];
-        spage[o + j] = cp[j];
+#pragma unroll 4
+      for (int j = lane; j < cnt; j += 32) {  // unrolled: the loads of four rounds in flight together
+        skey[o + j] = __ldcg(ck + j);
+        spage[o + j] = __ldcg(cp + j);
       }
     }
     __syncthreads();
