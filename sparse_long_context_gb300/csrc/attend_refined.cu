@@ -877,6 +877,7 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
   __shared__ uint64_t full[W][S];
   __shared__ float sM[W][8], sL[W][8], sF[W][8];
   __shared__ float sHm[8], sHl[8];
+  __shared__ __align__(16) bf16 s_q[8 * 128];  // the segment's query heads
   const AttendArgs& a = ra.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, m = lane & 3;
@@ -910,6 +911,11 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
     const int nent = (int)(seg_end - e);
     const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + (int)(e - s_pref[row]);
     stage_page_list(sh.s_pg, kRefStaged, plist, 0, nent, a.Cap >> a.pshift, threadIdx.x, NT);
+    {
+      const uint4* qg = reinterpret_cast<const uint4*>(static_cast<const bf16*>(a.q) +
+                                                       ((size_t)b * a.Hq + (size_t)h * G) * D);
+      for (int i = threadIdx.x; i < G * D / 8; i += NT) reinterpret_cast<uint4*>(s_q)[i] = __ldg(qg + i);
+    }
     __syncthreads();
     const bool failed = sh.s_fail != 0;
     const int nblk = nent > warp ? (nent - warp + W - 1) / W : 0;  // this warp's blocks: warp + W j
@@ -949,9 +955,9 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
     float m_run = kNegInf, l_run = 0.f;
 #pragma unroll
     for (int t = 0; t < KS; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-    // Q is read where it is used (L1-resident): per block for the refined
+    // Q from shared memory where it is used: per block for the refined
     // weights, per group for the bf16 groups of the newest block
-    const bf16* qp = static_cast<const bf16*>(a.q) + ((size_t)b * a.Hq + (size_t)h * G + r) * D;
+    const bf16* qp = s_q + r * D;
     // the scales of the warp's next block (lane's channel quarter), in flight
     const bf16* srow = ra.scales + (size_t)row * (a.Cap >> a.pshift) * D + m * (D / 4);
     uint4 sv[NS];
@@ -975,7 +981,7 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
 #pragma unroll
           for (int s = 0; s < NS; ++s) {
             const uint4 cq =
-                r < G ? __ldg(reinterpret_cast<const uint4*>(qp + m * (D / 4) + 8 * s)) : make_uint4(0, 0, 0, 0);
+                r < G ? *reinterpret_cast<const uint4*>(qp + m * (D / 4) + 8 * s) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
               const uint32_t sw = (&sv[s].x)[p], qw = (&cq.x)[p];
@@ -1005,8 +1011,8 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
           uint32_t qa[KS][2];  // tma_group's fragments: a0 = Q[head r][16ks + 2m, +1], a2 = Q[r][16ks + 8 + 2m, +1]
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
-            qa[ks][0] = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * m)) : 0u;
-            qa[ks][1] = r < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * m)) : 0u;
+            qa[ks][0] = r < G ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * m) : 0u;
+            qa[ks][1] = r < G ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8 + 2 * m) : 0u;
           }
           tma_group<D>(stage, lim, qa, o, m_run, l_run, a.qscale, lane);
         }
