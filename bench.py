@@ -55,9 +55,9 @@ STEP_SOURCES_SHA256 = "b5c18b5bb3639e18f0c775ab1a5ebab5a4e7b7f423ec1d1392393fb86
 # (attend_stream_tma_kernel) on the ffd workload, from the committed capture
 # (profiles/topdelta_ffd_256k.md, read + written; the kept set is the seeded
 # workload's), under the same source-hash rule.
-FFD_ATTEND_TRAFFIC = 490.945280e6 + 3.271424e6
+FFD_ATTEND_TRAFFIC = 490.943488e6 + 3.329536e6
 FFD_ATTEND_SOURCES = ('attend_refined.cu', 'attend_tma.cuh', 'tma.cuh', 'mma.cuh', 'attend_common.cuh', 'common.cuh', 'status.cuh')
-FFD_ATTEND_SOURCES_SHA256 = "94b5f29e04f9daf321c053b1a19e97eb1f4f8ee05885e72b0e034c235c4d520c"
+FFD_ATTEND_SOURCES_SHA256 = "77dd9b41edd554570d5e144245731a0f80bf03910f0e190c3f690382bd18c055"
 
 
 def sources_sha256(files) -> str:
