@@ -57,7 +57,7 @@ STEP_SOURCES_SHA256 = "b5c18b5bb3639e18f0c775ab1a5ebab5a4e7b7f423ec1d1392393fb86
 # workload's), under the same source-hash rule.
 FFD_ATTEND_TRAFFIC = 490.943488e6 + 3.329536e6
 FFD_ATTEND_SOURCES = ('attend_refined.cu', 'attend_tma.cuh', 'tma.cuh', 'mma.cuh', 'attend_common.cuh', 'common.cuh', 'status.cuh')
-FFD_ATTEND_SOURCES_SHA256 = "77dd9b41edd554570d5e144245731a0f80bf03910f0e190c3f690382bd18c055"
+FFD_ATTEND_SOURCES_SHA256 = "abfc97ac9b5f75fcd21c567e5a3dd016e3b4d089eb3b7fe77233bd41225de9ad"
 
 
 def sources_sha256(files) -> str:

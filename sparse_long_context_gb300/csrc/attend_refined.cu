@@ -10,14 +10,14 @@
 // in one head, most of the context in another), so a fixed split count per
 // row leaves the kernel as slow as its longest row.  Here the rows' lists,
 // concatenated, are cut into one equal range of entries per CTA (one 8-warp
-// CTA per SM, stream-K style; attend_balanced_kernel).  Without codes the
-// bf16 keys are attended everywhere: by attend_stream_tma_kernel (the same
-// partition, every warp streaming its groups through its own ring of
-// tensor-map copies) where the shape allows tensor maps, else by the same
-// register-fed kernel.
+// CTA per SM, stream-K style).  Three kernels share that partition: where
+// the shape allows tensor maps, attend_stream_tma_kernel (bf16 keys) and
+// attend_refined_tma_kernel (refined keys, D = 128), in which every warp
+// streams its groups through its own ring of tensor-map copies; otherwise
+// the register-fed attend_balanced_kernel (either kind of key).
 //
-// Within an item a warp walks 16-token groups with two groups in flight in
-// registers (the shape of the register-fed attend).  Lane (r, m) owns the
+// In attend_balanced_kernel a warp walks 16-token groups with two groups in
+// flight in registers (the shape of the register-fed attend).  Lane (r, m) owns the
 // channels [m D/4, (m+1) D/4) of the score product and loads, for tokens r
 // and r + 8 of a group, either D/16 bytes of codes and D/4 bytes of
 // residuals (a refined group) or D/2 bytes of bf16 key (a group of the

@@ -93,10 +93,14 @@ def test_bad_page_ids_are_skipped_and_reported(path):
         PT.assert_close(s, outs["bad"][0][b, h * G:(h + 1) * G], ref, f"row {r}")
 
 
-def test_bad_block_ids_in_the_stream_k_attend_and_recall_are_reported():
+@pytest.mark.parametrize("refined", [False, True])
+def test_bad_block_ids_in_the_stream_k_attend_and_recall_are_reported(refined):
     s = W.spec("ffd", batch=1, ctx_len=64 * 40 + 9, capacity=64 * 48)
     host = W.generate(s)
     dw = PT.upload(s, host)
+    codes = scales = res = None
+    if refined:  # the refined (2-bit + 8-bit) keys on the tensor-map fed kernel
+        codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block)
     npool = s.capacity // s.block
     lists = np.full((s.rows, npool), -1, dtype=np.int32)
     count = np.zeros(s.rows, dtype=np.int32)
@@ -111,18 +115,18 @@ def test_bad_block_ids_in_the_stream_k_attend_and_recall_are_reported():
     clean[(clean < -1) | (clean >= npool)] = -1
     cnt = torch.from_numpy(count).cuda()
     assert _check_status() == L.SLS_OK
-    res = {}
+    outs = {}
     for name, lst in (("bad", bad), ("clean", clean)):
         idx = torch.from_numpy(lst).cuda()
-        out, _ = ops.refined_decode_attend_combine(dw.desc, dw.q, dw.K, dw.V, None, None, None, idx, cnt, dw.ctx)
-        res[name] = out.float().cpu().numpy()
+        out, _ = ops.refined_decode_attend_combine(dw.desc, dw.q, dw.K, dw.V, codes, scales, res, idx, cnt, dw.ctx)
+        outs[name] = out.float().cpu().numpy()
         assert _check_status() == (L.SLS_EDEVICE if name == "bad" else L.SLS_OK), name
         rec = ops.selection_recall(dw.desc, dw.q, dw.K, idx, dw.ctx, count=cnt)
         torch.cuda.synchronize()
         assert _check_status() == (L.SLS_EDEVICE if name == "bad" else L.SLS_OK), ("recall", name)
-        res[name + "_recall"] = rec.cpu().numpy()
-    np.testing.assert_allclose(res["bad"], res["clean"], rtol=1e-5, atol=1e-6)
-    np.testing.assert_allclose(res["bad_recall"], res["clean_recall"], rtol=1e-6)
+        outs[name + "_recall"] = rec.cpu().numpy()
+    np.testing.assert_allclose(outs["bad"], outs["clean"], rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(outs["bad_recall"], outs["clean_recall"], rtol=1e-6)
 
 
 @pytest.mark.parametrize("entry", ["attend_combine", "quest_step"])
