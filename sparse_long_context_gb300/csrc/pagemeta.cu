@@ -88,6 +88,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256)
 decode_append_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new, T* k, T* v, T* kmin, T* kmax,
                      int32_t* ctx_len, int32_t* pos_out, int Hkv, int Cap, int P, int pshift) {
+  // after the previous step (which reads ctx_len and the cache); the next
+  // kernel of the loop may then start its launch, and waits for this one
+  pdl_wait_then_release();
   const int b = blockIdx.x;
   const int t = ctx_len[b];
   __syncthreads();
@@ -186,6 +189,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(D)
 thumb_update_kernel(const T* __restrict__ k, const int32_t* __restrict__ pos, uint8_t* codes,
                     T* scales, int8_t* res, int Hkv, int Cap, int block, int nblk_cap) {
+  pdl_wait_then_release();
   const int row = blockIdx.x;
   const int t = pos[row / Hkv];
   if (t < 0 || t >= Cap || (t + 1) % block != 0) return;
@@ -236,9 +240,11 @@ cudaError_t launch_pagemeta_update(const Shape& s, const void* k, const int32_t*
 template <typename T, int D>
 static cudaError_t dec_append(const Shape& s, const void* k_new, const void* v_new, void* k, void* v, void* kmin,
                               void* kmax, int32_t* ctx_len, int32_t* pos_out, cudaStream_t st) {
-  decode_append_kernel<T, D><<<s.B, 256, 0, st>>>(
-      static_cast<const T*>(k_new), static_cast<const T*>(v_new), static_cast<T*>(k), static_cast<T*>(v),
-      static_cast<T*>(kmin), static_cast<T*>(kmax), ctx_len, pos_out, s.Hkv, s.Cap, s.P, s.pshift);
+  cudaError_t e = launch_pdl(decode_append_kernel<T, D>, dim3(s.B), dim3(256), 0, st,
+                             static_cast<const T*>(k_new), static_cast<const T*>(v_new), static_cast<T*>(k),
+                             static_cast<T*>(v), static_cast<T*>(kmin), static_cast<T*>(kmax), ctx_len, pos_out,
+                             s.Hkv, s.Cap, s.P, s.pshift);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -273,9 +279,10 @@ cudaError_t launch_thumb_build(const Shape& s, const void* k, const int32_t* ctx
 template <typename T, int D>
 static cudaError_t th_update(const Shape& s, const void* k, const int32_t* pos, int block,
                              uint8_t* codes, void* scales, int8_t* res, cudaStream_t st) {
-  thumb_update_kernel<T, D><<<s.B * s.Hkv, D, 0, st>>>(static_cast<const T*>(k), pos, codes,
-                                                        static_cast<T*>(scales), res, s.Hkv, s.Cap, block,
-                                                        s.Cap / block);
+  cudaError_t e = launch_pdl(thumb_update_kernel<T, D>, dim3(s.B * s.Hkv), dim3(D), 0, st,
+                             static_cast<const T*>(k), pos, codes, static_cast<T*>(scales), res, s.Hkv, s.Cap,
+                             block, s.Cap / block);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -530,8 +530,13 @@ def test_full_size_sampled_rows(name):
     host = W.generate(s)
     dw = PT.upload(s, host)
     sel, cnt, out, lse = PT.run_step(dw)   # default launch configuration, as benchmarked
+    # the first and last rows, every KV head of one sequence (the rows that share a q), and
+    # seeded others: 8 rows (or all of them)
     rng = np.random.default_rng(7)
-    rows = sorted(set([0, s.rows - 1] + rng.choice(s.rows, size=2, replace=False).tolist()))
+    b_mid = s.batch // 2
+    picked = {0, s.rows - 1} | {b_mid * s.num_kv_heads + h for h in range(s.num_kv_heads)}
+    others = [r for r in rng.permutation(s.rows).tolist() if r not in picked]
+    rows = sorted(picked | set(others[:max(0, 8 - len(picked))]))
     G = s.group
     ties = 0
     for r in rows:
