@@ -284,6 +284,7 @@ struct RefSmem {
   int s_tmp[kRefMaxWarps];
   int s_fail;
   int s_slot[kRefMaxContrib];
+  int s_lo[kRefMaxContrib + 1];  // first entry of every CTA's range, and the total
   int s_ncontrib;
   int s_last;
   float s_w[8][64], s_m[8], s_inv[8];
@@ -315,12 +316,17 @@ __device__ __forceinline__ int ref_scan(int v, int* tmp, int& total) {
 
 __device__ __forceinline__ long long range_lo(long long T, int c, int grid) { return T * c / grid; }
 
-// The CTA whose entry range [T c / grid, T (c+1) / grid) holds entry x < T.
-__device__ __forceinline__ int cta_of(long long x, long long T, int grid) {
-  int c = (int)min((long long)grid - 1, x * grid / T);
-  while (c + 1 < grid && range_lo(T, c + 1, grid) <= x) ++c;
-  while (c > 0 && range_lo(T, c, grid) > x) --c;
-  return c;
+// The CTA whose entry range [s_lo[c], s_lo[c + 1]) holds entry x < T: the
+// last c with s_lo[c] <= x (CTAs with empty ranges share their s_lo with the
+// next CTA, so the last of them is the one whose range is not empty).
+__device__ __forceinline__ int cta_of(const int* s_lo, int x, int grid) {
+  int l = 0, u = grid - 1;
+  while (l < u) {
+    const int mid = (l + u + 1) >> 1;
+    if (s_lo[mid] <= x) l = mid;
+    else u = mid - 1;
+  }
+  return l;
 }
 
 // Writes the finished output of one head: accumulator sum `av` and
@@ -364,6 +370,9 @@ __device__ __forceinline__ bool stream_k_begin(const AttendArgs& a, int rows, Re
     }
   }
   if (threadIdx.x == 0) s_pref[rows] = T;
+  // every CTA's range, once: the contributors of a shared row are read from
+  // here (a 64-bit division per CTA, in parallel)
+  for (int k = threadIdx.x; k <= grid; k += NT) sh.s_lo[k] = (int)range_lo(T, k, grid);
   __syncthreads();
 
   // rows with an empty list: output 0, lse -inf (or the sink alone)
@@ -374,8 +383,8 @@ __device__ __forceinline__ bool stream_k_begin(const AttendArgs& a, int rows, Re
       finish_head(a, (size_t)b * a.Hq + (size_t)h * G + i / D, h, i / D, kNegInf, 0.f, 0.f, i % D, D);
   }
   if (T == 0) return false;
-  lo = range_lo(T, c, grid);
-  hi = range_lo(T, c + 1, grid);
+  lo = sh.s_lo[c];
+  hi = sh.s_lo[c + 1];
   if (lo >= hi) return false;
   // the row holding entry lo: the last row whose first entry is <= lo
   {
@@ -432,11 +441,11 @@ __device__ __forceinline__ void finish_segment(const RefinedArgs& ra, RefSmem& s
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-      const int cf = cta_of(s_pref[row], T, grid), cl = cta_of((long long)s_pref[row + 1] - 1, T, grid);
+      const int cf = cta_of(sh.s_lo, s_pref[row], grid), cl = cta_of(sh.s_lo, s_pref[row + 1] - 1, grid);
       int n = 0;
       for (int k = cf; k <= cl && n < kRefMaxContrib; ++k) {
-        const long long klo = range_lo(T, k, grid);
-        if (klo < range_lo(T, k + 1, grid)) sh.s_slot[n++] = klo >= s_pref[row] ? 2 * k : 2 * k + 1;
+        const int klo = sh.s_lo[k];
+        if (klo < sh.s_lo[k + 1]) sh.s_slot[n++] = klo >= s_pref[row] ? 2 * k : 2 * k + 1;
       }
       sh.s_ncontrib = n;
       sh.s_last = atomicAdd(a.tickets + row, 1) == n - 1;
@@ -447,17 +456,31 @@ __device__ __forceinline__ void finish_segment(const RefinedArgs& ra, RefSmem& s
       __threadfence();
       auto slot_of = [&](int j) -> size_t { return (size_t)sh.s_slot[j]; };
       for (int g = warp; g < G; g += NW) {
-        float M = kNegInf;
-        for (int j = lane; j < ncontrib; j += 32) M = fmaxf(M, __ldcg(ra.pm + slot_of(j) * G + g));
+        // the first 64 contributors' max and sum in registers, loaded at once
+        float pm2[2], pl2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = lane + 32 * u;
+          pm2[u] = j < ncontrib ? __ldcg(ra.pm + slot_of(j) * G + g) : kNegInf;
+          pl2[u] = j < ncontrib ? __ldcg(ra.pl + slot_of(j) * G + g) : 0.f;
+        }
+        float M = fmaxf(pm2[0], pm2[1]);
+        for (int j = lane + 64; j < ncontrib; j += 32) M = fmaxf(M, __ldcg(ra.pm + slot_of(j) * G + g));
         M = warp_max(M);
         const float sk = a.sink ? a.sink[h * G + g] : kNegInf;
         M = fmaxf(M, sk);
         float Ls = 0.f;
-        for (int j = lane; j < ncontrib; j += 32) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = lane + 32 * u;
+          const float w = (pm2[u] == kNegInf || M == kNegInf) ? 0.f : expf(pm2[u] - M);
+          Ls += pl2[u] * w;
+          if (j < ncontrib) sh.s_w[g][j] = w;
+        }
+        for (int j = lane + 64; j < ncontrib; j += 32) {
           const float ms = __ldcg(ra.pm + slot_of(j) * G + g);
           const float w = (ms == kNegInf || M == kNegInf) ? 0.f : expf(ms - M);
           Ls += __ldcg(ra.pl + slot_of(j) * G + g) * w;
-          if (j < 64) sh.s_w[g][j] = w;
         }
         Ls = warp_sum(Ls);
         if (a.sink && M != kNegInf) Ls += expf(sk - M);
