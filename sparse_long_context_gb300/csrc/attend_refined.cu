@@ -672,11 +672,13 @@ struct StreamLayout {
 
 // First cache position of group gi of the segment and its token count
 // inside the context (<= 0: padded entry, bad page or past the context).
+// Page ids come from the staged copy s_pg, or from the list in global memory
+// when s_pg is null (before the staging barrier) or past the staged entries.
 __device__ __forceinline__ int stream_group_base(const AttendArgs& a, int N, const int* s_pg, const int32_t* plist,
                                                  int gi, int& lim) {
   const int j0 = gi << 4;
   const int e = j0 >> a.pshift;
-  const int pg = e < kRefStaged ? s_pg[e] : __ldg(plist + e);
+  const int pg = s_pg && e < kRefStaged ? s_pg[e] : __ldg(plist + e);
   lim = 0;
   if ((unsigned)pg >= (unsigned)(a.Cap >> a.pshift)) return 0;
   const int base = (pg << a.pshift) + (j0 & (a.P - 1));
@@ -730,18 +732,18 @@ attend_stream_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     const int N = clamp_len(a.ctx_len[b], a.Cap);
     const int nent = (int)(seg_end - e);
     const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + (int)(e - s_pref[row]);
-    stage_page_list(sh.s_pg, kRefStaged, plist, 0, nent, a.Cap >> a.pshift, threadIdx.x, NT);
-    __syncthreads();
-    const bool failed = sh.s_fail != 0;  // an earlier segment gave up: no more copies
+    // an earlier segment gave up: no more copies (set before that segment's closing barrier)
+    const bool failed = sh.s_fail != 0;
     const int ngroups = (nent << a.pshift) >> 4;
     const int nk = ngroups > warp ? (ngroups - warp + W - 1) / W : 0;  // this warp's groups: warp + W k
+    const int* pg_src = nullptr;  // page ids from global memory until the list is staged
 
     // lane 0: the copy of the warp's k-th group of the segment into its stage
     auto issue = [&](int k) {
       const uint32_t q = wseq + k;
       const int st = q % S;
       int lim;
-      const int base = stream_group_base(a, N, sh.s_pg, plist, warp + W * k, lim);
+      const int base = stream_group_base(a, N, pg_src, plist, warp + W * k, lim);
       if (plant && q == 0) {
         mbar_arrive_expect_tx(&full[warp][st], 16);  // no copy is issued: this phase never completes
       } else if (lim > 0) {
@@ -756,10 +758,16 @@ attend_stream_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     };
     // S - 1 groups in flight ahead of the one being scored: the stage of
     // group k + S - 1 is the one group k - 1 left, refilled before group k is
-    // scored
-    if (lane == 0 && !failed)
+    // scored.  The first copies leave before the list is staged (the ring is
+    // free since the previous segment's closing barrier).
+    if (lane == 0 && !failed) {
+      fence_proxy_async_smem();  // the merge's reads of the ring before the copies write it
       for (int k = 0; k < min(S - 1, nk); ++k) issue(k);
+    }
     __syncwarp();
+    stage_page_list(sh.s_pg, kRefStaged, plist, 0, nent, a.Cap >> a.pshift, threadIdx.x, NT);
+    __syncthreads();
+    pg_src = sh.s_pg;
 
     float o[KS][4];
     float m_run = kNegInf, l_run = 0.f;
@@ -933,16 +941,11 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
     const int N = clamp_len(a.ctx_len[b], a.Cap);
     const int nent = (int)(seg_end - e);
     const int32_t* plist = a.page_idx + (size_t)row * a.idx_stride + (int)(e - s_pref[row]);
-    stage_page_list(sh.s_pg, kRefStaged, plist, 0, nent, a.Cap >> a.pshift, threadIdx.x, NT);
-    {
-      const uint4* qg = reinterpret_cast<const uint4*>(static_cast<const bf16*>(a.q) +
-                                                       ((size_t)b * a.Hq + (size_t)h * G) * D);
-      for (int i = threadIdx.x; i < G * D / 8; i += NT) reinterpret_cast<uint4*>(s_q)[i] = __ldg(qg + i);
-    }
-    __syncthreads();
+    // an earlier segment gave up: no more copies (set before that segment's closing barrier)
     const bool failed = sh.s_fail != 0;
     const int nblk = nent > warp ? (nent - warp + W - 1) / W : 0;  // this warp's blocks: warp + W j
     const int nk = nblk * gpb;
+    const int* pg_src = nullptr;  // page ids from global memory until the list is staged
     auto page_of = [&](int eb) { return eb < kRefStaged ? sh.s_pg[eb] : __ldg(plist + eb); };
     // group k of this warp: group k % gpb of its block k / gpb
     auto group_of = [&](int k) { return (warp + W * (k / gpb)) * gpb + (k % gpb); };
@@ -952,7 +955,7 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
       const uint32_t q = wseq + k;
       const int st = q % S;
       int lim;
-      const int base = stream_group_base(a, N, sh.s_pg, plist, group_of(k), lim);
+      const int base = stream_group_base(a, N, pg_src, plist, group_of(k), lim);
       unsigned char* dst = wring + st * L::STAGE;
       const int y = row * a.Cap + base;
       if (plant && q == 0) {
@@ -970,9 +973,21 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
         mbar_arrive(&full[warp][st]);
       }
     };
-    if (lane == 0 && !failed)
+    // the first copies leave before the list and q are staged (the ring is
+    // free since the previous segment's closing barrier)
+    if (lane == 0 && !failed) {
+      fence_proxy_async_smem();  // the merge's reads of the ring before the copies write it
       for (int k = 0; k < min(S - 1, nk); ++k) issue(k);
+    }
     __syncwarp();
+    stage_page_list(sh.s_pg, kRefStaged, plist, 0, nent, a.Cap >> a.pshift, threadIdx.x, NT);
+    {
+      const uint4* qg = reinterpret_cast<const uint4*>(static_cast<const bf16*>(a.q) +
+                                                       ((size_t)b * a.Hq + (size_t)h * G) * D);
+      for (int i = threadIdx.x; i < G * D / 8; i += NT) reinterpret_cast<uint4*>(s_q)[i] = __ldg(qg + i);
+    }
+    __syncthreads();
+    pg_src = sh.s_pg;
 
     float o[KS][4];
     float m_run = kNegInf, l_run = 0.f;
