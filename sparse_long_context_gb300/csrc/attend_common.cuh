@@ -80,7 +80,7 @@ __device__ __forceinline__ int token_position(const AttendArgs& a, int pg, int j
 // writes the merged output.  Nothing waits on another CTA.  The weights
 // exp(m_s - M) of all splits are formed in parallel (a lane per split), then
 // the accumulators are gathered with independent 16-byte loads.
-constexpr int kCombineMaxS = 64;  // splits whose weights are kept in shared memory
+constexpr int kCombineMaxS = 64;  // splits whose weights are kept in shared memory (two per lane)
 
 template <typename T, int D, int NT>
 __device__ __forceinline__ void combine_row_if_last(const AttendArgs& a, int row, int nseg) {
@@ -101,17 +101,31 @@ __device__ __forceinline__ void combine_row_if_last(const AttendArgs& a, int row
   for (int g = warp; g < a.G; g += NW) {
     const float* mp = a.m_part + (hq0 + g) * a.S;
     const float* lp = a.l_part + (hq0 + g) * a.S;
-    float M = kNegInf;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldcg(mp + s));
+    // the first 64 splits' max and sum in registers, loaded at once
+    float m2[2], l2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int s = lane + 32 * u;
+      m2[u] = s < S ? __ldcg(mp + s) : kNegInf;
+      l2[u] = s < S ? __ldcg(lp + s) : 0.f;
+    }
+    float M = fmaxf(m2[0], m2[1]);
+    for (int s = lane + 64; s < S; s += 32) M = fmaxf(M, __ldcg(mp + s));
     M = warp_max(M);
     const float sk = a.sink ? a.sink[h * a.G + g] : kNegInf;
     M = fmaxf(M, sk);
     float Ls = 0.f;
-    for (int s = lane; s < S; s += 32) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int s = lane + 32 * u;
+      const float w = (m2[u] == kNegInf || M == kNegInf) ? 0.f : expf(m2[u] - M);
+      Ls += l2[u] * w;
+      if (s < S) s_w[g][s] = w;  // kCombineMaxS = 64
+    }
+    for (int s = lane + 64; s < S; s += 32) {
       const float ms = __ldcg(mp + s);
       const float w = (ms == kNegInf || M == kNegInf) ? 0.f : expf(ms - M);
       Ls += __ldcg(lp + s) * w;
-      if (s < kCombineMaxS) s_w[g][s] = w;
     }
     Ls = warp_sum(Ls);
     if (a.sink && M != kNegInf) Ls += expf(sk - M);
