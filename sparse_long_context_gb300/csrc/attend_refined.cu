@@ -28,7 +28,10 @@
 //   q s                      is exact in fp32 (bf16 x bf16) and splits into
 //                            fp16 hi + lo (q s - hi is exact in fp32),
 //   S^T = (Q s)_hi N + (Q s)_lo N   accumulated in fp32,
-// which is 508 q . k~ to about 2^-22 relative (|q s| < 65504 assumed).
+// which is 508 q . k~ to about 2^-22 relative (|q s| < 65504 assumed).  The
+// heads' hi parts fill A rows 0-7 and their lo parts rows 8-15 of the same
+// MMA (at most 8 heads), so both products cost one MMA per k-step; the
+// accumulator rows r and r + 8 are then added.
 // Softmax and O^T += V^T P^T follow the register-fed attend.
 #include <cuda_fp16.h>
 
@@ -61,6 +64,21 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The refined scores' MMAs carry the heads' q s hi parts in A rows 0-7 and
+// the lo parts in rows 8-15 (at most 8 heads), so one MMA forms both: the
+// score of head r is the sum of accumulator rows r and r + 8 (entries 0, 1
+// and 2, 3 of a lane), folded here into entries 0, 1 (rows 8-15 are unused
+// after this).
+__device__ __forceinline__ void refined_fold(float (&sc)[2][2][4]) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      sc[nt][c][0] += sc[nt][c][2];
+      sc[nt][c][1] += sc[nt][c][3];
+    }
 }
 
 __device__ __forceinline__ uint2 ldg_stream2(const void* p) {
@@ -222,12 +240,12 @@ __device__ __forceinline__ void compute_rgroup(const RGroup<D>& g, const Refined
         const uint32_t w0 = rw[2 * s], w1 = rw[2 * s + 1];
         uint32_t n[4];
         refined_step(c16, w0, w1, n);
-        mma_f16(sc[nt][0], hi[0], 0u, hi[1], 0u, n[0], n[1]);
-        mma_f16(sc[nt][1], hi[2], 0u, hi[3], 0u, n[2], n[3]);
-        mma_f16(sc[nt][0], lo[0], 0u, lo[1], 0u, n[0], n[1]);
-        mma_f16(sc[nt][1], lo[2], 0u, lo[3], 0u, n[2], n[3]);
+        // A rows 0-7: the heads' hi parts, rows 8-15: their lo parts
+        mma_f16(sc[nt][0], hi[0], lo[0], hi[1], lo[1], n[0], n[1]);
+        mma_f16(sc[nt][1], hi[2], lo[2], hi[3], lo[3], n[2], n[3]);
       }
     }
+    refined_fold(sc);
   } else {
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
@@ -882,12 +900,12 @@ __device__ __forceinline__ void refined_scores_smem(uint32_t stage, const uint32
     for (int nt = 0; nt < 2; ++nt) {
       uint32_t n[4];
       refined_step(cw[nt][s >> 1] >> (16 * (s & 1)), rw[nt][2 * s], rw[nt][2 * s + 1], n);
-      mma_f16(sc[nt][0], hi[s][0], 0u, hi[s][1], 0u, n[0], n[1]);
-      mma_f16(sc[nt][1], hi[s][2], 0u, hi[s][3], 0u, n[2], n[3]);
-      mma_f16(sc[nt][0], lo[s][0], 0u, lo[s][1], 0u, n[0], n[1]);
-      mma_f16(sc[nt][1], lo[s][2], 0u, lo[s][3], 0u, n[2], n[3]);
+      // A rows 0-7: the heads' hi parts, rows 8-15: their lo parts
+      mma_f16(sc[nt][0], hi[s][0], lo[s][0], hi[s][1], lo[s][1], n[0], n[1]);
+      mma_f16(sc[nt][1], hi[s][2], lo[s][2], hi[s][3], lo[s][3], n[2], n[3]);
     }
   }
+  refined_fold(sc);
 }
 
 template <int W, int S>
