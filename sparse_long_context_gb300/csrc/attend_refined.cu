@@ -9,8 +9,8 @@
 // Top-delta keeps a different number of blocks in every row (a few percent
 // in one head, most of the context in another), so a fixed split count per
 // row leaves the kernel as slow as its longest row.  Here the rows' lists,
-// concatenated, are cut into one equal range of entries per CTA (one 8-warp
-// CTA per SM, stream-K style).  Three kernels share that partition: where
+// concatenated, are cut into one equal range of entries per CTA (one CTA
+// per SM, stream-K style: 8 warps, 12 in the refined tensor-map kernel).  Three kernels share that partition: where
 // the shape allows tensor maps, attend_stream_tma_kernel (bf16 keys) and
 // attend_refined_tma_kernel (refined keys, D = 128), in which every warp
 // streams its groups through its own ring of tensor-map copies; otherwise
@@ -1132,8 +1132,11 @@ size_t refined_workspace(const Shape& s) {
 // 16-token groups at D = 128 (four at D = 64): the ring depth beyond that
 // bought nothing measurable, and more warps or CTAs per SM were slower.
 constexpr int kStreamWarps = 8;
-// Stages per warp of the refined kernel: its groups take longer to score
-// than to copy, and three stages measured the same as two.
+// The refined kernel: its groups take longer to score than to copy, so it
+// wants warps rather than stages.  Twelve warps (at most 170 registers a
+// thread) with two stages each fill the shared memory; three stages measured
+// the same as two, and 10 and 12 warps were 6% and 11% faster than 8.
+constexpr int kRefinedWarps = 12;
 constexpr int kRefinedStages = 2;
 
 template <int D>
@@ -1157,7 +1160,7 @@ static cudaError_t stream_tma_launch(const Shape& s, const RefinedArgs& ra, cuda
 // The refined attend on tensor-map fed rings (D = 128; the bf16 kernel's
 // grid).
 static cudaError_t refined_tma_launch(const Shape& s, const RefinedArgs& ra, cudaStream_t st, bool* handled) {
-  constexpr int D = 128, W = kStreamWarps, S = kRefinedStages;
+  constexpr int D = 128, W = kRefinedWarps, S = kRefinedStages;
   CUtensorMap tk, tv, tc, tr;
   const uint64_t tokens = (uint64_t)s.B * s.Hkv * s.Cap;
   if (!encode_rows_map(&tk, ra.a.k, tokens, D) || !encode_rows_map(&tv, ra.a.v, tokens, D) ||
