@@ -45,19 +45,19 @@ METRIC = "decode-step µs and achieved HBM GB/s (% of GB300 peak) for select+att
 # written; traffic grows with the rows, so x4 for batch 32).  Reported only
 # for that workload and only while the kernel's sources hash to the ones
 # captured; otherwise null.
-STEP_TRAFFIC_B32 = 4 * (50.470656e6 + 0.113664e6)
+STEP_TRAFFIC_B32 = 4 * (50.470656e6 + 0.101632e6)
 STEP_SOURCES = ("quest_step.cu", "attend_tma.cuh", "tma.cuh", "mma.cuh", "attend_common.cuh", "common.cuh",
                 "status.cuh")
-STEP_SOURCES_SHA256 = "b5c18b5bb3639e18f0c775ab1a5ebab5a4e7b7f423ec1d1392393fb866f629e3"
+STEP_SOURCES_SHA256 = "a55d7811c3f7b3e114d0b70d4b5f02d64f96135c2122dd7d5d16c9577bbe5bfd"
 
 
 # DRAM bytes per launch of the top-delta step's bf16-key attend
 # (attend_stream_tma_kernel) on the ffd workload, from the committed capture
 # (profiles/topdelta_ffd_256k.md, read + written; the kept set is the seeded
 # workload's), under the same source-hash rule.
-FFD_ATTEND_TRAFFIC = 490.943488e6 + 3.329536e6
+FFD_ATTEND_TRAFFIC = 490.998016e6 + 3.556096e6
 FFD_ATTEND_SOURCES = ('attend_refined.cu', 'attend_tma.cuh', 'tma.cuh', 'mma.cuh', 'attend_common.cuh', 'common.cuh', 'status.cuh')
-FFD_ATTEND_SOURCES_SHA256 = "abfc97ac9b5f75fcd21c567e5a3dd016e3b4d089eb3b7fe77233bd41225de9ad"
+FFD_ATTEND_SOURCES_SHA256 = "96a2e4a98425757cda54c391645546a8cd992906cfebfd618cff7fa8d1ed11b5"
 
 
 def sources_sha256(files) -> str:
