@@ -57,7 +57,7 @@ STEP_SOURCES_SHA256 = "a55d7811c3f7b3e114d0b70d4b5f02d64f96135c2122dd7d5d16c9577
 # workload's), under the same source-hash rule.
 FFD_ATTEND_TRAFFIC = 490.998016e6 + 3.556096e6
 FFD_ATTEND_SOURCES = ('attend_refined.cu', 'attend_tma.cuh', 'tma.cuh', 'mma.cuh', 'attend_common.cuh', 'common.cuh', 'status.cuh')
-FFD_ATTEND_SOURCES_SHA256 = "96a2e4a98425757cda54c391645546a8cd992906cfebfd618cff7fa8d1ed11b5"
+FFD_ATTEND_SOURCES_SHA256 = "d965897f4b75f9191a76c3ebf252149f3ed7ba44ab06019331d731d1ed5eb988"
 
 
 def sources_sha256(files) -> str:

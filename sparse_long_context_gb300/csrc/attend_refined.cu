@@ -1118,7 +1118,7 @@ bool refined_supported(const Shape& s) {
   return s.dtype == 1 && s.G <= 8 && s.P >= 16 && (s.D == 64 || s.D == 128) && s.B * s.Hkv <= kRefMaxRows;
 }
 
-// one 8-warp CTA per SM (the register budget)
+// one CTA per SM (8 warps, 12 in the refined tensor-map kernel: the register budget)
 static int balanced_grid() { return std::min(sm_count(), kRefMaxContrib); }
 
 size_t refined_workspace(const Shape& s) {
