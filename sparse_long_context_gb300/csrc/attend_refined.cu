@@ -9,8 +9,9 @@
 // Top-delta keeps a different number of blocks in every row (a few percent
 // in one head, most of the context in another), so a fixed split count per
 // row leaves the kernel as slow as its longest row.  Here the rows' lists,
-// concatenated, are cut into one equal range of entries per CTA (one CTA
-// per SM, stream-K style: 8 warps, 12 in the refined tensor-map kernel).  Three kernels share that partition: where
+// concatenated, are cut into one range of entries per CTA (one CTA per SM,
+// stream-K style: 8 warps, 12 in the refined tensor-map kernel), equal but
+// for a CTA whose range crosses a row start, which takes a little less.  Three kernels share that partition: where
 // the shape allows tensor maps, attend_stream_tma_kernel (bf16 keys) and
 // attend_refined_tma_kernel (refined keys, D = 128), in which every warp
 // streams its groups through its own ring of tensor-map copies; otherwise
@@ -332,7 +333,12 @@ __device__ __forceinline__ int ref_scan(int v, int* tmp, int& total) {
   return before + x - v;
 }
 
-__device__ __forceinline__ long long range_lo(long long T, int c, int grid) { return T * c / grid; }
+// Work of a CTA's row change in the stream-K kernels (drain, merge, partial
+// and refill), in tokens of the list, as measured best on the 256k top-delta
+// workload (0 to 1536 swept): 768 for bf16 keys (and the register-fed
+// kernel), 1024 for the refined kernel, whose 12 warps merge more state.
+constexpr int kSegCostTokens = 768;
+constexpr int kSegCostTokensRefined = 1024;
 
 // The CTA whose entry range [s_lo[c], s_lo[c + 1]) holds entry x < T: the
 // last c with s_lo[c] <= x (CTAs with empty ranges share their s_lo with the
@@ -370,7 +376,8 @@ __device__ __forceinline__ void finish_head(const AttendArgs& a, size_t hq, int 
 // [lo, hi) with the row holding lo.  False when the CTA has no entries.
 template <int D, int NT>
 __device__ __forceinline__ bool stream_k_begin(const AttendArgs& a, int rows, RefSmem& sh, int* s_pref, int& T,
-                                               long long& lo, long long& hi, int& row) {
+                                               long long& lo, long long& hi, int& row,
+                                               int seg_cost_tokens = kSegCostTokens) {
   const int G = a.G, grid = gridDim.x, c = blockIdx.x;
   const int RPT = (rows + NT - 1) / NT;
   const int r0 = threadIdx.x * RPT;
@@ -388,9 +395,28 @@ __device__ __forceinline__ bool stream_k_begin(const AttendArgs& a, int rows, Re
     }
   }
   if (threadIdx.x == 0) s_pref[rows] = T;
-  // every CTA's range, once: the contributors of a shared row are read from
-  // here (a 64-bit division per CTA, in parallel)
-  for (int k = threadIdx.x; k <= grid; k += NT) sh.s_lo[k] = (int)range_lo(T, k, grid);
+  __syncthreads();
+  // Every CTA's range, once, a CTA per thread (the contributors of a shared
+  // row are read from here).  The ranges are equal in a list where every row
+  // start after the first counts seg_cost_tokens of extra work: a CTA whose
+  // range crosses a row start drains, merges and refills its rings there, so
+  // it takes that much less of the real list.  Row r's entries x sit at
+  // x + beta r; the entries of CTA k start at the first real entry at or
+  // after phantom position Tp k / grid.
+  {
+    const long long beta = seg_cost_tokens >> a.pshift;
+    const long long Tp = (long long)T + beta * (rows - 1);
+    for (int k = threadIdx.x; k <= grid; k += NT) {
+      const long long Lp = Tp * k / grid;
+      int l = 0, u = rows - 1;  // the last row whose phantom start is <= Lp
+      while (l < u) {
+        const int mid = (l + u + 1) >> 1;
+        if (s_pref[mid] + beta * mid <= Lp) l = mid;
+        else u = mid - 1;
+      }
+      sh.s_lo[k] = (int)min(Lp - beta * l, (long long)s_pref[l + 1]);
+    }
+  }
   __syncthreads();
 
   // rows with an empty list: output 0, lse -inf (or the sink alone)
@@ -552,7 +578,8 @@ __device__ __forceinline__ void finish_segment(const RefinedArgs& ra, RefSmem& s
 
 // Stream-K over the rows' lists (top-delta keeps a different number of
 // blocks in every row): the lists, concatenated row after row (T entries),
-// are cut into one equal range of entries per CTA.  A CTA attends the row
+// are cut into one range of entries per CTA (equal, but for the row-change
+// cost that stream_k_begin charges a CTA crossing a row start).  A CTA attends the row
 // segments of its range; a row entirely inside the range is finished in
 // place, a row shared with neighbouring CTAs gets a partial from each of
 // them (slot 2c for the segment a CTA's range starts in, 2c + 1 for the one
@@ -945,7 +972,8 @@ attend_refined_tma_kernel(const __grid_constant__ CUtensorMap tk, const __grid_c
   pdl_wait_then_release();
   int T, row;
   long long lo, hi;
-  if (!stream_k_begin<D, NT>(a, rows, sh, s_pref, T, lo, hi, row)) return;  // after its barrier: inits visible
+  // after its barrier: inits visible
+  if (!stream_k_begin<D, NT>(a, rows, sh, s_pref, T, lo, hi, row, kSegCostTokensRefined)) return;
 
   const bool plant = a.test_wait && c == 0 && warp == 0;
   const uint32_t tries = plant ? kTestWaitTries : kWaitTries;
