@@ -55,9 +55,9 @@ STEP_SOURCES_SHA256 = "a55d7811c3f7b3e114d0b70d4b5f02d64f96135c2122dd7d5d16c9577
 # (attend_stream_tma_kernel) on the ffd workload, from the committed capture
 # (profiles/topdelta_ffd_256k.md, read + written; the kept set is the seeded
 # workload's), under the same source-hash rule.
-FFD_ATTEND_TRAFFIC = 490.998016e6 + 3.556096e6
+FFD_ATTEND_TRAFFIC = 490.973696e6 + 3.187712e6
 FFD_ATTEND_SOURCES = ('attend_refined.cu', 'attend_tma.cuh', 'tma.cuh', 'mma.cuh', 'attend_common.cuh', 'common.cuh', 'status.cuh')
-FFD_ATTEND_SOURCES_SHA256 = "d965897f4b75f9191a76c3ebf252149f3ed7ba44ab06019331d731d1ed5eb988"
+FFD_ATTEND_SOURCES_SHA256 = "7ca3dc828056ddc2a8b7855a6d641a64ef1291ac2ac8c654e11ea71018a27c60"
 
 
 def sources_sha256(files) -> str:
