@@ -57,7 +57,7 @@ STEP_SOURCES_SHA256 = "a55d7811c3f7b3e114d0b70d4b5f02d64f96135c2122dd7d5d16c9577
 # workload's), under the same source-hash rule.
 FFD_ATTEND_TRAFFIC = 490.973696e6 + 3.187712e6
 FFD_ATTEND_SOURCES = ('attend_refined.cu', 'attend_tma.cuh', 'tma.cuh', 'mma.cuh', 'attend_common.cuh', 'common.cuh', 'status.cuh')
-FFD_ATTEND_SOURCES_SHA256 = "7ca3dc828056ddc2a8b7855a6d641a64ef1291ac2ac8c654e11ea71018a27c60"
+FFD_ATTEND_SOURCES_SHA256 = "9717fadbd32d4e7cecc3dc4e33e65abd9b13a93053d2b4e02423068159baf6e6"
 
 
 def sources_sha256(files) -> str:

@@ -11,11 +11,12 @@
 // row leaves the kernel as slow as its longest row.  Here the rows' lists,
 // concatenated, are cut into one range of entries per CTA (one CTA per SM,
 // stream-K style: 8 warps, 12 in the refined tensor-map kernel), equal but
-// for a CTA whose range crosses a row start, which takes a little less.  Three kernels share that partition: where
-// the shape allows tensor maps, attend_stream_tma_kernel (bf16 keys) and
-// attend_refined_tma_kernel (refined keys, D = 128), in which every warp
-// streams its groups through its own ring of tensor-map copies; otherwise
-// the register-fed attend_balanced_kernel (either kind of key).
+// for a CTA whose range crosses a row start, which takes a little less.
+// Three kernels share that partition: where the shape allows tensor maps,
+// attend_stream_tma_kernel (bf16 keys) and attend_refined_tma_kernel
+// (refined keys, D = 128), in which every warp streams its groups through
+// its own ring of tensor-map copies; otherwise the register-fed
+// attend_balanced_kernel (either kind of key).
 //
 // In attend_balanced_kernel a warp walks 16-token groups with two groups in
 // flight in registers (the shape of the register-fed attend).  Lane (r, m) owns the
