@@ -145,6 +145,64 @@ def test_refined_step_matches_oracle(key, no_tma):
     print(f"{key}: boundary ties {ties}")
 
 
+@pytest.mark.parametrize("refined", [False, True])
+def test_stream_k_with_more_rows_than_ctas(refined):
+    """192 rows of 7-8 blocks against one CTA per SM: most CTA ranges hold
+    several whole rows and start or end inside others, and the row-start
+    cost the partition charges outweighs the real entries (every partition
+    boundary case at once).  Lists: empty, one block, every block, or a
+    random subset; outputs against the oracle's attention on the same sets
+    (refined keys: the oracle's refined attention)."""
+    s = W.spec("ffd", batch=24, ctx_len=[64 * 7 + 5 + 13 * (b % 5) for b in range(24)], capacity=64 * 8)
+    assert s.rows > 152
+    host = W.generate(s)
+    dw = PT.upload(s, host)
+    codes = scales = res = None
+    if refined:
+        codes, scales, res = ops.thumb_residual_build(dw.desc, dw.K, dw.ctx, s.block)
+    rng = np.random.default_rng(11)
+    width = s.capacity // s.block
+    idx = np.full((s.rows, width), -1, dtype=np.int32)
+    count = np.zeros(s.rows, dtype=np.int32)
+    lists = []
+    for r in range(s.rows):
+        nb = -(-int(host.ctx_len[r // s.num_kv_heads]) // s.block)
+        kind = r % 5
+        if kind == 0:
+            blocks = np.zeros(0, dtype=np.int64)
+        elif kind == 1:
+            blocks = np.array([nb - 1])
+        elif kind == 2:
+            blocks = np.arange(nb)
+        else:
+            blocks = np.sort(rng.choice(nb, size=int(rng.integers(1, nb + 1)), replace=False))
+        lists.append(blocks)
+        idx[r, :len(blocks)] = blocks
+        count[r] = len(blocks)
+    ops.get_stats(reset=True)
+    out, lse = ops.refined_decode_attend_combine(dw.desc, dw.q, dw.K, dw.V, codes, scales, res,
+                                                 torch.from_numpy(idx).cuda(), torch.from_numpy(count).cuda(),
+                                                 dw.ctx, sink=dw.sink)
+    ops.pipeline_check()
+    st = ops.get_stats(reset=True)
+    assert st["attend_refined_tma" if refined else "attend_stream_k_tma"] == 1, st
+    out = out.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy()
+    G = s.group
+    for b in range(s.batch):
+        for h in range(s.num_kv_heads):
+            r = b * s.num_kv_heads + h
+            if refined:
+                o_ref, l_ref = _refined_oracle(s, host, b, h, lists[r])
+            else:
+                q, K, V, sink = _row_inputs(s, host, b, h)
+                o_ref, l_ref = O.sparse_attention_row(q, K, V, lists[r], int(host.ctx_len[b]), s.page_size,
+                                                      s.scale, sink)
+            PT.assert_close(s, out[b, h * G:(h + 1) * G], o_ref, f"row {r}")
+            fin = np.isfinite(l_ref)
+            np.testing.assert_allclose(lse[b, h * G:(h + 1) * G][fin], l_ref[fin], rtol=1e-4, atol=1e-4)
+
+
 def test_refined_scores_differ_from_exact_ones():
     """The refined path really scores with k~: against the exact-key step on
     the same selection the outputs differ (slightly), and both stay within
